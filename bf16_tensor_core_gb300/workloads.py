@@ -1,0 +1,161 @@
+"""Seeded synthetic inputs for the dense GEMM (no GEMM arithmetic lives here).
+
+This module is the one piece both the CUDA path's tests/benchmark and the CPU
+oracle's tests use: it only draws and stores input values.  Values are drawn in
+f64 on the torch CPU generator and rounded to nearest-even into the stored
+dtype; the stored bytes are the inputs both sides read.
+
+The five named workloads follow the shapes, dtypes, layouts and value
+distributions of the GEMMs discussed on the pages:
+  * 512^3 and 4096^3 / 8192^3 square products ("Optimizing GEMMs using tcgen05 -
+    Part 2", section 5 onward, measures 4096^3 fp16),
+  * a prefill-shaped 2048 x 11008 x 4096 projection with a per-column bias
+    ("02 - Tiled wmma f16 prefill GEMM", sections 1-2: prefill of a 7B model at
+    2K tokens; synthetic N(0, 0.02) weights stand in for trained ones),
+  * a ragged 1000 x 3000 x 2050 product with B stored transposed (N x K, the NT
+    layout of that page's gemm_f16_nt kernel) and alpha/beta on an input C.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+
+import torch
+
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    dtype_in: str = "f16"
+    dtype_out: str = "f32"
+    layoutA: str = "row"        # row: M x K (K contiguous); col: stored K x M
+    layoutB: str = "row"        # row: K x N (N contiguous); col: stored N x K
+    alpha: float = 1.0
+    beta: float = 0.0
+    dist_a: tuple = ("uniform", -1.0, 1.0)
+    dist_b: tuple = ("uniform", -1.0, 1.0)
+    dist_bias: tuple | None = None
+    dist_cin: tuple | None = None
+    seed: int = 0
+    note: str = field(default="", compare=False)
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+def _seed(cfg: int) -> int:
+    return 20261202 + 100 * cfg
+
+
+# The five workloads, in order (index 1..5).
+WORKLOADS = {
+    1: Workload("gemm_512_f16_f32", 512, 512, 512, "f16", "f32", "row", "row", 1.0, 0.0,
+                ("uniform", -1.0, 1.0), ("uniform", -1.0, 1.0), None, None, _seed(1),
+                "512^3, f16 in U[-1,1], f32 out"),
+    2: Workload("gemm_4096_f16_f16", 4096, 4096, 4096, "f16", "f16", "row", "row", 1.0, 0.0,
+                ("normal_sqrtk",), ("normal_sqrtk",), None, None, _seed(2),
+                "4096^3, f16 in N(0,1)/sqrt(K), f16 out"),
+    3: Workload("prefill_2048x11008x4096_bf16_bias", 2048, 11008, 4096, "bf16", "bf16", "row", "row",
+                1.0, 0.0, ("normal", 1.0), ("normal", 0.02), ("normal", 0.02), None, _seed(3),
+                "prefill projection, bf16 in, bf16 out, fused per-column bias"),
+    4: Workload("ragged_1000x3000x2050_nt_f32_ab", 1000, 3000, 2050, "f16", "f32", "row", "col",
+                0.5, 1.0, ("uniform", -1.0, 1.0), ("uniform", -1.0, 1.0), None, ("uniform", -1.0, 1.0),
+                _seed(4), "ragged edges, B stored N x K, alpha=0.5, beta=1 on C_in"),
+    5: Workload("gemm_8192_f16_f16", 8192, 8192, 8192, "f16", "f16", "row", "row", 1.0, 0.0,
+                ("normal_sqrtk",), ("normal_sqrtk",), None, None, _seed(5),
+                "8192^3, f16 in N(0,1)/sqrt(K), f16 out"),
+}
+
+
+def _draw(shape, dist, K, g) -> torch.Tensor:
+    kind = dist[0]
+    if kind == "uniform":
+        lo, hi = dist[1], dist[2]
+        return torch.rand(shape, generator=g, dtype=torch.float64) * (hi - lo) + lo
+    if kind == "normal":
+        return torch.randn(shape, generator=g, dtype=torch.float64) * dist[1]
+    if kind == "normal_sqrtk":
+        return torch.randn(shape, generator=g, dtype=torch.float64) / math.sqrt(max(K, 1))
+    raise ValueError(f"unknown distribution {dist}")
+
+
+def stored_shape_a(w: Workload, lda: int | None = None):
+    if w.layoutA == "row":
+        return (w.M, lda or w.K)
+    return (w.K, lda or w.M)
+
+
+def stored_shape_b(w: Workload, ldb: int | None = None):
+    if w.layoutB == "row":
+        return (w.K, ldb or w.N)
+    return (w.N, ldb or w.K)
+
+
+def generate(w: Workload, *, lda=None, ldb=None, ldc=None) -> dict:
+    """Draw A, B, then bias or C_in (in that order) on the CPU generator seeded with w.seed.
+
+    Returns CPU tensors in the stored layout: A, B (dtype_in), bias (N, dtype_out)
+    or None, Cin (M x ldc, dtype_out) or None.  Padding columns of a wider leading
+    dimension are drawn too (their values never enter the product).
+    """
+    g = torch.Generator().manual_seed(w.seed)
+    din = DTYPES[w.dtype_in]
+    dout = DTYPES[w.dtype_out]
+    A = _draw(stored_shape_a(w, lda), w.dist_a, w.K, g).to(din)
+    B = _draw(stored_shape_b(w, ldb), w.dist_b, w.K, g).to(din)
+    bias = _draw((w.N,), w.dist_bias, w.K, g).to(dout) if w.dist_bias else None
+    Cin = _draw((w.M, ldc or w.N), w.dist_cin, w.K, g).to(dout) if w.dist_cin else None
+    return {"A": A, "B": B, "bias": bias, "Cin": Cin}
+
+
+def problem(M, N, K, *, dtype_in="f16", dtype_out="f32", layoutA="row", layoutB="row",
+            alpha=1.0, beta=0.0, bias=False, seed=1, name="problem",
+            dist=("uniform", -1.0, 1.0)) -> Workload:
+    """An ad-hoc workload (tail sweeps, layout and dtype coverage)."""
+    return Workload(name, M, N, K, dtype_in, dtype_out, layoutA, layoutB, alpha, beta,
+                    dist, dist, dist if bias else None, dist if beta != 0.0 else None, seed)
+
+
+def with_changes(w: Workload, **kw) -> Workload:
+    return replace(w, **kw)
+
+
+# ----------------------------------------------------------------------------------------
+# structured inputs whose products have closed forms (used by exactness tests)
+# ----------------------------------------------------------------------------------------
+def identity(rows: int, cols: int, dtype: str) -> torch.Tensor:
+    """rows x cols partial identity: 1 where i == j."""
+    t = torch.zeros(rows, cols, dtype=torch.float64)
+    n = min(rows, cols)
+    t[torch.arange(n), torch.arange(n)] = 1.0
+    return t.to(DTYPES[dtype])
+
+
+def permutation(n: int, seed: int) -> torch.Tensor:
+    """A random permutation of range(n) (int64)."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randperm(n, generator=g)
+
+
+def permutation_matrix(perm: torch.Tensor, dtype: str) -> torch.Tensor:
+    """P with P[i, perm[i]] = 1, so (P @ X)[i] = X[perm[i]]."""
+    n = perm.numel()
+    t = torch.zeros(n, n, dtype=torch.float64)
+    t[torch.arange(n), perm] = 1.0
+    return t.to(DTYPES[dtype])
+
+
+def ones(rows: int, cols: int, dtype: str) -> torch.Tensor:
+    return torch.ones(rows, cols, dtype=DTYPES[dtype])
+
+
+def small_ints(rows: int, cols: int, dtype: str, seed: int, lo: int = -3, hi: int = 3) -> torch.Tensor:
+    """Integers uniform in [lo, hi] (exact in f16 and bf16)."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(lo, hi + 1, (rows, cols), generator=g, dtype=torch.int64).to(DTYPES[dtype])

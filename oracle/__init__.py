@@ -1,0 +1,11 @@
+"""CPU oracle for the dense GEMM (test infrastructure only).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never loads it and
+shares no code with it.
+"""
+from .oracle import (  # noqa: F401
+    OR_F16, OR_BF16, OR_F32, OR_ROW, OR_COL,
+    build, lib_path, decode_f16, decode_bf16, decode_f32,
+    gemm_ref, ulp_out, tolerance, check, error_metrics, epilogue_magnitude, num_cpus, decode,
+)
