@@ -1,0 +1,592 @@
+// Host side of the C ABI declared in include/gemm.h: handle, validation, planning, tensor-map
+// cache, operand repack, dispatch and error reporting.  No device code lives here except what
+// the kernel headers declare.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/gemm.h"
+#include "gemm_kernel.cuh"
+#include "gemm_launch.h"
+
+using namespace gb300;
+
+namespace {
+
+// ---------------------------------------------------------------- configuration table
+template <int CG, int BN, int ST>
+constexpr ConfigDesc make_desc(int id) {
+    return ConfigDesc{id, CG, BN, ST, TileConfig<CG, BN, ST>::kSmemBytes, TileConfig<CG, BN, ST>::kThreads};
+}
+
+const ConfigDesc kConfigs[kNumConfigs] = {
+    make_desc<1, 256, 4>(0),  // 1 SM, 128 x 256 tile
+    make_desc<2, 256, 6>(1),  // 2-SM cluster, 256 x 256 tile
+    make_desc<1, 128, 6>(2),  // 1 SM, 128 x 128 tile
+    make_desc<2, 128, 8>(3),  // 2-SM cluster, 256 x 128 tile
+};
+
+// Relative tensor-core efficiency assumed per config when choosing one for a shape (larger
+// tiles amortise the per-stage cost and need less L2 bandwidth per flop).
+const double kConfigEfficiency[kNumConfigs] = {0.88, 1.00, 0.72, 0.93};
+
+enum FaultSite { FAULT_NONE = 0, FAULT_OPTIN = 1, FAULT_TMAP = 2, FAULT_LAUNCH = 4, FAULT_ALLOC = 8 };
+
+int read_fault_env() {
+    // Host-side fault injection for tests: GEMM_TEST_FAIL=optin,tmap,launch,alloc
+    const char* e = std::getenv("GEMM_TEST_FAIL");
+    if (!e) return FAULT_NONE;
+    int f = FAULT_NONE;
+    std::string s(e);
+    if (s.find("optin") != std::string::npos) f |= FAULT_OPTIN;
+    if (s.find("tmap") != std::string::npos) f |= FAULT_TMAP;
+    if (s.find("launch") != std::string::npos) f |= FAULT_LAUNCH;
+    if (s.find("alloc") != std::string::npos) f |= FAULT_ALLOC;
+    return f;
+}
+
+int elt_bytes(int dt) { return dt == GEMM_F32 ? 4 : 2; }
+
+struct TmapKey {
+    const void* ptr;
+    int dtype;
+    uint64_t dim0, dim1, stride;
+    uint32_t box0, box1;
+    bool operator==(const TmapKey& o) const {
+        return ptr == o.ptr && dtype == o.dtype && dim0 == o.dim0 && dim1 == o.dim1 && stride == o.stride &&
+               box0 == o.box0 && box1 == o.box1;
+    }
+};
+
+struct TmapEntry {
+    TmapKey key;
+    CUtensorMap map;
+};
+
+}  // namespace
+
+struct gemm_ctx {
+    int device = 0;
+    int num_sms = 0;
+    int max_clusters[kNumConfigs] = {0, 0, 0, 0};
+    gemm_options_t opt{};
+    unsigned long long* d_status = nullptr;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    std::string err;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    std::vector<TmapEntry> cache;
+    size_t cache_next = 0;
+    int faults = FAULT_NONE;
+    int64_t launches = 0;
+};
+
+namespace {
+
+gemm_status_t fail(gemm_handle_t h, gemm_status_t s, const std::string& msg) {
+    if (h) h->err = msg;
+    return s;
+}
+
+gemm_status_t cuda_fail(gemm_handle_t h, const char* what, cudaError_t e) {
+    return fail(h, GEMM_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+struct Validated {
+    gemm_plan_t plan;
+    std::string err;
+};
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+// Pure host planning: validation, config choice, grid and workspace.
+gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int din, int dout,
+                        int la, int lb, float beta, int num_sms, int max_clusters, int config, gemm_plan_t* out,
+                        std::string* err) {
+    std::memset(out, 0, sizeof(*out));
+    out->config = -1;
+    if (M < 0 || N < 0 || K < 0) { *err = "M, N and K must be >= 0"; return GEMM_ERR_INVALID_ARG; }
+    const int64_t kMaxDim = (int64_t)1 << 31;
+    if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) { *err = "M, N and K must be < 2^31"; return GEMM_ERR_INVALID_ARG; }
+    if (din != GEMM_F16 && din != GEMM_BF16) { *err = "dtype_in must be GEMM_F16 or GEMM_BF16"; return GEMM_ERR_INVALID_ARG; }
+    if (dout != GEMM_F16 && dout != GEMM_BF16 && dout != GEMM_F32) { *err = "dtype_out must be F16, BF16 or F32"; return GEMM_ERR_INVALID_ARG; }
+    if ((la != GEMM_ROW && la != GEMM_COL) || (lb != GEMM_ROW && lb != GEMM_COL)) { *err = "layout must be GEMM_ROW or GEMM_COL"; return GEMM_ERR_INVALID_ARG; }
+    const int64_t a_inner = la == GEMM_ROW ? K : M;
+    const int64_t b_inner = lb == GEMM_ROW ? N : K;
+    if (lda < std::max<int64_t>(1, a_inner)) { *err = "lda too small"; return GEMM_ERR_INVALID_ARG; }
+    if (ldb < std::max<int64_t>(1, b_inner)) { *err = "ldb too small"; return GEMM_ERR_INVALID_ARG; }
+    if (ldc < std::max<int64_t>(1, N)) { *err = "ldc too small"; return GEMM_ERR_INVALID_ARG; }
+    if (num_sms <= 0) { *err = "num_sms must be > 0"; return GEMM_ERR_INVALID_ARG; }
+    if (config < -1 || config >= kNumConfigs) { *err = "no such config"; return GEMM_ERR_UNSUPPORTED; }
+    if (max_clusters <= 0) max_clusters = num_sms / 2;
+    if (M == 0 || N == 0) { out->kernels = 0; return GEMM_OK; }
+    if (K == 0) { out->kernels = 1; return GEMM_OK; }
+
+    int best = config;
+    if (best < 0) {
+        double best_cost = 1e300;
+        for (int c = 0; c < kNumConfigs; ++c) {
+            const ConfigDesc& d = kConfigs[c];
+            const int slots = d.cta_group == 2 ? max_clusters : num_sms;
+            if (slots <= 0) continue;
+            const int64_t bm = 128 * d.cta_group;
+            const int64_t tiles = ((M + bm - 1) / bm) * ((N + d.block_n - 1) / d.block_n);
+            const int64_t waves = (tiles + slots - 1) / slots;
+            const double cost = (double)waves * (double)(bm * d.block_n) / (d.cta_group * kConfigEfficiency[c]);
+            if (cost < best_cost * (1.0 - 1e-9)) { best_cost = cost; best = c; }
+        }
+    }
+    const ConfigDesc& d = kConfigs[best];
+    if (d.cta_group == 2 && max_clusters <= 0) { *err = "2-SM clusters do not fit"; return GEMM_ERR_UNSUPPORTED; }
+    out->config = best;
+    out->cta_group = d.cta_group;
+    out->block_m = 128 * d.cta_group;
+    out->block_n = d.block_n;
+    out->block_k = 64;
+    out->stages = d.stages;
+    out->tiles_m = (int)((M + out->block_m - 1) / out->block_m);
+    out->tiles_n = (int)((N + out->block_n - 1) / out->block_n);
+    const int64_t tiles = (int64_t)out->tiles_m * out->tiles_n;
+    const int slots = d.cta_group == 2 ? max_clusters : num_sms;
+    out->clusters = (int)std::min<int64_t>(tiles, slots);
+    out->raster_group = std::min(out->tiles_m, 8);
+    out->tma_store = (beta == 0.0f && (ldc * elt_bytes(dout)) % 16 == 0) ? 1 : 0;
+    out->repack_a = (lda * 2) % 16 != 0;
+    out->repack_b = (ldb * 2) % 16 != 0;
+    int64_t ws = 0;
+    if (out->repack_a) ws += round_up((la == GEMM_ROW ? M : K) * round_up(a_inner, 8) * 2, 256);
+    if (out->repack_b) ws += round_up((lb == GEMM_ROW ? K : N) * round_up(b_inner, 8) * 2, 256);
+    out->workspace_bytes = ws;
+    out->kernels = 1 + out->repack_a + out->repack_b;
+    return GEMM_OK;
+}
+
+// Tensor map of a 2-D row-major array: dim0 contiguous, dim1 rows of `stride_bytes`.
+gemm_status_t get_tmap(gemm_handle_t h, const void* ptr, CUtensorMapDataType dt, uint64_t dim0, uint64_t dim1,
+                       uint64_t stride_bytes, uint32_t box0, uint32_t box1, CUtensorMap* out) {
+    TmapKey key{ptr, (int)dt, dim0, dim1, stride_bytes, box0, box1};
+    for (const TmapEntry& e : h->cache)
+        if (e.key == key) { *out = e.map; return GEMM_OK; }
+    if (h->faults & FAULT_TMAP) return fail(h, GEMM_ERR_CUDA, "cuTensorMapEncodeTiled: forced failure (GEMM_TEST_FAIL=tmap)");
+    CUtensorMap m;
+    const cuuint64_t dims[2] = {dim0, dim1};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {box0, box1};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = h->encode(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char buf[256];
+        std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed (%d) dims {%llu,%llu} stride %llu box {%u,%u}",
+                      (int)r, (unsigned long long)dim0, (unsigned long long)dim1, (unsigned long long)stride_bytes,
+                      box0, box1);
+        return fail(h, GEMM_ERR_CUDA, buf);
+    }
+    const size_t kCacheSize = 32;
+    if (h->cache.size() < kCacheSize) {
+        h->cache.push_back(TmapEntry{key, m});
+    } else {
+        h->cache[h->cache_next] = TmapEntry{key, m};
+        h->cache_next = (h->cache_next + 1) % kCacheSize;
+    }
+    *out = m;
+    return GEMM_OK;
+}
+
+gemm_status_t ensure_workspace(gemm_handle_t h, size_t bytes) {
+    if (bytes <= h->ws_bytes) return GEMM_OK;
+    if (h->faults & FAULT_ALLOC) return fail(h, GEMM_ERR_OOM, "workspace allocation: forced failure (GEMM_TEST_FAIL=alloc)");
+    if (h->ws) { cudaFree(h->ws); h->ws = nullptr; h->ws_bytes = 0; }
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(h, GEMM_ERR_OOM, std::string("workspace cudaMalloc: ") + cudaGetErrorString(e));
+    }
+    h->ws = p;
+    h->ws_bytes = bytes;
+    return GEMM_OK;
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    bool changed = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+            if (cudaSetDevice(dev) == cudaSuccess) changed = true;
+        }
+    }
+    ~DeviceGuard() {
+        if (changed) cudaSetDevice(prev);
+    }
+};
+
+uint32_t make_idesc(int din, int a_mn, int b_mn, int mma_m, int mma_n) {
+    // tcgen05 instruction descriptor, kind::f16: D f32 (bits 4-5 = 1); A/B format 0 f16, 1 bf16
+    // (bits 7-9, 10-12); A/B major 0 K, 1 MN (bits 15, 16); N >> 3 (bits 17-22); M >> 4 (24-28).
+    const uint32_t fmt = din == GEMM_BF16 ? 1u : 0u;
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(mma_n >> 3) << 17) | ((uint32_t)(mma_m >> 4) << 24);
+}
+
+}  // namespace
+
+namespace gb300 {
+
+const ConfigDesc* config_desc(int id) { return (id >= 0 && id < kNumConfigs) ? &kConfigs[id] : nullptr; }
+
+const void* config_kernel(int id, int out) {
+    switch (id) {
+        case 0: return cfg0_kernel(out);
+        case 1: return cfg1_kernel(out);
+        case 2: return cfg2_kernel(out);
+        case 3: return cfg3_kernel(out);
+        default: return nullptr;
+    }
+}
+
+cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, const CUtensorMap& a,
+                          const CUtensorMap& b, const CUtensorMap& c, const KernelParams& p) {
+    const ConfigDesc* d = config_desc(id);
+    if (!d) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)grid_ctas, 1, 1);
+    lc.blockDim = dim3((unsigned)d->threads, 1, 1);
+    lc.dynamicSmemBytes = (size_t)d->smem_bytes;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)d->cta_group;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    switch (id) {
+        case 0: return cfg0_launch(out, lc, a, b, c, p);
+        case 1: return cfg1_launch(out, lc, a, b, c, p);
+        case 2: return cfg2_launch(out, lc, a, b, c, p);
+        case 3: return cfg3_launch(out, lc, a, b, c, p);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gb300
+
+extern "C" {
+
+void gemm_options_default(gemm_options_t* opt) {
+    if (!opt) return;
+    std::memset(opt, 0, sizeof(*opt));
+    opt->struct_size = (int)sizeof(gemm_options_t);
+    opt->config = -1;
+    opt->timeout_ms = 2000;
+    opt->sync_check = 0;
+    opt->raster_group = 0;
+    opt->max_clusters = 0;
+    opt->debug_skip_stage = -1;
+}
+
+const char* gemm_status_string(gemm_status_t s) {
+    switch (s) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+        case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED";
+        case GEMM_ERR_ALIGNMENT: return "GEMM_ERR_ALIGNMENT";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+        case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+        case GEMM_ERR_OOM: return "GEMM_ERR_OOM";
+        default: return "GEMM_ERR_UNKNOWN";
+    }
+}
+
+int gemm_num_configs(void) { return kNumConfigs; }
+
+gemm_status_t gemm_config_info(int id, gemm_config_info_t* out) {
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    const ConfigDesc* d = config_desc(id);
+    if (!d) return GEMM_ERR_UNSUPPORTED;
+    out->id = d->id;
+    out->cta_group = d->cta_group;
+    out->block_m = 128 * d->cta_group;
+    out->block_n = d->block_n;
+    out->block_k = 64;
+    out->stages = d->stages;
+    out->smem_bytes = d->smem_bytes;
+    out->threads = d->threads;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                        gemm_dtype_t dtype_in, gemm_dtype_t dtype_out, gemm_layout_t layoutA, gemm_layout_t layoutB,
+                        float beta, int num_sms, int max_clusters, int config, gemm_plan_t* out) {
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    std::string err;
+    return plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, num_sms, max_clusters,
+                     config, out, &err);
+}
+
+gemm_status_t gemm_create(gemm_handle_t* out, int device, const gemm_options_t* opt) {
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    gemm_options_t o;
+    gemm_options_default(&o);
+    if (opt) {
+        if (opt->struct_size != (int)sizeof(gemm_options_t)) return GEMM_ERR_INVALID_ARG;
+        o = *opt;
+    }
+    if (o.config < -1 || o.config >= kNumConfigs || o.timeout_ms <= 0 || o.raster_group < 0 || o.max_clusters < 0)
+        return GEMM_ERR_INVALID_ARG;
+    int count = 0;
+    cudaError_t e = cudaGetDeviceCount(&count);
+    if (e != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+    if (device < 0 || device >= count) return GEMM_ERR_INVALID_ARG;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED;
+
+    gemm_ctx* h = new (std::nothrow) gemm_ctx();
+    if (!h) return GEMM_ERR_OOM;
+    h->device = device;
+    h->opt = o;
+    h->faults = read_fault_env();
+    DeviceGuard guard(device);
+    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        cudaGetLastError();
+        delete h;
+        return GEMM_ERR_CUDA;
+    }
+    gemm_status_t st = GEMM_OK;
+    // Opt every kernel into its dynamic shared memory here, never inside a capture window.
+    for (int c = 0; c < kNumConfigs && st == GEMM_OK; ++c) {
+        const ConfigDesc* d = config_desc(c);
+        for (int outk = 0; outk < kNumOut && st == GEMM_OK; ++outk) {
+            const void* fn = config_kernel(c, outk);
+            cudaError_t ea = (h->faults & FAULT_OPTIN) ? cudaErrorInvalidValue
+                             : cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_bytes);
+            if (ea != cudaSuccess) {
+                cudaGetLastError();
+                st = GEMM_ERR_CUDA;
+            }
+        }
+        if (st == GEMM_OK) {
+            int nclusters = h->num_sms / d->cta_group;
+            if (d->cta_group == 2) {
+                cudaLaunchConfig_t lc = {};
+                lc.gridDim = dim3((unsigned)(h->num_sms - h->num_sms % 2), 1, 1);
+                lc.blockDim = dim3((unsigned)d->threads, 1, 1);
+                lc.dynamicSmemBytes = (size_t)d->smem_bytes;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 2;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                lc.attrs = attr;
+                lc.numAttrs = 1;
+                int n = 0;
+                if (cudaOccupancyMaxActiveClusters(&n, config_kernel(c, OUT_F16), &lc) != cudaSuccess) {
+                    cudaGetLastError();
+                    n = 0;
+                }
+                nclusters = n;
+            }
+            h->max_clusters[c] = nclusters;
+        }
+    }
+    if (st != GEMM_OK) {
+        delete h;
+        return st;
+    }
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        delete h;
+        return GEMM_ERR_CUDA;
+    }
+    h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    e = cudaMalloc(&h->d_status, 64);
+    if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 64);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        if (h->d_status) cudaFree(h->d_status);
+        delete h;
+        return GEMM_ERR_OOM;
+    }
+    *out = h;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_destroy(gemm_handle_t h) {
+    if (!h) return GEMM_OK;
+    {
+        DeviceGuard guard(h->device);
+        cudaDeviceSynchronize();
+        if (h->ws) cudaFree(h->ws);
+        if (h->d_status) cudaFree(h->d_status);
+    }
+    delete h;
+    return GEMM_OK;
+}
+
+const char* gemm_last_error(gemm_handle_t h) { return h ? h->err.c_str() : "null handle"; }
+
+int64_t gemm_launch_count(gemm_handle_t h) { return h ? h->launches : 0; }
+
+gemm_status_t gemm_get_device_status(gemm_handle_t h, void* stream) {
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    DeviceGuard guard(h->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(h, "cudaStreamSynchronize", e);
+    unsigned long long word = 0;
+    e = cudaMemcpy(&word, h->d_status, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(h, "reading the status word", e);
+    if (word == 0) return GEMM_OK;
+    e = cudaMemset(h->d_status, 0, sizeof(word));
+    if (e != cudaSuccess) return cuda_fail(h, "clearing the status word", e);
+    const unsigned code = (unsigned)(word & 0xff);
+    const unsigned role = (unsigned)((word >> 8) & 0xff);
+    const unsigned stage = (unsigned)((word >> 16) & 0xffff);
+    const unsigned tile = (unsigned)(word >> 32);
+    static const char* roles[] = {"?", "producer", "mma", "epilogue"};
+    char buf[256];
+    std::snprintf(buf, sizeof(buf), "device wait expired: code %u role %s tile %u stage %u", code,
+                  roles[role < 4 ? role : 0], tile, stage);
+    h->err = buf;
+    return GEMM_ERR_TIMEOUT;
+}
+
+gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                       int64_t ldb, void* C, int64_t ldc, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                       gemm_layout_t layoutA, gemm_layout_t layoutB, float alpha, float beta, const void* bias,
+                       void* stream) {
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    h->err.clear();
+    gemm_plan_t plan;
+    std::string err;
+    gemm_status_t st = plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, h->num_sms,
+                                 h->opt.config >= 0 ? h->max_clusters[h->opt.config] : h->max_clusters[1],
+                                 h->opt.config, &plan, &err);
+    if (st != GEMM_OK) return fail(h, st, err);
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C) return fail(h, GEMM_ERR_INVALID_ARG, "C is NULL");
+    if (K > 0 && (!A || !B)) return fail(h, GEMM_ERR_INVALID_ARG, "A or B is NULL");
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) % 16) != 0 || (reinterpret_cast<uintptr_t>(B) % 16) != 0))
+        return fail(h, GEMM_ERR_ALIGNMENT, "A and B must be 16-byte aligned");
+    DeviceGuard guard(h->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
+
+    if (K == 0) {
+        if (h->faults & FAULT_LAUNCH) return fail(h, GEMM_ERR_CUDA, "kernel launch: forced failure (GEMM_TEST_FAIL=launch)");
+        cudaError_t e = launch_scale_bias(out_kind, C, ldc, bias, beta, M, N, h->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(h, "scale/bias kernel launch", e);
+        h->launches += 1;
+    } else {
+        // Operand repack to a 16-byte pitch where TMA cannot address the caller's layout.
+        const void* a_ptr = A;
+        const void* b_ptr = B;
+        int64_t lda_eff = lda, ldb_eff = ldb;
+        if (plan.repack_a || plan.repack_b) {
+            st = ensure_workspace(h, (size_t)plan.workspace_bytes);
+            if (st != GEMM_OK) return st;
+            char* ws = static_cast<char*>(h->ws);
+            if (plan.repack_a) {
+                const int64_t rows = layoutA == GEMM_ROW ? M : K;
+                const int64_t cols = layoutA == GEMM_ROW ? K : M;
+                lda_eff = round_up(cols, 8);
+                cudaError_t e = launch_repack_u16(A, lda, ws, lda_eff, rows, cols, s);
+                if (e != cudaSuccess) return cuda_fail(h, "repack of A", e);
+                a_ptr = ws;
+                ws += round_up(rows * lda_eff * 2, 256);
+                h->launches += 1;
+            }
+            if (plan.repack_b) {
+                const int64_t rows = layoutB == GEMM_ROW ? K : N;
+                const int64_t cols = layoutB == GEMM_ROW ? N : K;
+                ldb_eff = round_up(cols, 8);
+                cudaError_t e = launch_repack_u16(B, ldb, ws, ldb_eff, rows, cols, s);
+                if (e != cudaSuccess) return cuda_fail(h, "repack of B", e);
+                b_ptr = ws;
+                h->launches += 1;
+            }
+        }
+        const ConfigDesc* d = config_desc(plan.config);
+        const CUtensorMapDataType tin =
+            dtype_in == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        const int bnc = d->block_n / d->cta_group;
+        CUtensorMap ta, tb, tc;
+        std::memset(&tc, 0, sizeof(tc));
+        if (layoutA == GEMM_ROW)  // K-major: box {64 K, 128 M}
+            st = get_tmap(h, a_ptr, tin, (uint64_t)K, (uint64_t)M, (uint64_t)lda_eff * 2, 64, 128, &ta);
+        else  // M-major: box {64 M, 64 K}
+            st = get_tmap(h, a_ptr, tin, (uint64_t)M, (uint64_t)K, (uint64_t)lda_eff * 2, 64, 64, &ta);
+        if (st != GEMM_OK) return st;
+        if (layoutB == GEMM_ROW)  // N-major: box {64 N, 64 K}
+            st = get_tmap(h, b_ptr, tin, (uint64_t)N, (uint64_t)K, (uint64_t)ldb_eff * 2, 64, 64, &tb);
+        else  // K-major: box {64 K, BN/cta_group N}
+            st = get_tmap(h, b_ptr, tin, (uint64_t)K, (uint64_t)N, (uint64_t)ldb_eff * 2, 64, (uint32_t)bnc, &tb);
+        if (st != GEMM_OK) return st;
+        const int eb = elt_bytes(dtype_out);
+        const bool c_aligned = (reinterpret_cast<uintptr_t>(C) % 16) == 0 && (ldc * eb) % 16 == 0;
+        const int use_tma_store = (plan.tma_store && c_aligned) ? 1 : 0;
+        if (use_tma_store) {
+            const CUtensorMapDataType tcd = dtype_out == GEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                            : dtype_out == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+            const uint32_t box0 = dtype_out == GEMM_F32 ? 32 : 64;   // one 128-byte line per row
+            st = get_tmap(h, C, tcd, (uint64_t)N, (uint64_t)M, (uint64_t)ldc * eb, box0, 32, &tc);
+            if (st != GEMM_OK) return st;
+        }
+        KernelParams p;
+        std::memset(&p, 0, sizeof(p));
+        p.M = (int)M;
+        p.N = (int)N;
+        p.K = (int)K;
+        p.tiles_m = plan.tiles_m;
+        p.tiles_n = plan.tiles_n;
+        p.num_tiles = plan.tiles_m * plan.tiles_n;
+        p.k_tiles = (int)((K + 63) / 64);
+        p.raster_group = h->opt.raster_group > 0 ? std::min(h->opt.raster_group, plan.tiles_m) : plan.raster_group;
+        p.a_mn = layoutA == GEMM_COL ? 1 : 0;
+        p.b_mn = layoutB == GEMM_ROW ? 1 : 0;
+        p.idesc = make_idesc(dtype_in, p.a_mn, p.b_mn, 128 * d->cta_group, d->block_n);
+        p.C = C;
+        p.ldc = ldc;
+        p.bias = bias;
+        p.alpha = alpha;
+        p.beta = beta;
+        p.use_tma_store = use_tma_store;
+        p.c_vec_ok = c_aligned ? 1 : 0;
+        p.status = h->d_status;
+        p.timeout_ns = (unsigned long long)h->opt.timeout_ms * 1000000ull;
+        p.debug_skip_stage = h->opt.debug_skip_stage;
+        int clusters = plan.clusters;
+        if (h->opt.max_clusters > 0) clusters = std::min(clusters, h->opt.max_clusters);
+        if (h->faults & FAULT_LAUNCH) return fail(h, GEMM_ERR_CUDA, "kernel launch: forced failure (GEMM_TEST_FAIL=launch)");
+        cudaError_t e = config_launch(plan.config, out_kind, clusters * d->cta_group, s, ta, tb, tc, p);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return cuda_fail(h, "GEMM kernel launch", e);
+        }
+        h->launches += 1;
+    }
+    if (h->opt.sync_check) return gemm_get_device_status(h, stream);
+    return GEMM_OK;
+}
+
+}  // extern "C"

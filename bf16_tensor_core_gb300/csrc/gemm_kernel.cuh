@@ -1,0 +1,463 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+//   C <- alpha * op(A) * op(B) + beta * C + bias,  f16/bf16 operands, f32 accumulation in TMEM.
+//
+// Design (prior art: "Optimizing GEMMs using tcgen05 - Part 2"):
+//  * TMA loads with 128-byte swizzle into a STAGES-deep shared-memory ring guarded by
+//    mbarrier expect_tx / complete_tx (section 5.1), BK = 64 so one operand row is one
+//    128-byte swizzle span (section 7.3, "BK=64");
+//  * warp specialisation: warp 0 lane 0 produces (waits "slot free", arms, issues copies),
+//    warp 1 lane 0 issues tcgen05.mma and commits each slot back (section 5.2);
+//  * BN = 256 with the accumulator in 256 TMEM columns (section 6.1); the 2-SM variant runs
+//    one tcgen05.mma.cta_group::2 with M = 256 per cluster, each CTA loading its own 128 A
+//    rows and half of B, both CTAs' copies completing on the leader's barrier (section 6.2);
+//  * unlike the page's final kernel the grid is persistent: each cluster walks output tiles
+//    in grouped raster order and owns TWO TMEM accumulators (2 x BN columns), so the
+//    epilogue of tile i overlaps the mainloop of tile i+1 (the first item of section 8);
+//    descriptors are derived per slot without rebuilding (third item of section 8);
+//  * epilogue warps 2..5 drain TMEM with tcgen05.ld.32x32b (warp w reads lanes 32*(w%4)..),
+//    apply alpha / beta / bias in f32, round to the output type, and write C either through
+//    128-byte-swizzled shared memory and TMA tensor stores (section 7.2's idea, full 128-byte
+//    lines) or, when C's layout does not allow TMA, with masked vector stores.
+//
+// Every wait is bounded (global-timer limit); on expiry the kernel records the failure in a
+// device status word, lets in-flight copies and MMAs land, frees TMEM and returns.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx_sm103.cuh"
+
+namespace gb300 {
+
+enum : int { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 2 };  // same codes as gemm_dtype_t
+enum : int { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3 };
+enum : unsigned { STATUS_TIMEOUT = 1u };
+
+struct KernelParams {
+    int M, N, K;
+    int tiles_m, tiles_n, num_tiles, k_tiles;
+    int raster_group;
+    int a_mn, b_mn;            // 0: operand K-major in memory, 1: MN-major
+    uint32_t idesc;            // tcgen05 instruction descriptor (kind::f16)
+    void* C;
+    long long ldc;             // elements
+    const void* bias;          // N elements of the output type, or nullptr
+    float alpha, beta;
+    int use_tma_store;         // write C with TMA tensor stores (requires beta == 0)
+    int c_vec_ok;              // C rows may be accessed with 16-byte vectors
+    unsigned long long* status;
+    unsigned long long timeout_ns;
+    long long debug_skip_stage;  // test only: cluster 0's producer never issues this stage
+};
+
+template <int kCtaGroup, int kBN, int kStages>
+struct TileConfig {
+    static constexpr int kBM = 128;                    // rows per CTA (TMEM lanes)
+    static constexpr int kBK = 64;                     // 64 x 2 bytes = one 128-byte swizzle span
+    static constexpr int kBNC = kBN / kCtaGroup;       // B columns each CTA loads
+    static constexpr int kABytes = kBM * kBK * 2;      // 16 KB
+    static constexpr int kBBytes = kBNC * kBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kEpiWarps = 4;
+    static constexpr int kEpiBufBytes = 32 * 128;      // 32 rows x 128 bytes
+    static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+    static constexpr int kSmemBytes = kRingBytes + kEpiBytes + 1024;  // + alignment slack
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kAccCols = kBN;               // f32 accumulator columns per buffer
+    static constexpr int kTmemCols = (2 * kBN <= 32) ? 32 : (2 * kBN <= 64) ? 64 : (2 * kBN <= 128) ? 128
+                                     : (2 * kBN <= 256) ? 256 : 512;
+    static_assert(kBN % 64 == 0 && kBN <= 256, "BN must be a multiple of 64, at most 256");
+    static_assert(kBNC % 64 == 0, "each CTA loads whole 64-column B slabs");
+    static_assert(kSmemBytes <= 232448 - 512, "shared memory budget");
+};
+
+__device__ __forceinline__ void tile_coords(const KernelParams& p, int t, int& mb, int& nb) {
+    const int per_group = p.raster_group * p.tiles_n;
+    const int g = t / per_group;
+    const int first = g * p.raster_group;
+    const int gm = min(p.tiles_m - first, p.raster_group);
+    const int local = t - g * per_group;
+    mb = first + local % gm;
+    nb = local / gm;
+}
+
+template <int kCtaGroup>
+__device__ __forceinline__ void report_error(const KernelParams& p, int role, int tile, int stage,
+                                             volatile int* abort_flag) {
+    *abort_flag = 1;
+    if constexpr (kCtaGroup == 2) {
+        const uint32_t peer = cluster_ctarank() ^ 1u;
+        st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), peer), 1u);
+    }
+    const unsigned long long code = static_cast<unsigned long long>(STATUS_TIMEOUT) |
+                                    (static_cast<unsigned long long>(role & 0xff) << 8) |
+                                    (static_cast<unsigned long long>(stage & 0xffff) << 16) |
+                                    (static_cast<unsigned long long>(static_cast<uint32_t>(tile)) << 32);
+    atomicCAS(p.status, 0ull, code);
+}
+
+// ---------------------------------------------------------------- epilogue helpers
+template <int kOut>
+__device__ __forceinline__ float load_out(const void* base, long long idx) {
+    if constexpr (kOut == OUT_F32) return static_cast<const float*>(base)[idx];
+    else if constexpr (kOut == OUT_F16) return __half2float(static_cast<const __half*>(base)[idx]);
+    else return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[idx]);
+}
+
+template <int kOut>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    if constexpr (kOut == OUT_F16) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+// v[0..31] = alpha * acc + beta * C_in + bias for columns col0 .. col0+31 of `row`.
+template <int kOut>
+__device__ __forceinline__ void epilogue_math(const KernelParams& p, const uint32_t (&acc)[32], float (&v)[32],
+                                              int row, int col0) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
+    if (p.alpha != 1.0f) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= p.alpha;
+    }
+    if (p.beta != 0.0f && row < p.M) {
+        const long long base = static_cast<long long>(row) * p.ldc + col0;
+        if (p.c_vec_ok && col0 + 32 <= p.N) {
+            if constexpr (kOut == OUT_F32) {
+                const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.C) + base);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 c = src[j];
+                    v[4 * j + 0] = fmaf(p.beta, c.x, v[4 * j + 0]);
+                    v[4 * j + 1] = fmaf(p.beta, c.y, v[4 * j + 1]);
+                    v[4 * j + 2] = fmaf(p.beta, c.z, v[4 * j + 2]);
+                    v[4 * j + 3] = fmaf(p.beta, c.w, v[4 * j + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = fmaf(p.beta, load_out<kOut>(p.C, base + i), v[i]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (col0 + i < p.N) v[i] = fmaf(p.beta, load_out<kOut>(p.C, base + i), v[i]);
+        }
+    }
+    if (p.bias != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (col0 + i < p.N) v[i] += load_out<kOut>(p.bias, col0 + i);
+    }
+}
+
+// Masked direct stores of 32 values of one row.
+template <int kOut>
+__device__ __forceinline__ void store_row_direct(const KernelParams& p, const float (&v)[32], int row, int col0) {
+    if (row >= p.M) return;
+    const long long base = static_cast<long long>(row) * p.ldc + col0;
+    if (p.c_vec_ok && col0 + 32 <= p.N) {
+        if constexpr (kOut == OUT_F32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.C) + base);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.C) + base);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                dst[j] = make_uint4(pack2<kOut>(v[8 * j + 0], v[8 * j + 1]), pack2<kOut>(v[8 * j + 2], v[8 * j + 3]),
+                                    pack2<kOut>(v[8 * j + 4], v[8 * j + 5]), pack2<kOut>(v[8 * j + 6], v[8 * j + 7]));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if (col0 + i < p.N) {
+                if constexpr (kOut == OUT_F32) static_cast<float*>(p.C)[base + i] = v[i];
+                else if constexpr (kOut == OUT_F16) static_cast<__half*>(p.C)[base + i] = __float2half_rn(v[i]);
+                else static_cast<__nv_bfloat16*>(p.C)[base + i] = __float2bfloat16_rn(v[i]);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// One warp drains its 32 TMEM lanes (32 rows) x BN columns of one accumulator buffer.
+template <int kOut, int kBN>
+__device__ __forceinline__ void epilogue_tile(const KernelParams& p, const CUtensorMap* tmC, uint32_t tbase,
+                                              int row0, int col_base, int lane, uint32_t stage_buf0,
+                                              uint32_t& chunk_ctr) {
+    const int row = row0 + lane;
+    if (p.use_tma_store) {
+        // A chunk is one 128-byte line per row: 64 columns of a 16-bit type, 32 of f32.
+        constexpr int kChunk = (kOut == OUT_F32) ? 32 : 64;
+        const bool warp_rows_in = row0 < p.M;
+#pragma unroll 1
+        for (int c = 0; c < kBN / kChunk; ++c) {
+            const int col0 = col_base + c * kChunk;
+            uint32_t words[32];
+            if constexpr (kOut == OUT_F32) {
+                uint32_t acc[32];
+                tmem_ld_32x32b_x32(tbase + c * 32, acc);
+                tmem_wait_ld();
+                float v[32];
+                epilogue_math<kOut>(p, acc, v, row, col0);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) words[i] = __float_as_uint(v[i]);
+            } else {
+                uint32_t acc0[32], acc1[32];
+                tmem_ld_32x32b_x32(tbase + c * 64, acc0);
+                tmem_ld_32x32b_x32(tbase + c * 64 + 32, acc1);
+                tmem_wait_ld();
+                float v[32];
+                epilogue_math<kOut>(p, acc0, v, row, col0);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) words[i] = pack2<kOut>(v[2 * i], v[2 * i + 1]);
+                epilogue_math<kOut>(p, acc1, v, row, col0 + 32);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) words[16 + i] = pack2<kOut>(v[2 * i], v[2 * i + 1]);
+            }
+            if (!warp_rows_in || col0 >= p.N) continue;   // whole box outside C (warp-uniform)
+            const uint32_t buf = stage_buf0 + (chunk_ctr & 1u) * 4096u;
+            if (lane == 0) bulk_wait_group_read<1>();     // the store that last used `buf` has read it
+            __syncwarp();
+            const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t piece = static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u);  // 128B swizzle
+                st_shared_v4(row_addr + piece * 16u, words[4 * j], words[4 * j + 1], words[4 * j + 2], words[4 * j + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(tmC, col0, row0, buf);
+                bulk_commit_group();
+            }
+            ++chunk_ctr;
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            const int col0 = col_base + c * 32;
+            uint32_t acc[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, acc);
+            tmem_wait_ld();
+            if (col0 >= p.N) continue;
+            float v[32];
+            epilogue_math<kOut>(p, acc, v, row, col0);
+            store_row_direct<kOut>(p, v, row, col0);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+template <int kCtaGroup, int kBN, int kStages, int kOut>
+__global__ void __launch_bounds__(TileConfig<kCtaGroup, kBN, kStages>::kThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
+    using Cfg = TileConfig<kCtaGroup, kBN, kStages>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_full[kStages];
+    __shared__ __align__(8) uint64_t bar_empty[kStages];
+    __shared__ __align__(8) uint64_t bar_tfull[2];
+    __shared__ __align__(8) uint64_t bar_tempty[2];
+    __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ uint32_t s_tmem_base;
+    __shared__ int s_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = (kCtaGroup == 2) ? cluster_ctarank() : 0u;
+    const int cluster_id = blockIdx.x / kCtaGroup;
+    const int num_clusters = gridDim.x / kCtaGroup;
+    const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t epi_smem = ring + Cfg::kRingBytes;
+    volatile int* abort_flag = &s_abort;
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&bar_full[s]), 1);
+            mbar_init(smem_u32(&bar_empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bar_tfull[b]), 1);
+            mbar_init(smem_u32(&bar_tempty[b]), Cfg::kEpiWarps * kCtaGroup);
+        }
+        mbar_init(smem_u32(&bar_drain), 1);
+        fence_barrier_init();
+    }
+    if (threadIdx.x == 32) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        if (p.use_tma_store) prefetch_tensormap(&tmC);
+    }
+    if (warp == 1) tmem_alloc<kCtaGroup>(smem_u32(&s_tmem_base), Cfg::kTmemCols);
+    tc_fence_before_sync();
+    __syncthreads();
+    if constexpr (kCtaGroup == 2) cluster_sync();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = s_tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            long long gstage = 0;
+            const uint32_t tx_bytes = static_cast<uint32_t>(Cfg::kStageBytes * kCtaGroup);
+            bool ok = true;
+            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+                int mb, nb;
+                tile_coords(p, t, mb, nb);
+                const int m0 = mb * (Cfg::kBM * kCtaGroup) + static_cast<int>(rank) * Cfg::kBM;
+                const int n0 = nb * kBN + static_cast<int>(rank) * Cfg::kBNC;
+                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                    if (!mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, p.timeout_ns, abort_flag)) {
+                        if (!*abort_flag) report_error<kCtaGroup>(p, ROLE_PRODUCER, t, static_cast<int>(stage), abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    const bool skip = (gstage == p.debug_skip_stage) && cluster_id == 0;
+                    if (!skip) {
+                        const uint32_t full_local = smem_u32(&bar_full[stage]);
+                        const uint32_t full_bar = (kCtaGroup == 2) ? mapa_shared(full_local, 0) : full_local;
+                        if (rank == 0) mbar_arrive_expect_tx(full_local, tx_bytes);
+                        const uint32_t sa = ring + stage * Cfg::kStageBytes;
+                        const uint32_t sb = sa + Cfg::kABytes;
+                        const int k0 = kt * Cfg::kBK;
+                        auto load = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1) {
+                            if constexpr (kCtaGroup == 2) tma_load_2d_pair(dst, map, c0, c1, full_bar);
+                            else tma_load_2d(dst, map, c0, c1, full_bar);
+                        };
+                        if (!p.a_mn) {
+                            load(sa, &tmA, k0, m0);                       // box {64 K, 128 M}
+                        } else {
+                            load(sa, &tmA, m0, k0);                       // box {64 M, 64 K} slabs
+                            load(sa + 8192u, &tmA, m0 + 64, k0);
+                        }
+                        if (!p.b_mn) {
+                            load(sb, &tmB, k0, n0);                       // box {64 K, BNC N}
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < Cfg::kBNC / 64; ++j)     // box {64 N, 64 K} slabs
+                                load(sb + static_cast<uint32_t>(j) * 8192u, &tmB, n0 + 64 * j, k0);
+                        }
+                    }
+                    ++gstage;
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (leader CTA)
+        if (lane == 0 && rank == 0) {
+            // K-major operand: 8-row groups 1024 bytes apart (SBO); a K=16 step is +32 bytes.
+            // MN-major operand: 64-element slabs 8192 bytes apart (LBO), 8-row K groups 1024
+            // bytes apart (SBO); a K=16 step is +2048 bytes.
+            const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
+            const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
+            const uint64_t a_kstep = p.a_mn ? (2048u >> 4) : (32u >> 4);
+            const uint64_t b_kstep = p.b_mn ? (2048u >> 4) : (32u >> 4);
+            const uint64_t a_desc0 = smem_desc_sw128(ring, a_lbo, 1024u);
+            const uint64_t b_desc0 = smem_desc_sw128(ring + Cfg::kABytes, b_lbo, 1024u);
+            const uint64_t stage_step = static_cast<uint64_t>(Cfg::kStageBytes >> 4);
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+                if (!mbar_wait_bounded<kCtaGroup == 2>(smem_u32(&bar_tempty[acc]), acc_phase ^ 1u, p.timeout_ns,
+                                                       abort_flag)) {
+                    if (!*abort_flag) report_error<kCtaGroup>(p, ROLE_MMA, t, 100 + static_cast<int>(acc), abort_flag);
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + acc * static_cast<uint32_t>(Cfg::kAccCols);
+                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                    if (!mbar_wait_bounded(smem_u32(&bar_full[stage]), phase, p.timeout_ns, abort_flag)) {
+                        if (!*abort_flag) report_error<kCtaGroup>(p, ROLE_MMA, t, static_cast<int>(stage), abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t ad = a_desc0 + stage * stage_step;
+                    const uint64_t bd = b_desc0 + stage * stage_step;
+#pragma unroll
+                    for (int k = 0; k < Cfg::kBK / 16; ++k)
+                        mma_f16<kCtaGroup>(d_tmem, ad + k * a_kstep, bd + k * b_kstep, p.idesc,
+                                           (kt > 0 || k > 0) ? 1u : 0u);
+                    mma_commit<kCtaGroup>(smem_u32(&bar_empty[stage]));   // slot free once these MMAs finish
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit<kCtaGroup>(smem_u32(&bar_tfull[acc]));         // accumulator ready
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            // Drain: every MMA this thread issued has completed once bar_drain flips.  This wait
+            // ignores the abort flag (only the time limit ends it): TMEM is freed after it.
+            mma_commit<kCtaGroup>(smem_u32(&bar_drain));
+            volatile int never = 0;
+            mbar_wait_bounded(smem_u32(&bar_drain), 0u, p.timeout_ns, &never);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue warps 2..5
+        const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
+        const int ew = warp - 2;
+        const uint32_t stage_buf0 = epi_smem + static_cast<uint32_t>(ew) * 2u * Cfg::kEpiBufBytes;
+        uint32_t acc = 0, acc_phase = 0, chunk_ctr = 0;
+        for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+            int mb, nb;
+            tile_coords(p, t, mb, nb);
+            bool ok = mbar_wait_bounded(smem_u32(&bar_tfull[acc]), acc_phase, p.timeout_ns, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0 && !*abort_flag)
+                    report_error<kCtaGroup>(p, ROLE_EPILOGUE, t, 200 + static_cast<int>(acc), abort_flag);
+                break;
+            }
+            tc_fence_after_sync();
+            const int row0 = mb * (Cfg::kBM * kCtaGroup) + static_cast<int>(rank) * Cfg::kBM + quarter * 32;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   acc * static_cast<uint32_t>(Cfg::kAccCols);
+            epilogue_tile<kOut, kBN>(p, &tmC, tbase, row0, nb * kBN, lane, stage_buf0, chunk_ctr);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t te = smem_u32(&bar_tempty[acc]);
+                if constexpr (kCtaGroup == 2) mbar_arrive_cluster(mapa_shared(te, 0));
+                else mbar_arrive_local(te);
+            }
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // ---------------------------------------------------------------- teardown
+    if (threadIdx.x == 0 && *abort_flag) {
+        // A bounded settle so copies issued before the abort land before shared memory goes away.
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 200000ull) { }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if constexpr (kCtaGroup == 2) cluster_sync();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc<kCtaGroup>(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+}  // namespace gb300

@@ -1,0 +1,52 @@
+// Host-side view of the kernel configurations (no device code).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gb300 {
+
+struct KernelParams;
+
+struct ConfigDesc {
+    int id;
+    int cta_group;
+    int block_n;
+    int stages;
+    int smem_bytes;
+    int threads;
+};
+
+constexpr int kNumConfigs = 4;
+constexpr int kNumOut = 3;  // OUT_F16, OUT_BF16, OUT_F32
+
+// Static description of config `id` (nullptr if out of range).
+const ConfigDesc* config_desc(int id);
+
+// Kernel entry for config `id` and output type `out` (for attributes and occupancy queries).
+const void* config_kernel(int id, int out);
+
+// Launch config `id` on `grid_ctas` CTAs (clusters of cta_group) on `stream`.
+cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, const CUtensorMap& a,
+                          const CUtensorMap& b, const CUtensorMap& c, const KernelParams& p);
+
+// Per-config translation units.
+const void* cfg0_kernel(int out);
+cudaError_t cfg0_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const KernelParams& p);
+const void* cfg1_kernel(int out);
+cudaError_t cfg1_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const KernelParams& p);
+const void* cfg2_kernel(int out);
+cudaError_t cfg2_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const KernelParams& p);
+const void* cfg3_kernel(int out);
+cudaError_t cfg3_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const KernelParams& p);
+
+// Auxiliary kernels (gemm_aux.cu).
+cudaError_t launch_repack_u16(const void* src, long long lds, void* dst, long long ldd, long long rows,
+                              long long cols, cudaStream_t stream);
+cudaError_t launch_scale_bias(int out, void* C, long long ldc, const void* bias, float beta, long long M,
+                              long long N, int num_sms, cudaStream_t stream);
+
+}  // namespace gb300

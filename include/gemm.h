@@ -1,0 +1,167 @@
+/*
+ * gemm.h - C ABI of the GB300 (sm_103a) dense GEMM library  libgemm_gb300.so
+ *
+ *   C <- alpha * op(A) * op(B) + beta * C + bias
+ *
+ * The operation is the dense matrix product C_ij = sum_k A_ik * B_kj
+ * (2*M*N*K flops) defined in "Matrix Multiplication: The Operation Behind
+ * Modern AI" (opening definition; section "One formula for every matmul"),
+ * with f16/bf16 operands and f32 accumulation as in "Optimizing GEMMs using
+ * tcgen05 - Part 2" (fp16 in, fp32 accumulate, section 5 onward) and the NT
+ * prefill GEMM of "02 - Tiled wmma f16 prefill GEMM" (section 3.2, B stored
+ * as od x id, i.e. N x K).  alpha, beta and the per-column bias form the
+ * fused epilogue (tcgen05 worklog, section 7: epilogue after the TMEM drain).
+ *
+ * Conventions
+ *   A is M x K, B is K x N, C is M x N; all matrices are dense, element
+ *   strides 1, leading dimensions in ELEMENTS.
+ *   layoutA  GEMM_ROW: A stored M x K row-major (K contiguous, lda >= K)
+ *            GEMM_COL: A stored K x M row-major (M contiguous, lda >= M)
+ *   layoutB  GEMM_ROW: B stored K x N row-major (N contiguous, ldb >= N)
+ *            GEMM_COL: B stored N x K row-major (K contiguous, ldb >= K)
+ *   C        always row-major M x N (ldc >= N), dtype_out.
+ *   bias     NULL or N elements of dtype_out, added to every row, NOT scaled
+ *            by alpha:  C_ij = alpha * S_ij + beta * C_ij + bias_j.
+ *   beta == 0: C is not read (NaN in C does not propagate).
+ *   K == 0:   C = beta * C + bias.   M == 0 or N == 0: no-op.
+ *   dtype_in in {GEMM_F16, GEMM_BF16} (A and B share it);
+ *   dtype_out in {GEMM_F32, GEMM_F16, GEMM_BF16}; the output is rounded to
+ *   nearest-even from the f32 epilogue value.
+ *
+ * Memory and ownership
+ *   A, B, C and bias are caller-owned DEVICE pointers on the handle's device;
+ *   the library never frees them.  A and B must be 16-byte aligned.  A leading
+ *   dimension whose byte pitch is not a multiple of 16 (e.g. lda = 2050 f16) is
+ *   legal: the operand is repacked into a handle-owned workspace with a 16-byte
+ *   pitch before the product (counted in the call's time).  The handle owns
+ *   that workspace (grown on demand, reused), the tensor-map cache and a
+ *   device status word.
+ *
+ * Asynchrony and streams
+ *   gemm_run only enqueues work on `stream` (a cudaStream_t passed as void*;
+ *   NULL = the legacy default stream) and returns.  Shared-memory opt-in for
+ *   every kernel instantiation happens in gemm_create, never inside a call
+ *   (cf. the prefill GEMM page, section 3.3: setting the attribute inside a
+ *   graph-capture window fails silently).  A call that grows the workspace
+ *   allocates device memory, so warm such shapes up before capturing a graph.
+ *   A handle must not be used by two host threads at once.
+ *
+ * Errors
+ *   Every entry point returns a gemm_status_t; nothing calls exit or abort.
+ *   Detail of the last failure is kept per handle (gemm_last_error).  Device
+ *   waits inside the kernels are bounded: on expiry a kernel records
+ *   {code, role, tile, stage} in the status word and returns cleanly;
+ *   gemm_get_device_status reports it as GEMM_ERR_TIMEOUT.
+ */
+#ifndef GB300_GEMM_H
+#define GB300_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gemm_ctx* gemm_handle_t; /* opaque, owned by the library */
+
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_F32 = 2 } gemm_dtype_t;
+typedef enum { GEMM_ROW = 0, GEMM_COL = 1 } gemm_layout_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,  /* negative size, ld too small, NULL with nonzero size, bad dtype/layout */
+    GEMM_ERR_UNSUPPORTED = 2,  /* device is not sm_103 (compute capability 10.3), or no such config   */
+    GEMM_ERR_ALIGNMENT = 3,    /* A or B base pointer not 16-byte aligned                              */
+    GEMM_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed; see gemm_last_error              */
+    GEMM_ERR_TIMEOUT = 5,      /* a bounded device wait expired (read by gemm_get_device_status)        */
+    GEMM_ERR_OOM = 6           /* workspace or handle allocation failed                                 */
+} gemm_status_t;
+
+/* Options for gemm_create.  Fill with gemm_options_default, then change fields. */
+typedef struct {
+    int struct_size;      /* sizeof(gemm_options_t), set by gemm_options_default              */
+    int config;           /* -1: choose per call; else a kernel config id (gemm_config_info)  */
+    int timeout_ms;       /* limit of every bounded device wait (default 2000)                */
+    int sync_check;       /* 1: gemm_run synchronises the stream and reads the status word    */
+    int raster_group;     /* output-tile rows per raster group; 0 = automatic                 */
+    int max_clusters;     /* cap on persistent clusters (0 = as many as fit on the device)    */
+    int debug_skip_stage; /* TEST ONLY: the producer of cluster 0 never issues this k-stage,
+                             so the MMA issuer's bounded wait expires (-1 = off)              */
+} gemm_options_t;
+
+/* Description of a kernel configuration. */
+typedef struct {
+    int id;
+    int cta_group;     /* 1: one CTA per output tile; 2: a 2-SM cluster issues cta_group::2 MMAs */
+    int block_m;       /* output-tile rows (128 * cta_group)                                      */
+    int block_n;       /* output-tile columns (= MMA N)                                           */
+    int block_k;       /* K elements per pipeline stage (64 = one 128-byte swizzle span)          */
+    int stages;        /* depth of the shared-memory ring                                         */
+    int smem_bytes;    /* dynamic shared memory per CTA                                           */
+    int threads;       /* threads per CTA                                                         */
+} gemm_config_info_t;
+
+/* What gemm_run would do for a problem (pure host computation, no device needed). */
+typedef struct {
+    int config;            /* chosen config id                                              */
+    int cta_group, block_m, block_n, block_k, stages;
+    int tiles_m, tiles_n;  /* output tiles                                                  */
+    int clusters;          /* persistent clusters launched (grid = clusters * cta_group)    */
+    int raster_group;      /* tile rows per raster group                                    */
+    int tma_store;         /* 1: epilogue writes C with TMA tensor stores; 0: st.global     */
+    int repack_a, repack_b;/* 1: operand copied to a 16-byte pitch workspace first          */
+    int64_t workspace_bytes;
+    int kernels;           /* kernel launches the call makes                                */
+} gemm_plan_t;
+
+/* Fill *opt with defaults (config -1, timeout 2000 ms, no sync check, automatic raster). */
+void gemm_options_default(gemm_options_t* opt);
+
+/* Create a handle on CUDA device `device` (opt NULL = defaults).  Checks that the device is
+ * sm_103, opts every kernel into its dynamic shared memory, resolves cuTensorMapEncodeTiled and
+ * allocates the device status word.  *out is NULL on failure. */
+gemm_status_t gemm_create(gemm_handle_t* out, int device, const gemm_options_t* opt);
+
+/* Enqueue C <- alpha*op(A)*op(B) + beta*C + bias on `stream`.  See the conventions above. */
+gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                       const void* A, int64_t lda, const void* B, int64_t ldb,
+                       void* C, int64_t ldc,
+                       gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                       gemm_layout_t layoutA, gemm_layout_t layoutB,
+                       float alpha, float beta, const void* bias, void* stream);
+
+/* Free the handle and everything it owns (waits for its device work first).  NULL is a no-op. */
+gemm_status_t gemm_destroy(gemm_handle_t h);
+
+/* Static, human-readable name of a status code. */
+const char* gemm_status_string(gemm_status_t s);
+
+/* Detail of the handle's last failure ("" if none).  Valid until the next call on h. */
+const char* gemm_last_error(gemm_handle_t h);
+
+/* Synchronise `stream`, read and clear the device status word.  Returns GEMM_ERR_TIMEOUT (with
+ * role, tile and stage in gemm_last_error) if a bounded wait expired since the last read. */
+gemm_status_t gemm_get_device_status(gemm_handle_t h, void* stream);
+
+/* Plan a call without running it: validation, config choice, grid, repack and workspace.
+ * beta: as for gemm_run (beta != 0 rules out the TMA-store epilogue, which never reads C);
+ * the plan assumes C is 16-byte aligned.  num_sms: the device's SM count (e.g. 152);
+ * max_clusters: co-resident 2-SM clusters (0 = num_sms / 2).  config: -1 automatic, else a
+ * config id.  Uses no device. */
+gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                        gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                        gemm_layout_t layoutA, gemm_layout_t layoutB, float beta,
+                        int num_sms, int max_clusters, int config, gemm_plan_t* out);
+
+/* Number of kernel configurations and their descriptions (ids 0 .. gemm_num_configs()-1). */
+int gemm_num_configs(void);
+gemm_status_t gemm_config_info(int id, gemm_config_info_t* out);
+
+/* Kernels launched through this handle since it was created. */
+int64_t gemm_launch_count(gemm_handle_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_GEMM_H */

@@ -1,0 +1,154 @@
+"""C-ABI boundary checks that need no GPU: the library loads, exports every declared symbol,
+validates arguments and plans calls (config choice, grid, repack, workspace) on the host."""
+import ctypes
+import os
+import subprocess
+import sys
+
+import pytest
+
+from bf16_tensor_core_gb300 import gemm as G
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    from bf16_tensor_core_gb300 import build
+    build.build()
+    return G.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = G.header_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/gemm.h but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", str(G.LIB_PATH)], capture_output=True, text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+    assert set(names) <= exported
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "GEMM_OK"), (1, "GEMM_ERR_INVALID_ARG"), (2, "GEMM_ERR_UNSUPPORTED"),
+                       (3, "GEMM_ERR_ALIGNMENT"), (4, "GEMM_ERR_CUDA"), (5, "GEMM_ERR_TIMEOUT"),
+                       (6, "GEMM_ERR_OOM")]:
+        assert G.gemm_status_string(code) == name
+    assert G.gemm_status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+def test_options_default(lib):
+    o = G.gemm_options_default()
+    assert o.struct_size == ctypes.sizeof(G.gemm_options_t)
+    assert o.config == -1 and o.timeout_ms == 2000 and o.debug_skip_stage == -1
+
+
+def test_config_table(lib):
+    n = G.gemm_num_configs()
+    assert n == 4
+    seen = set()
+    for i in range(n):
+        st, c = G.gemm_config_info(i)
+        assert st == G.GEMM_OK and c.id == i
+        assert c.block_m == 128 * c.cta_group and c.block_k == 64
+        assert c.block_n in (128, 256) and c.smem_bytes <= 232448 and c.threads == 192
+        seen.add((c.cta_group, c.block_n))
+    assert seen == {(1, 128), (1, 256), (2, 128), (2, 256)}
+    assert G.gemm_config_info(n)[0] == G.GEMM_ERR_UNSUPPORTED
+
+
+def test_null_handle_and_create_without_gpu(lib):
+    assert G.gemm_destroy(None) == G.GEMM_OK
+    assert lib.gemm_run(None, 1, 1, 1, None, 1, None, 1, None, 1, 0, 0, 0, 0, 1.0, 0.0, None, None) == \
+        G.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_create(None, 0, None) == G.GEMM_ERR_INVALID_ARG
+    import torch
+    if not torch.cuda.is_available():
+        st, h = G.gemm_create(0)
+        assert st in (G.GEMM_ERR_CUDA, G.GEMM_ERR_INVALID_ARG) and not h.value
+
+
+def plan(M, N, K, lda=None, ldb=None, ldc=None, din=0, dout=2, la=0, lb=0, beta=0.0, config=-1, sms=152):
+    lda = lda if lda is not None else (K if la == 0 else M)
+    ldb = ldb if ldb is not None else (N if lb == 0 else K)
+    ldc = ldc if ldc is not None else N
+    return G.gemm_plan(M, N, K, max(lda, 1), max(ldb, 1), max(ldc, 1), din, dout, la, lb, beta, sms, 0, config)
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(M=-1, N=4, K=4), G.GEMM_ERR_INVALID_ARG),
+    (dict(M=4, N=-1, K=4), G.GEMM_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=-1), G.GEMM_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=4, din=2), G.GEMM_ERR_INVALID_ARG),      # f32 operands are not a kind::f16 input
+    (dict(M=4, N=4, K=4, dout=7), G.GEMM_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=4, la=2), G.GEMM_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=8, lda=7), G.GEMM_ERR_INVALID_ARG),      # lda < K for row-major A
+    (dict(M=9, N=4, K=8, la=1, lda=8), G.GEMM_ERR_INVALID_ARG),  # lda < M for column-major A
+    (dict(M=4, N=9, K=8, ldb=8), G.GEMM_ERR_INVALID_ARG),      # ldb < N for row-major B
+    (dict(M=4, N=9, K=8, lb=1, ldb=7), G.GEMM_ERR_INVALID_ARG),  # ldb < K for B stored N x K
+    (dict(M=4, N=9, K=8, ldc=8), G.GEMM_ERR_INVALID_ARG),
+    (dict(M=2 ** 31, N=4, K=4), G.GEMM_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=4, config=9), G.GEMM_ERR_UNSUPPORTED),
+    (dict(M=4, N=4, K=4, sms=0), G.GEMM_ERR_INVALID_ARG),
+    (dict(M=4, N=4, K=4), G.GEMM_OK),
+])
+def test_plan_validation(lib, args, status):
+    st, _ = plan(**args)
+    assert st == status
+
+
+def test_plan_degenerate(lib):
+    st, p = plan(0, 100, 100)
+    assert st == G.GEMM_OK and p.kernels == 0
+    st, p = plan(100, 0, 100)
+    assert st == G.GEMM_OK and p.kernels == 0
+    st, p = plan(100, 100, 0)
+    assert st == G.GEMM_OK and p.kernels == 1
+
+
+def test_plan_tiles_and_grid(lib):
+    for cfg in range(4):
+        st, c = G.gemm_config_info(cfg)
+        st, p = plan(4096, 4096, 4096, dout=0, config=cfg)
+        assert st == G.GEMM_OK and p.config == cfg
+        assert p.tiles_m == 4096 // c.block_m and p.tiles_n == 4096 // c.block_n
+        slots = 152 // c.cta_group
+        assert p.clusters == min(p.tiles_m * p.tiles_n, slots)
+        assert p.tma_store == 1 and p.kernels == 1 and p.workspace_bytes == 0
+    st, p = plan(1000, 3000, 2050, config=1)
+    assert (p.tiles_m, p.tiles_n) == (4, 12)           # partial last tiles: 1000 = 3*256 + 232, 3000 = 11*256 + 184
+    st, p = plan(1, 1, 1, config=0)
+    assert (p.tiles_m, p.tiles_n, p.clusters) == (1, 1, 1)
+
+
+def test_plan_repack_and_workspace(lib):
+    # 2050 halves = 4100 bytes is not a multiple of 16: both operands go through the workspace
+    st, p = plan(1000, 3000, 2050, lda=2050, ldb=2050, la=0, lb=1, beta=1.0)
+    assert st == G.GEMM_OK
+    assert p.repack_a == 1 and p.repack_b == 1 and p.kernels == 3
+    a_bytes = -(-1000 * 2056 * 2 // 256) * 256
+    b_bytes = -(-3000 * 2056 * 2 // 256) * 256
+    assert p.workspace_bytes == a_bytes + b_bytes
+    assert p.tma_store == 0                             # beta != 0 reads C: direct-store epilogue
+    st, p = plan(64, 64, 64, lda=72, ldb=64)
+    assert p.repack_a == 0 and p.repack_b == 0 and p.workspace_bytes == 0
+    st, p = plan(64, 63, 64, ldc=63, dout=0)            # 126-byte rows: TMA cannot store C
+    assert p.tma_store == 0
+    st, p = plan(64, 60, 64, ldc=60, dout=2)            # 240-byte rows: TMA store is fine
+    assert p.tma_store == 1
+
+
+def test_plan_auto_choice_is_a_valid_config(lib):
+    for (M, N, K) in [(512, 512, 512), (4096, 4096, 4096), (2048, 11008, 4096), (1000, 3000, 2050),
+                      (8192, 8192, 8192), (1, 4096, 4096), (128, 128, 64)]:
+        st, p = plan(M, N, K, dout=0)
+        assert st == G.GEMM_OK and 0 <= p.config < 4
+        assert p.clusters >= 1 and p.raster_group >= 1 and p.raster_group <= p.tiles_m
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path):
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "from bf16_tensor_core_gb300 import gemm\n"
+            "try:\n    gemm.load_library(%r)\nexcept OSError as e:\n    print('LOUD', e)\n") % (
+        os.path.dirname(os.path.dirname(os.path.abspath(__file__))), str(tmp_path / "missing.so"))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
+    assert "LOUD" in r.stdout

@@ -1,0 +1,287 @@
+"""GPU parity tests: the CUDA path (through the C ABI) against the CPU oracle, element by element.
+
+Tolerance (per element): 1e-4 * K * max|A| * max|B| for f32 output, plus one output ulp of
+|C_ref| for f16/bf16 output, plus 4 f32 ulps of the epilogue operands (see oracle.check).
+Integer-valued inputs whose partial sums stay below 2^24 must match bit for bit.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bf16_tensor_core_gb300 import gemm as G
+from bf16_tensor_core_gb300 import workloads as W
+from gpu_cases import alloc_c, compare, device_inputs, run_gpu, sample_indices
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = [0, 1, 2, 3]
+
+
+@pytest.fixture(scope="module")
+def handles():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    hs = {c: G.Gemm(0, config=c, sync_check=1) for c in CONFIGS}
+    hs["auto"] = G.Gemm(0, sync_check=1)
+    yield hs
+    for h in hs.values():
+        h.close()
+
+
+def _run_check(h, w, *, ldc=None, rows=None, cols=None):
+    d = W.generate(w)
+    dd = device_inputs(d)
+    C = alloc_c(w, d, ldc)
+    run_gpu(h, w, dd, C)
+    torch.cuda.synchronize()
+    rep = compare(w, d, C, rows, cols)
+    assert rep["passed"], rep
+    return rep, C, d
+
+
+# ------------------------------------------------------------------------------ the five workloads
+@pytest.mark.parametrize("cfg", CONFIGS)
+@pytest.mark.parametrize("wid", [1, 4])
+def test_small_workloads_full_check(handles, cfg, wid):
+    """512^3 and the ragged 1000x3000x2050 case checked on every element, on every config."""
+    _run_check(handles[cfg], W.WORKLOADS[wid])
+
+
+@pytest.mark.parametrize("wid", [2, 3, 5])
+def test_large_workloads_sampled(handles, wid):
+    """Full-size 4096^3, the 2048x11008x4096 prefill projection and 8192^3 with the automatic
+    config (the one the benchmark times): sampled rows x all columns and all rows x sampled columns,
+    including every tile boundary."""
+    w = W.WORKLOADS[wid]
+    d = W.generate(w)
+    dd = device_inputs(d)
+    C = alloc_c(w, d)
+    run_gpu(handles["auto"], w, dd, C)
+    torch.cuda.synchronize()
+    rows = sample_indices(w.M, 48, seed=wid, tile=128)
+    cols = sample_indices(w.N, 48, seed=wid + 100, tile=64)
+    rep_r = compare(w, d, C, rows=rows)
+    assert rep_r["passed"], rep_r
+    rep_c = compare(w, d, C, cols=cols)
+    assert rep_c["passed"], rep_c
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+def test_prefill_shape_reduced_on_every_config(handles, cfg):
+    w = W.with_changes(W.WORKLOADS[3], M=384, N=1000, K=640, name="prefill_reduced")
+    _run_check(handles[cfg], w)
+
+
+# ------------------------------------------------------------------------------ tails and layouts
+TAIL_SHAPES = [(1, 1, 1), (1, 300, 70), (17, 33, 16), (127, 129, 64), (128, 128, 128), (129, 255, 65),
+               (255, 257, 129), (257, 127, 200), (300, 520, 1), (33, 600, 333), (640, 64, 8)]
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+@pytest.mark.parametrize("shape", TAIL_SHAPES)
+def test_tail_shapes(handles, cfg, shape):
+    M, N, K = shape
+    w = W.problem(M, N, K, dtype_in="f16", dtype_out="f32", seed=M * 7 + N * 3 + K)
+    _run_check(handles[cfg], w)
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+@pytest.mark.parametrize("la,lb", [("row", "row"), ("row", "col"), ("col", "row"), ("col", "col")])
+@pytest.mark.parametrize("din,dout", [("f16", "f32"), ("bf16", "bf16"), ("f16", "f16"), ("bf16", "f32")])
+def test_layouts_and_dtypes(handles, cfg, la, lb, din, dout):
+    w = W.problem(300, 392, 200, dtype_in=din, dtype_out=dout, layoutA=la, layoutB=lb, bias=True,
+                  seed=len(la) * 97 + len(lb) * 31 + len(din) * 7 + len(dout))
+    _run_check(handles[cfg], w)
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+def test_alpha_beta_bias(handles, cfg):
+    for (alpha, beta, dout) in [(0.5, 1.0, "f32"), (-2.0, 0.25, "f16"), (1.0, -1.0, "bf16"), (0.0, 2.0, "f32")]:
+        w = W.problem(260, 300, 150, dtype_out=dout, alpha=alpha, beta=beta, bias=True, seed=int(abs(alpha * 10)))
+        _run_check(handles[cfg], w)
+
+
+# ------------------------------------------------------------------------------ exactness
+@pytest.mark.parametrize("cfg", CONFIGS)
+def test_small_integers_bit_exact(handles, cfg):
+    """Integers in [-3, 3]: every partial sum is an integer below 2^24, so f32 accumulation is exact."""
+    M, N, K = 320, 384, 1100
+    for dt in ("f16", "bf16"):
+        A = W.small_ints(M, K, dt, 1)
+        B = W.small_ints(K, N, dt, 2)
+        C = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        handles[cfg].run(A.cuda(), B.cuda(), C)
+        torch.cuda.synchronize()
+        ref = A.to(torch.int64) @ B.to(torch.int64)
+        assert torch.equal(C.cpu(), ref.to(torch.float32)), dt
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+def test_identity_and_permutation_exact(handles, cfg):
+    n, N = 384, 200
+    B = W.generate(W.problem(n, N, n, seed=3))["B"]          # n x N
+    I = W.identity(n, n, "f16")
+    C = torch.empty(n, N, dtype=torch.float32, device="cuda")
+    handles[cfg].run(I.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    assert torch.equal(C.cpu(), B.to(torch.float32))
+    perm = W.permutation(n, 4)
+    P = W.permutation_matrix(perm, "f16")
+    handles[cfg].run(P.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    assert torch.equal(C.cpu(), B.to(torch.float32)[perm])
+    ones_a = W.ones(n, n, "f16")
+    handles[cfg].run(ones_a.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    col_sums = oracle.gemm_ref(n, N, n, ones_a, oracle.OR_ROW, B, oracle.OR_ROW, oracle.OR_F16)
+    rep = oracle.check(C.cpu().double().numpy(), col_sums, n, 1.0, float(B.abs().max()), oracle.OR_F32)
+    assert rep["passed"], rep
+
+
+# ------------------------------------------------------------------------------ edge cases
+def test_beta_zero_does_not_read_c(handles):
+    w = W.problem(200, 300, 100, dtype_out="f32", seed=5)
+    d = W.generate(w)
+    C = torch.full((w.M, w.N), float("nan"), device="cuda")
+    handles["auto"].run(d["A"].cuda(), d["B"].cuda(), C)
+    torch.cuda.synchronize()
+    assert torch.isfinite(C).all()
+    assert compare(w, d, C)["passed"]
+
+
+@pytest.mark.parametrize("dout", ["f32", "f16", "bf16"])
+def test_k_zero(handles, dout):
+    w = W.problem(70, 90, 0, dtype_out=dout, beta=0.5, bias=True, seed=9)
+    d = W.generate(w)
+    C = d["Cin"].cuda().clone()
+    A = torch.empty(70, 8, dtype=torch.float16, device="cuda")
+    B = torch.empty(8, 90, dtype=torch.float16, device="cuda")
+    handles["auto"].run(A, B, C, M=70, N=90, K=0, beta=0.5, bias=d["bias"].cuda())
+    torch.cuda.synchronize()
+    rep = compare(w, d, C)
+    assert rep["passed"], rep
+
+
+def test_m_or_n_zero_is_noop(handles):
+    C = torch.full((4, 4), 7.0, device="cuda")
+    A = torch.ones(4, 8, dtype=torch.float16, device="cuda")
+    B = torch.ones(8, 4, dtype=torch.float16, device="cuda")
+    handles["auto"].run(A, B, C, M=0, N=4, K=8)
+    handles["auto"].run(A, B, C, M=4, N=0, K=8)
+    torch.cuda.synchronize()
+    assert (C == 7.0).all()
+
+
+def test_unaligned_operand_is_rejected(handles):
+    A = torch.zeros(64 * 64 + 8, dtype=torch.float16, device="cuda")
+    B = torch.zeros(64, 64, dtype=torch.float16, device="cuda")
+    C = torch.zeros(64, 64, device="cuda")
+    Ash = A[1:1 + 64 * 64].view(64, 64)                        # 2-byte offset
+    st = handles["auto"].run(Ash, B, C, check=False)
+    assert st == G.GEMM_ERR_ALIGNMENT
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+def test_guard_band_untouched(handles, cfg):
+    """C inside a larger buffer: padding columns (ldc > N) and rows after M keep their sentinel."""
+    for dout in ("f32", "f16"):
+        w = W.problem(300, 200, 96, dtype_out=dout, bias=True, seed=11)
+        d = W.generate(w)
+        ldc = 264
+        buf = torch.full((w.M + 7, ldc), 12345.0, dtype=W.DTYPES[dout], device="cuda")
+        C = buf[: w.M]
+        handles[cfg].run(d["A"].cuda(), d["B"].cuda(), C, M=w.M, N=w.N, K=w.K, bias=d["bias"].cuda())
+        torch.cuda.synchronize()
+        assert (buf[:, w.N:] == 12345.0).all()
+        assert (buf[w.M:] == 12345.0).all()
+        assert compare(w, d, C)["passed"]
+
+
+def test_unaligned_ldc_uses_direct_stores(handles):
+    w = W.problem(130, 63, 70, dtype_out="f16", seed=13)
+    d = W.generate(w)
+    buf = torch.full((w.M, 63), float("nan"), dtype=torch.float16, device="cuda")
+    handles["auto"].run(d["A"].cuda(), d["B"].cuda(), buf)
+    torch.cuda.synchronize()
+    assert compare(w, d, buf)["passed"]
+
+
+def test_non_default_stream(handles):
+    w = W.problem(500, 700, 300, dtype_out="bf16", dtype_in="bf16", seed=17)
+    d = W.generate(w)
+    dd = device_inputs(d)
+    C = alloc_c(w, d)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        handles["auto"].run(dd["A"], dd["B"], C, stream=s.cuda_stream)
+    s.synchronize()
+    assert compare(w, d, C)["passed"]
+
+
+def test_launch_count(handles):
+    g = G.Gemm(0)
+    w = W.WORKLOADS[4]
+    d = W.generate(w)
+    dd = device_inputs(d)
+    C = alloc_c(w, d)
+    n0 = g.launches
+    run_gpu(g, w, dd, C)
+    assert g.launches - n0 == 3            # two operand repacks + the GEMM
+    A = torch.zeros(128, 128, dtype=torch.float16, device="cuda")
+    C2 = torch.zeros(128, 128, device="cuda")
+    n1 = g.launches
+    g.run(A, A, C2)
+    assert g.launches - n1 == 1
+    torch.cuda.synchronize()
+    g.close()
+
+
+# ------------------------------------------------------------------------------ failure detection
+@pytest.mark.parametrize("site,status", [("tmap", G.GEMM_ERR_CUDA), ("launch", G.GEMM_ERR_CUDA),
+                                         ("alloc", G.GEMM_ERR_OOM)])
+def test_host_fault_injection(handles, site, status, monkeypatch):
+    monkeypatch.setenv("GEMM_TEST_FAIL", site)
+    g = G.Gemm(0)
+    monkeypatch.delenv("GEMM_TEST_FAIL")
+    w = W.WORKLOADS[4] if site == "alloc" else W.problem(64, 64, 64, seed=1)
+    d = W.generate(w)
+    dd = device_inputs(d)
+    C = alloc_c(w, d)
+    st = g.run(dd["A"], dd["B"], C, M=w.M, N=w.N, K=w.K, layoutA=w.layoutA, layoutB=w.layoutB,
+               alpha=w.alpha, beta=w.beta, check=False)
+    assert st == status
+    assert "forced failure" in g.last_error()
+    g.close()
+    # the process and the device stay usable
+    _run_check(handles["auto"], W.problem(64, 64, 64, seed=2))
+
+
+def test_optin_fault_fails_create(monkeypatch):
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    monkeypatch.setenv("GEMM_TEST_FAIL", "optin")
+    st, h = G.gemm_create(0)
+    assert st == G.GEMM_ERR_CUDA and not h.value
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+def test_bounded_wait_expires_and_reports(handles, cfg):
+    """The producer of cluster 0 never issues stage 3, so the MMA issuer's wait runs out after
+    200 ms; the kernel records the timeout, frees its TMEM and returns; the next call works."""
+    g = G.Gemm(0, config=cfg, timeout_ms=200, debug_skip_stage=3)
+    w = W.problem(256, 256, 1024, seed=21)
+    d = W.generate(w)
+    dd = device_inputs(d)
+    C = alloc_c(w, d)
+    run_gpu(g, w, dd, C)
+    st = g.status()
+    assert st == G.GEMM_ERR_TIMEOUT, G.gemm_status_string(st)
+    assert "mma" in g.last_error() or "producer" in g.last_error() or "epilogue" in g.last_error()
+    assert g.status() == G.GEMM_OK       # the word was cleared
+    g.close()
+    _run_check(handles[cfg], W.problem(256, 256, 1024, seed=22))
