@@ -1,0 +1,403 @@
+"""Benchmark of the GB300 dense GEMM: one JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 1..5]
+
+A step is one gemm_run (the whole hot path: tensor maps, TMA ring, tcgen05 MMAs, epilogue)
+over the workload's seeded synthetic inputs.  Default workload: 4096^3, f16 in, f32
+accumulate, f16 out.  Timing: CUDA events on the launching stream around every gemm_run,
+after W untimed warm-up steps, with a 256 MiB write between steps so that every step starts
+with a cold L2 (the 96 MB working set would otherwise fit in the 129 MB L2).  The K timed
+steps are bracketed by a barrier and a device synchronise; the time is the max over ranks.
+Several GPUs (torchrun) run independent replicas of the same GEMM: the product has no data
+exchange, so there is no collective in the timed path (weak scaling).
+
+--impl reference times the CPU oracle (plain f64 triple loop) on the same workload, one
+bounded block of C per step, on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+FLUSH_BYTES = 256 << 20
+METRIC = "GEMM TFLOP/s and % of dense f16 tensor roofline at 4096\u00b3 (1\u00d7GB300)"
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--config", type=int, default=-1)
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps, capped at 200")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks() -> tuple[dict, str]:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return json.loads(p.read_text()), "measured"
+        except Exception:
+            pass
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def _kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted((ROOT / "bf16_tensor_core_gb300" / "csrc").glob("*")):
+        if f.suffix in (".cu", ".cuh", ".h"):
+            h.update(f.name.encode())
+            h.update(f.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload_name: str):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None, None
+    try:
+        d = json.loads(p.read_text())
+        e = d.get(workload_name)
+        if e and e.get("kernel_hash") == _kernel_hash():
+            return e.get("dram_bytes_per_launch"), e.get("source")
+    except Exception:
+        pass
+    return None, None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples, kept only inside [t_start, t_end]."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-i", device_id,
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> list[list[str]]:
+        if not self.proc:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        return [[c.strip() for c in ln.split(",")] for ln in out.splitlines() if ln.count(",") >= 9]
+
+    @staticmethod
+    def summarize(rows, t0: float, t1: float) -> dict:
+        sel = []
+        for r in rows:
+            try:
+                ts = _dt.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            if t0 <= ts <= t1:
+                sel.append(r)
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[2]) for r in sel if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in sel if r[3].replace(".", "").isdigit()]
+        pw = [float(r[4]) for r in sel if r[4].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in sel for n, v in zip(names, r[6:10]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(sel)}
+
+
+def _cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_block_time(w, d, rows: int, cols: int, nthreads: int) -> tuple[float, float]:
+    """Time the oracle on the block C[0:rows, 0:cols] (full K).  Returns (seconds, flops)."""
+    import oracle
+    A = d["A"][:rows] if w.layoutA == "row" else d["A"][:, :rows].contiguous()
+    B = d["B"][:, :cols].contiguous() if w.layoutB == "row" else d["B"][:cols]
+    Cin = d["Cin"][:rows, :cols].contiguous() if d["Cin"] is not None else None
+    bias = d["bias"][:cols].contiguous() if d["bias"] is not None else None
+    code = {"f16": oracle.OR_F16, "bf16": oracle.OR_BF16, "f32": oracle.OR_F32}
+    t0 = time.perf_counter()
+    oracle.gemm_ref(rows, cols, w.K, A, oracle.OR_ROW if w.layoutA == "row" else oracle.OR_COL, B,
+                    oracle.OR_ROW if w.layoutB == "row" else oracle.OR_COL, code[w.dtype_in], alpha=w.alpha,
+                    beta=w.beta, Cin=Cin, dtype_cin=code[w.dtype_out], bias=bias, dtype_bias=code[w.dtype_out],
+                    nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * rows * cols * w.K
+
+
+def cpu_baseline(w, d, budget_s: float) -> dict:
+    """The oracle as it stands, all host cores, on a bounded block of the workload."""
+    cores = _cpu_cores()
+    rows, cols = min(w.M, cores), w.N
+    dt, fl = oracle_block_time(w, d, rows, cols, cores)
+    scale = max(1, int(budget_s / max(dt, 1e-3)))
+    rows2 = min(w.M, rows * scale)
+    rows2 = max(cores, rows2 - rows2 % cores) if rows2 >= cores else rows2
+    if rows2 > rows:
+        dt, fl = oracle_block_time(w, d, rows2, cols, cores)
+        rows = rows2
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of {w.M} x all {cols} columns, full K={w.K}; {dt:.1f} s on {cores} threads",
+            "seconds": dt}
+
+
+def _workload(args):
+    from bf16_tensor_core_gb300 import workloads as W
+    return W.WORKLOADS[args.workload]
+
+
+def _config_dict(w, args, extra=None) -> dict:
+    c = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype_in": w.dtype_in, "dtype_out": w.dtype_out,
+         "layoutA": w.layoutA, "layoutB": w.layoutB, "alpha": w.alpha, "beta": w.beta,
+         "bias": w.dist_bias is not None, "inputs": "seeded synthetic, " + w.note,
+         "l2": f"{FLUSH_BYTES >> 20} MiB write between timed steps (cold L2 every step)",
+         "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ------------------------------------------------------------------------------------------ reference
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from bf16_tensor_core_gb300 import workloads as W
+    w = _workload(args)
+    d = W.generate(w)
+    cores = _cpu_cores()
+    total_steps = args.steps + args.warmup
+    # Block per step sized so the whole run stays within a few minutes.
+    budget = max(0.01, min(2.0, 150.0 / max(total_steps, 1)))
+    rows, cols = min(w.M, cores), min(w.N, 256)
+    dt, _ = oracle_block_time(w, d, rows, cols, cores)
+    while dt < budget / 2 and (rows < w.M or cols < w.N):
+        if cols < w.N:
+            cols = min(w.N, cols * 2)
+        else:
+            rows = min(w.M, rows * 2)
+        dt, _ = oracle_block_time(w, d, rows, cols, cores)
+    while dt > budget and cols > 16:
+        cols = max(16, cols // 2)
+        dt, _ = oracle_block_time(w, d, rows, cols, cores)
+    for _ in range(args.warmup):
+        oracle_block_time(w, d, rows, cols, cores)
+    tot, flops = 0.0, 0.0
+    for _ in range(args.steps):
+        t, f = oracle_block_time(w, d, rows, cols, cores)
+        tot += t
+        flops += f
+    value = flops / tot / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 0, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": _config_dict(w, args, {"sample_per_step": f"C[0:{rows}, 0:{cols}] with full K={w.K}"}),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"per step the block C[0:{rows}, 0:{cols}], full K={w.K}"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------ ours
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    from bf16_tensor_core_gb300 import gemm as G
+    from bf16_tensor_core_gb300 import workloads as W
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = _workload(args)
+    d = W.generate(w)
+    A = d["A"].to(dev)
+    B = d["B"].to(dev)
+    bias = d["bias"].to(dev) if d["bias"] is not None else None
+    Cin_host = d["Cin"]
+    C = (Cin_host.to(dev).clone() if Cin_host is not None
+         else torch.empty(w.M, w.N, dtype=W.DTYPES[w.dtype_out], device=dev))
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    g = G.Gemm(local, config=args.config)
+    stream = torch.cuda.current_stream(dev)
+    s_handle = stream.cuda_stream
+
+    def step():
+        g.run(A, B, C, M=w.M, N=w.N, K=w.K, layoutA=w.layoutA, layoutB=w.layoutB, alpha=w.alpha, beta=w.beta,
+              bias=bias, stream=s_handle)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # warm-up
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = g.status()
+    if st != G.GEMM_OK:
+        raise RuntimeError(f"warm-up failed: {g.last_error()}")
+
+    uuid = str(torch.cuda.get_device_properties(local).uuid)
+    dev_id = uuid if uuid.startswith("GPU-") else ("GPU-" + uuid)
+    sampler = ClockSampler(dev_id)
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches0 = g.launches
+    barrier()
+    torch.cuda.synchronize()
+    t_start = time.time()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_end = time.time()
+    launches = g.launches - launches0
+    clock_rows = sampler.stop()
+    clocks = ClockSampler.summarize(clock_rows, t_start, t_end)
+    st = g.status()
+    if st != G.GEMM_OK:
+        raise RuntimeError(f"timed run failed: {g.last_error()}")
+    times_ms = np.array([e0.elapsed_time(e1) for e0, e1 in evs])
+    total_s = float(times_ms.sum()) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s = float(t.item())
+    value = world * w.flops * args.steps / total_s / 1e12
+    ms_per_step = total_s / args.steps * 1e3
+
+    # end to end through the public call with host buffers
+    e2e = None
+    if not args.no_e2e:
+        n_e2e = args.e2e_steps or min(args.steps, 200)
+        A_pin = d["A"].pin_memory()
+        B_pin = d["B"].pin_memory()
+        Cin_pin = Cin_host.pin_memory() if Cin_host is not None else None
+        C_pin = torch.empty(w.M, w.N, dtype=W.DTYPES[w.dtype_out]).pin_memory()
+        h2d = A_pin.numel() * A_pin.element_size() + B_pin.numel() * B_pin.element_size()
+        if Cin_pin is not None:
+            h2d += Cin_pin.numel() * Cin_pin.element_size()
+        d2h = C_pin.numel() * C_pin.element_size()
+
+        def e2e_step():
+            A.copy_(A_pin, non_blocking=True)
+            B.copy_(B_pin, non_blocking=True)
+            if Cin_pin is not None:
+                C.copy_(Cin_pin, non_blocking=True)
+            step()
+            C_pin.copy_(C, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        t_e2e = e0.elapsed_time(e1) / 1e3
+        if world > 1:
+            t = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_e2e = float(t.item())
+        e2e = {"value": world * w.flops * n_e2e / t_e2e / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "note": "pinned host A, B (and C_in) copied in, gemm_run, C copied out, every step"}
+
+    if rank != 0:
+        return
+    peaks, src = _peaks()
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    achieved = w.flops / (ms_per_step / 1e3) / 1e12
+    traffic, traffic_src = _traffic(w.name)
+    n_sms = torch.cuda.get_device_properties(local).multi_processor_count
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": traffic,
+            "peak_source": f"{src}: cuBLAS bf16 burst (f16 and bf16 share the dense tensor rate)",
+            "kernel": "gb300::gemm_tc_kernel", "algorithmic_flops_per_launch": w.flops,
+            "avg_launch_ms": ms_per_step}
+    if traffic is not None:
+        roof["traffic_source"] = traffic_src
+    if clocks.get("sm_mhz"):
+        clk_peak = 8192.0 * n_sms * clocks["sm_mhz"] * 1e6 / 1e12
+        roof["clock_roofline_tflops"] = clk_peak
+        roof["frac_of_clock_roofline"] = achieved / clk_peak
+        roof["clock_roofline_note"] = "8192 dense f16 FLOP/clk/SM x SMs x median SM clock in the timed window"
+    line = {"metric": METRIC,
+            "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype_in, "data": "synthetic", "impl": "ours",
+            "config": _config_dict(w, args, {"kernel_config": args.config, "timing": "CUDA events around each "
+                                             "gemm_run on its stream"}),
+            "roofline": roof, "clocks": clocks, "gpu_launches": launches, "e2e": e2e}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, d, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = _args()
+    rank, world, local = _dist()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (torch.cuda.is_available() and args.impl == "ours") else "gloo"
+        dist.init_process_group(backend)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, int(os.environ.get("LOCAL_RANK", "0")))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -36,7 +36,7 @@ const ConfigDesc kConfigs[kNumConfigs] = {
 
 // Relative tensor-core efficiency assumed per config when choosing one for a shape (larger
 // tiles amortise the per-stage cost and need less L2 bandwidth per flop).
-const double kConfigEfficiency[kNumConfigs] = {0.88, 1.00, 0.72, 0.93};
+const double kConfigEfficiency[kNumConfigs] = {0.94, 1.00, 0.70, 0.65};
 
 enum FaultSite { FAULT_NONE = 0, FAULT_OPTIN = 1, FAULT_TMAP = 2, FAULT_LAUNCH = 4, FAULT_ALLOC = 8 };
 
