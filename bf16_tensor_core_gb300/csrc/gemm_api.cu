@@ -590,3 +590,229 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
 }
 
 }  // extern "C"
+
+// ============================================================================================
+// gemm_run_noalloc: the same product for callers that must not allocate device memory.
+//
+// Its only scratch need is the operand repack (a 16-bit operand whose byte pitch is not a
+// multiple of 16 is copied to a 16-byte pitch before the TMA can read it).  Here that scratch is
+// a file-scope device array of fixed size, loaded with this library's module, instead of the
+// handle-owned workspace that gemm_run grows with cudaMalloc.  Host code cannot use the array's
+// name as a device address: per device, the first call looks the address up with
+// cudaGetSymbolAddress (with that device current) and every launch receives that pointer.
+// ============================================================================================
+#include <functional>
+#include <mutex>
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GEMM_NOALLOC_SCRATCH_BYTES];
+static __device__ unsigned long long g_noalloc_status;  // bounded-wait word of these calls
+
+constexpr int kNoallocMaxDevices = 64;
+
+struct NoallocDevice {
+    std::once_flag once;
+    gemm_status_t setup_status = GEMM_ERR_CUDA;
+    int num_sms = 0;
+    int max_clusters[kNumConfigs] = {0, 0, 0, 0};
+    void* scratch = nullptr;                 // device address of g_noalloc_scratch
+    unsigned long long* status = nullptr;    // device address of g_noalloc_status
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+};
+
+NoallocDevice g_noalloc_dev[kNoallocMaxDevices];
+
+// One-time set-up on the current device `dev`: shared-memory opt-in, occupancy, the tensor-map
+// encoder and the device addresses of the file-scope scratch and status word.
+void noalloc_setup(int dev, NoallocDevice& nd) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nd.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        nd.setup_status = GEMM_ERR_CUDA;
+        return;
+    }
+    if (major != 10 || minor != 3) {
+        nd.setup_status = GEMM_ERR_UNSUPPORTED;
+        return;
+    }
+    for (int c = 0; c < kNumConfigs; ++c) {
+        const ConfigDesc* d = config_desc(c);
+        for (int outk = 0; outk < kNumOut; ++outk) {
+            if (cudaFuncSetAttribute(config_kernel(c, outk), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     d->smem_bytes) != cudaSuccess) {
+                cudaGetLastError();
+                nd.setup_status = GEMM_ERR_CUDA;
+                return;
+            }
+        }
+        int n = nd.num_sms / d->cta_group;
+        if (d->cta_group == 2) {
+            cudaLaunchConfig_t lc = {};
+            lc.gridDim = dim3((unsigned)(nd.num_sms - nd.num_sms % 2), 1, 1);
+            lc.blockDim = dim3((unsigned)d->threads, 1, 1);
+            lc.dynamicSmemBytes = (size_t)d->smem_bytes;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            lc.attrs = attr;
+            lc.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, config_kernel(c, OUT_F16), &lc) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+        }
+        nd.max_clusters[c] = n;
+    }
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        nd.setup_status = GEMM_ERR_CUDA;
+        return;
+    }
+    nd.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    if (cudaGetSymbolAddress(&nd.scratch, g_noalloc_scratch) != cudaSuccess || !nd.scratch ||
+        cudaGetSymbolAddress(reinterpret_cast<void**>(&nd.status), g_noalloc_status) != cudaSuccess ||
+        !nd.status) {
+        cudaGetLastError();
+        nd.scratch = nullptr;
+        nd.status = nullptr;
+        nd.setup_status = GEMM_ERR_CUDA;
+        return;
+    }
+    if (cudaMemset(nd.status, 0, sizeof(unsigned long long)) != cudaSuccess) {
+        cudaGetLastError();
+        nd.setup_status = GEMM_ERR_CUDA;
+        return;
+    }
+    nd.setup_status = GEMM_OK;
+}
+
+gemm_status_t noalloc_tmap(const NoallocDevice& nd, const void* ptr, CUtensorMapDataType dt, uint64_t dim0,
+                           uint64_t dim1, uint64_t stride_bytes, uint32_t box0, uint32_t box1, CUtensorMap* out) {
+    const cuuint64_t dims[2] = {dim0, dim1};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {box0, box1};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = nd.encode(out, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                                          int64_t ldb, void* C, int64_t ldc, gemm_dtype_t dtype_in,
+                                          gemm_dtype_t dtype_out, gemm_layout_t layoutA, gemm_layout_t layoutB,
+                                          float alpha, float beta, const void* bias, void* stream) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kNoallocMaxDevices) return GEMM_ERR_UNSUPPORTED;
+    NoallocDevice& nd = g_noalloc_dev[dev];
+    std::call_once(nd.once, noalloc_setup, dev, std::ref(nd));
+    if (nd.setup_status != GEMM_OK) return nd.setup_status;
+
+    // Validation and planning (shared with gemm_plan); the message sink reserves its buffer once
+    // per thread, so reporting an invalid argument does not grow it.
+    static thread_local std::string sink(64, '\0');
+    gemm_plan_t plan;
+    gemm_status_t st = plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, nd.num_sms,
+                                 nd.max_clusters[1], -1, &plan, &sink);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C) return GEMM_ERR_INVALID_ARG;
+    if (K > 0 && (!A || !B)) return GEMM_ERR_INVALID_ARG;
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) % 16) != 0 || (reinterpret_cast<uintptr_t>(B) % 16) != 0))
+        return GEMM_ERR_ALIGNMENT;
+    if (plan.workspace_bytes > (int64_t)GEMM_NOALLOC_SCRATCH_BYTES) return GEMM_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
+    if (K == 0) {
+        return launch_scale_bias(out_kind, C, ldc, bias, beta, M, N, nd.num_sms, s) == cudaSuccess ? GEMM_OK
+                                                                                                 : GEMM_ERR_CUDA;
+    }
+    // Repack into the file-scope scratch.  Every byte the GEMM then reads is written by this call
+    // first, so nothing in the scratch has to start at zero.
+    const void* a_ptr = A;
+    const void* b_ptr = B;
+    int64_t lda_eff = lda, ldb_eff = ldb;
+    char* ws = static_cast<char*>(nd.scratch);
+    if (plan.repack_a) {
+        const int64_t rows = layoutA == GEMM_ROW ? M : K;
+        const int64_t cols = layoutA == GEMM_ROW ? K : M;
+        lda_eff = round_up(cols, 8);
+        if (launch_repack_u16(A, lda, ws, lda_eff, rows, cols, s) != cudaSuccess) return GEMM_ERR_CUDA;
+        a_ptr = ws;
+        ws += round_up(rows * lda_eff * 2, 256);
+    }
+    if (plan.repack_b) {
+        const int64_t rows = layoutB == GEMM_ROW ? K : N;
+        const int64_t cols = layoutB == GEMM_ROW ? N : K;
+        ldb_eff = round_up(cols, 8);
+        if (launch_repack_u16(B, ldb, ws, ldb_eff, rows, cols, s) != cudaSuccess) return GEMM_ERR_CUDA;
+        b_ptr = ws;
+    }
+    const ConfigDesc* d = config_desc(plan.config);
+    const CUtensorMapDataType tin =
+        dtype_in == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const int bnc = d->block_n / d->cta_group;
+    CUtensorMap ta, tb, tc;
+    std::memset(&tc, 0, sizeof(tc));
+    st = layoutA == GEMM_ROW ? noalloc_tmap(nd, a_ptr, tin, (uint64_t)K, (uint64_t)M, (uint64_t)lda_eff * 2, 64, 128, &ta)
+                             : noalloc_tmap(nd, a_ptr, tin, (uint64_t)M, (uint64_t)K, (uint64_t)lda_eff * 2, 64, 64, &ta);
+    if (st != GEMM_OK) return st;
+    st = layoutB == GEMM_ROW
+             ? noalloc_tmap(nd, b_ptr, tin, (uint64_t)N, (uint64_t)K, (uint64_t)ldb_eff * 2, 64, 64, &tb)
+             : noalloc_tmap(nd, b_ptr, tin, (uint64_t)K, (uint64_t)N, (uint64_t)ldb_eff * 2, 64, (uint32_t)bnc, &tb);
+    if (st != GEMM_OK) return st;
+    const int eb = elt_bytes(dtype_out);
+    const bool c_aligned = (reinterpret_cast<uintptr_t>(C) % 16) == 0 && (ldc * eb) % 16 == 0;
+    const int use_tma_store = (plan.tma_store && c_aligned) ? 1 : 0;
+    if (use_tma_store) {
+        const CUtensorMapDataType tcd = dtype_out == GEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                        : dtype_out == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        st = noalloc_tmap(nd, C, tcd, (uint64_t)N, (uint64_t)M, (uint64_t)ldc * eb, dtype_out == GEMM_F32 ? 32 : 64, 32,
+                          &tc);
+        if (st != GEMM_OK) return st;
+    }
+    KernelParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.tiles_m = plan.tiles_m;
+    p.tiles_n = plan.tiles_n;
+    p.num_tiles = plan.tiles_m * plan.tiles_n;
+    p.k_tiles = (int)((K + 63) / 64);
+    p.raster_group = plan.raster_group;
+    p.a_mn = layoutA == GEMM_COL ? 1 : 0;
+    p.b_mn = layoutB == GEMM_ROW ? 1 : 0;
+    p.idesc = make_idesc(dtype_in, p.a_mn, p.b_mn, 128 * d->cta_group, d->block_n);
+    p.C = C;
+    p.ldc = ldc;
+    p.bias = bias;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.use_tma_store = use_tma_store;
+    p.c_vec_ok = c_aligned ? 1 : 0;
+    p.status = nd.status;
+    p.timeout_ns = 2000ull * 1000000ull;
+    p.debug_skip_stage = -1;
+    cudaError_t e = config_launch(plan.config, out_kind, plan.clusters * d->cta_group, s, ta, tb, tc, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}

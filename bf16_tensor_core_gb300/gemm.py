@@ -89,6 +89,8 @@ def load_library(path: Path | str | None = None):
     lib.gemm_config_info.restype = ci
     lib.gemm_launch_count.argtypes = [vp]
     lib.gemm_launch_count.restype = i64
+    lib.gemm_run_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ci, ci, ci, ci, cf, cf, vp, vp]
+    lib.gemm_run_noalloc.restype = ci
     if path is None:
         _lib = lib
     return lib
@@ -154,6 +156,12 @@ def gemm_config_info(i: int) -> tuple[int, gemm_config_info_t]:
 
 def gemm_launch_count(h) -> int:
     return load_library().gemm_launch_count(h)
+
+
+def gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, dtype_in, dtype_out, layoutA, layoutB,
+                     alpha, beta, bias, stream) -> int:
+    return load_library().gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, dtype_in, dtype_out, layoutA,
+                                           layoutB, alpha, beta, bias, stream)
 
 
 # ------------------------------------------------------------------ torch convenience wrapper

@@ -160,6 +160,40 @@ gemm_status_t gemm_config_info(int id, gemm_config_info_t* out);
 /* Kernels launched through this handle since it was created. */
 int64_t gemm_launch_count(gemm_handle_t h);
 
+/* Size of the fixed device scratch that gemm_run_noalloc uses for operand repacks. */
+#define GEMM_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* gemm_run_noalloc - the same product as gemm_run, for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this entry point; it exists for the library's users.  Some
+ * callers must not allocate device memory: an application whose device memory is owned by
+ * another allocator (a framework's caching pool, or a budget carved out up front) cannot let a
+ * library call cudaMalloc behind that allocator's back, and a latency-critical loop cannot afford
+ * cudaMalloc / cudaFree, which may synchronise the whole device.  This call takes no handle and
+ * calls no cudaMalloc, cudaFree or other allocating routine.  Arguments, layouts, semantics and
+ * the returned codes are those of gemm_run (on the current device, on `stream`), except:
+ *   - Scratch: an operand whose byte pitch is not a multiple of 16 is repacked into a file-scope
+ *     device array of GEMM_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU loading this library's
+ *     module holds until the process exits.  A call whose repack needs more than that returns
+ *     GEMM_ERR_UNSUPPORTED without launching anything.  Operands with 16-byte pitches use no
+ *     scratch at all.
+ *   - Set-up: the first call on each device opts the kernels into their shared memory, queries
+ *     the device and looks up the scratch's device address (cudaGetSymbolAddress) with that
+ *     device current.  Make that first call before any stream capture begins.
+ *   - Sharing: every call on a device uses the same scratch, which keeps the previous call's
+ *     contents; this call writes every byte it later reads, so nothing has to start at zero.
+ *     Calls whose work overlaps on the GPU (for example on two streams) race on the scratch:
+ *     order them on one stream or with events.
+ *   - Errors: there is no handle, hence no gemm_last_error text; the kernels' bounded waits
+ *     record into a library-internal word that this entry point does not report.
+ */
+gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K,
+                               const void* A, int64_t lda, const void* B, int64_t ldb,
+                               void* C, int64_t ldc,
+                               gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                               gemm_layout_t layoutA, gemm_layout_t layoutB,
+                               float alpha, float beta, const void* bias, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
