@@ -67,11 +67,12 @@ def _peaks() -> tuple[dict, str]:
 
 
 def _kernel_hash() -> str:
+    """Hash of the GEMM kernel's own sources (the kernel template, its PTX wrappers, its TUs)."""
     h = hashlib.sha256()
-    for f in sorted((ROOT / "bf16_tensor_core_gb300" / "csrc").glob("*")):
-        if f.suffix in (".cu", ".cuh", ".h"):
-            h.update(f.name.encode())
-            h.update(f.read_bytes())
+    csrc = ROOT / "bf16_tensor_core_gb300" / "csrc"
+    for f in [csrc / "gemm_kernel.cuh", csrc / "ptx_sm103.cuh", *sorted(csrc.glob("gemm_cfg*.cu"))]:
+        h.update(f.name.encode())
+        h.update(f.read_bytes())
     return h.hexdigest()[:16]
 
 

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -87,6 +88,10 @@ struct gemm_ctx {
     size_t cache_next = 0;
     int faults = FAULT_NONE;
     int64_t launches = 0;
+    unsigned* sk_flags = nullptr;   // zeroed at creation; stream-K flags carry the launch epoch
+    float* sk_part = nullptr;       // stream-K partials (grown on demand)
+    size_t sk_part_bytes = 0;
+    unsigned epoch = 0;
 };
 
 namespace {
@@ -100,17 +105,12 @@ gemm_status_t cuda_fail(gemm_handle_t h, const char* what, cudaError_t e) {
     return fail(h, GEMM_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
-struct Validated {
-    gemm_plan_t plan;
-    std::string err;
-};
-
 int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
 // Pure host planning: validation, config choice, grid and workspace.
 gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int din, int dout,
-                        int la, int lb, float beta, int num_sms, int max_clusters, int config, gemm_plan_t* out,
-                        std::string* err) {
+                        int la, int lb, float beta, int num_sms, int max_clusters, int config, int stream_k,
+                        int cluster_cap, gemm_plan_t* out, std::string* err) {
     std::memset(out, 0, sizeof(*out));
     out->config = -1;
     if (M < 0 || N < 0 || K < 0) { *err = "M, N and K must be >= 0"; return GEMM_ERR_INVALID_ARG; }
@@ -126,21 +126,30 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     if (ldc < std::max<int64_t>(1, N)) { *err = "ldc too small"; return GEMM_ERR_INVALID_ARG; }
     if (num_sms <= 0) { *err = "num_sms must be > 0"; return GEMM_ERR_INVALID_ARG; }
     if (config < -1 || config >= kNumConfigs) { *err = "no such config"; return GEMM_ERR_UNSUPPORTED; }
+    if (stream_k < -1 || stream_k > 1) { *err = "stream_k must be -1, 0 or 1"; return GEMM_ERR_INVALID_ARG; }
     if (max_clusters <= 0) max_clusters = num_sms / 2;
     if (M == 0 || N == 0) { out->kernels = 0; return GEMM_OK; }
     if (K == 0) { out->kernels = 1; return GEMM_OK; }
 
+    auto slots_of = [&](const ConfigDesc& d) {
+        int slots = d.cta_group == 2 ? max_clusters : num_sms;
+        if (cluster_cap > 0) slots = std::min(slots, cluster_cap);
+        return slots;
+    };
     int best = config;
     if (best < 0) {
         double best_cost = 1e300;
         for (int c = 0; c < kNumConfigs; ++c) {
             const ConfigDesc& d = kConfigs[c];
-            const int slots = d.cta_group == 2 ? max_clusters : num_sms;
+            const int slots = slots_of(d);
             if (slots <= 0) continue;
             const int64_t bm = 128 * d.cta_group;
             const int64_t tiles = ((M + bm - 1) / bm) * ((N + d.block_n - 1) / d.block_n);
-            const int64_t waves = (tiles + slots - 1) / slots;
-            const double cost = (double)waves * (double)(bm * d.block_n) / (d.cta_group * kConfigEfficiency[c]);
+            // Whole waves, or (with the stream-K tail) the exact share plus a small fix-up cost.
+            double waves = (double)((tiles + slots - 1) / slots);
+            if (stream_k != 0 && tiles > slots && tiles % slots != 0)
+                waves = std::min(waves, (double)tiles / slots + 0.08);
+            const double cost = waves * (double)(bm * d.block_n) / (d.cta_group * kConfigEfficiency[c]);
             if (cost < best_cost * (1.0 - 1e-9)) { best_cost = cost; best = c; }
         }
     }
@@ -155,7 +164,8 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     out->tiles_m = (int)((M + out->block_m - 1) / out->block_m);
     out->tiles_n = (int)((N + out->block_n - 1) / out->block_n);
     const int64_t tiles = (int64_t)out->tiles_m * out->tiles_n;
-    const int slots = d.cta_group == 2 ? max_clusters : num_sms;
+    const int slots = slots_of(d);
+    if (slots <= 0) { *err = "no cluster fits"; return GEMM_ERR_UNSUPPORTED; }
     out->clusters = (int)std::min<int64_t>(tiles, slots);
     out->raster_group = std::min(out->tiles_m, 8);
     out->tma_store = (beta == 0.0f && (ldc * elt_bytes(dout)) % 16 == 0) ? 1 : 0;
@@ -164,7 +174,17 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     int64_t ws = 0;
     if (out->repack_a) ws += round_up((la == GEMM_ROW ? M : K) * round_up(a_inner, 8) * 2, 256);
     if (out->repack_b) ws += round_up((lb == GEMM_ROW ? K : N) * round_up(b_inner, 8) * 2, 256);
-    out->workspace_bytes = ws;
+    // Stream-K tail: worthwhile when the last wave would leave more than 15% of the clusters idle.
+    const int P = out->clusters;
+    if (stream_k != 0 && tiles > P && tiles % P != 0) {
+        const double waves = (double)tiles / P;
+        if (stream_k == 1 || std::ceil(waves) - waves > 0.15) {
+            out->stream_k = 1;
+            out->dp_tiles = (int)((tiles / P - 1) * P);
+            out->sk_partial_bytes = round_up((int64_t)P * d.cta_group * 128 * d.block_n * 4, 256);
+        }
+    }
+    out->workspace_bytes = ws + out->sk_partial_bytes;
     out->kernels = 1 + out->repack_a + out->repack_b;
     return GEMM_OK;
 }
@@ -293,6 +313,7 @@ void gemm_options_default(gemm_options_t* opt) {
     opt->raster_group = 0;
     opt->max_clusters = 0;
     opt->debug_skip_stage = -1;
+    opt->stream_k = -1;
 }
 
 const char* gemm_status_string(gemm_status_t s) {
@@ -327,11 +348,11 @@ gemm_status_t gemm_config_info(int id, gemm_config_info_t* out) {
 
 gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                         gemm_dtype_t dtype_in, gemm_dtype_t dtype_out, gemm_layout_t layoutA, gemm_layout_t layoutB,
-                        float beta, int num_sms, int max_clusters, int config, gemm_plan_t* out) {
+                        float beta, int num_sms, int max_clusters, int config, int stream_k, gemm_plan_t* out) {
     if (!out) return GEMM_ERR_INVALID_ARG;
     std::string err;
     return plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, num_sms, max_clusters,
-                     config, out, &err);
+                     config, stream_k, 0, out, &err);
 }
 
 gemm_status_t gemm_create(gemm_handle_t* out, int device, const gemm_options_t* opt) {
@@ -343,7 +364,8 @@ gemm_status_t gemm_create(gemm_handle_t* out, int device, const gemm_options_t* 
         if (opt->struct_size != (int)sizeof(gemm_options_t)) return GEMM_ERR_INVALID_ARG;
         o = *opt;
     }
-    if (o.config < -1 || o.config >= kNumConfigs || o.timeout_ms <= 0 || o.raster_group < 0 || o.max_clusters < 0)
+    if (o.config < -1 || o.config >= kNumConfigs || o.timeout_ms <= 0 || o.raster_group < 0 || o.max_clusters < 0 ||
+        o.stream_k < -1 || o.stream_k > 1)
         return GEMM_ERR_INVALID_ARG;
     int count = 0;
     cudaError_t e = cudaGetDeviceCount(&count);
@@ -420,9 +442,14 @@ gemm_status_t gemm_create(gemm_handle_t* out, int device, const gemm_options_t* 
     h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     e = cudaMalloc(&h->d_status, 64);
     if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 64);
+    // One flag per (cluster, CTA rank, epilogue warp) for the stream-K hand-off.
+    const size_t flag_bytes = (size_t)h->num_sms * 4 * sizeof(unsigned);
+    if (e == cudaSuccess) e = cudaMalloc(&h->sk_flags, flag_bytes);
+    if (e == cudaSuccess) e = cudaMemset(h->sk_flags, 0, flag_bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
         if (h->d_status) cudaFree(h->d_status);
+        if (h->sk_flags) cudaFree(h->sk_flags);
         delete h;
         return GEMM_ERR_OOM;
     }
@@ -437,6 +464,8 @@ gemm_status_t gemm_destroy(gemm_handle_t h) {
         cudaDeviceSynchronize();
         if (h->ws) cudaFree(h->ws);
         if (h->d_status) cudaFree(h->d_status);
+        if (h->sk_flags) cudaFree(h->sk_flags);
+        if (h->sk_part) cudaFree(h->sk_part);
     }
     delete h;
     return GEMM_OK;
@@ -480,7 +509,7 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
     std::string err;
     gemm_status_t st = plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, h->num_sms,
                                  h->opt.config >= 0 ? h->max_clusters[h->opt.config] : h->max_clusters[1],
-                                 h->opt.config, &plan, &err);
+                                 h->opt.config, h->opt.stream_k, h->opt.max_clusters, &plan, &err);
     if (st != GEMM_OK) return fail(h, st, err);
     if (M == 0 || N == 0) return GEMM_OK;
     if (!C) return fail(h, GEMM_ERR_INVALID_ARG, "C is NULL");
@@ -502,7 +531,7 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
         const void* b_ptr = B;
         int64_t lda_eff = lda, ldb_eff = ldb;
         if (plan.repack_a || plan.repack_b) {
-            st = ensure_workspace(h, (size_t)plan.workspace_bytes);
+            st = ensure_workspace(h, (size_t)(plan.workspace_bytes - plan.sk_partial_bytes));
             if (st != GEMM_OK) return st;
             char* ws = static_cast<char*>(h->ws);
             if (plan.repack_a) {
@@ -575,8 +604,29 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
         p.status = h->d_status;
         p.timeout_ns = (unsigned long long)h->opt.timeout_ms * 1000000ull;
         p.debug_skip_stage = h->opt.debug_skip_stage;
-        int clusters = plan.clusters;
-        if (h->opt.max_clusters > 0) clusters = std::min(clusters, h->opt.max_clusters);
+        const int clusters = plan.clusters;
+        if (plan.stream_k) {
+            if ((size_t)plan.sk_partial_bytes > h->sk_part_bytes) {
+                if (h->faults & FAULT_ALLOC)
+                    return fail(h, GEMM_ERR_OOM, "stream-K partials: forced failure (GEMM_TEST_FAIL=alloc)");
+                if (h->sk_part) { cudaFree(h->sk_part); h->sk_part = nullptr; h->sk_part_bytes = 0; }
+                cudaError_t ea = cudaMalloc(reinterpret_cast<void**>(&h->sk_part), (size_t)plan.sk_partial_bytes);
+                if (ea != cudaSuccess) {
+                    cudaGetLastError();
+                    return fail(h, GEMM_ERR_OOM, std::string("stream-K partials cudaMalloc: ") + cudaGetErrorString(ea));
+                }
+                h->sk_part_bytes = (size_t)plan.sk_partial_bytes;
+            }
+            if (++h->epoch == 0) ++h->epoch;
+            const long long sk_total = (long long)(p.num_tiles - plan.dp_tiles) * p.k_tiles;
+            p.sk_enabled = 1;
+            p.dp_tiles = plan.dp_tiles;
+            p.sk_base = sk_total / clusters;
+            p.sk_extra = (int)(sk_total % clusters);
+            p.sk_partials = h->sk_part;
+            p.sk_flags = h->sk_flags;
+            p.epoch = h->epoch;
+        }
         if (h->faults & FAULT_LAUNCH) return fail(h, GEMM_ERR_CUDA, "kernel launch: forced failure (GEMM_TEST_FAIL=launch)");
         cudaError_t e = config_launch(plan.config, out_kind, clusters * d->cta_group, s, ta, tb, tc, p);
         if (e != cudaSuccess) {
@@ -727,7 +777,7 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     static thread_local std::string sink(64, '\0');
     gemm_plan_t plan;
     gemm_status_t st = plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, nd.num_sms,
-                                 nd.max_clusters[1], -1, &plan, &sink);
+                                 nd.max_clusters[1], -1, 0, 0, &plan, &sink);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
     if (!C) return GEMM_ERR_INVALID_ARG;

@@ -51,6 +51,67 @@ struct KernelParams {
     unsigned long long* status;
     unsigned long long timeout_ns;
     long long debug_skip_stage;  // test only: cluster 0's producer never issues this stage
+    // Stream-K tail (sk_enabled != 0): tiles [0, dp_tiles) are walked data-parallel; the k-iterations
+    // of tiles [dp_tiles, num_tiles) are divided evenly over the clusters (sk_base or sk_base + 1
+    // each, the first sk_extra clusters taking one more).  Every range is at least k_tiles long, so
+    // a split tile has exactly two segments: the head [0, k1) and the tail [k1, k_tiles) computed by
+    // the next cluster, which parks its f32 partial in sk_partials and raises its flags to `epoch`.
+    int sk_enabled;
+    int dp_tiles;
+    long long sk_base;
+    int sk_extra;
+    float* sk_partials;        // [cluster][cta rank][BN / 4][128 rows][4] f32
+    unsigned* sk_flags;        // [cluster][cta rank][4 epilogue warps]
+    unsigned epoch;            // launch counter of the handle, never 0
+};
+
+enum : int { UNIT_FULL = 0, UNIT_HEAD = 1, UNIT_TAIL = 2 };
+
+struct Unit {
+    int tile;
+    int k0, k1;   // k-tile range [k0, k1) of this tile computed here
+    int kind;     // UNIT_FULL, UNIT_HEAD (adds the next cluster's partial), UNIT_TAIL (writes a partial)
+};
+
+// The deterministic sequence of work units of one cluster, identical in every role.
+struct UnitIter {
+    int next_dp, dp_limit, stride;
+    long long it, it_end;
+
+    __device__ __forceinline__ void init(const KernelParams& p, int cluster, int num_clusters) {
+        next_dp = cluster;
+        stride = num_clusters;
+        dp_limit = p.sk_enabled ? p.dp_tiles : p.num_tiles;
+        if (p.sk_enabled) {
+            it = static_cast<long long>(cluster) * p.sk_base + min(cluster, p.sk_extra);
+            it_end = it + p.sk_base + (cluster < p.sk_extra ? 1 : 0);
+        } else {
+            it = it_end = 0;
+        }
+    }
+
+    __device__ __forceinline__ bool next(const KernelParams& p, Unit& u) {
+        if (next_dp < dp_limit) {
+            u.tile = next_dp;
+            u.k0 = 0;
+            u.k1 = p.k_tiles;
+            u.kind = UNIT_FULL;
+            next_dp += stride;
+            return true;
+        }
+        if (it < it_end) {
+            const long long rel = it / p.k_tiles;
+            const int k0 = static_cast<int>(it - rel * p.k_tiles);
+            const long long seg_end = min((rel + 1) * p.k_tiles, it_end);
+            u.tile = p.dp_tiles + static_cast<int>(rel);
+            u.k0 = k0;
+            u.k1 = k0 + static_cast<int>(seg_end - it);
+            u.kind = (k0 == 0 && u.k1 == p.k_tiles) ? UNIT_FULL : (k0 == 0 ? UNIT_HEAD : UNIT_TAIL);
+            it = seg_end;
+            return true;
+        }
+        return false;
+    }
 };
 
 template <int kCtaGroup, int kBN, int kStages>
@@ -193,12 +254,43 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// Stream-K partial layout inside one CTA's slot: [BN / 4 column quads][128 rows][4 f32], so a warp
+// moving one quad of its 32 rows touches 512 contiguous bytes.
+__device__ __forceinline__ void add_partial_32(uint32_t (&acc)[32], const float* part, int col, int prow) {
+    const float4* src = reinterpret_cast<const float4*>(part);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float4 v = __ldcg(&src[(col / 4 + j) * 128 + prow]);
+        acc[4 * j + 0] = __float_as_uint(__uint_as_float(acc[4 * j + 0]) + v.x);
+        acc[4 * j + 1] = __float_as_uint(__uint_as_float(acc[4 * j + 1]) + v.y);
+        acc[4 * j + 2] = __float_as_uint(__uint_as_float(acc[4 * j + 2]) + v.z);
+        acc[4 * j + 3] = __float_as_uint(__uint_as_float(acc[4 * j + 3]) + v.w);
+    }
+}
+
 // One warp drains its 32 TMEM lanes (32 rows) x BN columns of one accumulator buffer.
+//   out_part != nullptr: a stream-K tail segment; the raw f32 sums go to the partial slot, C is untouched.
+//   add_part != nullptr: a stream-K head segment; the next cluster's partial is added before the epilogue.
 template <int kOut, int kBN>
 __device__ __forceinline__ void epilogue_tile(const KernelParams& p, const CUtensorMap* tmC, uint32_t tbase,
-                                              int row0, int col_base, int lane, uint32_t stage_buf0,
-                                              uint32_t& chunk_ctr) {
+                                              int row0, int col_base, int lane, int prow, uint32_t stage_buf0,
+                                              uint32_t& chunk_ctr, const float* add_part, float* out_part) {
     const int row = row0 + lane;
+    if (out_part != nullptr) {
+        float4* dst = reinterpret_cast<float4*>(out_part);
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t acc[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, acc);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                __stcg(&dst[(c * 8 + j) * 128 + prow],
+                       make_float4(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]),
+                                   __uint_as_float(acc[4 * j + 2]), __uint_as_float(acc[4 * j + 3])));
+        }
+        return;
+    }
     if (p.use_tma_store) {
         // A chunk is one 128-byte line per row: 64 columns of a 16-bit type, 32 of f32.
         constexpr int kChunk = (kOut == OUT_F32) ? 32 : 64;
@@ -211,6 +303,7 @@ __device__ __forceinline__ void epilogue_tile(const KernelParams& p, const CUten
                 uint32_t acc[32];
                 tmem_ld_32x32b_x32(tbase + c * 32, acc);
                 tmem_wait_ld();
+                if (add_part) add_partial_32(acc, add_part, c * 32, prow);
                 float v[32];
                 epilogue_math<kOut>(p, acc, v, row, col0);
 #pragma unroll
@@ -220,6 +313,10 @@ __device__ __forceinline__ void epilogue_tile(const KernelParams& p, const CUten
                 tmem_ld_32x32b_x32(tbase + c * 64, acc0);
                 tmem_ld_32x32b_x32(tbase + c * 64 + 32, acc1);
                 tmem_wait_ld();
+                if (add_part) {
+                    add_partial_32(acc0, add_part, c * 64, prow);
+                    add_partial_32(acc1, add_part, c * 64 + 32, prow);
+                }
                 float v[32];
                 epilogue_math<kOut>(p, acc0, v, row, col0);
 #pragma unroll
@@ -254,9 +351,36 @@ __device__ __forceinline__ void epilogue_tile(const KernelParams& p, const CUten
             tmem_ld_32x32b_x32(tbase + c * 32, acc);
             tmem_wait_ld();
             if (col0 >= p.N) continue;
+            if (add_part) add_partial_32(acc, add_part, c * 32, prow);
             float v[32];
             epilogue_math<kOut>(p, acc, v, row, col0);
             store_row_direct<kOut>(p, v, row, col0);
+        }
+    }
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned* addr, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* addr) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
+// Bounded wait for a stream-K flag written by another cluster of this grid (all clusters are
+// co-resident: the grid never exceeds the device's active-cluster capacity).
+__device__ __forceinline__ bool wait_flag_bounded(const unsigned* flag, unsigned want, uint64_t timeout_ns,
+                                                  const volatile int* abort_flag) {
+    if (ld_acquire_gpu(flag) == want) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(flag) == want) return true;
+        if ((i & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > timeout_ns) return false;
         }
     }
 }
@@ -317,14 +441,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             long long gstage = 0;
             const uint32_t tx_bytes = static_cast<uint32_t>(Cfg::kStageBytes * kCtaGroup);
             bool ok = true;
-            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+            UnitIter units;
+            units.init(p, cluster_id, num_clusters);
+            Unit u;
+            while (ok && units.next(p, u)) {
                 int mb, nb;
-                tile_coords(p, t, mb, nb);
+                tile_coords(p, u.tile, mb, nb);
                 const int m0 = mb * (Cfg::kBM * kCtaGroup) + static_cast<int>(rank) * Cfg::kBM;
                 const int n0 = nb * kBN + static_cast<int>(rank) * Cfg::kBNC;
-                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                for (int kt = u.k0; kt < u.k1; ++kt) {
                     if (!mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, p.timeout_ns, abort_flag)) {
-                        if (!*abort_flag) report_error<kCtaGroup>(p, ROLE_PRODUCER, t, static_cast<int>(stage), abort_flag);
+                        if (!*abort_flag) report_error<kCtaGroup>(p, ROLE_PRODUCER, u.tile, static_cast<int>(stage), abort_flag);
                         ok = false;
                         break;
                     }
@@ -374,17 +501,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint64_t stage_step = static_cast<uint64_t>(Cfg::kStageBytes >> 4);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+            UnitIter units;
+            units.init(p, cluster_id, num_clusters);
+            Unit u;
+            while (ok && units.next(p, u)) {
                 if (!mbar_wait_bounded<kCtaGroup == 2>(smem_u32(&bar_tempty[acc]), acc_phase ^ 1u, p.timeout_ns,
                                                        abort_flag)) {
-                    if (!*abort_flag) report_error<kCtaGroup>(p, ROLE_MMA, t, 100 + static_cast<int>(acc), abort_flag);
+                    if (!*abort_flag) report_error<kCtaGroup>(p, ROLE_MMA, u.tile, 100 + static_cast<int>(acc), abort_flag);
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * static_cast<uint32_t>(Cfg::kAccCols);
-                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                for (int kt = u.k0; kt < u.k1; ++kt) {
                     if (!mbar_wait_bounded(smem_u32(&bar_full[stage]), phase, p.timeout_ns, abort_flag)) {
-                        if (!*abort_flag) report_error<kCtaGroup>(p, ROLE_MMA, t, static_cast<int>(stage), abort_flag);
+                        if (!*abort_flag) report_error<kCtaGroup>(p, ROLE_MMA, u.tile, static_cast<int>(stage), abort_flag);
                         ok = false;
                         break;
                     }
@@ -394,7 +524,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                     for (int k = 0; k < Cfg::kBK / 16; ++k)
                         mma_f16<kCtaGroup>(d_tmem, ad + k * a_kstep, bd + k * b_kstep, p.idesc,
-                                           (kt > 0 || k > 0) ? 1u : 0u);
+                                           (kt > u.k0 || k > 0) ? 1u : 0u);
                     mma_commit<kCtaGroup>(smem_u32(&bar_empty[stage]));   // slot free once these MMAs finish
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
@@ -413,29 +543,61 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ------------------------------------------------------------ epilogue warps 2..5
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
         const int ew = warp - 2;
+        const int prow = quarter * 32 + lane;         // row within this CTA's 128
         const uint32_t stage_buf0 = epi_smem + static_cast<uint32_t>(ew) * 2u * Cfg::kEpiBufBytes;
+        const size_t slot_floats = static_cast<size_t>(kCtaGroup) * 128 * kBN;
         uint32_t acc = 0, acc_phase = 0, chunk_ctr = 0;
-        for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+        UnitIter units;
+        units.init(p, cluster_id, num_clusters);
+        Unit u;
+        while (units.next(p, u)) {
             int mb, nb;
-            tile_coords(p, t, mb, nb);
+            tile_coords(p, u.tile, mb, nb);
             bool ok = mbar_wait_bounded(smem_u32(&bar_tfull[acc]), acc_phase, p.timeout_ns, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 if (lane == 0 && !*abort_flag)
-                    report_error<kCtaGroup>(p, ROLE_EPILOGUE, t, 200 + static_cast<int>(acc), abort_flag);
+                    report_error<kCtaGroup>(p, ROLE_EPILOGUE, u.tile, 200 + static_cast<int>(acc), abort_flag);
                 break;
             }
             tc_fence_after_sync();
+            const float* add_part = nullptr;
+            float* out_part = nullptr;
+            if (u.kind == UNIT_TAIL) {
+                out_part = p.sk_partials + static_cast<size_t>(cluster_id) * slot_floats +
+                           static_cast<size_t>(rank) * 128 * kBN;
+            } else if (u.kind == UNIT_HEAD) {
+                // The tail [k1, k_tiles) of this tile is the first unit of the next cluster.
+                const int src = cluster_id + 1;
+                const unsigned* flag = p.sk_flags + (static_cast<size_t>(src) * kCtaGroup + rank) * 4 + quarter;
+                bool ready = true;
+                if (lane == 0) ready = wait_flag_bounded(flag, p.epoch, p.timeout_ns, abort_flag);
+                ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+                if (!ready) {
+                    if (lane == 0 && !*abort_flag)
+                        report_error<kCtaGroup>(p, ROLE_EPILOGUE, u.tile, 300 + quarter, abort_flag);
+                    break;
+                }
+                add_part = p.sk_partials + static_cast<size_t>(src) * slot_floats +
+                           static_cast<size_t>(rank) * 128 * kBN;
+            }
             const int row0 = mb * (Cfg::kBM * kCtaGroup) + static_cast<int>(rank) * Cfg::kBM + quarter * 32;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    acc * static_cast<uint32_t>(Cfg::kAccCols);
-            epilogue_tile<kOut, kBN>(p, &tmC, tbase, row0, nb * kBN, lane, stage_buf0, chunk_ctr);
+            epilogue_tile<kOut, kBN>(p, &tmC, tbase, row0, nb * kBN, lane, prow, stage_buf0, chunk_ctr, add_part,
+                                     out_part);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
                 const uint32_t te = smem_u32(&bar_tempty[acc]);
                 if constexpr (kCtaGroup == 2) mbar_arrive_cluster(mapa_shared(te, 0));
                 else mbar_arrive_local(te);
+                if (u.kind == UNIT_TAIL) {
+                    // Every lane's partial stores precede this release (warp barrier, then fence).
+                    __threadfence();
+                    st_release_gpu(p.sk_flags + (static_cast<size_t>(cluster_id) * kCtaGroup + rank) * 4 + quarter,
+                                   p.epoch);
+                }
             }
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;

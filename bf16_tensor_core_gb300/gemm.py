@@ -27,7 +27,7 @@ LAYOUT_CODES = {"row": GEMM_ROW, "col": GEMM_COL}
 class gemm_options_t(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_int), ("config", ctypes.c_int), ("timeout_ms", ctypes.c_int),
                 ("sync_check", ctypes.c_int), ("raster_group", ctypes.c_int), ("max_clusters", ctypes.c_int),
-                ("debug_skip_stage", ctypes.c_int)]
+                ("debug_skip_stage", ctypes.c_int), ("stream_k", ctypes.c_int)]
 
 
 class gemm_config_info_t(ctypes.Structure):
@@ -41,7 +41,8 @@ class gemm_plan_t(ctypes.Structure):
                 ("block_n", ctypes.c_int), ("block_k", ctypes.c_int), ("stages", ctypes.c_int),
                 ("tiles_m", ctypes.c_int), ("tiles_n", ctypes.c_int), ("clusters", ctypes.c_int),
                 ("raster_group", ctypes.c_int), ("tma_store", ctypes.c_int), ("repack_a", ctypes.c_int),
-                ("repack_b", ctypes.c_int), ("workspace_bytes", ctypes.c_int64), ("kernels", ctypes.c_int)]
+                ("repack_b", ctypes.c_int), ("workspace_bytes", ctypes.c_int64), ("kernels", ctypes.c_int),
+                ("stream_k", ctypes.c_int), ("dp_tiles", ctypes.c_int), ("sk_partial_bytes", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -80,7 +81,7 @@ def load_library(path: Path | str | None = None):
     lib.gemm_last_error.restype = ctypes.c_char_p
     lib.gemm_get_device_status.argtypes = [vp, vp]
     lib.gemm_get_device_status.restype = ci
-    lib.gemm_plan.argtypes = [i64, i64, i64, i64, i64, i64, ci, ci, ci, ci, cf, ci, ci, ci,
+    lib.gemm_plan.argtypes = [i64, i64, i64, i64, i64, i64, ci, ci, ci, ci, cf, ci, ci, ci, ci,
                               ctypes.POINTER(gemm_plan_t)]
     lib.gemm_plan.restype = ci
     lib.gemm_num_configs.argtypes = []
@@ -138,10 +139,10 @@ def gemm_get_device_status(h, stream=None) -> int:
 
 
 def gemm_plan(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta=0.0, num_sms=152,
-              max_clusters=0, config=-1) -> tuple[int, gemm_plan_t]:
+              max_clusters=0, config=-1, stream_k=-1) -> tuple[int, gemm_plan_t]:
     p = gemm_plan_t()
     st = load_library().gemm_plan(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, num_sms,
-                                  max_clusters, config, ctypes.byref(p))
+                                  max_clusters, config, stream_k, ctypes.byref(p))
     return st, p
 
 

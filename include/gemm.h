@@ -87,6 +87,7 @@ typedef struct {
     int max_clusters;     /* cap on persistent clusters (0 = as many as fit on the device)    */
     int debug_skip_stage; /* TEST ONLY: the producer of cluster 0 never issues this k-stage,
                              so the MMA issuer's bounded wait expires (-1 = off)              */
+    int stream_k;         /* tail-wave balancing: -1 automatic, 0 off, 1 whenever possible   */
 } gemm_options_t;
 
 /* Description of a kernel configuration. */
@@ -110,8 +111,11 @@ typedef struct {
     int raster_group;      /* tile rows per raster group                                    */
     int tma_store;         /* 1: epilogue writes C with TMA tensor stores; 0: st.global     */
     int repack_a, repack_b;/* 1: operand copied to a 16-byte pitch workspace first          */
-    int64_t workspace_bytes;
+    int64_t workspace_bytes; /* repack workspace + stream-K partials                        */
     int kernels;           /* kernel launches the call makes                                */
+    int stream_k;          /* 1: the last wave(s) are split evenly by k-iterations          */
+    int dp_tiles;          /* tiles walked whole before the stream-K region                 */
+    int64_t sk_partial_bytes; /* part of workspace_bytes holding stream-K f32 partials      */
 } gemm_plan_t;
 
 /* Fill *opt with defaults (config -1, timeout 2000 ms, no sync check, automatic raster). */
@@ -147,11 +151,11 @@ gemm_status_t gemm_get_device_status(gemm_handle_t h, void* stream);
  * beta: as for gemm_run (beta != 0 rules out the TMA-store epilogue, which never reads C);
  * the plan assumes C is 16-byte aligned.  num_sms: the device's SM count (e.g. 152);
  * max_clusters: co-resident 2-SM clusters (0 = num_sms / 2).  config: -1 automatic, else a
- * config id.  Uses no device. */
+ * config id.  stream_k: as in gemm_options_t.  Uses no device. */
 gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                         gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
                         gemm_layout_t layoutA, gemm_layout_t layoutB, float beta,
-                        int num_sms, int max_clusters, int config, gemm_plan_t* out);
+                        int num_sms, int max_clusters, int config, int stream_k, gemm_plan_t* out);
 
 /* Number of kernel configurations and their descriptions (ids 0 .. gemm_num_configs()-1). */
 int gemm_num_configs(void);

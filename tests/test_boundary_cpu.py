@@ -67,11 +67,11 @@ def test_null_handle_and_create_without_gpu(lib):
         assert st in (G.GEMM_ERR_CUDA, G.GEMM_ERR_INVALID_ARG) and not h.value
 
 
-def plan(M, N, K, lda=None, ldb=None, ldc=None, din=0, dout=2, la=0, lb=0, beta=0.0, config=-1, sms=152):
+def plan(M, N, K, lda=None, ldb=None, ldc=None, din=0, dout=2, la=0, lb=0, beta=0.0, config=-1, sms=152, sk=-1):
     lda = lda if lda is not None else (K if la == 0 else M)
     ldb = ldb if ldb is not None else (N if lb == 0 else K)
     ldc = ldc if ldc is not None else N
-    return G.gemm_plan(M, N, K, max(lda, 1), max(ldb, 1), max(ldc, 1), din, dout, la, lb, beta, sms, 0, config)
+    return G.gemm_plan(M, N, K, max(lda, 1), max(ldb, 1), max(ldc, 1), din, dout, la, lb, beta, sms, 0, config, sk)
 
 
 @pytest.mark.parametrize("args,status", [
@@ -113,7 +113,8 @@ def test_plan_tiles_and_grid(lib):
         assert p.tiles_m == 4096 // c.block_m and p.tiles_n == 4096 // c.block_n
         slots = 152 // c.cta_group
         assert p.clusters == min(p.tiles_m * p.tiles_n, slots)
-        assert p.tma_store == 1 and p.kernels == 1 and p.workspace_bytes == 0
+        assert p.tma_store == 1 and p.kernels == 1
+        assert p.workspace_bytes == p.sk_partial_bytes
     st, p = plan(1000, 3000, 2050, config=1)
     assert (p.tiles_m, p.tiles_n) == (4, 12)           # partial last tiles: 1000 = 3*256 + 232, 3000 = 11*256 + 184
     st, p = plan(1, 1, 1, config=0)
@@ -127,7 +128,7 @@ def test_plan_repack_and_workspace(lib):
     assert p.repack_a == 1 and p.repack_b == 1 and p.kernels == 3
     a_bytes = -(-1000 * 2056 * 2 // 256) * 256
     b_bytes = -(-3000 * 2056 * 2 // 256) * 256
-    assert p.workspace_bytes == a_bytes + b_bytes
+    assert p.workspace_bytes == a_bytes + b_bytes + p.sk_partial_bytes
     assert p.tma_store == 0                             # beta != 0 reads C: direct-store epilogue
     st, p = plan(64, 64, 64, lda=72, ldb=64)
     assert p.repack_a == 0 and p.repack_b == 0 and p.workspace_bytes == 0
@@ -152,3 +153,66 @@ def test_python_binding_fails_loudly_without_library(tmp_path):
         os.path.dirname(os.path.dirname(os.path.abspath(__file__))), str(tmp_path / "missing.so"))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
     assert "LOUD" in r.stdout
+
+
+# ------------------------------------------------------------------------------ stream-K tail
+def test_plan_stream_k(lib):
+    st, p = plan(4096, 4096, 4096, dout=0, config=1)            # 256 tiles over 76 clusters: 3.37 waves
+    assert st == G.GEMM_OK and p.stream_k == 1 and p.clusters == 76
+    assert p.dp_tiles == (256 // 76 - 1) * 76
+    assert p.sk_partial_bytes == 76 * 2 * 128 * 256 * 4
+    st, p = plan(4096, 4096, 4096, dout=0, config=1, sk=0)
+    assert p.stream_k == 0 and p.sk_partial_bytes == 0 and p.workspace_bytes == 0
+    st, p = plan(256 * 19, 256 * 8, 1024, config=1)              # 152 tiles = 2 whole waves
+    assert p.stream_k == 0
+    st, p = plan(1024, 1024, 1024, config=1)                     # 16 tiles < 76 clusters
+    assert p.stream_k == 0
+    st, p = plan(256 * 9, 256 * 9, 512, config=1, sk=1)          # 81 tiles: forced on
+    assert p.stream_k == 1 and p.dp_tiles == 0
+    st, p = plan(256 * 16, 256 * 19, 512, config=1)              # 304 tiles = 4.0 waves exactly
+    assert p.stream_k == 0
+    st, p = plan(256 * 11, 256 * 14, 512, config=1)              # 154 tiles = 2.03 waves: last wave 3% full
+    assert p.stream_k == 1
+
+
+def sk_units(T, P, KT, dp_tiles, cluster):
+    """Python model of the kernel's per-cluster unit sequence (UnitIter)."""
+    total = (T - dp_tiles) * KT
+    base, extra = total // P, total % P
+    out = [(t, 0, KT, "full") for t in range(cluster, dp_tiles, P)]
+    it = cluster * base + min(cluster, extra)
+    end = it + base + (1 if cluster < extra else 0)
+    while it < end:
+        rel, k0 = divmod(it, KT)
+        seg_end = min((rel + 1) * KT, end)
+        k1 = k0 + seg_end - it
+        kind = "full" if (k0 == 0 and k1 == KT) else ("head" if k0 == 0 else "tail")
+        out.append((dp_tiles + rel, k0, k1, kind))
+        it = seg_end
+    return out
+
+
+@pytest.mark.parametrize("T,P,KT", [(256, 76, 64), (1024, 76, 128), (344, 76, 64), (81, 76, 5), (170, 152, 8),
+                                    (77, 76, 1), (151, 76, 3), (100, 7, 13)])
+def test_stream_k_schedule_covers_every_k_iteration_once(T, P, KT):
+    dp_tiles = (T // P - 1) * P
+    cover = {}
+    for c in range(P):
+        units = sk_units(T, P, KT, dp_tiles, c)
+        assert sum(1 for u in units if u[3] == "tail") <= 1           # one partial slot per cluster
+        tails = [i for i, u in enumerate(units) if u[3] == "tail"]
+        heads = [i for i, u in enumerate(units) if u[3] == "head"]
+        n_dp = sum(1 for u in units if u[0] < dp_tiles)
+        assert not tails or tails == [n_dp]                           # the tail segment comes first
+        assert not heads or heads == [len(units) - 1]                 # the head segment comes last
+        for (t, k0, k1, kind) in units:
+            assert 0 <= t < T and 0 <= k0 < k1 <= KT
+            for k in range(k0, k1):
+                assert (t, k) not in cover
+                cover[(t, k)] = (c, kind)
+            if kind == "head":                                        # the rest is the next cluster's tail
+                nxt = sk_units(T, P, KT, dp_tiles, c + 1)
+                assert (t, k1, KT, "tail") in nxt
+            if kind == "tail":
+                assert k1 == KT and c > 0
+    assert len(cover) == T * KT

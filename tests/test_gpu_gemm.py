@@ -285,3 +285,47 @@ def test_bounded_wait_expires_and_reports(handles, cfg):
     assert g.status() == G.GEMM_OK       # the word was cleared
     g.close()
     _run_check(handles[cfg], W.problem(256, 256, 1024, seed=22))
+
+
+# ------------------------------------------------------------------------------ stream-K tail
+SK_CASES = {
+    0: dict(M=2126, N=2460, K=300, dtype_out="f16", bias=True),               # 17 x 10 = 170 tiles > 152
+    1: dict(M=2274, N=2300, K=700, dtype_out="bf16", dtype_in="bf16"),       # 9 x 9 = 81 tiles > 76
+    2: dict(M=1650, N=1640, K=200, dtype_out="f32", alpha=0.5, beta=1.0),   # 13 x 13 = 169 > 152
+    3: dict(M=2250, N=1250, K=450, dtype_out="f32", layoutB="col"),         # 9 x 10 = 90 > 76
+}
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+def test_stream_k_tail_parity(cfg):
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    c = dict(SK_CASES[cfg])
+    w = W.problem(c.pop("M"), c.pop("N"), c.pop("K"), seed=100 + cfg, **c)
+    st, plan = G.gemm_plan(w.M, w.N, w.K, w.K if w.layoutA == "row" else w.M, w.N if w.layoutB == "row" else w.K,
+                           w.N, G.DTYPE_CODES[w.dtype_in], G.DTYPE_CODES[w.dtype_out], G.LAYOUT_CODES[w.layoutA],
+                           G.LAYOUT_CODES[w.layoutB], w.beta, torch.cuda.get_device_properties(0).multi_processor_count,
+                           0, cfg, 1)
+    assert st == G.GEMM_OK and plan.stream_k == 1
+    with G.Gemm(0, config=cfg, stream_k=1, sync_check=1) as g:
+        for _ in range(2):                          # the second launch runs with the next epoch
+            _run_check(g, w)
+
+
+def test_stream_k_matches_data_parallel_on_integers():
+    """Split tiles add two partial sums; with small integers both schedules are exact and equal."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    M, N, K = 2304, 2304, 1280                      # 81 tiles of 256 x 256 on 76 clusters
+    A = W.small_ints(M, K, "f16", 5).cuda()
+    B = W.small_ints(K, N, "f16", 6).cuda()
+    outs = []
+    for sk in (0, 1):
+        C = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        with G.Gemm(0, config=1, stream_k=sk, sync_check=1) as g:
+            g.run(A, B, C)
+        outs.append(C)
+    torch.cuda.synchronize()
+    ref = (A.cpu().to(torch.int64) @ B.cpu().to(torch.int64)).to(torch.float32)
+    assert torch.equal(outs[0].cpu(), ref)
+    assert torch.equal(outs[1].cpu(), ref)
