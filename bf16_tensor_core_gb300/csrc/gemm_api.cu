@@ -1,6 +1,6 @@
 // Host side of the C ABI declared in include/gemm.h: handle, validation, planning, tensor-map
-// cache, operand repack, dispatch and error reporting.  No device code lives here except what
-// the kernel headers declare.
+// cache, operand repack, stream-K buffers, dispatch and error reporting.  The only device code
+// here is the file-scope scratch of gemm_run_noalloc.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -11,6 +11,8 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -23,21 +25,29 @@ using namespace gb300;
 namespace {
 
 // ---------------------------------------------------------------- configuration table
-template <int CG, int BN, int ST>
+template <int CG, int PAIRS, int BN, int ST, int BK>
 constexpr ConfigDesc make_desc(int id) {
-    return ConfigDesc{id, CG, BN, ST, TileConfig<CG, BN, ST>::kSmemBytes, TileConfig<CG, BN, ST>::kThreads};
+    return ConfigDesc{id, CG, PAIRS, BN, BK, ST, TileConfig<CG, BN, ST, BK>::kSmemBytes,
+                      TileConfig<CG, BN, ST, BK>::kThreads};
 }
 
 const ConfigDesc kConfigs[kNumConfigs] = {
-    make_desc<1, 256, 4>(0),  // 1 SM, 128 x 256 tile
-    make_desc<2, 256, 6>(1),  // 2-SM cluster, 256 x 256 tile
-    make_desc<1, 128, 6>(2),  // 1 SM, 128 x 128 tile
-    make_desc<2, 128, 8>(3),  // 2-SM cluster, 256 x 128 tile
+    make_desc<1, 1, 256, 4, 64>(0),   // 1 SM, 128 x 256 tile
+    make_desc<2, 1, 256, 6, 64>(1),   // 2-SM pair, 256 x 256 tile
+    make_desc<1, 1, 128, 6, 64>(2),   // 1 SM, 128 x 128 tile
+    make_desc<2, 1, 128, 8, 64>(3),   // 2-SM pair, 256 x 128 tile
+    make_desc<2, 2, 256, 6, 64>(4),   // two 2-SM pairs sharing B by multicast, 512 x 256 tile
+    make_desc<2, 1, 256, 3, 128>(5),  // 2-SM pair, 256 x 256 tile, 128-wide K stages
+    make_desc<2, 2, 256, 3, 128>(6),  // two pairs sharing B, 512 x 256 tile, 128-wide K stages
+    make_desc<2, 1, 512, 4, 64>(7),   // 2-SM pair, 256 x 512 tile (two N=256 MMAs per K step)
 };
 
 // Relative tensor-core efficiency assumed per config when choosing one for a shape (larger
-// tiles amortise the per-stage cost and need less L2 bandwidth per flop).
-const double kConfigEfficiency[kNumConfigs] = {0.94, 1.00, 0.70, 0.65};
+// tiles need fewer loads per flop; the mainloop is bound by the TMA load rate per SM).
+const double kConfigEfficiency[kNumConfigs] = {0.85, 0.95, 0.70, 0.62, 0.94, 1.00, 0.96, 0.88};
+
+int cluster_ctas(const ConfigDesc& d) { return d.cta_group * d.pairs; }
+int block_m(const ConfigDesc& d) { return 128 * cluster_ctas(d); }
 
 enum FaultSite { FAULT_NONE = 0, FAULT_OPTIN = 1, FAULT_TMAP = 2, FAULT_LAUNCH = 4, FAULT_ALLOC = 8 };
 
@@ -55,6 +65,68 @@ int read_fault_env() {
 }
 
 int elt_bytes(int dt) { return dt == GEMM_F32 ? 4 : 2; }
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+// What a device offers each config: SM count, co-resident clusters, the tensor-map encoder.
+struct DevInfo {
+    int num_sms = 0;
+    int slots[kNumConfigs] = {};                 // clusters of each config that fit at once
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+};
+
+// Opt every kernel into its shared memory (never inside a capture window), count the clusters
+// of each config that fit, resolve the encoder.  `dev` must be current.
+gemm_status_t query_device(int dev, bool force_optin_failure, DevInfo* info) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&info->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED;
+    for (int c = 0; c < kNumConfigs; ++c) {
+        const ConfigDesc* d = config_desc(c);
+        for (int outk = 0; outk < kNumOut; ++outk) {
+            cudaError_t ea = force_optin_failure ? cudaErrorInvalidValue
+                             : cudaFuncSetAttribute(config_kernel(c, outk), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    d->smem_bytes);
+            if (ea != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_CUDA;
+            }
+        }
+        const int csize = cluster_ctas(*d);
+        int n = info->num_sms;
+        if (csize > 1) {
+            cudaLaunchConfig_t lc = {};
+            lc.gridDim = dim3((unsigned)(info->num_sms - info->num_sms % csize), 1, 1);
+            lc.blockDim = dim3((unsigned)d->threads, 1, 1);
+            lc.dynamicSmemBytes = (size_t)d->smem_bytes;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)csize;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            lc.attrs = attr;
+            lc.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, config_kernel(c, OUT_F16), &lc) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+        }
+        info->slots[c] = n;
+    }
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    info->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return GEMM_OK;
+}
 
 struct TmapKey {
     const void* ptr;
@@ -76,14 +148,12 @@ struct TmapEntry {
 
 struct gemm_ctx {
     int device = 0;
-    int num_sms = 0;
-    int max_clusters[kNumConfigs] = {0, 0, 0, 0};
+    DevInfo dev;
     gemm_options_t opt{};
     unsigned long long* d_status = nullptr;
     void* ws = nullptr;
     size_t ws_bytes = 0;
     std::string err;
-    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     std::vector<TmapEntry> cache;
     size_t cache_next = 0;
     int faults = FAULT_NONE;
@@ -105,12 +175,12 @@ gemm_status_t cuda_fail(gemm_handle_t h, const char* what, cudaError_t e) {
     return fail(h, GEMM_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
-int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
-
-// Pure host planning: validation, config choice, grid and workspace.
+// Pure host planning: validation, config choice, grid, stream-K split and workspace.
+//   slots[c]     clusters of config c that fit on the device at once
+//   cluster_cap  optional cap on launched clusters (0 = none)
 gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int din, int dout,
-                        int la, int lb, float beta, int num_sms, int max_clusters, int config, int stream_k,
-                        int cluster_cap, gemm_plan_t* out, std::string* err) {
+                        int la, int lb, float beta, const int* slots, int config, int stream_k, int cluster_cap,
+                        gemm_plan_t* out, std::string* err) {
     std::memset(out, 0, sizeof(*out));
     out->config = -1;
     if (M < 0 || N < 0 || K < 0) { *err = "M, N and K must be >= 0"; return GEMM_ERR_INVALID_ARG; }
@@ -124,49 +194,46 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     if (lda < std::max<int64_t>(1, a_inner)) { *err = "lda too small"; return GEMM_ERR_INVALID_ARG; }
     if (ldb < std::max<int64_t>(1, b_inner)) { *err = "ldb too small"; return GEMM_ERR_INVALID_ARG; }
     if (ldc < std::max<int64_t>(1, N)) { *err = "ldc too small"; return GEMM_ERR_INVALID_ARG; }
-    if (num_sms <= 0) { *err = "num_sms must be > 0"; return GEMM_ERR_INVALID_ARG; }
     if (config < -1 || config >= kNumConfigs) { *err = "no such config"; return GEMM_ERR_UNSUPPORTED; }
     if (stream_k < -1 || stream_k > 1) { *err = "stream_k must be -1, 0 or 1"; return GEMM_ERR_INVALID_ARG; }
-    if (max_clusters <= 0) max_clusters = num_sms / 2;
     if (M == 0 || N == 0) { out->kernels = 0; return GEMM_OK; }
     if (K == 0) { out->kernels = 1; return GEMM_OK; }
 
-    auto slots_of = [&](const ConfigDesc& d) {
-        int slots = d.cta_group == 2 ? max_clusters : num_sms;
-        if (cluster_cap > 0) slots = std::min(slots, cluster_cap);
-        return slots;
+    auto slots_of = [&](int c) {
+        int s = slots[c];
+        if (cluster_cap > 0) s = std::min(s, cluster_cap);
+        return s;
     };
     int best = config;
     if (best < 0) {
         double best_cost = 1e300;
         for (int c = 0; c < kNumConfigs; ++c) {
             const ConfigDesc& d = kConfigs[c];
-            const int slots = slots_of(d);
-            if (slots <= 0) continue;
-            const int64_t bm = 128 * d.cta_group;
+            const int s = slots_of(c);
+            if (s <= 0) continue;
+            const int64_t bm = block_m(d);
             const int64_t tiles = ((M + bm - 1) / bm) * ((N + d.block_n - 1) / d.block_n);
             // Whole waves, or (with the stream-K tail) the exact share plus a small fix-up cost.
-            double waves = (double)((tiles + slots - 1) / slots);
-            if (stream_k != 0 && tiles > slots && tiles % slots != 0)
-                waves = std::min(waves, (double)tiles / slots + 0.08);
-            const double cost = waves * (double)(bm * d.block_n) / (d.cta_group * kConfigEfficiency[c]);
+            double waves = (double)((tiles + s - 1) / s);
+            if (stream_k != 0 && tiles > s && tiles % s != 0) waves = std::min(waves, (double)tiles / s + 0.08);
+            const double cost = waves * (double)(bm * d.block_n) / (cluster_ctas(d) * kConfigEfficiency[c]);
             if (cost < best_cost * (1.0 - 1e-9)) { best_cost = cost; best = c; }
         }
+        if (best < 0) { *err = "no config fits on this device"; return GEMM_ERR_UNSUPPORTED; }
     }
     const ConfigDesc& d = kConfigs[best];
-    if (d.cta_group == 2 && max_clusters <= 0) { *err = "2-SM clusters do not fit"; return GEMM_ERR_UNSUPPORTED; }
+    const int P = slots_of(best);
+    if (P <= 0) { *err = "clusters of this config do not fit"; return GEMM_ERR_UNSUPPORTED; }
     out->config = best;
     out->cta_group = d.cta_group;
-    out->block_m = 128 * d.cta_group;
+    out->block_m = block_m(d);
     out->block_n = d.block_n;
-    out->block_k = 64;
+    out->block_k = d.block_k;
     out->stages = d.stages;
     out->tiles_m = (int)((M + out->block_m - 1) / out->block_m);
     out->tiles_n = (int)((N + out->block_n - 1) / out->block_n);
     const int64_t tiles = (int64_t)out->tiles_m * out->tiles_n;
-    const int slots = slots_of(d);
-    if (slots <= 0) { *err = "no cluster fits"; return GEMM_ERR_UNSUPPORTED; }
-    out->clusters = (int)std::min<int64_t>(tiles, slots);
+    out->clusters = (int)std::min<int64_t>(tiles, P);
     out->raster_group = std::min(out->tiles_m, 8);
     out->tma_store = (beta == 0.0f && (ldc * elt_bytes(dout)) % 16 == 0) ? 1 : 0;
     out->repack_a = (lda * 2) % 16 != 0;
@@ -175,13 +242,13 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     if (out->repack_a) ws += round_up((la == GEMM_ROW ? M : K) * round_up(a_inner, 8) * 2, 256);
     if (out->repack_b) ws += round_up((lb == GEMM_ROW ? K : N) * round_up(b_inner, 8) * 2, 256);
     // Stream-K tail: worthwhile when the last wave would leave more than 15% of the clusters idle.
-    const int P = out->clusters;
-    if (stream_k != 0 && tiles > P && tiles % P != 0) {
-        const double waves = (double)tiles / P;
+    const int C = out->clusters;
+    if (stream_k != 0 && tiles > C && tiles % C != 0) {
+        const double waves = (double)tiles / C;
         if (stream_k == 1 || std::ceil(waves) - waves > 0.15) {
             out->stream_k = 1;
-            out->dp_tiles = (int)((tiles / P - 1) * P);
-            out->sk_partial_bytes = round_up((int64_t)P * d.cta_group * 128 * d.block_n * 4, 256);
+            out->dp_tiles = (int)((tiles / C - 1) * C);
+            out->sk_partial_bytes = round_up((int64_t)C * cluster_ctas(d) * 128 * d.block_n * 4, 256);
         }
     }
     out->workspace_bytes = ws + out->sk_partial_bytes;
@@ -189,26 +256,176 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     return GEMM_OK;
 }
 
-// Tensor map of a 2-D row-major array: dim0 contiguous, dim1 rows of `stride_bytes`.
-gemm_status_t get_tmap(gemm_handle_t h, const void* ptr, CUtensorMapDataType dt, uint64_t dim0, uint64_t dim1,
-                       uint64_t stride_bytes, uint32_t box0, uint32_t box1, CUtensorMap* out) {
+uint32_t make_idesc(int din, int a_mn, int b_mn, int mma_m, int mma_n) {
+    // tcgen05 instruction descriptor, kind::f16: D f32 (bits 4-5 = 1); A/B format 0 f16, 1 bf16
+    // (bits 7-9, 10-12); A/B major 0 K, 1 MN (bits 15, 16); N >> 3 (bits 17-22); M >> 4 (24-28).
+    const uint32_t fmt = din == GEMM_BF16 ? 1u : 0u;
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(mma_n >> 3) << 17) | ((uint32_t)(mma_m >> 4) << 24);
+}
+
+// Tensor-map encoder used by the launch: cached per handle, or direct.
+using TmapFn = std::function<gemm_status_t(const void*, CUtensorMapDataType, uint64_t, uint64_t, uint64_t, uint32_t,
+                                           uint32_t, CUtensorMap*)>;
+
+gemm_status_t encode_tmap(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* ptr, CUtensorMapDataType dt,
+                          uint64_t dim0, uint64_t dim1, uint64_t stride_bytes, uint32_t box0, uint32_t box1,
+                          CUtensorMap* out) {
+    const cuuint64_t dims[2] = {dim0, dim1};
+    const cuuint64_t strides[1] = {stride_bytes};
+    const cuuint32_t box[2] = {box0, box1};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(out, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Everything the GEMM launch needs once operands are TMA-addressable.
+struct LaunchArgs {
+    const gemm_plan_t* plan;
+    int64_t M, N, K;
+    const void* A;
+    int64_t lda;
+    const void* B;
+    int64_t ldb;
+    void* C;
+    int64_t ldc;
+    int din, dout, la, lb;
+    float alpha, beta;
+    const void* bias;
+    unsigned long long* status;
+    unsigned long long timeout_ns;
+    long long debug_skip_stage;
+    int raster_group;           // 0 = the plan's
+    float* sk_partials;
+    unsigned* sk_flags;
+    unsigned epoch;
+    cudaStream_t stream;
+};
+
+// Encode the tensor maps, fill the kernel parameters and launch the planned config.
+gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char** what, cudaError_t* cuda_err) {
+    const gemm_plan_t& plan = *a.plan;
+    const ConfigDesc* d = config_desc(plan.config);
+    const CUtensorMapDataType tin =
+        a.din == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    // B columns one TMA box covers: a CTA's share of the tile, split once more between the
+    // pairs of a multicast cluster.
+    const int mma_n = std::min(d->block_n, 256);
+    const uint32_t b_box_n = (uint32_t)(mma_n / d->cta_group / d->pairs);
+    CUtensorMap ta, tb, tc;
+    std::memset(&tc, 0, sizeof(tc));
+    *what = "tensor map of A";
+    const uint32_t bk = (uint32_t)d->block_k;
+    gemm_status_t st = a.la == GEMM_ROW  // K-major: box {64 K, 128 M}; M-major: box {64 M, BK K}
+                           ? tmap(a.A, tin, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.lda * 2, 64, 128, &ta)
+                           : tmap(a.A, tin, (uint64_t)a.M, (uint64_t)a.K, (uint64_t)a.lda * 2, 64, bk, &ta);
+    if (st != GEMM_OK) return st;
+    *what = "tensor map of B";
+    st = a.lb == GEMM_ROW  // N-major: box {64 N, BK K}; K-major: box {64 K, b_box_n N}
+             ? tmap(a.B, tin, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.ldb * 2, 64, bk, &tb)
+             : tmap(a.B, tin, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.ldb * 2, 64, b_box_n, &tb);
+    if (st != GEMM_OK) return st;
+    const int eb = elt_bytes(a.dout);
+    const bool c_aligned = (reinterpret_cast<uintptr_t>(a.C) % 16) == 0 && (a.ldc * eb) % 16 == 0;
+    const int use_tma_store = (plan.tma_store && c_aligned) ? 1 : 0;
+    if (use_tma_store) {
+        *what = "tensor map of C";
+        const CUtensorMapDataType tcd = a.dout == GEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                        : a.dout == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const uint32_t box0 = a.dout == GEMM_F32 ? 32 : 64;   // one 128-byte line per row
+        st = tmap(a.C, tcd, (uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.ldc * eb, box0, 32, &tc);
+        if (st != GEMM_OK) return st;
+    }
+    KernelParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.M = (int)a.M;
+    p.N = (int)a.N;
+    p.K = (int)a.K;
+    p.tiles_m = plan.tiles_m;
+    p.tiles_n = plan.tiles_n;
+    p.num_tiles = plan.tiles_m * plan.tiles_n;
+    p.k_tiles = (int)((a.K + d->block_k - 1) / d->block_k);
+    p.raster_group = a.raster_group > 0 ? std::min(a.raster_group, plan.tiles_m) : plan.raster_group;
+    p.a_mn = a.la == GEMM_COL ? 1 : 0;
+    p.b_mn = a.lb == GEMM_ROW ? 1 : 0;
+    p.idesc = make_idesc(a.din, p.a_mn, p.b_mn, 128 * d->cta_group, mma_n);
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.bias = a.bias;
+    p.alpha = a.alpha;
+    p.beta = a.beta;
+    p.use_tma_store = use_tma_store;
+    p.c_vec_ok = c_aligned ? 1 : 0;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    p.debug_skip_stage = a.debug_skip_stage;
+    if (plan.stream_k) {
+        const long long sk_total = (long long)(p.num_tiles - plan.dp_tiles) * p.k_tiles;
+        p.sk_enabled = 1;
+        p.dp_tiles = plan.dp_tiles;
+        p.sk_base = sk_total / plan.clusters;
+        p.sk_extra = (int)(sk_total % plan.clusters);
+        p.sk_partials = a.sk_partials;
+        p.sk_flags = a.sk_flags;
+        p.epoch = a.epoch;
+    }
+    *what = "GEMM kernel launch";
+    cudaError_t e = config_launch(plan.config, a.dout == GEMM_F32 ? OUT_F32 : (a.dout == GEMM_F16 ? OUT_F16 : OUT_BF16),
+                                  plan.clusters * cluster_ctas(*d), a.stream, ta, tb, tc, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *cuda_err = e;
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+// Repack the operands whose byte pitch TMA cannot use into `ws` (16-byte pitch).  Updates the
+// operand pointers and leading dimensions; counts launches.
+cudaError_t repack_operands(const gemm_plan_t& plan, int64_t M, int64_t N, int64_t K, int la, int lb, void* ws,
+                            const void** A, int64_t* lda, const void** B, int64_t* ldb, cudaStream_t s,
+                            int64_t* launches, const char** what) {
+    char* w = static_cast<char*>(ws);
+    if (plan.repack_a) {
+        const int64_t rows = la == GEMM_ROW ? M : K;
+        const int64_t cols = la == GEMM_ROW ? K : M;
+        const int64_t ld = round_up(cols, 8);
+        *what = "repack of A";
+        cudaError_t e = launch_repack_u16(*A, *lda, w, ld, rows, cols, s);
+        if (e != cudaSuccess) return e;
+        *A = w;
+        *lda = ld;
+        w += round_up(rows * ld * 2, 256);
+        ++*launches;
+    }
+    if (plan.repack_b) {
+        const int64_t rows = lb == GEMM_ROW ? K : N;
+        const int64_t cols = lb == GEMM_ROW ? N : K;
+        const int64_t ld = round_up(cols, 8);
+        *what = "repack of B";
+        cudaError_t e = launch_repack_u16(*B, *ldb, w, ld, rows, cols, s);
+        if (e != cudaSuccess) return e;
+        *B = w;
+        *ldb = ld;
+        ++*launches;
+    }
+    return cudaSuccess;
+}
+
+gemm_status_t get_tmap_cached(gemm_handle_t h, const void* ptr, CUtensorMapDataType dt, uint64_t dim0, uint64_t dim1,
+                              uint64_t stride_bytes, uint32_t box0, uint32_t box1, CUtensorMap* out) {
     TmapKey key{ptr, (int)dt, dim0, dim1, stride_bytes, box0, box1};
     for (const TmapEntry& e : h->cache)
         if (e.key == key) { *out = e.map; return GEMM_OK; }
     if (h->faults & FAULT_TMAP) return fail(h, GEMM_ERR_CUDA, "cuTensorMapEncodeTiled: forced failure (GEMM_TEST_FAIL=tmap)");
     CUtensorMap m;
-    const cuuint64_t dims[2] = {dim0, dim1};
-    const cuuint64_t strides[1] = {stride_bytes};
-    const cuuint32_t box[2] = {box0, box1};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = h->encode(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
+    if (encode_tmap(h->dev.encode, ptr, dt, dim0, dim1, stride_bytes, box0, box1, &m) != GEMM_OK) {
         char buf[256];
-        std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed (%d) dims {%llu,%llu} stride %llu box {%u,%u}",
-                      (int)r, (unsigned long long)dim0, (unsigned long long)dim1, (unsigned long long)stride_bytes,
-                      box0, box1);
+        std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed: dims {%llu,%llu} stride %llu box {%u,%u}",
+                      (unsigned long long)dim0, (unsigned long long)dim1, (unsigned long long)stride_bytes, box0, box1);
         return fail(h, GEMM_ERR_CUDA, buf);
     }
     const size_t kCacheSize = 32;
@@ -222,18 +439,18 @@ gemm_status_t get_tmap(gemm_handle_t h, const void* ptr, CUtensorMapDataType dt,
     return GEMM_OK;
 }
 
-gemm_status_t ensure_workspace(gemm_handle_t h, size_t bytes) {
-    if (bytes <= h->ws_bytes) return GEMM_OK;
-    if (h->faults & FAULT_ALLOC) return fail(h, GEMM_ERR_OOM, "workspace allocation: forced failure (GEMM_TEST_FAIL=alloc)");
-    if (h->ws) { cudaFree(h->ws); h->ws = nullptr; h->ws_bytes = 0; }
+gemm_status_t ensure_buffer(gemm_handle_t h, void** buf, size_t* have, size_t bytes, const char* what) {
+    if (bytes <= *have) return GEMM_OK;
+    if (h->faults & FAULT_ALLOC) return fail(h, GEMM_ERR_OOM, std::string(what) + ": forced failure (GEMM_TEST_FAIL=alloc)");
+    if (*buf) { cudaFree(*buf); *buf = nullptr; *have = 0; }
     void* p = nullptr;
     cudaError_t e = cudaMalloc(&p, bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return fail(h, GEMM_ERR_OOM, std::string("workspace cudaMalloc: ") + cudaGetErrorString(e));
+        return fail(h, GEMM_ERR_OOM, std::string(what) + " cudaMalloc: " + cudaGetErrorString(e));
     }
-    h->ws = p;
-    h->ws_bytes = bytes;
+    *buf = p;
+    *have = bytes;
     return GEMM_OK;
 }
 
@@ -250,14 +467,6 @@ struct DeviceGuard {
     }
 };
 
-uint32_t make_idesc(int din, int a_mn, int b_mn, int mma_m, int mma_n) {
-    // tcgen05 instruction descriptor, kind::f16: D f32 (bits 4-5 = 1); A/B format 0 f16, 1 bf16
-    // (bits 7-9, 10-12); A/B major 0 K, 1 MN (bits 15, 16); N >> 3 (bits 17-22); M >> 4 (24-28).
-    const uint32_t fmt = din == GEMM_BF16 ? 1u : 0u;
-    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
-           ((uint32_t)(mma_n >> 3) << 17) | ((uint32_t)(mma_m >> 4) << 24);
-}
-
 }  // namespace
 
 namespace gb300 {
@@ -270,6 +479,10 @@ const void* config_kernel(int id, int out) {
         case 1: return cfg1_kernel(out);
         case 2: return cfg2_kernel(out);
         case 3: return cfg3_kernel(out);
+        case 4: return cfg4_kernel(out);
+        case 5: return cfg5_kernel(out);
+        case 6: return cfg6_kernel(out);
+        case 7: return cfg7_kernel(out);
         default: return nullptr;
     }
 }
@@ -285,7 +498,7 @@ cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, c
     lc.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)d->cta_group;
+    attr[0].val.clusterDim.x = (unsigned)cluster_ctas(*d);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
@@ -295,6 +508,10 @@ cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, c
         case 1: return cfg1_launch(out, lc, a, b, c, p);
         case 2: return cfg2_launch(out, lc, a, b, c, p);
         case 3: return cfg3_launch(out, lc, a, b, c, p);
+        case 4: return cfg4_launch(out, lc, a, b, c, p);
+        case 5: return cfg5_launch(out, lc, a, b, c, p);
+        case 6: return cfg6_launch(out, lc, a, b, c, p);
+        case 7: return cfg7_launch(out, lc, a, b, c, p);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -337,12 +554,13 @@ gemm_status_t gemm_config_info(int id, gemm_config_info_t* out) {
     if (!d) return GEMM_ERR_UNSUPPORTED;
     out->id = d->id;
     out->cta_group = d->cta_group;
-    out->block_m = 128 * d->cta_group;
+    out->block_m = block_m(*d);
     out->block_n = d->block_n;
-    out->block_k = 64;
+    out->block_k = d->block_k;
     out->stages = d->stages;
     out->smem_bytes = d->smem_bytes;
     out->threads = d->threads;
+    out->pairs = d->pairs;
     return GEMM_OK;
 }
 
@@ -350,9 +568,16 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
                         gemm_dtype_t dtype_in, gemm_dtype_t dtype_out, gemm_layout_t layoutA, gemm_layout_t layoutB,
                         float beta, int num_sms, int max_clusters, int config, int stream_k, gemm_plan_t* out) {
     if (!out) return GEMM_ERR_INVALID_ARG;
+    if (num_sms <= 0) return GEMM_ERR_INVALID_ARG;
+    if (max_clusters <= 0) max_clusters = num_sms / 2;
+    int slots[kNumConfigs];
+    for (int c = 0; c < kNumConfigs; ++c) {
+        const ConfigDesc& d = kConfigs[c];
+        slots[c] = d.cta_group == 1 ? num_sms : max_clusters / d.pairs;
+    }
     std::string err;
-    return plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, num_sms, max_clusters,
-                     config, stream_k, 0, out, &err);
+    return plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, slots, config, stream_k, 0,
+                     out, &err);
 }
 
 gemm_status_t gemm_create(gemm_handle_t* out, int device, const gemm_options_t* opt) {
@@ -371,13 +596,6 @@ gemm_status_t gemm_create(gemm_handle_t* out, int device, const gemm_options_t* 
     cudaError_t e = cudaGetDeviceCount(&count);
     if (e != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
     if (device < 0 || device >= count) return GEMM_ERR_INVALID_ARG;
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_CUDA;
-    }
-    if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED;
 
     gemm_ctx* h = new (std::nothrow) gemm_ctx();
     if (!h) return GEMM_ERR_OOM;
@@ -385,65 +603,15 @@ gemm_status_t gemm_create(gemm_handle_t* out, int device, const gemm_options_t* 
     h->opt = o;
     h->faults = read_fault_env();
     DeviceGuard guard(device);
-    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
-        cudaGetLastError();
-        delete h;
-        return GEMM_ERR_CUDA;
-    }
-    gemm_status_t st = GEMM_OK;
-    // Opt every kernel into its dynamic shared memory here, never inside a capture window.
-    for (int c = 0; c < kNumConfigs && st == GEMM_OK; ++c) {
-        const ConfigDesc* d = config_desc(c);
-        for (int outk = 0; outk < kNumOut && st == GEMM_OK; ++outk) {
-            const void* fn = config_kernel(c, outk);
-            cudaError_t ea = (h->faults & FAULT_OPTIN) ? cudaErrorInvalidValue
-                             : cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, d->smem_bytes);
-            if (ea != cudaSuccess) {
-                cudaGetLastError();
-                st = GEMM_ERR_CUDA;
-            }
-        }
-        if (st == GEMM_OK) {
-            int nclusters = h->num_sms / d->cta_group;
-            if (d->cta_group == 2) {
-                cudaLaunchConfig_t lc = {};
-                lc.gridDim = dim3((unsigned)(h->num_sms - h->num_sms % 2), 1, 1);
-                lc.blockDim = dim3((unsigned)d->threads, 1, 1);
-                lc.dynamicSmemBytes = (size_t)d->smem_bytes;
-                cudaLaunchAttribute attr[1];
-                attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = 2;
-                attr[0].val.clusterDim.y = 1;
-                attr[0].val.clusterDim.z = 1;
-                lc.attrs = attr;
-                lc.numAttrs = 1;
-                int n = 0;
-                if (cudaOccupancyMaxActiveClusters(&n, config_kernel(c, OUT_F16), &lc) != cudaSuccess) {
-                    cudaGetLastError();
-                    n = 0;
-                }
-                nclusters = n;
-            }
-            h->max_clusters[c] = nclusters;
-        }
-    }
+    gemm_status_t st = query_device(device, (h->faults & FAULT_OPTIN) != 0, &h->dev);
     if (st != GEMM_OK) {
         delete h;
         return st;
     }
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
-        cudaGetLastError();
-        delete h;
-        return GEMM_ERR_CUDA;
-    }
-    h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     e = cudaMalloc(&h->d_status, 64);
     if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 64);
-    // One flag per (cluster, CTA rank, epilogue warp) for the stream-K hand-off.
-    const size_t flag_bytes = (size_t)h->num_sms * 4 * sizeof(unsigned);
+    // One flag per (CTA of the grid, epilogue warp) for the stream-K hand-off.
+    const size_t flag_bytes = (size_t)h->dev.num_sms * 4 * sizeof(unsigned);
     if (e == cudaSuccess) e = cudaMalloc(&h->sk_flags, flag_bytes);
     if (e == cudaSuccess) e = cudaMemset(h->sk_flags, 0, flag_bytes);
     if (e != cudaSuccess) {
@@ -507,8 +675,7 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
     h->err.clear();
     gemm_plan_t plan;
     std::string err;
-    gemm_status_t st = plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, h->num_sms,
-                                 h->opt.config >= 0 ? h->max_clusters[h->opt.config] : h->max_clusters[1],
+    gemm_status_t st = plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, h->dev.slots,
                                  h->opt.config, h->opt.stream_k, h->opt.max_clusters, &plan, &err);
     if (st != GEMM_OK) return fail(h, st, err);
     if (M == 0 || N == 0) return GEMM_OK;
@@ -519,120 +686,42 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
     DeviceGuard guard(h->device);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
+    if (h->faults & FAULT_LAUNCH) return fail(h, GEMM_ERR_CUDA, "kernel launch: forced failure (GEMM_TEST_FAIL=launch)");
 
     if (K == 0) {
-        if (h->faults & FAULT_LAUNCH) return fail(h, GEMM_ERR_CUDA, "kernel launch: forced failure (GEMM_TEST_FAIL=launch)");
-        cudaError_t e = launch_scale_bias(out_kind, C, ldc, bias, beta, M, N, h->num_sms, s);
+        cudaError_t e = launch_scale_bias(out_kind, C, ldc, bias, beta, M, N, h->dev.num_sms, s);
         if (e != cudaSuccess) return cuda_fail(h, "scale/bias kernel launch", e);
         h->launches += 1;
     } else {
-        // Operand repack to a 16-byte pitch where TMA cannot address the caller's layout.
         const void* a_ptr = A;
         const void* b_ptr = B;
         int64_t lda_eff = lda, ldb_eff = ldb;
+        const char* what = "";
         if (plan.repack_a || plan.repack_b) {
-            st = ensure_workspace(h, (size_t)(plan.workspace_bytes - plan.sk_partial_bytes));
+            st = ensure_buffer(h, &h->ws, &h->ws_bytes, (size_t)(plan.workspace_bytes - plan.sk_partial_bytes),
+                               "workspace allocation");
             if (st != GEMM_OK) return st;
-            char* ws = static_cast<char*>(h->ws);
-            if (plan.repack_a) {
-                const int64_t rows = layoutA == GEMM_ROW ? M : K;
-                const int64_t cols = layoutA == GEMM_ROW ? K : M;
-                lda_eff = round_up(cols, 8);
-                cudaError_t e = launch_repack_u16(A, lda, ws, lda_eff, rows, cols, s);
-                if (e != cudaSuccess) return cuda_fail(h, "repack of A", e);
-                a_ptr = ws;
-                ws += round_up(rows * lda_eff * 2, 256);
-                h->launches += 1;
-            }
-            if (plan.repack_b) {
-                const int64_t rows = layoutB == GEMM_ROW ? K : N;
-                const int64_t cols = layoutB == GEMM_ROW ? N : K;
-                ldb_eff = round_up(cols, 8);
-                cudaError_t e = launch_repack_u16(B, ldb, ws, ldb_eff, rows, cols, s);
-                if (e != cudaSuccess) return cuda_fail(h, "repack of B", e);
-                b_ptr = ws;
-                h->launches += 1;
-            }
+            cudaError_t e = repack_operands(plan, M, N, K, layoutA, layoutB, h->ws, &a_ptr, &lda_eff, &b_ptr, &ldb_eff,
+                                            s, &h->launches, &what);
+            if (e != cudaSuccess) return cuda_fail(h, what, e);
         }
-        const ConfigDesc* d = config_desc(plan.config);
-        const CUtensorMapDataType tin =
-            dtype_in == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-        const int bnc = d->block_n / d->cta_group;
-        CUtensorMap ta, tb, tc;
-        std::memset(&tc, 0, sizeof(tc));
-        if (layoutA == GEMM_ROW)  // K-major: box {64 K, 128 M}
-            st = get_tmap(h, a_ptr, tin, (uint64_t)K, (uint64_t)M, (uint64_t)lda_eff * 2, 64, 128, &ta);
-        else  // M-major: box {64 M, 64 K}
-            st = get_tmap(h, a_ptr, tin, (uint64_t)M, (uint64_t)K, (uint64_t)lda_eff * 2, 64, 64, &ta);
-        if (st != GEMM_OK) return st;
-        if (layoutB == GEMM_ROW)  // N-major: box {64 N, 64 K}
-            st = get_tmap(h, b_ptr, tin, (uint64_t)N, (uint64_t)K, (uint64_t)ldb_eff * 2, 64, 64, &tb);
-        else  // K-major: box {64 K, BN/cta_group N}
-            st = get_tmap(h, b_ptr, tin, (uint64_t)K, (uint64_t)N, (uint64_t)ldb_eff * 2, 64, (uint32_t)bnc, &tb);
-        if (st != GEMM_OK) return st;
-        const int eb = elt_bytes(dtype_out);
-        const bool c_aligned = (reinterpret_cast<uintptr_t>(C) % 16) == 0 && (ldc * eb) % 16 == 0;
-        const int use_tma_store = (plan.tma_store && c_aligned) ? 1 : 0;
-        if (use_tma_store) {
-            const CUtensorMapDataType tcd = dtype_out == GEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                            : dtype_out == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-            const uint32_t box0 = dtype_out == GEMM_F32 ? 32 : 64;   // one 128-byte line per row
-            st = get_tmap(h, C, tcd, (uint64_t)N, (uint64_t)M, (uint64_t)ldc * eb, box0, 32, &tc);
-            if (st != GEMM_OK) return st;
-        }
-        KernelParams p;
-        std::memset(&p, 0, sizeof(p));
-        p.M = (int)M;
-        p.N = (int)N;
-        p.K = (int)K;
-        p.tiles_m = plan.tiles_m;
-        p.tiles_n = plan.tiles_n;
-        p.num_tiles = plan.tiles_m * plan.tiles_n;
-        p.k_tiles = (int)((K + 63) / 64);
-        p.raster_group = h->opt.raster_group > 0 ? std::min(h->opt.raster_group, plan.tiles_m) : plan.raster_group;
-        p.a_mn = layoutA == GEMM_COL ? 1 : 0;
-        p.b_mn = layoutB == GEMM_ROW ? 1 : 0;
-        p.idesc = make_idesc(dtype_in, p.a_mn, p.b_mn, 128 * d->cta_group, d->block_n);
-        p.C = C;
-        p.ldc = ldc;
-        p.bias = bias;
-        p.alpha = alpha;
-        p.beta = beta;
-        p.use_tma_store = use_tma_store;
-        p.c_vec_ok = c_aligned ? 1 : 0;
-        p.status = h->d_status;
-        p.timeout_ns = (unsigned long long)h->opt.timeout_ms * 1000000ull;
-        p.debug_skip_stage = h->opt.debug_skip_stage;
-        const int clusters = plan.clusters;
         if (plan.stream_k) {
-            if ((size_t)plan.sk_partial_bytes > h->sk_part_bytes) {
-                if (h->faults & FAULT_ALLOC)
-                    return fail(h, GEMM_ERR_OOM, "stream-K partials: forced failure (GEMM_TEST_FAIL=alloc)");
-                if (h->sk_part) { cudaFree(h->sk_part); h->sk_part = nullptr; h->sk_part_bytes = 0; }
-                cudaError_t ea = cudaMalloc(reinterpret_cast<void**>(&h->sk_part), (size_t)plan.sk_partial_bytes);
-                if (ea != cudaSuccess) {
-                    cudaGetLastError();
-                    return fail(h, GEMM_ERR_OOM, std::string("stream-K partials cudaMalloc: ") + cudaGetErrorString(ea));
-                }
-                h->sk_part_bytes = (size_t)plan.sk_partial_bytes;
-            }
+            void* part = h->sk_part;
+            st = ensure_buffer(h, &part, &h->sk_part_bytes, (size_t)plan.sk_partial_bytes, "stream-K partials");
+            h->sk_part = static_cast<float*>(part);
+            if (st != GEMM_OK) return st;
             if (++h->epoch == 0) ++h->epoch;
-            const long long sk_total = (long long)(p.num_tiles - plan.dp_tiles) * p.k_tiles;
-            p.sk_enabled = 1;
-            p.dp_tiles = plan.dp_tiles;
-            p.sk_base = sk_total / clusters;
-            p.sk_extra = (int)(sk_total % clusters);
-            p.sk_partials = h->sk_part;
-            p.sk_flags = h->sk_flags;
-            p.epoch = h->epoch;
         }
-        if (h->faults & FAULT_LAUNCH) return fail(h, GEMM_ERR_CUDA, "kernel launch: forced failure (GEMM_TEST_FAIL=launch)");
-        cudaError_t e = config_launch(plan.config, out_kind, clusters * d->cta_group, s, ta, tb, tc, p);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return cuda_fail(h, "GEMM kernel launch", e);
-        }
+        LaunchArgs la{&plan, M, N, K, a_ptr, lda_eff, b_ptr, ldb_eff, C, ldc, dtype_in, dtype_out, layoutA, layoutB,
+                      alpha, beta, bias, h->d_status, (unsigned long long)h->opt.timeout_ms * 1000000ull,
+                      h->opt.debug_skip_stage, h->opt.raster_group, h->sk_part, h->sk_flags, h->epoch, s};
+        TmapFn tmap = [h](const void* ptr, CUtensorMapDataType dt, uint64_t d0, uint64_t d1, uint64_t stride,
+                          uint32_t b0, uint32_t b1, CUtensorMap* m) {
+            return get_tmap_cached(h, ptr, dt, d0, d1, stride, b0, b1, m);
+        };
+        cudaError_t ce = cudaSuccess;
+        st = launch_planned(la, tmap, &what, &ce);
+        if (st != GEMM_OK) return ce != cudaSuccess ? cuda_fail(h, what, ce) : st;
         h->launches += 1;
     }
     if (h->opt.sync_check) return gemm_get_device_status(h, stream);
@@ -650,10 +739,8 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
 // handle-owned workspace that gemm_run grows with cudaMalloc.  Host code cannot use the array's
 // name as a device address: per device, the first call looks the address up with
 // cudaGetSymbolAddress (with that device current) and every launch receives that pointer.
+// This entry point never uses the stream-K schedule, which needs partial buffers.
 // ============================================================================================
-#include <functional>
-#include <mutex>
-
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GEMM_NOALLOC_SCRATCH_BYTES];
@@ -664,11 +751,9 @@ constexpr int kNoallocMaxDevices = 64;
 struct NoallocDevice {
     std::once_flag once;
     gemm_status_t setup_status = GEMM_ERR_CUDA;
-    int num_sms = 0;
-    int max_clusters[kNumConfigs] = {0, 0, 0, 0};
+    DevInfo info;
     void* scratch = nullptr;                 // device address of g_noalloc_scratch
     unsigned long long* status = nullptr;    // device address of g_noalloc_status
-    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
 };
 
 NoallocDevice g_noalloc_dev[kNoallocMaxDevices];
@@ -676,57 +761,8 @@ NoallocDevice g_noalloc_dev[kNoallocMaxDevices];
 // One-time set-up on the current device `dev`: shared-memory opt-in, occupancy, the tensor-map
 // encoder and the device addresses of the file-scope scratch and status word.
 void noalloc_setup(int dev, NoallocDevice& nd) {
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&nd.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-        cudaGetLastError();
-        nd.setup_status = GEMM_ERR_CUDA;
-        return;
-    }
-    if (major != 10 || minor != 3) {
-        nd.setup_status = GEMM_ERR_UNSUPPORTED;
-        return;
-    }
-    for (int c = 0; c < kNumConfigs; ++c) {
-        const ConfigDesc* d = config_desc(c);
-        for (int outk = 0; outk < kNumOut; ++outk) {
-            if (cudaFuncSetAttribute(config_kernel(c, outk), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     d->smem_bytes) != cudaSuccess) {
-                cudaGetLastError();
-                nd.setup_status = GEMM_ERR_CUDA;
-                return;
-            }
-        }
-        int n = nd.num_sms / d->cta_group;
-        if (d->cta_group == 2) {
-            cudaLaunchConfig_t lc = {};
-            lc.gridDim = dim3((unsigned)(nd.num_sms - nd.num_sms % 2), 1, 1);
-            lc.blockDim = dim3((unsigned)d->threads, 1, 1);
-            lc.dynamicSmemBytes = (size_t)d->smem_bytes;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            lc.attrs = attr;
-            lc.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, config_kernel(c, OUT_F16), &lc) != cudaSuccess) {
-                cudaGetLastError();
-                n = 0;
-            }
-        }
-        nd.max_clusters[c] = n;
-    }
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn) {
-        cudaGetLastError();
-        nd.setup_status = GEMM_ERR_CUDA;
-        return;
-    }
-    nd.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    nd.setup_status = query_device(dev, false, &nd.info);
+    if (nd.setup_status != GEMM_OK) return;
     if (cudaGetSymbolAddress(&nd.scratch, g_noalloc_scratch) != cudaSuccess || !nd.scratch ||
         cudaGetSymbolAddress(reinterpret_cast<void**>(&nd.status), g_noalloc_status) != cudaSuccess ||
         !nd.status) {
@@ -742,18 +778,6 @@ void noalloc_setup(int dev, NoallocDevice& nd) {
         return;
     }
     nd.setup_status = GEMM_OK;
-}
-
-gemm_status_t noalloc_tmap(const NoallocDevice& nd, const void* ptr, CUtensorMapDataType dt, uint64_t dim0,
-                           uint64_t dim1, uint64_t stride_bytes, uint32_t box0, uint32_t box1, CUtensorMap* out) {
-    const cuuint64_t dims[2] = {dim0, dim1};
-    const cuuint64_t strides[1] = {stride_bytes};
-    const cuuint32_t box[2] = {box0, box1};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = nd.encode(out, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 }  // namespace
@@ -776,8 +800,8 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     // per thread, so reporting an invalid argument does not grow it.
     static thread_local std::string sink(64, '\0');
     gemm_plan_t plan;
-    gemm_status_t st = plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, nd.num_sms,
-                                 nd.max_clusters[1], -1, 0, 0, &plan, &sink);
+    gemm_status_t st = plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, nd.info.slots, -1,
+                                 0, 0, &plan, &sink);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
     if (!C) return GEMM_ERR_INVALID_ARG;
@@ -788,81 +812,25 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
     if (K == 0) {
-        return launch_scale_bias(out_kind, C, ldc, bias, beta, M, N, nd.num_sms, s) == cudaSuccess ? GEMM_OK
-                                                                                                 : GEMM_ERR_CUDA;
+        return launch_scale_bias(out_kind, C, ldc, bias, beta, M, N, nd.info.num_sms, s) == cudaSuccess ? GEMM_OK
+                                                                                                      : GEMM_ERR_CUDA;
     }
     // Repack into the file-scope scratch.  Every byte the GEMM then reads is written by this call
     // first, so nothing in the scratch has to start at zero.
     const void* a_ptr = A;
     const void* b_ptr = B;
-    int64_t lda_eff = lda, ldb_eff = ldb;
-    char* ws = static_cast<char*>(nd.scratch);
-    if (plan.repack_a) {
-        const int64_t rows = layoutA == GEMM_ROW ? M : K;
-        const int64_t cols = layoutA == GEMM_ROW ? K : M;
-        lda_eff = round_up(cols, 8);
-        if (launch_repack_u16(A, lda, ws, lda_eff, rows, cols, s) != cudaSuccess) return GEMM_ERR_CUDA;
-        a_ptr = ws;
-        ws += round_up(rows * lda_eff * 2, 256);
-    }
-    if (plan.repack_b) {
-        const int64_t rows = layoutB == GEMM_ROW ? K : N;
-        const int64_t cols = layoutB == GEMM_ROW ? N : K;
-        ldb_eff = round_up(cols, 8);
-        if (launch_repack_u16(B, ldb, ws, ldb_eff, rows, cols, s) != cudaSuccess) return GEMM_ERR_CUDA;
-        b_ptr = ws;
-    }
-    const ConfigDesc* d = config_desc(plan.config);
-    const CUtensorMapDataType tin =
-        dtype_in == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const int bnc = d->block_n / d->cta_group;
-    CUtensorMap ta, tb, tc;
-    std::memset(&tc, 0, sizeof(tc));
-    st = layoutA == GEMM_ROW ? noalloc_tmap(nd, a_ptr, tin, (uint64_t)K, (uint64_t)M, (uint64_t)lda_eff * 2, 64, 128, &ta)
-                             : noalloc_tmap(nd, a_ptr, tin, (uint64_t)M, (uint64_t)K, (uint64_t)lda_eff * 2, 64, 64, &ta);
-    if (st != GEMM_OK) return st;
-    st = layoutB == GEMM_ROW
-             ? noalloc_tmap(nd, b_ptr, tin, (uint64_t)N, (uint64_t)K, (uint64_t)ldb_eff * 2, 64, 64, &tb)
-             : noalloc_tmap(nd, b_ptr, tin, (uint64_t)K, (uint64_t)N, (uint64_t)ldb_eff * 2, 64, (uint32_t)bnc, &tb);
-    if (st != GEMM_OK) return st;
-    const int eb = elt_bytes(dtype_out);
-    const bool c_aligned = (reinterpret_cast<uintptr_t>(C) % 16) == 0 && (ldc * eb) % 16 == 0;
-    const int use_tma_store = (plan.tma_store && c_aligned) ? 1 : 0;
-    if (use_tma_store) {
-        const CUtensorMapDataType tcd = dtype_out == GEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                        : dtype_out == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-        st = noalloc_tmap(nd, C, tcd, (uint64_t)N, (uint64_t)M, (uint64_t)ldc * eb, dtype_out == GEMM_F32 ? 32 : 64, 32,
-                          &tc);
-        if (st != GEMM_OK) return st;
-    }
-    KernelParams p;
-    std::memset(&p, 0, sizeof(p));
-    p.M = (int)M;
-    p.N = (int)N;
-    p.K = (int)K;
-    p.tiles_m = plan.tiles_m;
-    p.tiles_n = plan.tiles_n;
-    p.num_tiles = plan.tiles_m * plan.tiles_n;
-    p.k_tiles = (int)((K + 63) / 64);
-    p.raster_group = plan.raster_group;
-    p.a_mn = layoutA == GEMM_COL ? 1 : 0;
-    p.b_mn = layoutB == GEMM_ROW ? 1 : 0;
-    p.idesc = make_idesc(dtype_in, p.a_mn, p.b_mn, 128 * d->cta_group, d->block_n);
-    p.C = C;
-    p.ldc = ldc;
-    p.bias = bias;
-    p.alpha = alpha;
-    p.beta = beta;
-    p.use_tma_store = use_tma_store;
-    p.c_vec_ok = c_aligned ? 1 : 0;
-    p.status = nd.status;
-    p.timeout_ns = 2000ull * 1000000ull;
-    p.debug_skip_stage = -1;
-    cudaError_t e = config_launch(plan.config, out_kind, plan.clusters * d->cta_group, s, ta, tb, tc, p);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
+    int64_t lda_eff = lda, ldb_eff = ldb, launches = 0;
+    const char* what = "";
+    if (repack_operands(plan, M, N, K, layoutA, layoutB, nd.scratch, &a_ptr, &lda_eff, &b_ptr, &ldb_eff, s, &launches,
+                        &what) != cudaSuccess)
         return GEMM_ERR_CUDA;
-    }
-    return GEMM_OK;
+    LaunchArgs la{&plan, M, N, K, a_ptr, lda_eff, b_ptr, ldb_eff, C, ldc, dtype_in, dtype_out, layoutA, layoutB,
+                  alpha, beta, bias, nd.status, 2000ull * 1000000ull, -1, 0, nullptr, nullptr, 0, s};
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = nd.info.encode;
+    TmapFn tmap = [enc](const void* ptr, CUtensorMapDataType dt, uint64_t d0, uint64_t d1, uint64_t stride,
+                        uint32_t b0, uint32_t b1, CUtensorMap* m) {
+        return encode_tmap(enc, ptr, dt, d0, d1, stride, b0, b1, m);
+    };
+    cudaError_t ce = cudaSuccess;
+    return launch_planned(la, tmap, &what, &ce);
 }

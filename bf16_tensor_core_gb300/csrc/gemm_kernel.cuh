@@ -114,13 +114,17 @@ struct UnitIter {
     }
 };
 
-template <int kCtaGroup, int kBN, int kStages>
+template <int kCtaGroup, int kBN, int kStages, int kBKc = 64>
 struct TileConfig {
     static constexpr int kBM = 128;                    // rows per CTA (TMEM lanes)
-    static constexpr int kBK = 64;                     // 64 x 2 bytes = one 128-byte swizzle span
+    static constexpr int kBK = kBKc;                   // K per stage: 64 or 128
+    static constexpr int kKChunks = kBK / 64;          // 64-wide K chunks (one 128-byte swizzle span each)
     static constexpr int kBNC = kBN / kCtaGroup;       // B columns each CTA loads
-    static constexpr int kABytes = kBM * kBK * 2;      // 16 KB
+    static constexpr int kABytes = kBM * kBK * 2;      // 16 or 32 KB
     static constexpr int kBBytes = kBNC * kBK * 2;
+    static constexpr int kAChunkBytes = kBM * 128;     // one 64-wide K chunk of a K-major A tile
+    static constexpr int kBChunkBytes = kBNC * 128;    // one 64-wide K chunk of a K-major B tile
+    static constexpr int kSlabBytes = kBK * 128;       // one 64-wide MN slab of an MN-major tile
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kEpiWarps = 4;
@@ -128,11 +132,17 @@ struct TileConfig {
     static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
     static constexpr int kSmemBytes = kRingBytes + kEpiBytes + 1024;  // + alignment slack
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kMmaN = kBN < 256 ? kBN : 256; // N of one tcgen05.mma (at most 256)
+    static constexpr int kNHalves = kBN / kMmaN;       // MMAs per K step that cover the tile's N
+    static constexpr int kHalfCols = kMmaN / kCtaGroup; // B columns of one MMA that a CTA holds
     static constexpr int kAccCols = kBN;               // f32 accumulator columns per buffer
-    static constexpr int kTmemCols = (2 * kBN <= 32) ? 32 : (2 * kBN <= 64) ? 64 : (2 * kBN <= 128) ? 128
-                                     : (2 * kBN <= 256) ? 256 : 512;
-    static_assert(kBN % 64 == 0 && kBN <= 256, "BN must be a multiple of 64, at most 256");
-    static_assert(kBNC % 64 == 0, "each CTA loads whole 64-column B slabs");
+    static constexpr int kAccBufs = (2 * kBN <= 512) ? 2 : 1;   // TMEM has 512 columns
+    static constexpr int kTmemCols = (kAccBufs * kBN <= 32) ? 32 : (kAccBufs * kBN <= 64) ? 64
+                                     : (kAccBufs * kBN <= 128) ? 128 : (kAccBufs * kBN <= 256) ? 256 : 512;
+    static_assert(kBN % 64 == 0 && kBN <= 512, "BN must be a multiple of 64, at most 512");
+    static_assert(kBN <= 256 || kBN % 256 == 0, "BN above 256 must be a multiple of 256");
+    static_assert(kBK == 64 || kBK == 128, "BK must be 64 or 128");
+    static_assert(kHalfCols % 64 == 0, "each CTA loads whole 64-column B slabs");
     static_assert(kSmemBytes <= 232448 - 512, "shared memory budget");
 };
 
@@ -146,13 +156,14 @@ __device__ __forceinline__ void tile_coords(const KernelParams& p, int t, int& m
     nb = local / gm;
 }
 
-template <int kCtaGroup>
+template <int kClusterCtas>
 __device__ __forceinline__ void report_error(const KernelParams& p, int role, int tile, int stage,
                                              volatile int* abort_flag) {
     *abort_flag = 1;
-    if constexpr (kCtaGroup == 2) {
-        const uint32_t peer = cluster_ctarank() ^ 1u;
-        st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), peer), 1u);
+    if constexpr (kClusterCtas > 1) {
+        const uint32_t me = cluster_ctarank();
+        for (uint32_t r = 0; r < static_cast<uint32_t>(kClusterCtas); ++r)
+            if (r != me) st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), r), 1u);
     }
     const unsigned long long code = static_cast<unsigned long long>(STATUS_TIMEOUT) |
                                     (static_cast<unsigned long long>(role & 0xff) << 8) |
@@ -386,11 +397,18 @@ __device__ __forceinline__ bool wait_flag_bounded(const unsigned* flag, unsigned
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int kCtaGroup, int kBN, int kStages, int kOut>
-__global__ void __launch_bounds__(TileConfig<kCtaGroup, kBN, kStages>::kThreads, 1)
+// kPairs == 2 (with kCtaGroup == 2): a 4-CTA cluster of two 2-SM pairs stacked along M.  Both pairs
+// need the same B columns, so each pair loads half of every B stage and multicasts it to the
+// matching CTA of the other pair: the cluster reads B from L2 once for 512 output rows.
+template <int kCtaGroup, int kPairs, int kBN, int kStages, int kBK, int kOut>
+__global__ void __launch_bounds__(TileConfig<kCtaGroup, kBN, kStages, kBK>::kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
-    using Cfg = TileConfig<kCtaGroup, kBN, kStages>;
+    using Cfg = TileConfig<kCtaGroup, kBN, kStages, kBK>;
+    static_assert(kPairs == 1 || kCtaGroup == 2, "pairs of CTAs need cta_group::2");
+    static_assert(kPairs == 1 || Cfg::kNHalves == 1, "B multicast is built for one MMA per K step");
+    constexpr int kClusterCtas = kCtaGroup * kPairs;
+    constexpr int kClusterRows = Cfg::kBM * kClusterCtas;      // output rows of one cluster tile
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages];
     __shared__ __align__(8) uint64_t bar_empty[kStages];
@@ -402,9 +420,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = (kCtaGroup == 2) ? cluster_ctarank() : 0u;
-    const int cluster_id = blockIdx.x / kCtaGroup;
-    const int num_clusters = gridDim.x / kCtaGroup;
+    const uint32_t rank = (kClusterCtas > 1) ? cluster_ctarank() : 0u;
+    const uint32_t prank = rank & static_cast<uint32_t>(kCtaGroup - 1);   // rank within the 2-SM pair
+    const uint32_t pair = rank / kCtaGroup;                                // which pair of the cluster
+    const uint32_t lrank = rank - prank;                                   // MMA-issuing CTA of my pair
+    const uint16_t pair_mask = static_cast<uint16_t>(((1u << kCtaGroup) - 1u) << lrank);
+    const uint16_t all_mask = static_cast<uint16_t>((1u << kClusterCtas) - 1u);
+    const int cluster_id = blockIdx.x / kClusterCtas;
+    const int num_clusters = gridDim.x / kClusterCtas;
     const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t epi_smem = ring + Cfg::kRingBytes;
     volatile int* abort_flag = &s_abort;
@@ -413,7 +436,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         s_abort = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&bar_full[s]), 1);
-            mbar_init(smem_u32(&bar_empty[s]), 1);
+            mbar_init(smem_u32(&bar_empty[s]), kPairs);   // one commit from each pair that reads the slot
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bar_tfull[b]), 1);
@@ -430,7 +453,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (warp == 1) tmem_alloc<kCtaGroup>(smem_u32(&s_tmem_base), Cfg::kTmemCols);
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (kCtaGroup == 2) cluster_sync();
+    if constexpr (kClusterCtas > 1) cluster_sync();
     tc_fence_after_sync();
     const uint32_t tmem_base = s_tmem_base;
 
@@ -447,19 +470,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             while (ok && units.next(p, u)) {
                 int mb, nb;
                 tile_coords(p, u.tile, mb, nb);
-                const int m0 = mb * (Cfg::kBM * kCtaGroup) + static_cast<int>(rank) * Cfg::kBM;
-                const int n0 = nb * kBN + static_cast<int>(rank) * Cfg::kBNC;
+                const int m0 = mb * kClusterRows + static_cast<int>(rank) * Cfg::kBM;
+                const int n0 = nb * kBN + static_cast<int>(prank) * Cfg::kBNC;   // (kNHalves == 1)
                 for (int kt = u.k0; kt < u.k1; ++kt) {
                     if (!mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, p.timeout_ns, abort_flag)) {
-                        if (!*abort_flag) report_error<kCtaGroup>(p, ROLE_PRODUCER, u.tile, static_cast<int>(stage), abort_flag);
+                        if (!*abort_flag) report_error<kClusterCtas>(p, ROLE_PRODUCER, u.tile, static_cast<int>(stage), abort_flag);
                         ok = false;
                         break;
                     }
                     const bool skip = (gstage == p.debug_skip_stage) && cluster_id == 0;
                     if (!skip) {
                         const uint32_t full_local = smem_u32(&bar_full[stage]);
-                        const uint32_t full_bar = (kCtaGroup == 2) ? mapa_shared(full_local, 0) : full_local;
-                        if (rank == 0) mbar_arrive_expect_tx(full_local, tx_bytes);
+                        const uint32_t full_bar = (kCtaGroup == 2) ? mapa_shared(full_local, lrank) : full_local;
+                        if (prank == 0) mbar_arrive_expect_tx(full_local, tx_bytes);
                         const uint32_t sa = ring + stage * Cfg::kStageBytes;
                         const uint32_t sb = sa + Cfg::kABytes;
                         const int k0 = kt * Cfg::kBK;
@@ -468,17 +491,52 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             else tma_load_2d(dst, map, c0, c1, full_bar);
                         };
                         if (!p.a_mn) {
-                            load(sa, &tmA, k0, m0);                       // box {64 K, 128 M}
-                        } else {
-                            load(sa, &tmA, m0, k0);                       // box {64 M, 64 K} slabs
-                            load(sa + 8192u, &tmA, m0 + 64, k0);
-                        }
-                        if (!p.b_mn) {
-                            load(sb, &tmB, k0, n0);                       // box {64 K, BNC N}
-                        } else {
 #pragma unroll
-                            for (int j = 0; j < Cfg::kBNC / 64; ++j)     // box {64 N, 64 K} slabs
-                                load(sb + static_cast<uint32_t>(j) * 8192u, &tmB, n0 + 64 * j, k0);
+                            for (int c = 0; c < Cfg::kKChunks; ++c)      // box {64 K, 128 M} per K chunk
+                                load(sa + static_cast<uint32_t>(c * Cfg::kAChunkBytes), &tmA, k0 + 64 * c, m0);
+                        } else {
+                            load(sa, &tmA, m0, k0);                       // box {64 M, BK K} slabs
+                            load(sa + static_cast<uint32_t>(Cfg::kSlabBytes), &tmA, m0 + 64, k0);
+                        }
+                        if constexpr (kPairs == 1) {
+                            // For each MMA N half h the CTA holds columns
+                            // [nb*BN + h*kMmaN + prank*kHalfCols, +kHalfCols).
+#pragma unroll
+                            for (int h = 0; h < Cfg::kNHalves; ++h) {
+                                const int nh = nb * kBN + h * Cfg::kMmaN + static_cast<int>(prank) * Cfg::kHalfCols;
+                                if (!p.b_mn) {
+#pragma unroll
+                                    for (int c = 0; c < Cfg::kKChunks; ++c)  // box {64 K, kHalfCols N} per K chunk
+                                        load(sb + static_cast<uint32_t>(c * Cfg::kBChunkBytes + h * Cfg::kHalfCols * 128),
+                                             &tmB, k0 + 64 * c, nh);
+                                } else {
+#pragma unroll
+                                    for (int j = 0; j < Cfg::kHalfCols / 64; ++j)  // box {64 N, BK K} slabs
+                                        load(sb + static_cast<uint32_t>((h * (Cfg::kHalfCols / 64) + j) * Cfg::kSlabBytes),
+                                             &tmB, nh + 64 * j, k0);
+                                }
+                            }
+                        } else {
+                            // This pair loads part `pair` of the CTA's B columns and multicasts it to
+                            // the CTA with the same rank-in-pair in every pair of the cluster.
+                            constexpr int kPart = Cfg::kBNC / kPairs;     // B columns per part
+                            const uint16_t mc = static_cast<uint16_t>(((1u << prank) | (1u << (prank + 2))));
+                            const int nb0 = n0 + kPart * static_cast<int>(pair);
+                            if (!p.b_mn) {
+                                // rows [pair * kPart, +kPart) of every K chunk: box {64 K, kPart N}
+                                const uint32_t db = sb + pair * static_cast<uint32_t>(kPart * 128);
+#pragma unroll
+                                for (int c = 0; c < Cfg::kKChunks; ++c)
+                                    tma_load_2d_pair_mc(db + static_cast<uint32_t>(c * Cfg::kBChunkBytes), &tmB,
+                                                        k0 + 64 * c, nb0, full_bar, mc);
+                            } else {
+                                // slabs [pair * kPart / 64, +kPart / 64): box {64 N, BK K}
+                                const uint32_t db = sb + pair * static_cast<uint32_t>((kPart / 64) * Cfg::kSlabBytes);
+#pragma unroll
+                                for (int j = 0; j < kPart / 64; ++j)
+                                    tma_load_2d_pair_mc(db + static_cast<uint32_t>(j * Cfg::kSlabBytes), &tmB,
+                                                        nb0 + 64 * j, k0, full_bar, mc);
+                            }
                         }
                     }
                     ++gstage;
@@ -488,14 +546,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader CTA)
-        if (lane == 0 && rank == 0) {
-            // K-major operand: 8-row groups 1024 bytes apart (SBO); a K=16 step is +32 bytes.
-            // MN-major operand: 64-element slabs 8192 bytes apart (LBO), 8-row K groups 1024
+        if (lane == 0 && prank == 0) {
+            // K-major operand: 8-row groups 1024 bytes apart (SBO); a K=16 step is +32 bytes inside a
+            // 64-wide K chunk, and the next chunk starts one chunk (rows x 128 bytes) further.
+            // MN-major operand: 64-element slabs BK x 128 bytes apart (LBO), 8-row K groups 1024
             // bytes apart (SBO); a K=16 step is +2048 bytes.
-            const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
-            const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
-            const uint64_t a_kstep = p.a_mn ? (2048u >> 4) : (32u >> 4);
-            const uint64_t b_kstep = p.b_mn ? (2048u >> 4) : (32u >> 4);
+            const uint32_t a_lbo = p.a_mn ? static_cast<uint32_t>(Cfg::kSlabBytes) : 16u;
+            const uint32_t b_lbo = p.b_mn ? static_cast<uint32_t>(Cfg::kSlabBytes) : 16u;
+            uint64_t a_koff[Cfg::kBK / 16], b_koff[Cfg::kBK / 16], b_hoff[Cfg::kNHalves];
+#pragma unroll
+            for (int k = 0; k < Cfg::kBK / 16; ++k) {
+                a_koff[k] = (p.a_mn ? 2048u * k : static_cast<uint32_t>((k >> 2) * Cfg::kAChunkBytes + (k & 3) * 32)) >> 4;
+                b_koff[k] = (p.b_mn ? 2048u * k : static_cast<uint32_t>((k >> 2) * Cfg::kBChunkBytes + (k & 3) * 32)) >> 4;
+            }
+            // Start of N half h inside a B stage: its slabs (MN-major) or its rows (K-major).
+#pragma unroll
+            for (int h = 0; h < Cfg::kNHalves; ++h)
+                b_hoff[h] = (p.b_mn ? static_cast<uint32_t>(h * (Cfg::kHalfCols / 64) * Cfg::kSlabBytes)
+                                    : static_cast<uint32_t>(h * Cfg::kHalfCols * 128)) >> 4;
             const uint64_t a_desc0 = smem_desc_sw128(ring, a_lbo, 1024u);
             const uint64_t b_desc0 = smem_desc_sw128(ring + Cfg::kABytes, b_lbo, 1024u);
             const uint64_t stage_step = static_cast<uint64_t>(Cfg::kStageBytes >> 4);
@@ -507,14 +575,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             while (ok && units.next(p, u)) {
                 if (!mbar_wait_bounded<kCtaGroup == 2>(smem_u32(&bar_tempty[acc]), acc_phase ^ 1u, p.timeout_ns,
                                                        abort_flag)) {
-                    if (!*abort_flag) report_error<kCtaGroup>(p, ROLE_MMA, u.tile, 100 + static_cast<int>(acc), abort_flag);
+                    if (!*abort_flag) report_error<kClusterCtas>(p, ROLE_MMA, u.tile, 100 + static_cast<int>(acc), abort_flag);
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * static_cast<uint32_t>(Cfg::kAccCols);
                 for (int kt = u.k0; kt < u.k1; ++kt) {
                     if (!mbar_wait_bounded(smem_u32(&bar_full[stage]), phase, p.timeout_ns, abort_flag)) {
-                        if (!*abort_flag) report_error<kCtaGroup>(p, ROLE_MMA, u.tile, static_cast<int>(stage), abort_flag);
+                        if (!*abort_flag) report_error<kClusterCtas>(p, ROLE_MMA, u.tile, static_cast<int>(stage), abort_flag);
                         ok = false;
                         break;
                     }
@@ -523,19 +591,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const uint64_t bd = b_desc0 + stage * stage_step;
 #pragma unroll
                     for (int k = 0; k < Cfg::kBK / 16; ++k)
-                        mma_f16<kCtaGroup>(d_tmem, ad + k * a_kstep, bd + k * b_kstep, p.idesc,
-                                           (kt > u.k0 || k > 0) ? 1u : 0u);
-                    mma_commit<kCtaGroup>(smem_u32(&bar_empty[stage]));   // slot free once these MMAs finish
+#pragma unroll
+                        for (int h = 0; h < Cfg::kNHalves; ++h)
+                            mma_f16<kCtaGroup>(d_tmem + static_cast<uint32_t>(h * Cfg::kMmaN), ad + a_koff[k],
+                                               bd + b_hoff[h] + b_koff[k], p.idesc, (kt > u.k0 || k > 0) ? 1u : 0u);
+                    mma_commit<kCtaGroup>(smem_u32(&bar_empty[stage]), all_mask);  // slot free in every CTA it feeds
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                mma_commit<kCtaGroup>(smem_u32(&bar_tfull[acc]));         // accumulator ready
-                acc ^= 1u;
-                if (acc == 0) acc_phase ^= 1u;
+                mma_commit<kCtaGroup>(smem_u32(&bar_tfull[acc]), pair_mask);  // accumulator ready
+                if (++acc == static_cast<uint32_t>(Cfg::kAccBufs)) { acc = 0; acc_phase ^= 1u; }
             }
             // Drain: every MMA this thread issued has completed once bar_drain flips.  This wait
             // ignores the abort flag (only the time limit ends it): TMEM is freed after it.
-            mma_commit<kCtaGroup>(smem_u32(&bar_drain));
+            mma_commit<kCtaGroup>(smem_u32(&bar_drain), pair_mask);
             volatile int never = 0;
             mbar_wait_bounded(smem_u32(&bar_drain), 0u, p.timeout_ns, &never);
         }
@@ -545,7 +614,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int ew = warp - 2;
         const int prow = quarter * 32 + lane;         // row within this CTA's 128
         const uint32_t stage_buf0 = epi_smem + static_cast<uint32_t>(ew) * 2u * Cfg::kEpiBufBytes;
-        const size_t slot_floats = static_cast<size_t>(kCtaGroup) * 128 * kBN;
+        const size_t slot_floats = static_cast<size_t>(kClusterCtas) * 128 * kBN;
         uint32_t acc = 0, acc_phase = 0, chunk_ctr = 0;
         UnitIter units;
         units.init(p, cluster_id, num_clusters);
@@ -557,7 +626,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 if (lane == 0 && !*abort_flag)
-                    report_error<kCtaGroup>(p, ROLE_EPILOGUE, u.tile, 200 + static_cast<int>(acc), abort_flag);
+                    report_error<kClusterCtas>(p, ROLE_EPILOGUE, u.tile, 200 + static_cast<int>(acc), abort_flag);
                 break;
             }
             tc_fence_after_sync();
@@ -569,19 +638,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             } else if (u.kind == UNIT_HEAD) {
                 // The tail [k1, k_tiles) of this tile is the first unit of the next cluster.
                 const int src = cluster_id + 1;
-                const unsigned* flag = p.sk_flags + (static_cast<size_t>(src) * kCtaGroup + rank) * 4 + quarter;
+                const unsigned* flag = p.sk_flags + (static_cast<size_t>(src) * kClusterCtas + rank) * 4 + quarter;
                 bool ready = true;
                 if (lane == 0) ready = wait_flag_bounded(flag, p.epoch, p.timeout_ns, abort_flag);
                 ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
                 if (!ready) {
                     if (lane == 0 && !*abort_flag)
-                        report_error<kCtaGroup>(p, ROLE_EPILOGUE, u.tile, 300 + quarter, abort_flag);
+                        report_error<kClusterCtas>(p, ROLE_EPILOGUE, u.tile, 300 + quarter, abort_flag);
                     break;
                 }
                 add_part = p.sk_partials + static_cast<size_t>(src) * slot_floats +
                            static_cast<size_t>(rank) * 128 * kBN;
             }
-            const int row0 = mb * (Cfg::kBM * kCtaGroup) + static_cast<int>(rank) * Cfg::kBM + quarter * 32;
+            const int row0 = mb * kClusterRows + static_cast<int>(rank) * Cfg::kBM + quarter * 32;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    acc * static_cast<uint32_t>(Cfg::kAccCols);
             epilogue_tile<kOut, kBN>(p, &tmC, tbase, row0, nb * kBN, lane, prow, stage_buf0, chunk_ctr, add_part,
@@ -590,17 +659,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             __syncwarp();
             if (lane == 0) {
                 const uint32_t te = smem_u32(&bar_tempty[acc]);
-                if constexpr (kCtaGroup == 2) mbar_arrive_cluster(mapa_shared(te, 0));
+                if constexpr (kCtaGroup == 2) mbar_arrive_cluster(mapa_shared(te, lrank));
                 else mbar_arrive_local(te);
                 if (u.kind == UNIT_TAIL) {
                     // Every lane's partial stores precede this release (warp barrier, then fence).
                     __threadfence();
-                    st_release_gpu(p.sk_flags + (static_cast<size_t>(cluster_id) * kCtaGroup + rank) * 4 + quarter,
+                    st_release_gpu(p.sk_flags + (static_cast<size_t>(cluster_id) * kClusterCtas + rank) * 4 + quarter,
                                    p.epoch);
                 }
             }
-            acc ^= 1u;
-            if (acc == 0) acc_phase ^= 1u;
+            if (++acc == static_cast<uint32_t>(Cfg::kAccBufs)) { acc = 0; acc_phase ^= 1u; }
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
@@ -614,7 +682,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (kCtaGroup == 2) cluster_sync();
+    if constexpr (kClusterCtas > 1) cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();

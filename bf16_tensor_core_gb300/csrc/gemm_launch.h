@@ -10,13 +10,15 @@ struct KernelParams;
 struct ConfigDesc {
     int id;
     int cta_group;
+    int pairs;        // 2-SM pairs per cluster (2: B multicast between the pairs)
     int block_n;
+    int block_k;      // K per pipeline stage (64 or 128)
     int stages;
     int smem_bytes;
     int threads;
 };
 
-constexpr int kNumConfigs = 4;
+constexpr int kNumConfigs = 8;
 constexpr int kNumOut = 3;  // OUT_F16, OUT_BF16, OUT_F32
 
 // Static description of config `id` (nullptr if out of range).
@@ -41,6 +43,18 @@ cudaError_t cfg2_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap
                         const CUtensorMap& c, const KernelParams& p);
 const void* cfg3_kernel(int out);
 cudaError_t cfg3_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const KernelParams& p);
+const void* cfg4_kernel(int out);
+cudaError_t cfg4_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const KernelParams& p);
+const void* cfg5_kernel(int out);
+cudaError_t cfg5_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const KernelParams& p);
+const void* cfg6_kernel(int out);
+cudaError_t cfg6_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const KernelParams& p);
+const void* cfg7_kernel(int out);
+cudaError_t cfg7_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& c, const KernelParams& p);
 
 // Auxiliary kernels (gemm_aux.cu).

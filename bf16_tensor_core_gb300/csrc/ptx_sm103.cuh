@@ -126,6 +126,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
                  : "memory");
 }
 
+// Same as tma_load_2d_pair, multicast: the box lands at the same shared-memory offset in every
+// CTA of `cta_mask`, and each destination's bytes complete on the barrier at `bar`'s offset in
+// the even (MMA-issuing) CTA of that destination's pair.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                    uint32_t bar, uint16_t cta_mask) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+                 ".cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;"
+                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask)
+                 : "memory");
+}
+
 // 2-D tiled store of one box from shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t c0, int32_t c1, uint32_t src) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
@@ -203,16 +214,15 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
 }
 
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
-// kCtaGroup == 2: the arrive goes to the barrier at the same offset in both CTAs of the pair.
+// kCtaGroup == 2: the arrive goes to the barrier at the same offset in every CTA of `cta_mask`.
 template <int kCtaGroup>
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
+__device__ __forceinline__ void mma_commit(uint32_t bar, uint16_t cta_mask = 0x3) {
     if constexpr (kCtaGroup == 1) {
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                      :: "r"(bar) : "memory");
     } else {
-        const uint16_t mask = 0x3;
         asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-                     " [%0], %1;" :: "r"(bar), "h"(mask) : "memory");
+                     " [%0], %1;" :: "r"(bar), "h"(cta_mask) : "memory");
     }
 }
 

@@ -33,7 +33,7 @@ class gemm_options_t(ctypes.Structure):
 class gemm_config_info_t(ctypes.Structure):
     _fields_ = [("id", ctypes.c_int), ("cta_group", ctypes.c_int), ("block_m", ctypes.c_int),
                 ("block_n", ctypes.c_int), ("block_k", ctypes.c_int), ("stages", ctypes.c_int),
-                ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int)]
+                ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int), ("pairs", ctypes.c_int)]
 
 
 class gemm_plan_t(ctypes.Structure):

@@ -94,12 +94,13 @@ typedef struct {
 typedef struct {
     int id;
     int cta_group;     /* 1: one CTA per output tile; 2: a 2-SM cluster issues cta_group::2 MMAs */
-    int block_m;       /* output-tile rows (128 * cta_group)                                      */
+    int block_m;       /* output-tile rows (128 * cta_group * pairs)                              */
     int block_n;       /* output-tile columns (= MMA N)                                           */
     int block_k;       /* K elements per pipeline stage (64 = one 128-byte swizzle span)          */
     int stages;        /* depth of the shared-memory ring                                         */
     int smem_bytes;    /* dynamic shared memory per CTA                                           */
     int threads;       /* threads per CTA                                                         */
+    int pairs;         /* 2-SM pairs per cluster; 2: the pairs share B by TMA multicast           */
 } gemm_config_info_t;
 
 /* What gemm_run would do for a problem (pure host computation, no device needed). */

@@ -44,15 +44,19 @@ def test_options_default(lib):
 
 def test_config_table(lib):
     n = G.gemm_num_configs()
-    assert n == 4
+    assert n == 8
     seen = set()
     for i in range(n):
         st, c = G.gemm_config_info(i)
         assert st == G.GEMM_OK and c.id == i
-        assert c.block_m == 128 * c.cta_group and c.block_k == 64
-        assert c.block_n in (128, 256) and c.smem_bytes <= 232448 and c.threads == 192
-        seen.add((c.cta_group, c.block_n))
-    assert seen == {(1, 128), (1, 256), (2, 128), (2, 256)}
+        assert c.block_m == 128 * c.cta_group * c.pairs and c.block_k in (64, 128)
+        assert c.block_n in (128, 256, 512) and c.smem_bytes <= 232448 and c.threads == 192
+        assert c.pairs == 1 or c.cta_group == 2
+        stage = (128 + c.block_n // c.cta_group) * c.block_k * 2
+        assert c.smem_bytes >= c.stages * stage
+        seen.add((c.cta_group, c.pairs, c.block_n, c.block_k))
+    assert seen == {(1, 1, 128, 64), (1, 1, 256, 64), (2, 1, 128, 64), (2, 1, 256, 64), (2, 2, 256, 64),
+                    (2, 1, 256, 128), (2, 2, 256, 128), (2, 1, 512, 64)}
     assert G.gemm_config_info(n)[0] == G.GEMM_ERR_UNSUPPORTED
 
 
@@ -106,12 +110,12 @@ def test_plan_degenerate(lib):
 
 
 def test_plan_tiles_and_grid(lib):
-    for cfg in range(4):
+    for cfg in range(G.gemm_num_configs()):
         st, c = G.gemm_config_info(cfg)
         st, p = plan(4096, 4096, 4096, dout=0, config=cfg)
         assert st == G.GEMM_OK and p.config == cfg
         assert p.tiles_m == 4096 // c.block_m and p.tiles_n == 4096 // c.block_n
-        slots = 152 // c.cta_group
+        slots = 152 // (c.cta_group * c.pairs)
         assert p.clusters == min(p.tiles_m * p.tiles_n, slots)
         assert p.tma_store == 1 and p.kernels == 1
         assert p.workspace_bytes == p.sk_partial_bytes
@@ -142,7 +146,7 @@ def test_plan_auto_choice_is_a_valid_config(lib):
     for (M, N, K) in [(512, 512, 512), (4096, 4096, 4096), (2048, 11008, 4096), (1000, 3000, 2050),
                       (8192, 8192, 8192), (1, 4096, 4096), (128, 128, 64)]:
         st, p = plan(M, N, K, dout=0)
-        assert st == G.GEMM_OK and 0 <= p.config < 4
+        assert st == G.GEMM_OK and 0 <= p.config < G.gemm_num_configs()
         assert p.clusters >= 1 and p.raster_group >= 1 and p.raster_group <= p.tiles_m
 
 

@@ -17,7 +17,7 @@ from gpu_cases import alloc_c, compare, device_inputs, run_gpu, sample_indices
 
 pytestmark = pytest.mark.gpu
 
-CONFIGS = [0, 1, 2, 3]
+CONFIGS = [0, 1, 2, 3, 4, 5, 6, 7]
 
 
 @pytest.fixture(scope="module")
@@ -293,6 +293,10 @@ SK_CASES = {
     1: dict(M=2274, N=2300, K=700, dtype_out="bf16", dtype_in="bf16"),       # 9 x 9 = 81 tiles > 76
     2: dict(M=1650, N=1640, K=200, dtype_out="f32", alpha=0.5, beta=1.0),   # 13 x 13 = 169 > 152
     3: dict(M=2250, N=1250, K=450, dtype_out="f32", layoutB="col"),         # 9 x 10 = 90 > 76
+    4: dict(M=2460, N=2274, K=576, dtype_out="f16", bias=True),               # 5 x 9 = 45 > 38
+    5: dict(M=2274, N=2300, K=700, dtype_out="f32", layoutA="col"),         # 81 tiles > 76, 6 k-tiles of 128
+    6: dict(M=2460, N=2274, K=900, dtype_out="bf16", dtype_in="bf16", layoutB="col"),   # 45 tiles > 38
+    7: dict(M=2250, N=4500, K=320, dtype_out="f16", bias=True, layoutB="col"),  # 9 x 9 = 81 tiles > 76
 }
 
 
