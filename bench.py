@@ -297,6 +297,7 @@ def run_ours(args, rank, world, local):
     barrier()
     t_end = time.time()
     launches = g.launches - launches0
+    plan = g.last_plan()
     clock_rows = sampler.stop()
     clocks = ClockSampler.summarize(clock_rows, t_start, t_end)
     st = g.status()
@@ -375,8 +376,11 @@ def run_ours(args, rank, world, local):
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype_in, "data": "synthetic", "impl": "ours",
-            "config": _config_dict(w, args, {"kernel_config": args.config, "timing": "CUDA events around each "
-                                             "gemm_run on its stream"}),
+            "config": _config_dict(w, args, {"kernel_config": plan.get("config", args.config),
+                                             "plan": {k: plan[k] for k in ("block_m", "block_n", "block_k", "stages",
+                                                                           "tiles_m", "tiles_n", "clusters",
+                                                                           "stream_k", "dp_tiles") if k in plan},
+                                             "timing": "CUDA events around each gemm_run on its stream"}),
             "roofline": roof, "clocks": clocks, "gpu_launches": launches, "e2e": e2e}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, d, args.cpu_seconds)

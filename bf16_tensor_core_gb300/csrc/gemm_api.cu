@@ -162,6 +162,8 @@ struct gemm_ctx {
     float* sk_part = nullptr;       // stream-K partials (grown on demand)
     size_t sk_part_bytes = 0;
     unsigned epoch = 0;
+    gemm_plan_t last_plan{};        // plan of the last successful gemm_run
+    bool has_plan = false;
 };
 
 namespace {
@@ -643,6 +645,12 @@ const char* gemm_last_error(gemm_handle_t h) { return h ? h->err.c_str() : "null
 
 int64_t gemm_launch_count(gemm_handle_t h) { return h ? h->launches : 0; }
 
+gemm_status_t gemm_last_plan(gemm_handle_t h, gemm_plan_t* out) {
+    if (!h || !out || !h->has_plan) return GEMM_ERR_INVALID_ARG;
+    *out = h->last_plan;
+    return GEMM_OK;
+}
+
 gemm_status_t gemm_get_device_status(gemm_handle_t h, void* stream) {
     if (!h) return GEMM_ERR_INVALID_ARG;
     DeviceGuard guard(h->device);
@@ -724,6 +732,8 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
         if (st != GEMM_OK) return ce != cudaSuccess ? cuda_fail(h, what, ce) : st;
         h->launches += 1;
     }
+    h->last_plan = plan;
+    h->has_plan = true;
     if (h->opt.sync_check) return gemm_get_device_status(h, stream);
     return GEMM_OK;
 }

@@ -90,6 +90,8 @@ def load_library(path: Path | str | None = None):
     lib.gemm_config_info.restype = ci
     lib.gemm_launch_count.argtypes = [vp]
     lib.gemm_launch_count.restype = i64
+    lib.gemm_last_plan.argtypes = [vp, ctypes.POINTER(gemm_plan_t)]
+    lib.gemm_last_plan.restype = ci
     lib.gemm_run_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ci, ci, ci, ci, cf, cf, vp, vp]
     lib.gemm_run_noalloc.restype = ci
     if path is None:
@@ -159,6 +161,11 @@ def gemm_launch_count(h) -> int:
     return load_library().gemm_launch_count(h)
 
 
+def gemm_last_plan(h) -> tuple[int, gemm_plan_t]:
+    p = gemm_plan_t()
+    return load_library().gemm_last_plan(h, ctypes.byref(p)), p
+
+
 def gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, dtype_in, dtype_out, layoutA, layoutB,
                      alpha, beta, bias, stream) -> int:
     return load_library().gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, dtype_in, dtype_out, layoutA,
@@ -210,6 +217,10 @@ class Gemm:
     @property
     def launches(self) -> int:
         return gemm_launch_count(self.h)
+
+    def last_plan(self) -> dict:
+        st, p = gemm_last_plan(self.h)
+        return p.as_dict() if st == GEMM_OK else {}
 
     def run(self, A, B, C, *, M=None, N=None, K=None, layoutA="row", layoutB="row", alpha=1.0, beta=0.0,
             bias=None, stream=None, check=True) -> int:

@@ -165,6 +165,10 @@ gemm_status_t gemm_config_info(int id, gemm_config_info_t* out);
 /* Kernels launched through this handle since it was created. */
 int64_t gemm_launch_count(gemm_handle_t h);
 
+/* The plan of the handle's last successful gemm_run (config, tiles, clusters launched, stream-K
+ * split, repacks).  GEMM_ERR_INVALID_ARG before the first call or for NULL arguments. */
+gemm_status_t gemm_last_plan(gemm_handle_t h, gemm_plan_t* out);
+
 /* Size of the fixed device scratch that gemm_run_noalloc uses for operand repacks. */
 #define GEMM_NOALLOC_SCRATCH_BYTES (32u << 20)
 
