@@ -128,19 +128,36 @@ gemm_status_t query_device(int dev, bool force_optin_failure, DevInfo* info) {
     return GEMM_OK;
 }
 
-struct TmapKey {
+// A 2-D or 3-D tiled tensor map: dims[0] contiguous, strides in bytes for dims 1..rank-1.
+struct TmapDesc {
     const void* ptr;
-    int dtype;
-    uint64_t dim0, dim1, stride;
-    uint32_t box0, box1;
-    bool operator==(const TmapKey& o) const {
-        return ptr == o.ptr && dtype == o.dtype && dim0 == o.dim0 && dim1 == o.dim1 && stride == o.stride &&
-               box0 == o.box0 && box1 == o.box1;
+    CUtensorMapDataType dt;
+    int rank;
+    uint64_t dims[3];
+    uint64_t strides[2];
+    uint32_t box[3];
+    bool operator==(const TmapDesc& o) const {
+        if (ptr != o.ptr || dt != o.dt || rank != o.rank) return false;
+        for (int i = 0; i < rank; ++i)
+            if (dims[i] != o.dims[i] || box[i] != o.box[i]) return false;
+        for (int i = 0; i + 1 < rank; ++i)
+            if (strides[i] != o.strides[i]) return false;
+        return true;
     }
 };
 
+TmapDesc tmap2d(const void* ptr, CUtensorMapDataType dt, uint64_t d0, uint64_t d1, uint64_t stride, uint32_t b0,
+                uint32_t b1) {
+    return TmapDesc{ptr, dt, 2, {d0, d1, 1}, {stride, 0}, {b0, b1, 1}};
+}
+
+TmapDesc tmap3d(const void* ptr, CUtensorMapDataType dt, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+    return TmapDesc{ptr, dt, 3, {d0, d1, d2}, {s1, s2}, {b0, b1, b2}};
+}
+
 struct TmapEntry {
-    TmapKey key;
+    TmapDesc key;
     CUtensorMap map;
 };
 
@@ -157,6 +174,7 @@ struct gemm_ctx {
     std::vector<TmapEntry> cache;
     size_t cache_next = 0;
     int faults = FAULT_NONE;
+    bool force_2d = false;          // GEMM_TMA_RANK=2 (tuning): never use 3-D operand maps
     int64_t launches = 0;
     unsigned* sk_flags = nullptr;   // zeroed at creation; stream-K flags carry the launch epoch
     float* sk_part = nullptr;       // stream-K partials (grown on demand)
@@ -267,18 +285,15 @@ uint32_t make_idesc(int din, int a_mn, int b_mn, int mma_m, int mma_n) {
 }
 
 // Tensor-map encoder used by the launch: cached per handle, or direct.
-using TmapFn = std::function<gemm_status_t(const void*, CUtensorMapDataType, uint64_t, uint64_t, uint64_t, uint32_t,
-                                           uint32_t, CUtensorMap*)>;
+using TmapFn = std::function<gemm_status_t(const TmapDesc&, CUtensorMap*)>;
 
-gemm_status_t encode_tmap(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* ptr, CUtensorMapDataType dt,
-                          uint64_t dim0, uint64_t dim1, uint64_t stride_bytes, uint32_t box0, uint32_t box1,
-                          CUtensorMap* out) {
-    const cuuint64_t dims[2] = {dim0, dim1};
-    const cuuint64_t strides[1] = {stride_bytes};
-    const cuuint32_t box[2] = {box0, box1};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(out, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+gemm_status_t encode_tmap(PFN_cuTensorMapEncodeTiled_v12000 encode, const TmapDesc& d, CUtensorMap* out) {
+    const cuuint64_t dims[3] = {d.dims[0], d.dims[1], d.dims[2]};
+    const cuuint64_t strides[2] = {d.strides[0], d.strides[1]};
+    const cuuint32_t box[3] = {d.box[0], d.box[1], d.box[2]};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(out, d.dt, (cuuint32_t)d.rank, const_cast<void*>(d.ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -304,6 +319,7 @@ struct LaunchArgs {
     unsigned* sk_flags;
     unsigned epoch;
     cudaStream_t stream;
+    bool force_2d;              // tuning: one 2-D box per slab even where a 3-D box would do
 };
 
 // Encode the tensor maps, fill the kernel parameters and launch the planned config.
@@ -312,22 +328,50 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
     const ConfigDesc* d = config_desc(plan.config);
     const CUtensorMapDataType tin =
         a.din == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    // B columns one TMA box covers: a CTA's share of the tile, split once more between the
+    // B columns one TMA box covers: a CTA's share of one MMA's N, split once more between the
     // pairs of a multicast cluster.
     const int mma_n = std::min(d->block_n, 256);
     const uint32_t b_box_n = (uint32_t)(mma_n / d->cta_group / d->pairs);
+    const uint32_t bk = (uint32_t)d->block_k;
+    const uint32_t kchunks = bk / 64;
+    const uint64_t M = (uint64_t)a.M, N = (uint64_t)a.N, K = (uint64_t)a.K;
     CUtensorMap ta, tb, tc;
     std::memset(&tc, 0, sizeof(tc));
+    // Where the extents divide evenly, a 3-D view (64-element slabs as the outer dimension) lets one
+    // TMA instruction fill a whole operand stage; otherwise one 2-D box per 64-element slab.
+    int a_3d = 0, b_3d = 0;
+    const bool allow_3d = !a.force_2d;
     *what = "tensor map of A";
-    const uint32_t bk = (uint32_t)d->block_k;
-    gemm_status_t st = a.la == GEMM_ROW  // K-major: box {64 K, 128 M}; M-major: box {64 M, BK K}
-                           ? tmap(a.A, tin, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.lda * 2, 64, 128, &ta)
-                           : tmap(a.A, tin, (uint64_t)a.M, (uint64_t)a.K, (uint64_t)a.lda * 2, 64, bk, &ta);
+    gemm_status_t st = GEMM_ERR_CUDA;
+    if (a.la == GEMM_ROW) {  // K-major
+        if (allow_3d && K % 64 == 0) {
+            st = tmap(tmap3d(a.A, tin, 64, M, K / 64, (uint64_t)a.lda * 2, 128, 64, 128, kchunks), &ta);
+            a_3d = st == GEMM_OK;
+        }
+        if (!a_3d) st = tmap(tmap2d(a.A, tin, K, M, (uint64_t)a.lda * 2, 64, 128), &ta);
+    } else {                 // M-major
+        if (allow_3d && M % 64 == 0) {
+            st = tmap(tmap3d(a.A, tin, 64, K, M / 64, (uint64_t)a.lda * 2, 128, 64, bk, 2), &ta);
+            a_3d = st == GEMM_OK;
+        }
+        if (!a_3d) st = tmap(tmap2d(a.A, tin, M, K, (uint64_t)a.lda * 2, 64, bk), &ta);
+    }
     if (st != GEMM_OK) return st;
     *what = "tensor map of B";
-    st = a.lb == GEMM_ROW  // N-major: box {64 N, BK K}; K-major: box {64 K, b_box_n N}
-             ? tmap(a.B, tin, (uint64_t)a.N, (uint64_t)a.K, (uint64_t)a.ldb * 2, 64, bk, &tb)
-             : tmap(a.B, tin, (uint64_t)a.K, (uint64_t)a.N, (uint64_t)a.ldb * 2, 64, b_box_n, &tb);
+    st = GEMM_ERR_CUDA;
+    if (a.lb == GEMM_ROW) {  // N-major
+        if (allow_3d && d->pairs == 1 && N % 64 == 0) {
+            st = tmap(tmap3d(a.B, tin, 64, K, N / 64, (uint64_t)a.ldb * 2, 128, 64, bk, b_box_n / 64), &tb);
+            b_3d = st == GEMM_OK;
+        }
+        if (!b_3d) st = tmap(tmap2d(a.B, tin, N, K, (uint64_t)a.ldb * 2, 64, bk), &tb);
+    } else {                 // K-major
+        if (allow_3d && d->pairs == 1 && d->block_n <= 256 && K % 64 == 0) {
+            st = tmap(tmap3d(a.B, tin, 64, N, K / 64, (uint64_t)a.ldb * 2, 128, 64, b_box_n, kchunks), &tb);
+            b_3d = st == GEMM_OK;
+        }
+        if (!b_3d) st = tmap(tmap2d(a.B, tin, K, N, (uint64_t)a.ldb * 2, 64, b_box_n), &tb);
+    }
     if (st != GEMM_OK) return st;
     const int eb = elt_bytes(a.dout);
     const bool c_aligned = (reinterpret_cast<uintptr_t>(a.C) % 16) == 0 && (a.ldc * eb) % 16 == 0;
@@ -338,7 +382,7 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
                                         : a.dout == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         const uint32_t box0 = a.dout == GEMM_F32 ? 32 : 64;   // one 128-byte line per row
-        st = tmap(a.C, tcd, (uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.ldc * eb, box0, 32, &tc);
+        st = tmap(tmap2d(a.C, tcd, N, M, (uint64_t)a.ldc * eb, box0, 32), &tc);
         if (st != GEMM_OK) return st;
     }
     KernelParams p;
@@ -353,6 +397,8 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
     p.raster_group = a.raster_group > 0 ? std::min(a.raster_group, plan.tiles_m) : plan.raster_group;
     p.a_mn = a.la == GEMM_COL ? 1 : 0;
     p.b_mn = a.lb == GEMM_ROW ? 1 : 0;
+    p.a_3d = a_3d;
+    p.b_3d = b_3d;
     p.idesc = make_idesc(a.din, p.a_mn, p.b_mn, 128 * d->cta_group, mma_n);
     p.C = a.C;
     p.ldc = a.ldc;
@@ -417,17 +463,16 @@ cudaError_t repack_operands(const gemm_plan_t& plan, int64_t M, int64_t N, int64
     return cudaSuccess;
 }
 
-gemm_status_t get_tmap_cached(gemm_handle_t h, const void* ptr, CUtensorMapDataType dt, uint64_t dim0, uint64_t dim1,
-                              uint64_t stride_bytes, uint32_t box0, uint32_t box1, CUtensorMap* out) {
-    TmapKey key{ptr, (int)dt, dim0, dim1, stride_bytes, box0, box1};
+gemm_status_t get_tmap_cached(gemm_handle_t h, const TmapDesc& key, CUtensorMap* out) {
     for (const TmapEntry& e : h->cache)
         if (e.key == key) { *out = e.map; return GEMM_OK; }
     if (h->faults & FAULT_TMAP) return fail(h, GEMM_ERR_CUDA, "cuTensorMapEncodeTiled: forced failure (GEMM_TEST_FAIL=tmap)");
     CUtensorMap m;
-    if (encode_tmap(h->dev.encode, ptr, dt, dim0, dim1, stride_bytes, box0, box1, &m) != GEMM_OK) {
+    if (encode_tmap(h->dev.encode, key, &m) != GEMM_OK) {
         char buf[256];
-        std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed: dims {%llu,%llu} stride %llu box {%u,%u}",
-                      (unsigned long long)dim0, (unsigned long long)dim1, (unsigned long long)stride_bytes, box0, box1);
+        std::snprintf(buf, sizeof(buf), "cuTensorMapEncodeTiled failed: rank %d dims {%llu,%llu,%llu} box {%u,%u,%u}",
+                      key.rank, (unsigned long long)key.dims[0], (unsigned long long)key.dims[1],
+                      (unsigned long long)key.dims[2], key.box[0], key.box[1], key.box[2]);
         return fail(h, GEMM_ERR_CUDA, buf);
     }
     const size_t kCacheSize = 32;
@@ -604,6 +649,7 @@ gemm_status_t gemm_create(gemm_handle_t* out, int device, const gemm_options_t* 
     h->device = device;
     h->opt = o;
     h->faults = read_fault_env();
+    if (const char* r = std::getenv("GEMM_TMA_RANK")) h->force_2d = std::atoi(r) == 2;
     DeviceGuard guard(device);
     gemm_status_t st = query_device(device, (h->faults & FAULT_OPTIN) != 0, &h->dev);
     if (st != GEMM_OK) {
@@ -722,11 +768,9 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
         }
         LaunchArgs la{&plan, M, N, K, a_ptr, lda_eff, b_ptr, ldb_eff, C, ldc, dtype_in, dtype_out, layoutA, layoutB,
                       alpha, beta, bias, h->d_status, (unsigned long long)h->opt.timeout_ms * 1000000ull,
-                      h->opt.debug_skip_stage, h->opt.raster_group, h->sk_part, h->sk_flags, h->epoch, s};
-        TmapFn tmap = [h](const void* ptr, CUtensorMapDataType dt, uint64_t d0, uint64_t d1, uint64_t stride,
-                          uint32_t b0, uint32_t b1, CUtensorMap* m) {
-            return get_tmap_cached(h, ptr, dt, d0, d1, stride, b0, b1, m);
-        };
+                      h->opt.debug_skip_stage, h->opt.raster_group, h->sk_part, h->sk_flags, h->epoch, s,
+                      h->force_2d};
+        TmapFn tmap = [h](const TmapDesc& desc, CUtensorMap* m) { return get_tmap_cached(h, desc, m); };
         cudaError_t ce = cudaSuccess;
         st = launch_planned(la, tmap, &what, &ce);
         if (st != GEMM_OK) return ce != cudaSuccess ? cuda_fail(h, what, ce) : st;
@@ -835,12 +879,9 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
                         &what) != cudaSuccess)
         return GEMM_ERR_CUDA;
     LaunchArgs la{&plan, M, N, K, a_ptr, lda_eff, b_ptr, ldb_eff, C, ldc, dtype_in, dtype_out, layoutA, layoutB,
-                  alpha, beta, bias, nd.status, 2000ull * 1000000ull, -1, 0, nullptr, nullptr, 0, s};
+                  alpha, beta, bias, nd.status, 2000ull * 1000000ull, -1, 0, nullptr, nullptr, 0, s, false};
     const PFN_cuTensorMapEncodeTiled_v12000 enc = nd.info.encode;
-    TmapFn tmap = [enc](const void* ptr, CUtensorMapDataType dt, uint64_t d0, uint64_t d1, uint64_t stride,
-                        uint32_t b0, uint32_t b1, CUtensorMap* m) {
-        return encode_tmap(enc, ptr, dt, d0, d1, stride, b0, b1, m);
-    };
+    TmapFn tmap = [enc](const TmapDesc& desc, CUtensorMap* m) { return encode_tmap(enc, desc, m); };
     cudaError_t ce = cudaSuccess;
     return launch_planned(la, tmap, &what, &ce);
 }

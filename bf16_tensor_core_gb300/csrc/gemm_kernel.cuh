@@ -41,6 +41,7 @@ struct KernelParams {
     int tiles_m, tiles_n, num_tiles, k_tiles;
     int raster_group;
     int a_mn, b_mn;            // 0: operand K-major in memory, 1: MN-major
+    int a_3d, b_3d;            // 1: the operand's tensor map is 3-D and one box covers the whole stage
     uint32_t idesc;            // tcgen05 instruction descriptor (kind::f16)
     void* C;
     long long ldc;             // elements
@@ -490,13 +491,25 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             if constexpr (kCtaGroup == 2) tma_load_2d_pair(dst, map, c0, c1, full_bar);
                             else tma_load_2d(dst, map, c0, c1, full_bar);
                         };
+                        auto load3 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2) {
+                            if constexpr (kCtaGroup == 2) tma_load_3d_pair(dst, map, c0, c1, c2, full_bar);
+                            else tma_load_3d(dst, map, c0, c1, c2, full_bar);
+                        };
                         if (!p.a_mn) {
+                            if (p.a_3d) {
+                                load3(sa, &tmA, 0, m0, kt * Cfg::kKChunks);   // box {64, 128 M, K chunks}
+                            } else {
 #pragma unroll
-                            for (int c = 0; c < Cfg::kKChunks; ++c)      // box {64 K, 128 M} per K chunk
-                                load(sa + static_cast<uint32_t>(c * Cfg::kAChunkBytes), &tmA, k0 + 64 * c, m0);
+                                for (int c = 0; c < Cfg::kKChunks; ++c)  // box {64 K, 128 M} per K chunk
+                                    load(sa + static_cast<uint32_t>(c * Cfg::kAChunkBytes), &tmA, k0 + 64 * c, m0);
+                            }
                         } else {
-                            load(sa, &tmA, m0, k0);                       // box {64 M, BK K} slabs
-                            load(sa + static_cast<uint32_t>(Cfg::kSlabBytes), &tmA, m0 + 64, k0);
+                            if (p.a_3d) {
+                                load3(sa, &tmA, 0, k0, m0 / 64);          // box {64, BK K, 2 M slabs}
+                            } else {
+                                load(sa, &tmA, m0, k0);                   // box {64 M, BK K} slabs
+                                load(sa + static_cast<uint32_t>(Cfg::kSlabBytes), &tmA, m0 + 64, k0);
+                            }
                         }
                         if constexpr (kPairs == 1) {
                             // For each MMA N half h the CTA holds columns
@@ -505,15 +518,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             for (int h = 0; h < Cfg::kNHalves; ++h) {
                                 const int nh = nb * kBN + h * Cfg::kMmaN + static_cast<int>(prank) * Cfg::kHalfCols;
                                 if (!p.b_mn) {
+                                    if (p.b_3d) {                         // box {64, kHalfCols N, K chunks}
+                                        load3(sb, &tmB, 0, nh, kt * Cfg::kKChunks);
+                                    } else {
 #pragma unroll
-                                    for (int c = 0; c < Cfg::kKChunks; ++c)  // box {64 K, kHalfCols N} per K chunk
-                                        load(sb + static_cast<uint32_t>(c * Cfg::kBChunkBytes + h * Cfg::kHalfCols * 128),
-                                             &tmB, k0 + 64 * c, nh);
+                                        for (int c = 0; c < Cfg::kKChunks; ++c)  // box {64 K, kHalfCols N} per K chunk
+                                            load(sb + static_cast<uint32_t>(c * Cfg::kBChunkBytes + h * Cfg::kHalfCols * 128),
+                                                 &tmB, k0 + 64 * c, nh);
+                                    }
                                 } else {
+                                    const uint32_t dh = sb + static_cast<uint32_t>(h * (Cfg::kHalfCols / 64) * Cfg::kSlabBytes);
+                                    if (p.b_3d) {                         // box {64, BK K, N slabs}
+                                        load3(dh, &tmB, 0, k0, nh / 64);
+                                    } else {
 #pragma unroll
-                                    for (int j = 0; j < Cfg::kHalfCols / 64; ++j)  // box {64 N, BK K} slabs
-                                        load(sb + static_cast<uint32_t>((h * (Cfg::kHalfCols / 64) + j) * Cfg::kSlabBytes),
-                                             &tmB, nh + 64 * j, k0);
+                                        for (int j = 0; j < Cfg::kHalfCols / 64; ++j)  // box {64 N, BK K} slabs
+                                            load(dh + static_cast<uint32_t>(j * Cfg::kSlabBytes), &tmB, nh + 64 * j, k0);
+                                    }
                                 }
                             }
                         } else {

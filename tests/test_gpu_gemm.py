@@ -333,3 +333,40 @@ def test_stream_k_matches_data_parallel_on_integers():
     ref = (A.cpu().to(torch.int64) @ B.cpu().to(torch.int64)).to(torch.float32)
     assert torch.equal(outs[0].cpu(), ref)
     assert torch.equal(outs[1].cpu(), ref)
+
+
+def test_three_d_and_two_d_tensor_maps_agree(monkeypatch):
+    """Where the extents allow a 3-D operand map (one box per stage) the result must equal the
+    one-box-per-slab 2-D path bit for bit: same data in the same shared-memory layout."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    for (la, lb, cfg) in [("row", "row", 5), ("col", "col", 1), ("row", "col", 0), ("col", "row", 5)]:
+        w = W.problem(640, 768, 512, dtype_in="bf16", dtype_out="f32", layoutA=la, layoutB=lb, bias=True,
+                      seed=len(la) + 3 * len(lb) + cfg)
+        d = W.generate(w)
+        dd = device_inputs(d)
+        outs = []
+        for rank in ("2", "3"):
+            monkeypatch.setenv("GEMM_TMA_RANK", rank)
+            with G.Gemm(0, config=cfg, sync_check=1) as g:
+                C = alloc_c(w, d)
+                run_gpu(g, w, dd, C)
+                torch.cuda.synchronize()
+                outs.append(C.cpu())
+        assert torch.equal(outs[0], outs[1]), (la, lb, cfg)
+        assert compare(w, d, outs[1].cuda())["passed"]
+
+
+def test_last_plan_reports_the_run():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    with G.Gemm(0, config=5) as g:
+        assert g.last_plan() == {}
+        w = W.problem(600, 700, 256, seed=3)
+        d = W.generate(w)
+        dd = device_inputs(d)
+        C = alloc_c(w, d)
+        run_gpu(g, w, dd, C)
+        p = g.last_plan()
+        assert p["config"] == 5 and p["block_k"] == 128 and p["tiles_m"] == 3 and p["tiles_n"] == 3
+        assert 1 <= p["clusters"] <= 9
