@@ -659,7 +659,7 @@ gemm_status_t gemm_create(gemm_handle_t* out, int device, const gemm_options_t* 
     e = cudaMalloc(&h->d_status, 64);
     if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, 64);
     // One flag per (CTA of the grid, epilogue warp) for the stream-K hand-off.
-    const size_t flag_bytes = (size_t)h->dev.num_sms * 4 * sizeof(unsigned);
+    const size_t flag_bytes = (size_t)h->dev.num_sms * 8 * sizeof(unsigned);
     if (e == cudaSuccess) e = cudaMalloc(&h->sk_flags, flag_bytes);
     if (e == cudaSuccess) e = cudaMemset(h->sk_flags, 0, flag_bytes);
     if (e != cudaSuccess) {

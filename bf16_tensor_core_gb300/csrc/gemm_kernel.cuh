@@ -62,7 +62,7 @@ struct KernelParams {
     long long sk_base;
     int sk_extra;
     float* sk_partials;        // [cluster][cta rank][BN / 4][128 rows][4] f32
-    unsigned* sk_flags;        // [cluster][cta rank][4 epilogue warps]
+    unsigned* sk_flags;        // [cluster][cta rank][epilogue warp]
     unsigned epoch;            // launch counter of the handle, never 0
 };
 
@@ -128,9 +128,11 @@ struct TileConfig {
     static constexpr int kSlabBytes = kBK * 128;       // one 64-wide MN slab of an MN-major tile
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kEpiWarps = 4;
-    static constexpr int kEpiBufBytes = 32 * 128;      // 32 rows x 128 bytes
-    static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+    // Eight epilogue warps: warps w and w+4 read the same 32 TMEM lanes and split the columns.
+    static constexpr int kEpiWarps = 8;
+    static constexpr int kEpiCols = kBN / (kEpiWarps / 4);   // accumulator columns one warp drains
+    static constexpr int kEpiBufBytes = 32 * 128;      // 32 rows x 128 bytes, one staging buffer per warp
+    static constexpr int kEpiBytes = kEpiWarps * kEpiBufBytes;
     static constexpr int kSmemBytes = kRingBytes + kEpiBytes + 1024;  // + alignment slack
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
     static constexpr int kMmaN = kBN < 256 ? kBN : 256; // N of one tcgen05.mma (at most 256)
@@ -280,24 +282,25 @@ __device__ __forceinline__ void add_partial_32(uint32_t (&acc)[32], const float*
     }
 }
 
-// One warp drains its 32 TMEM lanes (32 rows) x BN columns of one accumulator buffer.
+// One warp drains its 32 TMEM lanes (32 rows) x kCols columns of one accumulator buffer, starting at
+// tile column pcol0 (tbase already points there).
 //   out_part != nullptr: a stream-K tail segment; the raw f32 sums go to the partial slot, C is untouched.
 //   add_part != nullptr: a stream-K head segment; the next cluster's partial is added before the epilogue.
-template <int kOut, int kBN>
+template <int kOut, int kCols>
 __device__ __forceinline__ void epilogue_tile(const KernelParams& p, const CUtensorMap* tmC, uint32_t tbase,
-                                              int row0, int col_base, int lane, int prow, uint32_t stage_buf0,
-                                              uint32_t& chunk_ctr, const float* add_part, float* out_part) {
+                                              int row0, int col_base, int pcol0, int lane, int prow,
+                                              uint32_t stage_buf, const float* add_part, float* out_part) {
     const int row = row0 + lane;
     if (out_part != nullptr) {
         float4* dst = reinterpret_cast<float4*>(out_part);
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int c = 0; c < kCols / 32; ++c) {
             uint32_t acc[32];
             tmem_ld_32x32b_x32(tbase + c * 32, acc);
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                __stcg(&dst[(c * 8 + j) * 128 + prow],
+                __stcg(&dst[(pcol0 / 4 + c * 8 + j) * 128 + prow],
                        make_float4(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]),
                                    __uint_as_float(acc[4 * j + 2]), __uint_as_float(acc[4 * j + 3])));
         }
@@ -308,14 +311,14 @@ __device__ __forceinline__ void epilogue_tile(const KernelParams& p, const CUten
         constexpr int kChunk = (kOut == OUT_F32) ? 32 : 64;
         const bool warp_rows_in = row0 < p.M;
 #pragma unroll 1
-        for (int c = 0; c < kBN / kChunk; ++c) {
+        for (int c = 0; c < kCols / kChunk; ++c) {
             const int col0 = col_base + c * kChunk;
             uint32_t words[32];
             if constexpr (kOut == OUT_F32) {
                 uint32_t acc[32];
                 tmem_ld_32x32b_x32(tbase + c * 32, acc);
                 tmem_wait_ld();
-                if (add_part) add_partial_32(acc, add_part, c * 32, prow);
+                if (add_part) add_partial_32(acc, add_part, pcol0 + c * 32, prow);
                 float v[32];
                 epilogue_math<kOut>(p, acc, v, row, col0);
 #pragma unroll
@@ -326,8 +329,8 @@ __device__ __forceinline__ void epilogue_tile(const KernelParams& p, const CUten
                 tmem_ld_32x32b_x32(tbase + c * 64 + 32, acc1);
                 tmem_wait_ld();
                 if (add_part) {
-                    add_partial_32(acc0, add_part, c * 64, prow);
-                    add_partial_32(acc1, add_part, c * 64 + 32, prow);
+                    add_partial_32(acc0, add_part, pcol0 + c * 64, prow);
+                    add_partial_32(acc1, add_part, pcol0 + c * 64 + 32, prow);
                 }
                 float v[32];
                 epilogue_math<kOut>(p, acc0, v, row, col0);
@@ -338,10 +341,9 @@ __device__ __forceinline__ void epilogue_tile(const KernelParams& p, const CUten
                 for (int i = 0; i < 16; ++i) words[16 + i] = pack2<kOut>(v[2 * i], v[2 * i + 1]);
             }
             if (!warp_rows_in || col0 >= p.N) continue;   // whole box outside C (warp-uniform)
-            const uint32_t buf = stage_buf0 + (chunk_ctr & 1u) * 4096u;
-            if (lane == 0) bulk_wait_group_read<1>();     // the store that last used `buf` has read it
+            if (lane == 0) bulk_wait_group_read<0>();     // the previous store has read the buffer
             __syncwarp();
-            const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128u;
+            const uint32_t row_addr = stage_buf + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t piece = static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u);  // 128B swizzle
@@ -350,20 +352,19 @@ __device__ __forceinline__ void epilogue_tile(const KernelParams& p, const CUten
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_store_2d(tmC, col0, row0, buf);
+                tma_store_2d(tmC, col0, row0, stage_buf);
                 bulk_commit_group();
             }
-            ++chunk_ctr;
         }
     } else {
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int c = 0; c < kCols / 32; ++c) {
             const int col0 = col_base + c * 32;
             uint32_t acc[32];
             tmem_ld_32x32b_x32(tbase + c * 32, acc);
             tmem_wait_ld();
             if (col0 >= p.N) continue;
-            if (add_part) add_partial_32(acc, add_part, c * 32, prow);
+            if (add_part) add_partial_32(acc, add_part, pcol0 + c * 32, prow);
             float v[32];
             epilogue_math<kOut>(p, acc, v, row, col0);
             store_row_direct<kOut>(p, v, row, col0);
@@ -630,13 +631,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             mbar_wait_bounded(smem_u32(&bar_drain), 0u, p.timeout_ns, &never);
         }
     } else {
-        // ------------------------------------------------------------ epilogue warps 2..5
+        // ------------------------------------------------------------ epilogue warps 2..9
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
         const int ew = warp - 2;
+        const int pcol0 = (ew / 4) * Cfg::kEpiCols;   // first tile column this warp drains
         const int prow = quarter * 32 + lane;         // row within this CTA's 128
-        const uint32_t stage_buf0 = epi_smem + static_cast<uint32_t>(ew) * 2u * Cfg::kEpiBufBytes;
+        const uint32_t stage_buf = epi_smem + static_cast<uint32_t>(ew) * Cfg::kEpiBufBytes;
         const size_t slot_floats = static_cast<size_t>(kClusterCtas) * 128 * kBN;
-        uint32_t acc = 0, acc_phase = 0, chunk_ctr = 0;
+        uint32_t acc = 0, acc_phase = 0;
         UnitIter units;
         units.init(p, cluster_id, num_clusters);
         Unit u;
@@ -659,7 +661,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             } else if (u.kind == UNIT_HEAD) {
                 // The tail [k1, k_tiles) of this tile is the first unit of the next cluster.
                 const int src = cluster_id + 1;
-                const unsigned* flag = p.sk_flags + (static_cast<size_t>(src) * kClusterCtas + rank) * 4 + quarter;
+                const unsigned* flag = p.sk_flags + (static_cast<size_t>(src) * kClusterCtas + rank) * Cfg::kEpiWarps + ew;
                 bool ready = true;
                 if (lane == 0) ready = wait_flag_bounded(flag, p.epoch, p.timeout_ns, abort_flag);
                 ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
@@ -673,9 +675,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             const int row0 = mb * kClusterRows + static_cast<int>(rank) * Cfg::kBM + quarter * 32;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   acc * static_cast<uint32_t>(Cfg::kAccCols);
-            epilogue_tile<kOut, kBN>(p, &tmC, tbase, row0, nb * kBN, lane, prow, stage_buf0, chunk_ctr, add_part,
-                                     out_part);
+                                   acc * static_cast<uint32_t>(Cfg::kAccCols) + static_cast<uint32_t>(pcol0);
+            epilogue_tile<kOut, Cfg::kEpiCols>(p, &tmC, tbase, row0, nb * kBN + pcol0, pcol0, lane, prow, stage_buf,
+                                               add_part, out_part);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
@@ -685,7 +687,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (u.kind == UNIT_TAIL) {
                     // Every lane's partial stores precede this release (warp barrier, then fence).
                     __threadfence();
-                    st_release_gpu(p.sk_flags + (static_cast<size_t>(cluster_id) * kClusterCtas + rank) * 4 + quarter,
+                    st_release_gpu(p.sk_flags + (static_cast<size_t>(cluster_id) * kClusterCtas + rank) * Cfg::kEpiWarps + ew,
                                    p.epoch);
                 }
             }

@@ -50,7 +50,7 @@ def test_config_table(lib):
         st, c = G.gemm_config_info(i)
         assert st == G.GEMM_OK and c.id == i
         assert c.block_m == 128 * c.cta_group * c.pairs and c.block_k in (64, 128)
-        assert c.block_n in (128, 256, 512) and c.smem_bytes <= 232448 and c.threads == 192
+        assert c.block_n in (128, 256, 512) and c.smem_bytes <= 232448 and c.threads == 320
         assert c.pairs == 1 or c.cta_group == 2
         stage = (128 + c.block_n // c.cta_group) * c.block_k * 2
         assert c.smem_bytes >= c.stages * stage
