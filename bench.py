@@ -92,6 +92,66 @@ def _traffic(workload_name: str):
     return None, None
 
 
+class NvmlSampler:
+    """SM clock, power and clock-event reasons read through NVML (read-only queries) by a thread
+    polling every ~0.5 ms, so that even a timed region of a few milliseconds gets samples."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str):
+        import ctypes
+        import threading
+        self.rows = []
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            dev = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(dev)) != 0:
+                return
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            u32, u64 = ctypes.c_uint, ctypes.c_ulonglong
+            mx = u32()
+            nv.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx))     # 1 = NVML_CLOCK_SM
+            self.max_mhz = mx.value
+
+            def run():
+                clk, pw, rs = u32(), u32(), u64()
+                while not self._stop.is_set():
+                    t = time.time()
+                    ok = nv.nvmlDeviceGetClockInfo(dev, 1, ctypes.byref(clk)) == 0
+                    nv.nvmlDeviceGetPowerUsage(dev, ctypes.byref(pw))
+                    reasons_fn(dev, ctypes.byref(rs))
+                    if ok:
+                        self.rows.append((t, clk.value, pw.value / 1000.0, rs.value))
+                    time.sleep(0.0005)
+            self._thread = threading.Thread(target=run, daemon=True)
+            self._thread.start()
+        except Exception:
+            self._thread = None
+
+    @property
+    def ok(self) -> bool:
+        return self._thread is not None
+
+    def stop(self):
+        self._stop.set()
+        if self._thread:
+            self._thread.join(timeout=2)
+
+    def summarize(self, t0: float, t1: float) -> dict:
+        sel = [r for r in self.rows if t0 <= r[0] <= t1]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": "nvml"}
+        reasons = sorted({n for r in sel for bit, n in self.REASONS.items() if r[3] & bit})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(r[2] for r in sel), "reasons": reasons, "samples": len(sel), "source": "nvml"}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples, kept only inside [t_start, t_end]."""
 
@@ -281,8 +341,11 @@ def run_ours(args, rank, world, local):
 
     uuid = str(torch.cuda.get_device_properties(local).uuid)
     dev_id = uuid if uuid.startswith("GPU-") else ("GPU-" + uuid)
-    sampler = ClockSampler(dev_id)
+    nvml = NvmlSampler(dev_id)
+    sampler = None if nvml.ok else ClockSampler(dev_id)
     time.sleep(0.3)
+    switch = sys.getswitchinterval()
+    sys.setswitchinterval(0.0002)          # let the sampler thread run between launches
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     launches0 = g.launches
     barrier()
@@ -296,10 +359,14 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     barrier()
     t_end = time.time()
+    sys.setswitchinterval(switch)
     launches = g.launches - launches0
     plan = g.last_plan()
-    clock_rows = sampler.stop()
-    clocks = ClockSampler.summarize(clock_rows, t_start, t_end)
+    if sampler is None:
+        nvml.stop()
+        clocks = nvml.summarize(t_start, t_end)
+    else:
+        clocks = ClockSampler.summarize(sampler.stop(), t_start, t_end)
     st = g.status()
     if st != G.GEMM_OK:
         raise RuntimeError(f"timed run failed: {g.last_error()}")

@@ -42,9 +42,11 @@ const ConfigDesc kConfigs[kNumConfigs] = {
     make_desc<2, 1, 512, 4, 64>(7),   // 2-SM pair, 256 x 512 tile (two N=256 MMAs per K step)
 };
 
-// Relative tensor-core efficiency assumed per config when choosing one for a shape (larger
-// tiles need fewer loads per flop; the mainloop is bound by the TMA load rate per SM).
-const double kConfigEfficiency[kNumConfigs] = {0.85, 0.95, 0.70, 0.62, 0.94, 1.00, 0.96, 0.88};
+// Mainloop efficiency per config (measured k-iteration time of one long-K tile against the
+// config's tensor-core time at 1.9 GHz, cold L2, GB300): small tiles need more operand bytes per
+// flop and are bound by the TMA load rate per SM.  Config 7 is derated for its single accumulator
+// (its epilogue does not overlap the next tile).
+const double kConfigEfficiency[kNumConfigs] = {0.73, 0.78, 0.40, 0.39, 0.80, 0.85, 0.84, 0.75};
 
 int cluster_ctas(const ConfigDesc& d) { return d.cta_group * d.pairs; }
 int block_m(const ConfigDesc& d) { return 128 * cluster_ctas(d); }
@@ -195,6 +197,69 @@ gemm_status_t cuda_fail(gemm_handle_t h, const char* what, cudaError_t e) {
     return fail(h, GEMM_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
+// Time model of one config on one shape, in microseconds, used to choose the config and the
+// schedule.  A k-iteration of a cluster costs the CTA's FLOPs at the tensor rate scaled by the
+// config's efficiency; the exposed epilogue moves one CTA row block of C; a stream-K fix-up costs
+// one partial write plus one partial read per contributing cluster at a per-SM copy rate.
+struct Schedule {
+    int clusters = 0;
+    int stream_k = 0;
+    int dp_tiles = 0;
+    double est_us = 0.0;
+};
+
+constexpr double kFlopPerUsPerSm = 8192.0 * 1900.0;   // dense f16 FLOP per SM-clock x clock (MHz)
+constexpr double kSmBytesPerUs = 150.0e3;             // one SM's copy rate to or from L2 (B/us)
+constexpr double kLaunchUs = 2.0;                     // prologue and pipeline fill of one launch
+constexpr double kStreamKUs = 4.5;                    // measured fixed cost of a stream-K schedule (partial
+                                                      // stores, flag release and acquire, the extra unit)
+constexpr int kMaxSplit = 8;                          // clusters sharing one tile (split-K)
+
+Schedule schedule(const ConfigDesc& d, double eff, int64_t M, int64_t N, int64_t K, int P, int stream_k,
+                  int out_bytes, float beta) {
+    const int64_t bm = block_m(d);
+    const int64_t T = ((M + bm - 1) / bm) * ((N + d.block_n - 1) / d.block_n);
+    const int64_t kt = (K + d.block_k - 1) / d.block_k;
+    const double t_iter = 2.0 * 128.0 * d.block_n * d.block_k / (eff * kFlopPerUsPerSm);
+    const double t_epi = 128.0 * d.block_n * out_bytes * (beta != 0.0f ? 2.0 : 1.0) / kSmBytesPerUs;
+    const double t_part = 128.0 * d.block_n * 4.0 / kSmBytesPerUs;
+    // Data-parallel: whole waves of whole tiles.
+    Schedule best;
+    best.clusters = (int)std::min<int64_t>(T, P);
+    best.est_us = kLaunchUs + (double)((T + P - 1) / P) * kt * t_iter + t_epi;
+    if (stream_k == 0 || kt < 2) return best;
+    auto consider = [&](int C, int64_t dp_tiles) {
+        const int64_t sk_iters = (T - dp_tiles) * kt;
+        const int64_t base = sk_iters / C, extra = sk_iters % C;
+        if (base < 1) return;
+        const int64_t per = base + (extra ? 1 : 0);
+        // Partials the busiest head adds: the ranges that start strictly inside one tile.
+        int64_t srcs = 0, run = 0, run_tile = -1;
+        for (int64_t c = 1; c < C; ++c) {
+            const int64_t st = c * base + std::min<int64_t>(c, extra);
+            if (st % kt == 0) continue;
+            run = (st / kt == run_tile) ? run + 1 : 1;
+            run_tile = st / kt;
+            srcs = std::max(srcs, run);
+        }
+        if (srcs > kMaxSplit - 1) return;
+        Schedule s;
+        s.clusters = C;
+        s.stream_k = 1;
+        s.dp_tiles = (int)dp_tiles;
+        s.est_us = kLaunchUs + kStreamKUs + (double)(dp_tiles / C) * kt * t_iter + per * t_iter + (1 + srcs) * t_part +
+                   t_epi;
+        if (stream_k == 1 ? (!best.stream_k || s.est_us < best.est_us) : s.est_us < best.est_us * 0.99) best = s;
+    };
+    if (T > P) {
+        if (T % P != 0) consider(P, (T / P - 1) * P);      // the last wave and a half split K-wise
+    } else {
+        for (int64_t split = 2; split <= kMaxSplit; ++split)  // fewer tiles than clusters: split K
+            consider((int)std::min<int64_t>(P, T * split), 0);
+    }
+    return best;
+}
+
 // Pure host planning: validation, config choice, grid, stream-K split and workspace.
 //   slots[c]     clusters of config c that fit on the device at once
 //   cluster_cap  optional cap on launched clusters (0 = none)
@@ -224,26 +289,22 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
         if (cluster_cap > 0) s = std::min(s, cluster_cap);
         return s;
     };
+    const int out_bytes = elt_bytes(dout);
     int best = config;
     if (best < 0) {
-        double best_cost = 1e300;
+        double best_us = 1e300;
         for (int c = 0; c < kNumConfigs; ++c) {
-            const ConfigDesc& d = kConfigs[c];
             const int s = slots_of(c);
             if (s <= 0) continue;
-            const int64_t bm = block_m(d);
-            const int64_t tiles = ((M + bm - 1) / bm) * ((N + d.block_n - 1) / d.block_n);
-            // Whole waves, or (with the stream-K tail) the exact share plus a small fix-up cost.
-            double waves = (double)((tiles + s - 1) / s);
-            if (stream_k != 0 && tiles > s && tiles % s != 0) waves = std::min(waves, (double)tiles / s + 0.08);
-            const double cost = waves * (double)(bm * d.block_n) / (cluster_ctas(d) * kConfigEfficiency[c]);
-            if (cost < best_cost * (1.0 - 1e-9)) { best_cost = cost; best = c; }
+            const Schedule sc = schedule(kConfigs[c], kConfigEfficiency[c], M, N, K, s, stream_k, out_bytes, beta);
+            if (sc.est_us < best_us * (1.0 - 1e-9)) { best_us = sc.est_us; best = c; }
         }
         if (best < 0) { *err = "no config fits on this device"; return GEMM_ERR_UNSUPPORTED; }
     }
     const ConfigDesc& d = kConfigs[best];
     const int P = slots_of(best);
     if (P <= 0) { *err = "clusters of this config do not fit"; return GEMM_ERR_UNSUPPORTED; }
+    const Schedule sc = schedule(d, kConfigEfficiency[best], M, N, K, P, stream_k, out_bytes, beta);
     out->config = best;
     out->cta_group = d.cta_group;
     out->block_m = block_m(d);
@@ -252,27 +313,21 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     out->stages = d.stages;
     out->tiles_m = (int)((M + out->block_m - 1) / out->block_m);
     out->tiles_n = (int)((N + out->block_n - 1) / out->block_n);
-    const int64_t tiles = (int64_t)out->tiles_m * out->tiles_n;
-    out->clusters = (int)std::min<int64_t>(tiles, P);
+    out->clusters = sc.clusters;
     out->raster_group = std::min(out->tiles_m, 8);
-    out->tma_store = (beta == 0.0f && (ldc * elt_bytes(dout)) % 16 == 0) ? 1 : 0;
+    out->tma_store = ((ldc * out_bytes) % 16 == 0) ? 1 : 0;
     out->repack_a = (lda * 2) % 16 != 0;
     out->repack_b = (ldb * 2) % 16 != 0;
     int64_t ws = 0;
     if (out->repack_a) ws += round_up((la == GEMM_ROW ? M : K) * round_up(a_inner, 8) * 2, 256);
     if (out->repack_b) ws += round_up((lb == GEMM_ROW ? K : N) * round_up(b_inner, 8) * 2, 256);
-    // Stream-K tail: worthwhile when the last wave would leave more than 15% of the clusters idle.
-    const int C = out->clusters;
-    if (stream_k != 0 && tiles > C && tiles % C != 0) {
-        const double waves = (double)tiles / C;
-        if (stream_k == 1 || std::ceil(waves) - waves > 0.15) {
-            out->stream_k = 1;
-            out->dp_tiles = (int)((tiles / C - 1) * C);
-            out->sk_partial_bytes = round_up((int64_t)C * cluster_ctas(d) * 128 * d.block_n * 4, 256);
-        }
+    if (sc.stream_k) {
+        out->stream_k = 1;
+        out->dp_tiles = sc.dp_tiles;
+        out->sk_partial_bytes = round_up((int64_t)sc.clusters * cluster_ctas(d) * 128 * d.block_n * 4, 256);
     }
     out->workspace_bytes = ws + out->sk_partial_bytes;
-    out->kernels = 1 + out->repack_a + out->repack_b;
+    out->kernels = 1 + ((out->repack_a || out->repack_b) ? 1 : 0);
     return GEMM_OK;
 }
 
@@ -431,35 +486,37 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
     return GEMM_OK;
 }
 
-// Repack the operands whose byte pitch TMA cannot use into `ws` (16-byte pitch).  Updates the
-// operand pointers and leading dimensions; counts launches.
+// Repack the operands whose byte pitch TMA cannot use into `ws` (16-byte pitch), both in one
+// launch.  Updates the operand pointers and leading dimensions; counts launches.
 cudaError_t repack_operands(const gemm_plan_t& plan, int64_t M, int64_t N, int64_t K, int la, int lb, void* ws,
-                            const void** A, int64_t* lda, const void** B, int64_t* ldb, cudaStream_t s,
-                            int64_t* launches, const char** what) {
+                            const void** A, int64_t* lda, const void** B, int64_t* ldb, int num_sms,
+                            cudaStream_t s, int64_t* launches, const char** what) {
     char* w = static_cast<char*>(ws);
+    RepackJobs jobs{};
     if (plan.repack_a) {
         const int64_t rows = la == GEMM_ROW ? M : K;
         const int64_t cols = la == GEMM_ROW ? K : M;
         const int64_t ld = round_up(cols, 8);
-        *what = "repack of A";
-        cudaError_t e = launch_repack_u16(*A, *lda, w, ld, rows, cols, s);
-        if (e != cudaSuccess) return e;
+        jobs.job[jobs.n++] = RepackJob{static_cast<const uint16_t*>(*A), *lda, reinterpret_cast<uint16_t*>(w), ld,
+                                       rows, cols};
         *A = w;
         *lda = ld;
         w += round_up(rows * ld * 2, 256);
-        ++*launches;
     }
     if (plan.repack_b) {
         const int64_t rows = lb == GEMM_ROW ? K : N;
         const int64_t cols = lb == GEMM_ROW ? N : K;
         const int64_t ld = round_up(cols, 8);
-        *what = "repack of B";
-        cudaError_t e = launch_repack_u16(*B, *ldb, w, ld, rows, cols, s);
-        if (e != cudaSuccess) return e;
+        jobs.job[jobs.n++] = RepackJob{static_cast<const uint16_t*>(*B), *ldb, reinterpret_cast<uint16_t*>(w), ld,
+                                       rows, cols};
         *B = w;
         *ldb = ld;
-        ++*launches;
     }
+    if (jobs.n == 0) return cudaSuccess;
+    *what = "repack of the operands";
+    cudaError_t e = launch_repack_u16(jobs, num_sms, s);
+    if (e != cudaSuccess) return e;
+    ++*launches;
     return cudaSuccess;
 }
 
@@ -756,7 +813,7 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
                                "workspace allocation");
             if (st != GEMM_OK) return st;
             cudaError_t e = repack_operands(plan, M, N, K, layoutA, layoutB, h->ws, &a_ptr, &lda_eff, &b_ptr, &ldb_eff,
-                                            s, &h->launches, &what);
+                                            h->dev.num_sms, s, &h->launches, &what);
             if (e != cudaSuccess) return cuda_fail(h, what, e);
         }
         if (plan.stream_k) {
@@ -875,8 +932,8 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     const void* b_ptr = B;
     int64_t lda_eff = lda, ldb_eff = ldb, launches = 0;
     const char* what = "";
-    if (repack_operands(plan, M, N, K, layoutA, layoutB, nd.scratch, &a_ptr, &lda_eff, &b_ptr, &ldb_eff, s, &launches,
-                        &what) != cudaSuccess)
+    if (repack_operands(plan, M, N, K, layoutA, layoutB, nd.scratch, &a_ptr, &lda_eff, &b_ptr, &ldb_eff,
+                        nd.info.num_sms, s, &launches, &what) != cudaSuccess)
         return GEMM_ERR_CUDA;
     LaunchArgs la{&plan, M, N, K, a_ptr, lda_eff, b_ptr, ldb_eff, C, ldc, dtype_in, dtype_out, layoutA, layoutB,
                   alpha, beta, bias, nd.status, 2000ull * 1000000ull, -1, 0, nullptr, nullptr, 0, s, false};

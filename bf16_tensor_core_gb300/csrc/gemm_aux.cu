@@ -2,6 +2,7 @@
 //  * repack of a 16-bit operand whose byte pitch is not a multiple of 16 into a workspace with a
 //    16-byte pitch (TMA tensor maps require 16-byte-multiple strides);
 //  * the K == 0 epilogue, C = beta * C + bias (the product of an empty sum is zero).
+#include <algorithm>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -12,39 +13,66 @@
 
 namespace gb300 {
 
-// Copy a rows x cols block of 16-bit elements from pitch `lds` to pitch `ldd` (elements).
-// When both pitches are even and cols is even, pairs move as 32-bit words.
-__global__ void repack_u16_kernel(const uint16_t* __restrict__ src, long long lds, uint16_t* __restrict__ dst,
-                                  long long ldd, long long rows, long long cols, int pairs) {
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    if (pairs) {
-        const long long wc = cols / 2;
-        const long long total = rows * wc;
-        for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-            const long long r = i / wc, c = i - r * wc;
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(src + r * lds + 2 * c);
-            *reinterpret_cast<uint32_t*>(dst + r * ldd + 2 * c) = w;
+// Copy rows x cols blocks of 16-bit elements from pitch `lds` to a pitch `ldd` that is a multiple
+// of 8 elements (16 bytes) on a 16-byte-aligned destination.  A warp moves 32 consecutive 16-byte
+// destination chunks of one row; each chunk is read with the widest loads the source address allows
+// (one 16-byte load, four 4-byte loads, or eight 2-byte loads) and written with one 16-byte store.
+// Destination columns [cols, ldd) are zero-filled.  blockIdx.y selects the job (A or B).
+__global__ void __launch_bounds__(256) repack_u16_kernel(RepackJobs jobs) {
+    const RepackJob j = blockIdx.y == 0 ? jobs.job[0] : jobs.job[1];   // (no dynamic index into the parameter)
+    const long long chunks = j.ldd / 8;
+    const long long segs = (chunks + 31) / 32;
+    const long long items = j.rows * segs;
+    const int lane = threadIdx.x & 31;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+    for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5); w < items;
+         w += warps) {
+        const long long r = w / segs;
+        const long long chunk = (w - r * segs) * 32 + lane;
+        if (chunk >= chunks) continue;
+        const long long c0 = chunk * 8;
+        const uint16_t* src = j.src + r * j.lds + c0;
+        uint4 out;
+        if (c0 + 8 <= j.cols) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+            if ((a & 15u) == 0) {
+                out = __ldg(reinterpret_cast<const uint4*>(src));
+            } else if ((a & 3u) == 0) {
+                const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src);
+                out = make_uint4(__ldg(s32), __ldg(s32 + 1), __ldg(s32 + 2), __ldg(s32 + 3));
+            } else {
+                uint32_t wds[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    wds[i] = static_cast<uint32_t>(__ldg(src + 2 * i)) | (static_cast<uint32_t>(__ldg(src + 2 * i + 1)) << 16);
+                out = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+            }
+        } else {
+            uint32_t wds[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (c0 + i < j.cols) wds[i / 2] |= static_cast<uint32_t>(__ldg(src + i)) << (16 * (i & 1));
+            out = make_uint4(wds[0], wds[1], wds[2], wds[3]);
         }
-    } else {
-        const long long total = rows * cols;
-        for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-            const long long r = i / cols, c = i - r * cols;
-            dst[r * ldd + c] = src[r * lds + c];
-        }
+        *reinterpret_cast<uint4*>(j.dst + r * j.ldd + c0) = out;
     }
 }
 
-cudaError_t launch_repack_u16(const void* src, long long lds, void* dst, long long ldd, long long rows,
-                              long long cols, cudaStream_t stream) {
-    if (rows <= 0 || cols <= 0) return cudaSuccess;
-    const int pairs = ((lds % 2) == 0 && (ldd % 2) == 0 && (cols % 2) == 0 &&
-                       (reinterpret_cast<uintptr_t>(src) % 4) == 0 && (reinterpret_cast<uintptr_t>(dst) % 4) == 0)
-                          ? 1 : 0;
-    const long long work = pairs ? rows * (cols / 2) : rows * cols;
-    long long blocks = (work + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    repack_u16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(src), lds, static_cast<uint16_t*>(dst), ldd, rows, cols, pairs);
+cudaError_t launch_repack_u16(const RepackJobs& jobs, int num_sms, cudaStream_t stream) {
+    if (jobs.n <= 0) return cudaSuccess;
+    long long items = 0;
+    for (int i = 0; i < jobs.n; ++i) {
+        const RepackJob& j = jobs.job[i];
+        if (j.ldd % 8 != 0 || j.ldd < j.cols || (reinterpret_cast<uintptr_t>(j.dst) & 15u) != 0 ||
+            (reinterpret_cast<uintptr_t>(j.src) & 1u) != 0)
+            return cudaErrorInvalidValue;
+        items = std::max(items, j.rows * ((j.ldd / 8 + 31) / 32));
+    }
+    if (items <= 0) return cudaSuccess;
+    long long blocks = (items + 7) / 8;
+    const long long cap = static_cast<long long>(num_sms > 0 ? num_sms : 152) * 8;
+    if (blocks > cap) blocks = cap;
+    repack_u16_kernel<<<dim3(static_cast<unsigned>(blocks), static_cast<unsigned>(jobs.n)), 256, 0, stream>>>(jobs);
     return cudaGetLastError();
 }
 

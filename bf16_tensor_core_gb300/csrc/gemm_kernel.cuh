@@ -47,16 +47,19 @@ struct KernelParams {
     long long ldc;             // elements
     const void* bias;          // N elements of the output type, or nullptr
     float alpha, beta;
-    int use_tma_store;         // write C with TMA tensor stores (requires beta == 0)
+    int use_tma_store;         // write C with TMA tensor stores (with beta != 0, C_in boxes arrive by TMA loads)
     int c_vec_ok;              // C rows may be accessed with 16-byte vectors
     unsigned long long* status;
     unsigned long long timeout_ns;
     long long debug_skip_stage;  // test only: cluster 0's producer never issues this stage
-    // Stream-K tail (sk_enabled != 0): tiles [0, dp_tiles) are walked data-parallel; the k-iterations
-    // of tiles [dp_tiles, num_tiles) are divided evenly over the clusters (sk_base or sk_base + 1
-    // each, the first sk_extra clusters taking one more).  Every range is at least k_tiles long, so
-    // a split tile has exactly two segments: the head [0, k1) and the tail [k1, k_tiles) computed by
-    // the next cluster, which parks its f32 partial in sk_partials and raises its flags to `epoch`.
+    // Stream-K (sk_enabled != 0): tiles [0, dp_tiles) are walked data-parallel; the k-iterations of
+    // tiles [dp_tiles, num_tiles) are divided evenly over the clusters (sk_base or sk_base + 1 each,
+    // the first sk_extra clusters taking one more).  Each cluster's range is contiguous, so only its
+    // first segment can start inside a tile (k0 > 0): that segment's f32 partial goes to the
+    // cluster's slot of sk_partials and its flags are raised to `epoch`.  The segment that starts a
+    // tile (the head, always a cluster's last) waits for the clusters after it that cover the rest
+    // of the tile -- one when ranges are at least k_tiles long, several when a tile is split K-wise
+    // over more clusters than there are tiles -- and adds their partials in cluster order.
     int sk_enabled;
     int dp_tiles;
     long long sk_base;
@@ -71,8 +74,13 @@ enum : int { UNIT_FULL = 0, UNIT_HEAD = 1, UNIT_TAIL = 2 };
 struct Unit {
     int tile;
     int k0, k1;   // k-tile range [k0, k1) of this tile computed here
-    int kind;     // UNIT_FULL, UNIT_HEAD (adds the next cluster's partial), UNIT_TAIL (writes a partial)
+    int kind;     // UNIT_FULL, UNIT_HEAD (adds the partials of the following clusters), UNIT_TAIL (writes a partial)
 };
+
+// First stream-K iteration of cluster c.
+__device__ __forceinline__ long long sk_range_start(const KernelParams& p, int c) {
+    return static_cast<long long>(c) * p.sk_base + min(c, p.sk_extra);
+}
 
 // The deterministic sequence of work units of one cluster, identical in every role.
 struct UnitIter {
@@ -84,7 +92,7 @@ struct UnitIter {
         stride = num_clusters;
         dp_limit = p.sk_enabled ? p.dp_tiles : p.num_tiles;
         if (p.sk_enabled) {
-            it = static_cast<long long>(cluster) * p.sk_base + min(cluster, p.sk_extra);
+            it = sk_range_start(p, cluster);
             it_end = it + p.sk_base + (cluster < p.sk_extra ? 1 : 0);
         } else {
             it = it_end = 0;
@@ -194,6 +202,37 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     }
 }
 
+// The two 16-bit values of a packed word (low half first), widened to f32.
+template <int kOut>
+__device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
+    if constexpr (kOut == OUT_F16) {
+        lo = __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+        hi = __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+    } else {
+        lo = __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(w & 0xffffu)));
+        hi = __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(w >> 16)));
+    }
+}
+
+// v[0..31] = alpha * acc + beta * cin + bias for columns col0 .. col0+31, C_in already in registers.
+template <int kOut>
+__device__ __forceinline__ void epilogue_math_cin(const KernelParams& p, const uint32_t (&acc)[32], float (&v)[32],
+                                                  const float (&cin)[32], int col0) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
+    if (p.alpha != 1.0f) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= p.alpha;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = fmaf(p.beta, cin[i], v[i]);
+    if (p.bias != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (col0 + i < p.N) v[i] += load_out<kOut>(p.bias, col0 + i);
+    }
+}
+
 // v[0..31] = alpha * acc + beta * C_in + bias for columns col0 .. col0+31 of `row`.
 template <int kOut>
 __device__ __forceinline__ void epilogue_math(const KernelParams& p, const uint32_t (&acc)[32], float (&v)[32],
@@ -263,33 +302,104 @@ __device__ __forceinline__ void store_row_direct(const KernelParams& p, const fl
     }
 }
 
+// Ask L2 for the C_in lines of `row`, columns [col0, col0 + kCols) clipped to N, while the
+// accumulator is still being computed: the epilogue then reads them from L2 instead of HBM.
+template <int kOut, int kCols>
+__device__ __forceinline__ void prefetch_c_rows(const KernelParams& p, int row, int col0) {
+    if (row >= p.M || col0 >= p.N) return;
+    constexpr int kElt = (kOut == OUT_F32) ? 4 : 2;
+    const char* base = static_cast<const char*>(p.C) + (static_cast<long long>(row) * p.ldc + col0) * kElt;
+    const int bytes = (min(kCols, p.N - col0)) * kElt;
+    const int first = static_cast<int>(reinterpret_cast<uintptr_t>(base) & 127u);
+    for (int off = -first; off < bytes; off += 128)
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(reinterpret_cast<uint64_t>(base + max(off, 0))));
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
 }
 
-// Stream-K partial layout inside one CTA's slot: [BN / 4 column quads][128 rows][4 f32], so a warp
-// moving one quad of its 32 rows touches 512 contiguous bytes.
-__device__ __forceinline__ void add_partial_32(uint32_t (&acc)[32], const float* part, int col, int prow) {
-    const float4* src = reinterpret_cast<const float4*>(part);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float4 v = __ldcg(&src[(col / 4 + j) * 128 + prow]);
-        acc[4 * j + 0] = __float_as_uint(__uint_as_float(acc[4 * j + 0]) + v.x);
-        acc[4 * j + 1] = __float_as_uint(__uint_as_float(acc[4 * j + 1]) + v.y);
-        acc[4 * j + 2] = __float_as_uint(__uint_as_float(acc[4 * j + 2]) + v.z);
-        acc[4 * j + 3] = __float_as_uint(__uint_as_float(acc[4 * j + 3]) + v.w);
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+// Stream-K partials.  Inside one CTA's slot the data of epilogue warp ew (its 32 rows x kCols
+// columns) is one contiguous block [kCols / 4 column quads][32 lanes][4 f32]: a warp store of one
+// quad is 512 contiguous bytes, and 64 columns (8 KB) are one contiguous piece.
+constexpr uint32_t kFixPieceBytes = 64 * 32 * 4;   // 64 columns x 32 rows of f32
+constexpr int kFixBufs = 3;                        // pieces in flight per warp
+
+// Head fix-up: add the partials of `count` consecutive clusters (slots `stride` floats apart,
+// `first` already at this warp's block) into this warp's accumulator columns in TMEM, in cluster
+// order.  The head is always its cluster's last unit, so the operand ring is idle: each warp stages
+// pieces through its own kFixBufs x 8 KB of it with bulk copies, kFixBufs in flight.
+template <int kCols>
+__device__ __forceinline__ bool head_fixup(uint32_t tbase, int lane, const float* first, int count, size_t stride,
+                                           uint32_t region, uint32_t bar0, uint64_t timeout_ns,
+                                           const volatile int* abort_flag) {
+    static_assert(kCols % 64 == 0, "whole 64-column pieces");
+    constexpr int kPieces = kCols / 64;
+    const int n = count * kPieces;
+    auto issue = [&](int i) {
+        const int src = i / kPieces;
+        const int pc = i - src * kPieces;
+        const uint32_t b = static_cast<uint32_t>(i % kFixBufs);
+        mbar_arrive_expect_tx(bar0 + 8u * b, kFixPieceBytes);
+        bulk_load_g2s(region + b * kFixPieceBytes, first + static_cast<size_t>(src) * stride + pc * (64 * 32),
+                      kFixPieceBytes, bar0 + 8u * b);
+    };
+    if (lane == 0) {
+        fence_proxy_async_global();   // the flags were acquired by this thread in the generic proxy
+        for (int i = 0; i < n && i < kFixBufs; ++i) issue(i);
     }
+    __syncwarp();
+#pragma unroll 1
+    for (int i = 0; i < n; ++i) {
+        const uint32_t b = static_cast<uint32_t>(i % kFixBufs);
+        bool ok = mbar_wait_bounded(bar0 + 8u * b, static_cast<uint32_t>((i / kFixBufs) & 1), timeout_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        const uint32_t buf = region + b * kFixPieceBytes;
+        const uint32_t tpiece = tbase + static_cast<uint32_t>((i % kPieces) * 64);
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+            uint32_t acc[32];
+            tmem_ld_32x32b_x32(tpiece + cc * 32, acc);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 v = ld_shared_f4(buf + static_cast<uint32_t>(((cc * 8 + j) * 32 + lane) * 16));
+                acc[4 * j + 0] = __float_as_uint(__uint_as_float(acc[4 * j + 0]) + v.x);
+                acc[4 * j + 1] = __float_as_uint(__uint_as_float(acc[4 * j + 1]) + v.y);
+                acc[4 * j + 2] = __float_as_uint(__uint_as_float(acc[4 * j + 2]) + v.z);
+                acc[4 * j + 3] = __float_as_uint(__uint_as_float(acc[4 * j + 3]) + v.w);
+            }
+            tmem_st_32x32b_x32(tpiece + cc * 32, acc);
+        }
+        tmem_wait_st();
+        __syncwarp();
+        if (lane == 0 && i + kFixBufs < n) {
+            fence_proxy_async_smem();   // this warp's reads of the buffer precede the next copy into it
+            issue(i + kFixBufs);
+        }
+    }
+    return true;
 }
 
 // One warp drains its 32 TMEM lanes (32 rows) x kCols columns of one accumulator buffer, starting at
 // tile column pcol0 (tbase already points there).
-//   out_part != nullptr: a stream-K tail segment; the raw f32 sums go to the partial slot, C is untouched.
-//   add_part != nullptr: a stream-K head segment; the next cluster's partial is added before the epilogue.
+//   out_part != nullptr: a stream-K tail segment; the raw f32 sums go to this warp's block of the
+//   partial slot (layout above), C is untouched.
+//   With beta != 0 on the TMA path, each box of C_in is first TMA-loaded into the warp's staging
+//   buffer (completing on cin_bar; *cin_uses counts this warp's loads for the barrier parity), read
+//   back row per lane, and the result overwrites it in place before the TMA store.
 template <int kOut, int kCols>
-__device__ __forceinline__ void epilogue_tile(const KernelParams& p, const CUtensorMap* tmC, uint32_t tbase,
-                                              int row0, int col_base, int pcol0, int lane, int prow,
-                                              uint32_t stage_buf, const float* add_part, float* out_part) {
+__device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUtensorMap* tmC, uint32_t tbase,
+                                              int row0, int col_base, int lane, uint32_t stage_buf,
+                                              float* out_part, uint32_t cin_bar, uint32_t* cin_uses,
+                                              const volatile int* abort_flag) {
     const int row = row0 + lane;
     if (out_part != nullptr) {
         float4* dst = reinterpret_cast<float4*>(out_part);
@@ -300,50 +410,80 @@ __device__ __forceinline__ void epilogue_tile(const KernelParams& p, const CUten
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                __stcg(&dst[(pcol0 / 4 + c * 8 + j) * 128 + prow],
+                __stcg(&dst[(c * 8 + j) * 32 + lane],
                        make_float4(__uint_as_float(acc[4 * j]), __uint_as_float(acc[4 * j + 1]),
                                    __uint_as_float(acc[4 * j + 2]), __uint_as_float(acc[4 * j + 3])));
         }
-        return;
+        return true;
     }
     if (p.use_tma_store) {
         // A chunk is one 128-byte line per row: 64 columns of a 16-bit type, 32 of f32.
         constexpr int kChunk = (kOut == OUT_F32) ? 32 : 64;
         const bool warp_rows_in = row0 < p.M;
+        const uint32_t row_addr = stage_buf + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll 1
         for (int c = 0; c < kCols / kChunk; ++c) {
             const int col0 = col_base + c * kChunk;
-            uint32_t words[32];
-            if constexpr (kOut == OUT_F32) {
-                uint32_t acc[32];
-                tmem_ld_32x32b_x32(tbase + c * 32, acc);
-                tmem_wait_ld();
-                if (add_part) add_partial_32(acc, add_part, pcol0 + c * 32, prow);
-                float v[32];
-                epilogue_math<kOut>(p, acc, v, row, col0);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) words[i] = __float_as_uint(v[i]);
-            } else {
-                uint32_t acc0[32], acc1[32];
-                tmem_ld_32x32b_x32(tbase + c * 64, acc0);
-                tmem_ld_32x32b_x32(tbase + c * 64 + 32, acc1);
-                tmem_wait_ld();
-                if (add_part) {
-                    add_partial_32(acc0, add_part, pcol0 + c * 64, prow);
-                    add_partial_32(acc1, add_part, pcol0 + c * 64 + 32, prow);
-                }
-                float v[32];
-                epilogue_math<kOut>(p, acc0, v, row, col0);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) words[i] = pack2<kOut>(v[2 * i], v[2 * i + 1]);
-                epilogue_math<kOut>(p, acc1, v, row, col0 + 32);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) words[16 + i] = pack2<kOut>(v[2 * i], v[2 * i + 1]);
+            const bool box_in = warp_rows_in && col0 < p.N;   // warp-uniform
+            const bool with_cin = box_in && p.beta != 0.0f;
+            if (with_cin && lane == 0) {
+                bulk_wait_group_read<0>();                    // the previous store has read the buffer
+                mbar_arrive_expect_tx(cin_bar, 32u * 128u);
+                tma_load_2d(stage_buf, tmC, col0, row0, cin_bar);
             }
-            if (!warp_rows_in || col0 >= p.N) continue;   // whole box outside C (warp-uniform)
-            if (lane == 0) bulk_wait_group_read<0>();     // the previous store has read the buffer
+            uint32_t words[32];
+            uint32_t acc0[32], acc1[32];
+            tmem_ld_32x32b_x32(tbase + c * (kChunk == 32 ? 32 : 64), acc0);
+            if constexpr (kChunk == 64) tmem_ld_32x32b_x32(tbase + c * 64 + 32, acc1);
+            tmem_wait_ld();
+            float v[32];
+            if (with_cin) {
+                const bool ok = mbar_wait_bounded(cin_bar, *cin_uses & 1u, p.timeout_ns, abort_flag);
+                ++*cin_uses;
+                if (!__all_sync(0xffffffffu, ok)) return false;
+                // Row `lane` of the box: 16-byte piece j sits at piece j ^ (lane & 7) (128-byte swizzle).
+                uint32_t cw[32];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 q = ld_shared_f4(row_addr + ((static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u)) * 16u));
+                    cw[4 * j + 0] = __float_as_uint(q.x);
+                    cw[4 * j + 1] = __float_as_uint(q.y);
+                    cw[4 * j + 2] = __float_as_uint(q.z);
+                    cw[4 * j + 3] = __float_as_uint(q.w);
+                }
+                float cin[32];
+                if constexpr (kOut == OUT_F32) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) cin[i] = __uint_as_float(cw[i]);
+                    epilogue_math_cin<kOut>(p, acc0, v, cin, col0);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) words[i] = __float_as_uint(v[i]);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) unpack2<kOut>(cw[16 * h + i], cin[2 * i], cin[2 * i + 1]);
+                        epilogue_math_cin<kOut>(p, h == 0 ? acc0 : acc1, v, cin, col0 + 32 * h);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) words[16 * h + i] = pack2<kOut>(v[2 * i], v[2 * i + 1]);
+                    }
+                }
+            } else {
+                epilogue_math<kOut>(p, acc0, v, row, col0);
+                if constexpr (kOut == OUT_F32) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) words[i] = __float_as_uint(v[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) words[i] = pack2<kOut>(v[2 * i], v[2 * i + 1]);
+                    epilogue_math<kOut>(p, acc1, v, row, col0 + 32);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) words[16 + i] = pack2<kOut>(v[2 * i], v[2 * i + 1]);
+                }
+            }
+            if (!box_in) continue;                            // whole box outside C
+            if (!with_cin && lane == 0) bulk_wait_group_read<0>();   // the previous store has read the buffer
             __syncwarp();
-            const uint32_t row_addr = stage_buf + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t piece = static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u);  // 128B swizzle
@@ -364,12 +504,12 @@ __device__ __forceinline__ void epilogue_tile(const KernelParams& p, const CUten
             tmem_ld_32x32b_x32(tbase + c * 32, acc);
             tmem_wait_ld();
             if (col0 >= p.N) continue;
-            if (add_part) add_partial_32(acc, add_part, pcol0 + c * 32, prow);
             float v[32];
             epilogue_math<kOut>(p, acc, v, row, col0);
             store_row_direct<kOut>(p, v, row, col0);
         }
     }
+    return true;
 }
 
 __device__ __forceinline__ void st_release_gpu(unsigned* addr, unsigned v) {
@@ -409,6 +549,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     using Cfg = TileConfig<kCtaGroup, kBN, kStages, kBK>;
     static_assert(kPairs == 1 || kCtaGroup == 2, "pairs of CTAs need cta_group::2");
     static_assert(kPairs == 1 || Cfg::kNHalves == 1, "B multicast is built for one MMA per K step");
+    static_assert(Cfg::kRingBytes >= Cfg::kEpiWarps * kFixBufs * static_cast<int>(kFixPieceBytes),
+                  "the head fix-up stages its pieces in the operand ring");
     constexpr int kClusterCtas = kCtaGroup * kPairs;
     constexpr int kClusterRows = Cfg::kBM * kClusterCtas;      // output rows of one cluster tile
     extern __shared__ uint8_t smem_raw[];
@@ -417,6 +559,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __shared__ __align__(8) uint64_t bar_tfull[2];
     __shared__ __align__(8) uint64_t bar_tempty[2];
     __shared__ __align__(8) uint64_t bar_drain;
+    __shared__ __align__(8) uint64_t bar_fix[Cfg::kEpiWarps * kFixBufs];   // stream-K head fix-up pieces
+    __shared__ __align__(8) uint64_t bar_cin[Cfg::kEpiWarps];              // C_in boxes (beta != 0, TMA path)
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
 
@@ -445,6 +589,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             mbar_init(smem_u32(&bar_tempty[b]), Cfg::kEpiWarps * kCtaGroup);
         }
         mbar_init(smem_u32(&bar_drain), 1);
+        for (int b = 0; b < Cfg::kEpiWarps * kFixBufs; ++b) mbar_init(smem_u32(&bar_fix[b]), 1);
+        for (int b = 0; b < Cfg::kEpiWarps; ++b) mbar_init(smem_u32(&bar_cin[b]), 1);
         fence_barrier_init();
     }
     if (threadIdx.x == 32) {
@@ -635,16 +781,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
         const int ew = warp - 2;
         const int pcol0 = (ew / 4) * Cfg::kEpiCols;   // first tile column this warp drains
-        const int prow = quarter * 32 + lane;         // row within this CTA's 128
         const uint32_t stage_buf = epi_smem + static_cast<uint32_t>(ew) * Cfg::kEpiBufBytes;
         const size_t slot_floats = static_cast<size_t>(kClusterCtas) * 128 * kBN;
-        uint32_t acc = 0, acc_phase = 0;
+        // This warp's block inside a CTA slot of the partials.
+        const size_t warp_block = static_cast<size_t>(rank) * 128 * kBN + static_cast<size_t>(ew) * Cfg::kEpiCols * 32;
+        uint32_t acc = 0, acc_phase = 0, cin_uses = 0;
         UnitIter units;
         units.init(p, cluster_id, num_clusters);
         Unit u;
         while (units.next(p, u)) {
             int mb, nb;
             tile_coords(p, u.tile, mb, nb);
+            const int row0 = mb * kClusterRows + static_cast<int>(rank) * Cfg::kBM + quarter * 32;
+            if (p.beta != 0.0f && u.kind != UNIT_TAIL)
+                prefetch_c_rows<kOut, Cfg::kEpiCols>(p, row0 + lane, nb * kBN + pcol0);
             bool ok = mbar_wait_bounded(smem_u32(&bar_tfull[acc]), acc_phase, p.timeout_ns, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
@@ -653,31 +803,41 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 break;
             }
             tc_fence_after_sync();
-            const float* add_part = nullptr;
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   acc * static_cast<uint32_t>(Cfg::kAccCols) + static_cast<uint32_t>(pcol0);
             float* out_part = nullptr;
             if (u.kind == UNIT_TAIL) {
-                out_part = p.sk_partials + static_cast<size_t>(cluster_id) * slot_floats +
-                           static_cast<size_t>(rank) * 128 * kBN;
+                out_part = p.sk_partials + static_cast<size_t>(cluster_id) * slot_floats + warp_block;
             } else if (u.kind == UNIT_HEAD) {
-                // The tail [k1, k_tiles) of this tile is the first unit of the next cluster.
-                const int src = cluster_id + 1;
-                const unsigned* flag = p.sk_flags + (static_cast<size_t>(src) * kClusterCtas + rank) * Cfg::kEpiWarps + ew;
+                // The rest of this tile, [k1, k_tiles), is the first unit of each following cluster
+                // whose range starts before the tile ends.
+                const long long tile_end = static_cast<long long>(u.tile - p.dp_tiles + 1) * p.k_tiles;
+                int n = 0;
                 bool ready = true;
-                if (lane == 0) ready = wait_flag_bounded(flag, p.epoch, p.timeout_ns, abort_flag);
+                for (int src = cluster_id + 1; src < num_clusters && sk_range_start(p, src) < tile_end; ++src, ++n) {
+                    const unsigned* flag =
+                        p.sk_flags + (static_cast<size_t>(src) * kClusterCtas + rank) * Cfg::kEpiWarps + ew;
+                    if (lane == 0 && ready) ready = wait_flag_bounded(flag, p.epoch, p.timeout_ns, abort_flag);
+                }
                 ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+                if (ready) {
+                    ready = head_fixup<Cfg::kEpiCols>(
+                        tbase, lane, p.sk_partials + static_cast<size_t>(cluster_id + 1) * slot_floats + warp_block, n,
+                        slot_floats, ring + static_cast<uint32_t>(ew) * kFixBufs * kFixPieceBytes,
+                        smem_u32(&bar_fix[ew * kFixBufs]), p.timeout_ns, abort_flag);
+                }
                 if (!ready) {
                     if (lane == 0 && !*abort_flag)
                         report_error<kClusterCtas>(p, ROLE_EPILOGUE, u.tile, 300 + quarter, abort_flag);
                     break;
                 }
-                add_part = p.sk_partials + static_cast<size_t>(src) * slot_floats +
-                           static_cast<size_t>(rank) * 128 * kBN;
             }
-            const int row0 = mb * kClusterRows + static_cast<int>(rank) * Cfg::kBM + quarter * 32;
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   acc * static_cast<uint32_t>(Cfg::kAccCols) + static_cast<uint32_t>(pcol0);
-            epilogue_tile<kOut, Cfg::kEpiCols>(p, &tmC, tbase, row0, nb * kBN + pcol0, pcol0, lane, prow, stage_buf,
-                                               add_part, out_part);
+            if (!epilogue_tile<kOut, Cfg::kEpiCols>(p, &tmC, tbase, row0, nb * kBN + pcol0, lane, stage_buf, out_part,
+                                                    smem_u32(&bar_cin[ew]), &cin_uses, abort_flag)) {
+                if (lane == 0 && !*abort_flag)
+                    report_error<kClusterCtas>(p, ROLE_EPILOGUE, u.tile, 400 + quarter, abort_flag);
+                break;
+            }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {

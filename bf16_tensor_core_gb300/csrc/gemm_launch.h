@@ -1,5 +1,6 @@
 // Host-side view of the kernel configurations (no device code).
 #pragma once
+#include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -58,8 +59,18 @@ cudaError_t cfg7_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap
                         const CUtensorMap& c, const KernelParams& p);
 
 // Auxiliary kernels (gemm_aux.cu).
-cudaError_t launch_repack_u16(const void* src, long long lds, void* dst, long long ldd, long long rows,
-                              long long cols, cudaStream_t stream);
+struct RepackJob {
+    const uint16_t* src;   // rows x cols elements at pitch lds (2-byte aligned)
+    long long lds;
+    uint16_t* dst;         // rows x ldd elements, 16-byte aligned, ldd a multiple of 8 and >= cols
+    long long ldd;
+    long long rows, cols;
+};
+struct RepackJobs {
+    RepackJob job[2];
+    int n;                 // jobs in use (0..2), all moved by one launch
+};
+cudaError_t launch_repack_u16(const RepackJobs& jobs, int num_sms, cudaStream_t stream);
 cudaError_t launch_scale_bias(int out, void* C, long long ldc, const void* bias, float beta, long long M,
                               long long N, int num_sms, cudaStream_t stream);
 

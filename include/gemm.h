@@ -110,7 +110,8 @@ typedef struct {
     int tiles_m, tiles_n;  /* output tiles                                                  */
     int clusters;          /* persistent clusters launched (grid = clusters * cta_group)    */
     int raster_group;      /* tile rows per raster group                                    */
-    int tma_store;         /* 1: epilogue writes C with TMA tensor stores; 0: st.global     */
+    int tma_store;         /* 1: epilogue moves C boxes by TMA (C_in loads when beta != 0,
+                              then tensor stores); 0: per-row st.global / ld.global        */
     int repack_a, repack_b;/* 1: operand copied to a 16-byte pitch workspace first          */
     int64_t workspace_bytes; /* repack workspace + stream-K partials                        */
     int kernels;           /* kernel launches the call makes                                */

@@ -129,11 +129,11 @@ def test_plan_repack_and_workspace(lib):
     # 2050 halves = 4100 bytes is not a multiple of 16: both operands go through the workspace
     st, p = plan(1000, 3000, 2050, lda=2050, ldb=2050, la=0, lb=1, beta=1.0)
     assert st == G.GEMM_OK
-    assert p.repack_a == 1 and p.repack_b == 1 and p.kernels == 3
+    assert p.repack_a == 1 and p.repack_b == 1 and p.kernels == 2
     a_bytes = -(-1000 * 2056 * 2 // 256) * 256
     b_bytes = -(-3000 * 2056 * 2 // 256) * 256
     assert p.workspace_bytes == a_bytes + b_bytes + p.sk_partial_bytes
-    assert p.tma_store == 0                             # beta != 0 reads C: direct-store epilogue
+    assert p.tma_store == 1                             # 12000-byte rows: C_in loaded and C stored by TMA
     st, p = plan(64, 64, 64, lda=72, ldb=64)
     assert p.repack_a == 0 and p.repack_b == 0 and p.workspace_bytes == 0
     st, p = plan(64, 63, 64, ldc=63, dout=0)            # 126-byte rows: TMA cannot store C
@@ -169,14 +169,16 @@ def test_plan_stream_k(lib):
     assert p.stream_k == 0 and p.sk_partial_bytes == 0 and p.workspace_bytes == 0
     st, p = plan(256 * 19, 256 * 8, 1024, config=1)              # 152 tiles = 2 whole waves
     assert p.stream_k == 0
-    st, p = plan(1024, 1024, 1024, config=1)                     # 16 tiles < 76 clusters
-    assert p.stream_k == 0
+    st, p = plan(1024, 1024, 1024, config=1, sk=0)               # 16 tiles < 76 clusters, split-K off
+    assert p.stream_k == 0 and p.clusters == 16
+    st, p = plan(1024, 1024, 1024, config=1, sk=1)               # split-K: each tile over several clusters
+    assert p.stream_k == 1 and p.dp_tiles == 0 and 16 < p.clusters <= 76
     st, p = plan(256 * 9, 256 * 9, 512, config=1, sk=1)          # 81 tiles: forced on
     assert p.stream_k == 1 and p.dp_tiles == 0
     st, p = plan(256 * 16, 256 * 19, 512, config=1)              # 304 tiles = 4.0 waves exactly
     assert p.stream_k == 0
-    st, p = plan(256 * 11, 256 * 14, 512, config=1)              # 154 tiles = 2.03 waves: last wave 3% full
-    assert p.stream_k == 1
+    st, p = plan(256 * 11, 256 * 14, 4096, config=1)             # 154 tiles = 2.03 waves: last wave 3% full
+    assert p.stream_k == 1 and p.dp_tiles == 76
 
 
 def sk_units(T, P, KT, dp_tiles, cluster):
@@ -196,10 +198,28 @@ def sk_units(T, P, KT, dp_tiles, cluster):
     return out
 
 
-@pytest.mark.parametrize("T,P,KT", [(256, 76, 64), (1024, 76, 128), (344, 76, 64), (81, 76, 5), (170, 152, 8),
-                                    (77, 76, 1), (151, 76, 3), (100, 7, 13)])
-def test_stream_k_schedule_covers_every_k_iteration_once(T, P, KT):
-    dp_tiles = (T // P - 1) * P
+def sk_sources(T, P, KT, dp_tiles, cluster, tile):
+    """Clusters whose partials the head of `tile` adds: the following ranges that start before the tile ends."""
+    total = (T - dp_tiles) * KT
+    base, extra = total // P, total % P
+    tile_end = (tile - dp_tiles + 1) * KT
+    out = []
+    src = cluster + 1
+    while src < P and src * base + min(src, extra) < tile_end:
+        out.append(src)
+        src += 1
+    return out
+
+
+SCHEDULES = [(256, 76, 64, None), (1024, 76, 128, None), (344, 76, 64, None), (81, 76, 5, None),
+             (170, 152, 8, None), (77, 76, 1, None), (151, 76, 3, None), (100, 7, 13, None),
+             # fewer tiles than clusters: tiles split K-wise over several clusters
+             (48, 76, 17, 0), (6, 48, 47, 0), (4, 32, 128, 0), (16, 128, 33, 0), (1, 8, 9, 0), (5, 37, 11, 0)]
+
+
+@pytest.mark.parametrize("T,P,KT,dp", SCHEDULES)
+def test_stream_k_schedule_covers_every_k_iteration_once(T, P, KT, dp):
+    dp_tiles = (T // P - 1) * P if dp is None else dp
     cover = {}
     for c in range(P):
         units = sk_units(T, P, KT, dp_tiles, c)
@@ -214,9 +234,17 @@ def test_stream_k_schedule_covers_every_k_iteration_once(T, P, KT):
             for k in range(k0, k1):
                 assert (t, k) not in cover
                 cover[(t, k)] = (c, kind)
-            if kind == "head":                                        # the rest is the next cluster's tail
-                nxt = sk_units(T, P, KT, dp_tiles, c + 1)
-                assert (t, k1, KT, "tail") in nxt
+            if kind == "head":
+                # The rest of the tile is exactly the first units of the source clusters, in order.
+                srcs = sk_sources(T, P, KT, dp_tiles, c, t)
+                assert srcs and srcs == list(range(c + 1, c + 1 + len(srcs)))
+                k = k1
+                for s in srcs:
+                    first = sk_units(T, P, KT, dp_tiles, s)[sum(1 for u in sk_units(T, P, KT, dp_tiles, s)
+                                                                if u[0] < dp_tiles)]
+                    assert first[0] == t and first[1] == k and first[3] == "tail"
+                    k = first[2]
+                assert k == KT
             if kind == "tail":
-                assert k1 == KT and c > 0
+                assert c > 0
     assert len(cover) == T * KT

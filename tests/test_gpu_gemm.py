@@ -231,7 +231,7 @@ def test_launch_count(handles):
     C = alloc_c(w, d)
     n0 = g.launches
     run_gpu(g, w, dd, C)
-    assert g.launches - n0 == 3            # two operand repacks + the GEMM
+    assert g.launches - n0 == 2            # one repack launch for both operands + the GEMM
     A = torch.zeros(128, 128, dtype=torch.float16, device="cuda")
     C2 = torch.zeros(128, 128, device="cuda")
     n1 = g.launches
@@ -333,6 +333,64 @@ def test_stream_k_matches_data_parallel_on_integers():
     ref = (A.cpu().to(torch.int64) @ B.cpu().to(torch.int64)).to(torch.float32)
     assert torch.equal(outs[0].cpu(), ref)
     assert torch.equal(outs[1].cpu(), ref)
+
+
+# Fewer tiles than clusters: each tile's K range is split over several clusters and the head adds
+# every following cluster's partial (split-K).  K is long enough for several sources per tile.
+SPLIT_CASES = {
+    0: dict(M=300, N=500, K=3000, dtype_out="f16", bias=True),               # 3 x 2 tiles, 47 k-tiles
+    1: dict(M=500, N=300, K=4100, dtype_out="bf16", dtype_in="bf16"),        # 2 x 2 tiles
+    2: dict(M=250, N=250, K=2500, dtype_out="f32", alpha=0.5, beta=1.0),     # 2 x 2 tiles
+    3: dict(M=700, N=250, K=1500, dtype_out="f32", layoutB="col"),           # 3 x 2 tiles
+    4: dict(M=1000, N=500, K=2100, dtype_out="f16", bias=True),              # 2 x 2 tiles on 38 clusters
+    5: dict(M=600, N=700, K=3000, dtype_out="f32", layoutA="col"),           # 3 x 3 tiles, 24 k-tiles of 128
+    6: dict(M=520, N=260, K=5000, dtype_out="bf16", dtype_in="bf16", layoutB="col"),
+    7: dict(M=300, N=1000, K=2000, dtype_out="f16", bias=True, layoutA="col"),
+}
+
+
+def _plan_for(w, cfg, sk):
+    return G.gemm_plan(w.M, w.N, w.K, w.K if w.layoutA == "row" else w.M, w.N if w.layoutB == "row" else w.K,
+                       w.N, G.DTYPE_CODES[w.dtype_in], G.DTYPE_CODES[w.dtype_out], G.LAYOUT_CODES[w.layoutA],
+                       G.LAYOUT_CODES[w.layoutB], w.beta, torch.cuda.get_device_properties(0).multi_processor_count,
+                       0, cfg, sk)
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+def test_split_k_parity(cfg):
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    c = dict(SPLIT_CASES[cfg])
+    w = W.problem(c.pop("M"), c.pop("N"), c.pop("K"), seed=200 + cfg, **c)
+    st, plan = _plan_for(w, cfg, 1)
+    assert st == G.GEMM_OK and plan.stream_k == 1 and plan.dp_tiles == 0
+    assert plan.clusters > plan.tiles_m * plan.tiles_n          # a tile spans several clusters
+    with G.Gemm(0, config=cfg, stream_k=1, sync_check=1) as g:
+        outs = []
+        for _ in range(2):                                      # the second launch runs with the next epoch
+            _, C, _ = _run_check(g, w)
+            outs.append(C.clone())
+        assert g.last_plan()["clusters"] == plan.clusters
+    assert torch.equal(outs[0], outs[1])                        # partials are added in a fixed order
+
+
+@pytest.mark.parametrize("cfg", [0, 2, 5])
+def test_split_k_matches_data_parallel_on_integers(cfg):
+    """Several partial sums per tile; with small integers every schedule is exact."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    M, N, K = 384, 512, 6144
+    A = W.small_ints(M, K, "f16", 15 + cfg).cuda()
+    B = W.small_ints(K, N, "f16", 16 + cfg).cuda()
+    ref = (A.cpu().to(torch.int64) @ B.cpu().to(torch.int64)).to(torch.float32)
+    for sk in (0, 1):
+        C = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        with G.Gemm(0, config=cfg, stream_k=sk, sync_check=1) as g:
+            g.run(A, B, C)
+            torch.cuda.synchronize()
+            plan = g.last_plan()
+        assert plan["stream_k"] == sk
+        assert torch.equal(C.cpu(), ref), (cfg, sk)
 
 
 def test_three_d_and_two_d_tensor_maps_agree(monkeypatch):
