@@ -159,3 +159,33 @@ def small_ints(rows: int, cols: int, dtype: str, seed: int, lo: int = -3, hi: in
     """Integers uniform in [lo, hi] (exact in f16 and bf16)."""
     g = torch.Generator().manual_seed(seed)
     return torch.randint(lo, hi + 1, (rows, cols), generator=g, dtype=torch.int64).to(DTYPES[dtype])
+
+
+# ----------------------------------------------------------------------------------------
+# Q4_0-quantised weights (bytes only: the dequantisation itself is the method's, not here)
+# ----------------------------------------------------------------------------------------
+Q4_0_BLOCK_BYTES = 18      # f16 scale + 16 bytes of nibbles per 32 weights
+
+
+def q4_0_blocks(N: int, K: int, seed: int, *, ldbq: int | None = None, scale: float = 0.02) -> torch.Tensor:
+    """N rows of K/32 random valid Q4_0 blocks as a uint8 tensor of shape (N, ldbq).
+
+    Block layout ("02 . 8m/8m(2) -- Tiled wmma f16 prefill GEMM", section 3.2): a little-endian
+    f16 scale d, then 16 bytes whose nibbles are the quantised weights.  d is drawn U[-2s, 2s] / 8
+    in f64 and rounded to f16, so |d * (q - 8)| <= 2 s stays far inside f16 (the page's test
+    draws "small d" for the same reason); nibbles are uniform in 0..15.  Padding bytes of a wider
+    pitch are drawn too (never read).
+    """
+    assert K % 32 == 0
+    nb = K // 32
+    pitch = ldbq or nb * Q4_0_BLOCK_BYTES
+    assert pitch >= nb * Q4_0_BLOCK_BYTES
+    g = torch.Generator().manual_seed(seed)
+    raw = torch.randint(0, 256, (N, pitch), generator=g, dtype=torch.int64).to(torch.uint8)
+    d = ((torch.rand((N, nb), generator=g, dtype=torch.float64) * 4.0 - 2.0) * scale / 8.0).to(torch.float16)
+    dbits = d.view(torch.int16).to(torch.int64) & 0xFFFF
+    blocks = raw[:, :nb * Q4_0_BLOCK_BYTES].reshape(N, nb, Q4_0_BLOCK_BYTES).clone()
+    blocks[:, :, 0] = (dbits & 0xFF).to(torch.uint8)
+    blocks[:, :, 1] = (dbits >> 8).to(torch.uint8)
+    raw[:, :nb * Q4_0_BLOCK_BYTES] = blocks.reshape(N, nb * Q4_0_BLOCK_BYTES)
+    return raw

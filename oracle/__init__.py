@@ -8,4 +8,5 @@ from .oracle import (  # noqa: F401
     OR_F16, OR_BF16, OR_F32, OR_ROW, OR_COL,
     build, lib_path, decode_f16, decode_bf16, decode_f32,
     gemm_ref, ulp_out, tolerance, check, error_metrics, epilogue_magnitude, num_cpus, decode,
+    f64_to_f16_bits, q4_0_to_f16, gemm_ref_q4_0,
 )

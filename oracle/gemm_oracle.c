@@ -236,3 +236,74 @@ int oracle_decode_array(const void* src, int dtype, int64_t n, double* dst) {
     for (int64_t i = 0; i < n; ++i) dst[i] = load_elem(src, i, dtype);
     return 0;
 }
+
+/* ==========================================================================
+ * Q4_0-quantised weights.
+ *
+ * Source: "02 . 8m/8m(2) -- Tiled wmma f16 prefill GEMM (LANDED)", section 3.2
+ * "Key code" (the Q4_0 dequantisation into an f16 scratch) and section 2.3 (the
+ * weights are dequantised to f16, then one f16 tensor-core GEMM with f32
+ * accumulation consumes them).  The block format as that page states it:
+ *   - a row of the weight matrix (one output column n of C) holds K weights along
+ *     K, in K/32 consecutive blocks of 18 bytes;
+ *   - a block is a binary16 scale d (2 bytes, little-endian) followed by 16 bytes
+ *     q[0..15];
+ *   - weight i (0 <= i < 16) of the block is the low nibble of q[i], weight 16+i
+ *     the high nibble of q[i];
+ *   - its value is d * (nibble - 8), formed in f32 and converted to f16 with
+ *     round-to-nearest-even.  The f32 product is exact (11 + 4 significand bits),
+ *     so the stored f16 is the exact product rounded once to binary16.
+ * The GEMM then reads those f16 values: C = alpha * A * W^T + beta * C_in + bias
+ * with W the N x K dequantised matrix, i.e. B stored N x K (layout COL).
+ * ========================================================================== */
+
+/* Round-to-nearest-even of a non-negative value y that is exactly an integer plus
+ * a fraction representable in f64. */
+static double rne(double y) {
+    const double f = floor(y);
+    const double r = y - f;
+    if (r > 0.5) return f + 1.0;
+    if (r < 0.5) return f;
+    return fmod(f, 2.0) == 0.0 ? f : f + 1.0;
+}
+
+/* f64 -> IEEE-754 binary16, round to nearest, ties to even, overflow to infinity
+ * (written from the format definition: 1 sign, 5 exponent bits with bias 15, 10
+ * fraction bits; subnormals are multiples of 2^-24). */
+uint16_t oracle_f64_to_f16(double x) {
+    if (isnan(x)) return 0x7e00u;
+    const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double a = fabs(x);
+    if (isinf(a)) return sign | 0x7c00u;
+    if (a == 0.0) return sign;
+    int E;
+    frexp(a, &E);                       /* a = m * 2^E, m in [0.5, 1): floor(log2 a) = E - 1 */
+    int e = E - 1;
+    if (e < -14) {                      /* subnormal range: units of 2^-24 */
+        const double n = rne(ldexp(a, 24));
+        return sign | (uint16_t)n;      /* n == 1024 is exactly the smallest normal's bits */
+    }
+    double n = rne(ldexp(a, 10 - e));   /* 1024 <= n <= 2048 */
+    if (n == 2048.0) { n = 1024.0; ++e; }
+    if (e > 15) return sign | 0x7c00u;
+    return sign | (uint16_t)(((e + 15) << 10) | ((int)n - 1024));
+}
+
+/* Dequantise N rows of K weights (K a multiple of 32) from Q4_0 blocks at row pitch
+ * ldbq bytes into binary16 bits, row n at out + n * ldo. */
+int oracle_q4_0_to_f16(const uint8_t* bq, int64_t ldbq, int64_t N, int64_t K, uint16_t* out, int64_t ldo) {
+    if (N < 0 || K < 0 || K % 32 != 0 || ldbq < K / 32 * 18 || ldo < K) return -1;
+    if (N > 0 && K > 0 && (!bq || !out)) return -1;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t b = 0; b < K / 32; ++b) {
+            const uint8_t* blk = bq + n * ldbq + b * 18;
+            const double d = oracle_f16_to_f64((uint16_t)(blk[0] | (blk[1] << 8)));
+            for (int i = 0; i < 16; ++i) {
+                const int lo = blk[2 + i] & 0x0f, hi = blk[2 + i] >> 4;
+                out[n * ldo + b * 32 + i] = oracle_f64_to_f16(d * (double)(lo - 8));
+                out[n * ldo + b * 32 + 16 + i] = oracle_f64_to_f16(d * (double)(hi - 8));
+            }
+        }
+    }
+    return 0;
+}

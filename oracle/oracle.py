@@ -64,6 +64,10 @@ def configure(lib):
     lib.oracle_decode_array.restype = ci
     lib.oracle_num_cpus.argtypes = []
     lib.oracle_num_cpus.restype = ci
+    lib.oracle_f64_to_f16.argtypes = [dbl]
+    lib.oracle_f64_to_f16.restype = ctypes.c_uint16
+    lib.oracle_q4_0_to_f16.argtypes = [vp, i64, i64, i64, vp, i64]
+    lib.oracle_q4_0_to_f16.restype = ci
     return lib
 
 
@@ -169,6 +173,37 @@ def gemm_ref(M, N, K, A, layoutA, B, layoutB, dtype_in, *, alpha=1.0, beta=0.0,
     if rc != 0:
         raise ValueError("oracle_gemm rejected its arguments")
     return out
+
+
+def f64_to_f16_bits(x: float) -> int:
+    """binary16 bits of x rounded to nearest, ties to even (the oracle's own encoder)."""
+    return int(_load().oracle_f64_to_f16(float(x)))
+
+
+def q4_0_to_f16(bq, N: int, K: int) -> np.ndarray:
+    """Dequantise Q4_0 weights to binary16 bit patterns.
+
+    ``bq``: uint8 array of shape (N, ldbq) holding N rows of K/32 blocks of 18 bytes
+    ("02 . 8m/8m(2) -- Tiled wmma f16 prefill GEMM", section 3.2).  Returns (N, K) uint16.
+    """
+    raw = np.ascontiguousarray(bq if not hasattr(bq, "numpy") else bq.detach().cpu().numpy(), dtype=np.uint8)
+    assert raw.ndim == 2 and raw.shape[0] == N
+    out = np.empty((N, K), dtype=np.uint16)
+    rc = _load().oracle_q4_0_to_f16(raw.ctypes.data if raw.size else None, raw.shape[1], N, K,
+                                    out.ctypes.data if out.size else None, K)
+    if rc != 0:
+        raise ValueError("oracle_q4_0_to_f16 rejected its arguments")
+    return out
+
+
+def gemm_ref_q4_0(M, N, K, A, layoutA, Bq, *, alpha=1.0, beta=0.0, Cin=None, dtype_cin=OR_F32,
+                  bias=None, dtype_bias=None, rows=None, cols=None, nthreads=0) -> np.ndarray:
+    """Unrounded f64 reference of alpha * A * W^T + beta * C_in + bias, W = dequantised Q4_0
+    weights (N x K, f16): the dequantisation followed by the plain GEMM definition."""
+    W = q4_0_to_f16(Bq, N, K)
+    return gemm_ref(M, N, K, A, layoutA, W, OR_COL, OR_F16, alpha=alpha, beta=beta, Cin=Cin,
+                    dtype_cin=dtype_cin, bias=bias, dtype_bias=dtype_bias, rows=rows, cols=cols,
+                    nthreads=nthreads)
 
 
 # --------------------------------------------------------------------------------------

@@ -22,9 +22,10 @@ import ctypes, sys
 sys.path[:0] = [{root!r}, {tests!r}]
 import oracle.oracle as om
 import test_oracle_pins as P
+import test_oracle_q4_0 as Q
 om._lib = om.configure(ctypes.CDLL({lib!r}))
 caught = []
-for pin in P.PINS:
+for pin in P.PINS + Q.PINS:
     try:
         pin()
     except Exception:
@@ -51,6 +52,16 @@ MUTANTS = {
                        "for (int64_t k = 0; k + 1 < j->K; ++k) {\n            const double a"),
     "cin_read_when_beta_zero": ("if (j->beta != 0.0) v +=", "if (1) v +="),
     "sign_dropped_f16": ("return sign ? -v : v;\n}\n\n/* bfloat16", "return v;\n}\n\n/* bfloat16"),
+    # Q4_0 dequantisation and the binary16 encoder
+    "q4_nibbles_swapped": ("const int lo = blk[2 + i] & 0x0f, hi = blk[2 + i] >> 4;",
+                           "const int hi = blk[2 + i] & 0x0f, lo = blk[2 + i] >> 4;"),
+    "q4_offset_7": ("d * (double)(lo - 8)", "d * (double)(lo - 7)"),
+    "q4_scale_big_endian": ("(uint16_t)(blk[0] | (blk[1] << 8))", "(uint16_t)(blk[1] | (blk[0] << 8))"),
+    "q4_block_stride_16": ("bq + n * ldbq + b * 18", "bq + n * ldbq + b * 16"),
+    "f16_truncates": ("if (r > 0.5) return f + 1.0;", "if (r > 2.0) return f + 1.0;"),
+    "f16_ties_away": ("return fmod(f, 2.0) == 0.0 ? f : f + 1.0;", "return f + 1.0;"),
+    "f16_subnormal_scale": ("rne(ldexp(a, 24))", "rne(ldexp(a, 23))"),
+    "f16_exponent_bias_enc": ("(((e + 15) << 10)", "(((e + 14) << 10)"),
 }
 
 
