@@ -25,10 +25,10 @@ using namespace gb300;
 namespace {
 
 // ---------------------------------------------------------------- configuration table
-template <int CG, int PAIRS, int BN, int ST, int BK>
+template <int CG, int PAIRS, int BN, int ST, int BK, bool Q4 = false>
 constexpr ConfigDesc make_desc(int id) {
-    return ConfigDesc{id, CG, PAIRS, BN, BK, ST, TileConfig<CG, BN, ST, BK>::kSmemBytes,
-                      TileConfig<CG, BN, ST, BK>::kThreads};
+    return ConfigDesc{id, CG, PAIRS, BN, BK, ST, TileConfig<CG, BN, ST, BK, Q4>::kSmemBytes,
+                      TileConfig<CG, BN, ST, BK, Q4>::kThreads, Q4 ? 1 : 0};
 }
 
 const ConfigDesc kConfigs[kNumConfigs] = {
@@ -40,13 +40,14 @@ const ConfigDesc kConfigs[kNumConfigs] = {
     make_desc<2, 1, 256, 3, 128>(5),  // 2-SM pair, 256 x 256 tile, 128-wide K stages
     make_desc<2, 2, 256, 3, 128>(6),  // two pairs sharing B, 512 x 256 tile, 128-wide K stages
     make_desc<2, 1, 512, 4, 64>(7),   // 2-SM pair, 256 x 512 tile (two N=256 MMAs per K step)
+    make_desc<2, 1, 256, 3, 128, true>(8),  // as 5, B dequantised from Q4_0 blocks in shared memory
 };
 
 // Mainloop efficiency per config (measured k-iteration time of one long-K tile against the
 // config's tensor-core time at 1.9 GHz, cold L2, GB300): small tiles need more operand bytes per
 // flop and are bound by the TMA load rate per SM.  Config 7 is derated for its single accumulator
 // (its epilogue does not overlap the next tile).
-const double kConfigEfficiency[kNumConfigs] = {0.73, 0.78, 0.40, 0.39, 0.80, 0.85, 0.84, 0.75};
+const double kConfigEfficiency[kNumConfigs] = {0.73, 0.78, 0.40, 0.39, 0.80, 0.85, 0.84, 0.75, 0.85};
 
 int cluster_ctas(const ConfigDesc& d) { return d.cta_group * d.pairs; }
 int block_m(const ConfigDesc& d) { return 128 * cluster_ctas(d); }
@@ -263,9 +264,10 @@ Schedule schedule(const ConfigDesc& d, double eff, int64_t M, int64_t N, int64_t
 // Pure host planning: validation, config choice, grid, stream-K split and workspace.
 //   slots[c]     clusters of config c that fit on the device at once
 //   cluster_cap  optional cap on launched clusters (0 = none)
+//   b_q4         1: B is Q4_0 weights (N rows of K/32 18-byte blocks, ldb = row pitch in bytes)
 gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int din, int dout,
                         int la, int lb, float beta, const int* slots, int config, int stream_k, int cluster_cap,
-                        gemm_plan_t* out, std::string* err) {
+                        gemm_plan_t* out, std::string* err, int b_q4 = 0) {
     std::memset(out, 0, sizeof(*out));
     out->config = -1;
     if (M < 0 || N < 0 || K < 0) { *err = "M, N and K must be >= 0"; return GEMM_ERR_INVALID_ARG; }
@@ -277,9 +279,19 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     const int64_t a_inner = la == GEMM_ROW ? K : M;
     const int64_t b_inner = lb == GEMM_ROW ? N : K;
     if (lda < std::max<int64_t>(1, a_inner)) { *err = "lda too small"; return GEMM_ERR_INVALID_ARG; }
-    if (ldb < std::max<int64_t>(1, b_inner)) { *err = "ldb too small"; return GEMM_ERR_INVALID_ARG; }
+    if (b_q4) {
+        if (din != GEMM_F16) { *err = "Q4_0 weights take f16 activations"; return GEMM_ERR_INVALID_ARG; }
+        if (K % 32 != 0) { *err = "K must be a multiple of 32 (whole Q4_0 blocks)"; return GEMM_ERR_INVALID_ARG; }
+        if (ldb < std::max<int64_t>(1, K / 32 * 18) || ldb % 2 != 0) {
+            *err = "ldbq must be even and at least K/32*18 bytes"; return GEMM_ERR_INVALID_ARG;
+        }
+    } else if (ldb < std::max<int64_t>(1, b_inner)) { *err = "ldb too small"; return GEMM_ERR_INVALID_ARG; }
     if (ldc < std::max<int64_t>(1, N)) { *err = "ldc too small"; return GEMM_ERR_INVALID_ARG; }
     if (config < -1 || config >= kNumConfigs) { *err = "no such config"; return GEMM_ERR_UNSUPPORTED; }
+    if (config >= 0 && kConfigs[config].b_q4 != b_q4) {
+        *err = b_q4 ? "this config does not take Q4_0 weights" : "this config only takes Q4_0 weights";
+        return GEMM_ERR_UNSUPPORTED;
+    }
     if (stream_k < -1 || stream_k > 1) { *err = "stream_k must be -1, 0 or 1"; return GEMM_ERR_INVALID_ARG; }
     if (M == 0 || N == 0) { out->kernels = 0; return GEMM_OK; }
     if (K == 0) { out->kernels = 1; return GEMM_OK; }
@@ -295,7 +307,7 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
         double best_us = 1e300;
         for (int c = 0; c < kNumConfigs; ++c) {
             const int s = slots_of(c);
-            if (s <= 0) continue;
+            if (s <= 0 || kConfigs[c].b_q4 != b_q4) continue;
             const Schedule sc = schedule(kConfigs[c], kConfigEfficiency[c], M, N, K, s, stream_k, out_bytes, beta);
             if (sc.est_us < best_us * (1.0 - 1e-9)) { best_us = sc.est_us; best = c; }
         }
@@ -317,7 +329,7 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     out->raster_group = std::min(out->tiles_m, 8);
     out->tma_store = ((ldc * out_bytes) % 16 == 0) ? 1 : 0;
     out->repack_a = (lda * 2) % 16 != 0;
-    out->repack_b = (ldb * 2) % 16 != 0;
+    out->repack_b = b_q4 ? 0 : (ldb * 2) % 16 != 0;
     int64_t ws = 0;
     if (out->repack_a) ws += round_up((la == GEMM_ROW ? M : K) * round_up(a_inner, 8) * 2, 256);
     if (out->repack_b) ws += round_up((lb == GEMM_ROW ? K : N) * round_up(b_inner, 8) * 2, 256);
@@ -414,7 +426,10 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
     if (st != GEMM_OK) return st;
     *what = "tensor map of B";
     st = GEMM_ERR_CUDA;
-    if (a.lb == GEMM_ROW) {  // N-major
+    if (d->b_q4) {           // B is read by the kernel's dequantisation warps, not by TMA
+        std::memset(&tb, 0, sizeof(tb));
+        st = GEMM_OK;
+    } else if (a.lb == GEMM_ROW) {  // N-major
         if (allow_3d && d->pairs == 1 && N % 64 == 0) {
             st = tmap(tmap3d(a.B, tin, 64, K, N / 64, (uint64_t)a.ldb * 2, 128, 64, bk, b_box_n / 64), &tb);
             b_3d = st == GEMM_OK;
@@ -451,7 +466,12 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
     p.k_tiles = (int)((a.K + d->block_k - 1) / d->block_k);
     p.raster_group = a.raster_group > 0 ? std::min(a.raster_group, plan.tiles_m) : plan.raster_group;
     p.a_mn = a.la == GEMM_COL ? 1 : 0;
-    p.b_mn = a.lb == GEMM_ROW ? 1 : 0;
+    p.b_mn = (a.lb == GEMM_ROW && !d->b_q4) ? 1 : 0;
+    if (d->b_q4) {
+        p.bq = static_cast<const uint8_t*>(a.B);
+        p.ldbq = a.ldb;
+        p.kblocks = (int)(a.K / 32);
+    }
     p.a_3d = a_3d;
     p.b_3d = b_3d;
     p.idesc = make_idesc(a.din, p.a_mn, p.b_mn, 128 * d->cta_group, mma_n);
@@ -587,6 +607,7 @@ const void* config_kernel(int id, int out) {
         case 5: return cfg5_kernel(out);
         case 6: return cfg6_kernel(out);
         case 7: return cfg7_kernel(out);
+        case 8: return cfg8_kernel(out);
         default: return nullptr;
     }
 }
@@ -616,6 +637,7 @@ cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, c
         case 5: return cfg5_launch(out, lc, a, b, c, p);
         case 6: return cfg6_launch(out, lc, a, b, c, p);
         case 7: return cfg7_launch(out, lc, a, b, c, p);
+        case 8: return cfg8_launch(out, lc, a, b, c, p);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -665,6 +687,7 @@ gemm_status_t gemm_config_info(int id, gemm_config_info_t* out) {
     out->smem_bytes = d->smem_bytes;
     out->threads = d->threads;
     out->pairs = d->pairs;
+    out->b_q4_0 = d->b_q4;
     return GEMM_OK;
 }
 
@@ -778,22 +801,29 @@ gemm_status_t gemm_get_device_status(gemm_handle_t h, void* stream) {
     return GEMM_ERR_TIMEOUT;
 }
 
-gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+}  // extern "C"
+
+namespace {
+
+// The body of gemm_run and gemm_run_q4_0 (b_q4 = 1: B is Q4_0 weights at row pitch ldb bytes).
+gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                        int64_t ldb, void* C, int64_t ldc, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
                        gemm_layout_t layoutA, gemm_layout_t layoutB, float alpha, float beta, const void* bias,
-                       void* stream) {
+                       void* stream, int b_q4) {
     if (!h) return GEMM_ERR_INVALID_ARG;
     h->err.clear();
     gemm_plan_t plan;
     std::string err;
     gemm_status_t st = plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, h->dev.slots,
-                                 h->opt.config, h->opt.stream_k, h->opt.max_clusters, &plan, &err);
+                                 h->opt.config, h->opt.stream_k, h->opt.max_clusters, &plan, &err, b_q4);
     if (st != GEMM_OK) return fail(h, st, err);
     if (M == 0 || N == 0) return GEMM_OK;
     if (!C) return fail(h, GEMM_ERR_INVALID_ARG, "C is NULL");
     if (K > 0 && (!A || !B)) return fail(h, GEMM_ERR_INVALID_ARG, "A or B is NULL");
-    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) % 16) != 0 || (reinterpret_cast<uintptr_t>(B) % 16) != 0))
-        return fail(h, GEMM_ERR_ALIGNMENT, "A and B must be 16-byte aligned");
+    if (K > 0 && (reinterpret_cast<uintptr_t>(A) % 16) != 0)
+        return fail(h, GEMM_ERR_ALIGNMENT, "A must be 16-byte aligned");
+    if (K > 0 && (reinterpret_cast<uintptr_t>(B) % (b_q4 ? 2 : 16)) != 0)
+        return fail(h, GEMM_ERR_ALIGNMENT, b_q4 ? "Q4_0 weights must be 2-byte aligned" : "B must be 16-byte aligned");
     DeviceGuard guard(h->device);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
@@ -836,6 +866,46 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
     h->last_plan = plan;
     h->has_plan = true;
     if (h->opt.sync_check) return gemm_get_device_status(h, stream);
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                       int64_t ldb, void* C, int64_t ldc, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                       gemm_layout_t layoutA, gemm_layout_t layoutB, float alpha, float beta, const void* bias,
+                       void* stream) {
+    return run_impl(h, M, N, K, A, lda, B, ldb, C, ldc, dtype_in, dtype_out, layoutA, layoutB, alpha, beta, bias,
+                    stream, 0);
+}
+
+gemm_status_t gemm_run_q4_0(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                            gemm_layout_t layoutA, const void* Bq, int64_t ldbq, void* C, int64_t ldc,
+                            gemm_dtype_t dtype_out, float alpha, float beta, const void* bias, void* stream) {
+    return run_impl(h, M, N, K, A, lda, Bq, ldbq, C, ldc, GEMM_F16, dtype_out, layoutA, GEMM_COL, alpha, beta, bias,
+                    stream, 1);
+}
+
+gemm_status_t gemm_dequant_q4_0(const void* Bq, int64_t ldbq, int64_t N, int64_t K, void* out, int64_t ldo,
+                                void* stream) {
+    if (N < 0 || K < 0 || K % 32 != 0) return GEMM_ERR_INVALID_ARG;
+    if (ldbq < K / 32 * 18 || ldbq % 2 != 0 || ldo < K) return GEMM_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return GEMM_OK;
+    if (!Bq || !out) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(Bq) % 2) != 0 || (reinterpret_cast<uintptr_t>(out) % 2) != 0)
+        return GEMM_ERR_ALIGNMENT;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    cudaError_t e = launch_dequant_q4_0(Bq, ldbq, N, K, out, ldo, sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
     return GEMM_OK;
 }
 

@@ -76,6 +76,64 @@ cudaError_t launch_repack_u16(const RepackJobs& jobs, int num_sms, cudaStream_t 
     return cudaGetLastError();
 }
 
+// Q4_0 weights -> f16 ("02 . 8m/8m(2) -- Tiled wmma f16 prefill GEMM", section 3.2: an f16 scale d
+// and 16 bytes per 32 weights; weight i is the low nibble of byte i, weight 16+i its high nibble;
+// value d * (q - 8) formed in f32, exact, then rounded to f16).  One thread per block.
+__global__ void __launch_bounds__(256) dequant_q4_0_kernel(const uint8_t* __restrict__ bq, long long ldbq,
+                                                           long long N, long long nblocks, __half* __restrict__ out,
+                                                           long long ldo) {
+    const long long total = N * nblocks;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < total; g += stride) {
+        const long long n = g / nblocks, b = g - n * nblocks;
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(bq + n * ldbq + b * 18);
+        const float d = __half2float(__ushort_as_half(__ldg(h)));
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t two = __ldg(h + 1 + i);                  // bytes 2i (low) and 2i+1 (high)
+            const uint32_t b0 = two & 0xffu, b1 = two >> 8;
+            // weights 2i, 2i+1 from the low nibbles; 16+2i, 16+2i+1 from the high nibbles
+            const __half2 lo = __floats2half2_rn(d * static_cast<float>(static_cast<int>(b0 & 15u) - 8),
+                                                 d * static_cast<float>(static_cast<int>(b1 & 15u) - 8));
+            const __half2 hi = __floats2half2_rn(d * static_cast<float>(static_cast<int>(b0 >> 4) - 8),
+                                                 d * static_cast<float>(static_cast<int>(b1 >> 4) - 8));
+            packed[i] = *reinterpret_cast<const uint32_t*>(&lo);
+            packed[8 + i] = *reinterpret_cast<const uint32_t*>(&hi);
+        }
+        __half* dst = out + n * ldo + b * 32;
+        if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) d4[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+        } else if ((reinterpret_cast<uintptr_t>(dst) & 3u) == 0) {
+            uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) d32[j] = packed[j];
+        } else {
+            uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                d16[2 * j] = static_cast<uint16_t>(packed[j] & 0xffffu);
+                d16[2 * j + 1] = static_cast<uint16_t>(packed[j] >> 16);
+            }
+        }
+    }
+}
+
+cudaError_t launch_dequant_q4_0(const void* bq, long long ldbq, long long N, long long K, void* out, long long ldo,
+                                int num_sms, cudaStream_t stream) {
+    const long long nblocks = K / 32;
+    const long long total = N * nblocks;
+    if (total <= 0) return cudaSuccess;
+    long long blocks = (total + 255) / 256;
+    const long long cap = static_cast<long long>(num_sms > 0 ? num_sms : 152) * 8;
+    if (blocks > cap) blocks = cap;
+    dequant_q4_0_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint8_t*>(bq), ldbq, N, nblocks, static_cast<__half*>(out), ldo);
+    return cudaGetLastError();
+}
+
 template <int kOut>
 __global__ void scale_bias_kernel(void* C, long long ldc, const void* bias, float beta, long long M, long long N) {
     const long long total = M * N;

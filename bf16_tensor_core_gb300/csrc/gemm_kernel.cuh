@@ -67,6 +67,10 @@ struct KernelParams {
     float* sk_partials;        // [cluster][cta rank][BN / 4][128 rows][4] f32
     unsigned* sk_flags;        // [cluster][cta rank][epilogue warp]
     unsigned epoch;            // launch counter of the handle, never 0
+    // Q4_0 B (kernels built with kQ4): N rows of K/32 blocks of 18 bytes at pitch ldbq bytes.
+    const uint8_t* bq;
+    long long ldbq;
+    int kblocks;               // K / 32
 };
 
 enum : int { UNIT_FULL = 0, UNIT_HEAD = 1, UNIT_TAIL = 2 };
@@ -123,7 +127,7 @@ struct UnitIter {
     }
 };
 
-template <int kCtaGroup, int kBN, int kStages, int kBKc = 64>
+template <int kCtaGroup, int kBN, int kStages, int kBKc = 64, bool kQ4 = false>
 struct TileConfig {
     static constexpr int kBM = 128;                    // rows per CTA (TMEM lanes)
     static constexpr int kBK = kBKc;                   // K per stage: 64 or 128
@@ -137,12 +141,14 @@ struct TileConfig {
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kRingBytes = kStages * kStageBytes;
     // Eight epilogue warps: warps w and w+4 read the same 32 TMEM lanes and split the columns.
-    static constexpr int kEpiWarps = 8;
+    // With Q4_0 B, four of them are dequantisation warps instead and four drain all columns.
+    static constexpr int kEpiWarps = kQ4 ? 4 : 8;
+    static constexpr int kDqWarps = kQ4 ? 4 : 0;
     static constexpr int kEpiCols = kBN / (kEpiWarps / 4);   // accumulator columns one warp drains
     static constexpr int kEpiBufBytes = 32 * 128;      // 32 rows x 128 bytes, one staging buffer per warp
     static constexpr int kEpiBytes = kEpiWarps * kEpiBufBytes;
     static constexpr int kSmemBytes = kRingBytes + kEpiBytes + 1024;  // + alignment slack
-    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kThreads = 64 + 32 * (kEpiWarps + kDqWarps);
     static constexpr int kMmaN = kBN < 256 ? kBN : 256; // N of one tcgen05.mma (at most 256)
     static constexpr int kNHalves = kBN / kMmaN;       // MMAs per K step that cover the tile's N
     static constexpr int kHalfCols = kMmaN / kCtaGroup; // B columns of one MMA that a CTA holds
@@ -155,6 +161,8 @@ struct TileConfig {
     static_assert(kBK == 64 || kBK == 128, "BK must be 64 or 128");
     static_assert(kHalfCols % 64 == 0, "each CTA loads whole 64-column B slabs");
     static_assert(kSmemBytes <= 232448 - 512, "shared memory budget");
+    static_assert(!kQ4 || (kBNC == 128 && kBK == 128 && kNHalves == 1),
+                  "Q4_0 B: one dequantisation lane per B row (128 per CTA), four blocks per stage");
 };
 
 __device__ __forceinline__ void tile_coords(const KernelParams& p, int t, int& mb, int& nb) {
@@ -538,15 +546,84 @@ __device__ __forceinline__ bool wait_flag_bounded(const unsigned* flag, unsigned
     }
 }
 
+// ---------------------------------------------------------------- Q4_0 B operand
+// Block format ("02 . 8m/8m(2) -- Tiled wmma f16 prefill GEMM", section 3.2): an f16 scale d and
+// 16 bytes q; weight i is the low nibble of q[i], weight 16+i its high nibble, value d * (q - 8)
+// rounded to f16.  Four blocks (128 K) of one B row per stage.
+struct Q4Row {
+    uint32_t d[4];      // f16 scale bits of each block (0: out of range, all weights 0)
+    uint32_t q[4][4];   // the 16 nibble bytes of each block as four little-endian words
+};
+
+__device__ __forceinline__ void q4_load_row(const KernelParams& p, int n, int kt, Q4Row& r) {
+    const int b0 = kt * 4;
+    const uint8_t* row = p.bq + static_cast<long long>(n) * p.ldbq;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        if (n < p.N && b0 + b < p.kblocks) {
+            // Blocks are 18 bytes, so only 2-byte alignment is guaranteed: nine 16-bit loads.
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(row + static_cast<long long>(b0 + b) * 18);
+            uint32_t v[9];
+#pragma unroll
+            for (int i = 0; i < 9; ++i) v[i] = __ldg(h + i);
+            r.d[b] = v[0];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) r.q[b][w] = v[1 + 2 * w] | (v[2 + 2 * w] << 16);
+        } else {
+            r.d[b] = 0u;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) r.q[b][w] = 0x88888888u;    // nibble 8: weight 0
+        }
+    }
+}
+
+// Two weights from the low (hi_half = 0) or high nibbles of bytes 2j and 2j+1 of word w, as f16x2
+// d * (q - 8): 0x6400 | q is the f16 1024 + q, minus 1032 is q - 8 exactly, and the product with
+// d is one correctly rounded f16 multiplication.
+__device__ __forceinline__ uint32_t q4_pair(uint32_t w, int j, bool high, __half2 d2) {
+    const uint32_t bytes = __byte_perm(w, 0u, j == 0 ? 0x4140u : 0x4342u);   // byte 2j -> [7:0], 2j+1 -> [23:16]
+    const uint32_t nib = high ? ((bytes >> 4) & 0x000F000Fu) : (bytes & 0x000F000Fu);
+    const uint32_t biased = nib | 0x64006400u;
+    __half2 h = *reinterpret_cast<const __half2*>(&biased);
+    h = __hsub2(h, __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6408u))));   // - 1032
+    h = __hmul2(h, d2);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Write row `row` (0..127) of the stage's K-major, 128-byte-swizzled B tile: 128 K = two 64-wide
+// chunks of 128 bytes; block b covers 16-byte pieces 4*(b%2)..+3 of chunk b/2.
+__device__ __forceinline__ void q4_store_row(uint32_t sb, int row, const Q4Row& r, uint32_t chunk_bytes) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(r.d[b])));
+        const uint32_t base = sb + static_cast<uint32_t>(b >> 1) * chunk_bytes + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) {
+            // pieces 0,1: weights 0..15 = low nibbles of q[0..15]; pieces 2,3: weights 16..31 = high nibbles.
+            const bool high = pc >= 2;
+            const int w0 = (pc & 1) * 2;          // q words holding bytes 8*(pc&1) .. +7
+            const uint32_t x0 = q4_pair(r.q[b][w0], 0, high, d2);
+            const uint32_t x1 = q4_pair(r.q[b][w0], 1, high, d2);
+            const uint32_t x2 = q4_pair(r.q[b][w0 + 1], 0, high, d2);
+            const uint32_t x3 = q4_pair(r.q[b][w0 + 1], 1, high, d2);
+            const uint32_t piece = static_cast<uint32_t>(4 * (b & 1) + pc) ^ (static_cast<uint32_t>(row) & 7u);
+            st_shared_v4(base + piece * 16u, x0, x1, x2, x3);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- the kernel
 // kPairs == 2 (with kCtaGroup == 2): a 4-CTA cluster of two 2-SM pairs stacked along M.  Both pairs
 // need the same B columns, so each pair loads half of every B stage and multicasts it to the
 // matching CTA of the other pair: the cluster reads B from L2 once for 512 output rows.
-template <int kCtaGroup, int kPairs, int kBN, int kStages, int kBK, int kOut>
-__global__ void __launch_bounds__(TileConfig<kCtaGroup, kBN, kStages, kBK>::kThreads, 1)
+// kQ4: B is Q4_0-quantised; dequantisation warps (after the epilogue warps) write each stage's
+// B tile into shared memory instead of the producer's TMA copies.
+template <int kCtaGroup, int kPairs, int kBN, int kStages, int kBK, int kOut, bool kQ4 = false>
+__global__ void __launch_bounds__(TileConfig<kCtaGroup, kBN, kStages, kBK, kQ4>::kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
-    using Cfg = TileConfig<kCtaGroup, kBN, kStages, kBK>;
+    using Cfg = TileConfig<kCtaGroup, kBN, kStages, kBK, kQ4>;
+    static_assert(!kQ4 || kPairs == 1, "Q4_0 B is built for one 2-SM pair per cluster");
     static_assert(kPairs == 1 || kCtaGroup == 2, "pairs of CTAs need cta_group::2");
     static_assert(kPairs == 1 || Cfg::kNHalves == 1, "B multicast is built for one MMA per K step");
     static_assert(Cfg::kRingBytes >= Cfg::kEpiWarps * kFixBufs * static_cast<int>(kFixPieceBytes),
@@ -581,7 +658,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (threadIdx.x == 0) {
         s_abort = 0;
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&bar_full[s]), 1);
+            // The producer's arrive (with the TMA byte count), plus one arrive per dequantisation
+            // warp of every CTA of the pair when B is dequantised in shared memory.
+            mbar_init(smem_u32(&bar_full[s]), 1 + Cfg::kDqWarps * kCtaGroup);
             mbar_init(smem_u32(&bar_empty[s]), kPairs);   // one commit from each pair that reads the slot
         }
         for (int b = 0; b < 2; ++b) {
@@ -610,7 +689,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             long long gstage = 0;
-            const uint32_t tx_bytes = static_cast<uint32_t>(Cfg::kStageBytes * kCtaGroup);
+            const uint32_t tx_bytes = static_cast<uint32_t>((kQ4 ? Cfg::kABytes : Cfg::kStageBytes) * kCtaGroup);
             bool ok = true;
             UnitIter units;
             units.init(p, cluster_id, num_clusters);
@@ -658,7 +737,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                 load(sa + static_cast<uint32_t>(Cfg::kSlabBytes), &tmA, m0 + 64, k0);
                             }
                         }
-                        if constexpr (kPairs == 1) {
+                        if constexpr (kQ4) {
+                            // B arrives from the dequantisation warps.
+                        } else if constexpr (kPairs == 1) {
                             // For each MMA N half h the CTA holds columns
                             // [nb*BN + h*kMmaN + prank*kHalfCols, +kHalfCols).
 #pragma unroll
@@ -749,7 +830,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * static_cast<uint32_t>(Cfg::kAccCols);
                 for (int kt = u.k0; kt < u.k1; ++kt) {
-                    if (!mbar_wait_bounded(smem_u32(&bar_full[stage]), phase, p.timeout_ns, abort_flag)) {
+                    // With dequantised B the peer CTA's warps arrive on this barrier too (release at
+                    // cluster scope), so the wait acquires at cluster scope.
+                    if (!mbar_wait_bounded<kQ4 && kCtaGroup == 2>(smem_u32(&bar_full[stage]), phase, p.timeout_ns,
+                                                                  abort_flag)) {
                         if (!*abort_flag) report_error<kClusterCtas>(p, ROLE_MMA, u.tile, static_cast<int>(stage), abort_flag);
                         ok = false;
                         break;
@@ -776,8 +860,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             volatile int never = 0;
             mbar_wait_bounded(smem_u32(&bar_drain), 0u, p.timeout_ns, &never);
         }
-    } else {
-        // ------------------------------------------------------------ epilogue warps 2..9
+    } else if (warp < 2 + Cfg::kEpiWarps) {
+        // ------------------------------------------------------------ epilogue warps
         const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
         const int ew = warp - 2;
         const int pcol0 = (ew / 4) * Cfg::kEpiCols;   // first tile column this warp drains
@@ -855,6 +939,53 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
+    } else if constexpr (kQ4) {
+        // ------------------------------------------------------------ Q4_0 dequantisation warps
+        // Lane `row` of warp dw owns B row dw * 32 + lane of this CTA's 128 (one output column n).
+        // Raw blocks of the next stage are loaded while the current one waits for its slot.
+        const int row = (warp - 2 - Cfg::kEpiWarps) * 32 + lane;
+        UnitIter units;
+        units.init(p, cluster_id, num_clusters);
+        Unit u;
+        bool valid = units.next(p, u);
+        int kt = valid ? u.k0 : 0;
+        auto row_of = [&](const Unit& uu) {
+            int mb, nb;
+            tile_coords(p, uu.tile, mb, nb);
+            return nb * kBN + static_cast<int>(prank) * Cfg::kBNC + row;
+        };
+        Q4Row cur, nxt;
+        int cur_tile = valid ? u.tile : 0;
+        if (valid) q4_load_row(p, row_of(u), kt, cur);
+        uint32_t stage = 0, phase = 0;
+        while (valid) {
+            // Advance to the next (unit, k-tile) and prefetch its raw blocks.
+            const int this_tile = cur_tile;
+            if (++kt >= u.k1) {
+                valid = units.next(p, u);
+                kt = valid ? u.k0 : 0;
+            }
+            if (valid) {
+                cur_tile = u.tile;
+                q4_load_row(p, row_of(u), kt, nxt);
+            }
+            bool ok = mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, p.timeout_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0 && !*abort_flag)
+                    report_error<kClusterCtas>(p, ROLE_PRODUCER, this_tile, 500 + static_cast<int>(stage), abort_flag);
+                break;
+            }
+            q4_store_row(ring + stage * Cfg::kStageBytes + Cfg::kABytes, row, cur, Cfg::kBChunkBytes);
+            asm volatile("fence.proxy.async;" ::: "memory");   // generic writes -> the MMA's async reads
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t full_local = smem_u32(&bar_full[stage]);
+                if constexpr (kCtaGroup == 2) mbar_arrive_cluster(mapa_shared(full_local, lrank));
+                else mbar_arrive_local(full_local);
+            }
+            cur = nxt;
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
     }
 
     // ---------------------------------------------------------------- teardown

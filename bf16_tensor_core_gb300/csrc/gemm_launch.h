@@ -17,9 +17,10 @@ struct ConfigDesc {
     int stages;
     int smem_bytes;
     int threads;
+    int b_q4;         // 1: B is Q4_0-quantised and dequantised in shared memory by the kernel
 };
 
-constexpr int kNumConfigs = 8;
+constexpr int kNumConfigs = 9;
 constexpr int kNumOut = 3;  // OUT_F16, OUT_BF16, OUT_F32
 
 // Static description of config `id` (nullptr if out of range).
@@ -58,6 +59,10 @@ const void* cfg7_kernel(int out);
 cudaError_t cfg7_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& c, const KernelParams& p);
 
+const void* cfg8_kernel(int out);
+cudaError_t cfg8_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const KernelParams& p);
+
 // Auxiliary kernels (gemm_aux.cu).
 struct RepackJob {
     const uint16_t* src;   // rows x cols elements at pitch lds (2-byte aligned)
@@ -71,6 +76,8 @@ struct RepackJobs {
     int n;                 // jobs in use (0..2), all moved by one launch
 };
 cudaError_t launch_repack_u16(const RepackJobs& jobs, int num_sms, cudaStream_t stream);
+cudaError_t launch_dequant_q4_0(const void* bq, long long ldbq, long long N, long long K, void* out, long long ldo,
+                                int num_sms, cudaStream_t stream);
 cudaError_t launch_scale_bias(int out, void* C, long long ldc, const void* bias, float beta, long long M,
                               long long N, int num_sms, cudaStream_t stream);
 

@@ -33,7 +33,8 @@ class gemm_options_t(ctypes.Structure):
 class gemm_config_info_t(ctypes.Structure):
     _fields_ = [("id", ctypes.c_int), ("cta_group", ctypes.c_int), ("block_m", ctypes.c_int),
                 ("block_n", ctypes.c_int), ("block_k", ctypes.c_int), ("stages", ctypes.c_int),
-                ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int), ("pairs", ctypes.c_int)]
+                ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int), ("pairs", ctypes.c_int),
+                ("b_q4_0", ctypes.c_int)]
 
 
 class gemm_plan_t(ctypes.Structure):
@@ -94,6 +95,10 @@ def load_library(path: Path | str | None = None):
     lib.gemm_last_plan.restype = ci
     lib.gemm_run_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ci, ci, ci, ci, cf, cf, vp, vp]
     lib.gemm_run_noalloc.restype = ci
+    lib.gemm_run_q4_0.argtypes = [vp, i64, i64, i64, vp, i64, ci, vp, i64, vp, i64, ci, cf, cf, vp, vp]
+    lib.gemm_run_q4_0.restype = ci
+    lib.gemm_dequant_q4_0.argtypes = [vp, i64, i64, i64, vp, i64, vp]
+    lib.gemm_dequant_q4_0.restype = ci
     if path is None:
         _lib = lib
     return lib
@@ -172,6 +177,15 @@ def gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, dtype_in, dtype_out, layou
                                            layoutB, alpha, beta, bias, stream)
 
 
+def gemm_run_q4_0(h, M, N, K, A, lda, layoutA, Bq, ldbq, C, ldc, dtype_out, alpha, beta, bias, stream) -> int:
+    return load_library().gemm_run_q4_0(h, M, N, K, A, lda, layoutA, Bq, ldbq, C, ldc, dtype_out, alpha, beta,
+                                        bias, stream)
+
+
+def gemm_dequant_q4_0(Bq, ldbq, N, K, out, ldo, stream) -> int:
+    return load_library().gemm_dequant_q4_0(Bq, ldbq, N, K, out, ldo, stream)
+
+
 # ------------------------------------------------------------------ torch convenience wrapper
 def _torch_code(t) -> int:
     import torch
@@ -239,6 +253,22 @@ class Gemm:
                       bias.data_ptr() if bias is not None else None, s)
         if check and st != GEMM_OK:
             raise GemmError(st, f"gemm_run: {gemm_status_string(st)}: {gemm_last_error(self.h)}")
+        return st
+
+    def run_q4_0(self, A, Bq, C, *, N, K=None, M=None, layoutA="row", alpha=1.0, beta=0.0, bias=None,
+                 stream=None, check=True) -> int:
+        """A: f16 activations (stored layout); Bq: uint8 tensor (N, ldbq) of Q4_0 blocks."""
+        import torch
+        la = LAYOUT_CODES[layoutA]
+        if M is None:
+            M = A.size(0) if la == GEMM_ROW else A.size(1)
+        if K is None:
+            K = A.size(1) if la == GEMM_ROW else A.size(0)
+        s = stream if stream is not None else torch.cuda.current_stream(C.device).cuda_stream
+        st = gemm_run_q4_0(self.h, M, N, K, A.data_ptr(), _ld(A), la, Bq.data_ptr(), _ld(Bq), C.data_ptr(), _ld(C),
+                           _torch_code(C), float(alpha), float(beta), bias.data_ptr() if bias is not None else None, s)
+        if check and st != GEMM_OK:
+            raise GemmError(st, f"gemm_run_q4_0: {gemm_status_string(st)}: {gemm_last_error(self.h)}")
         return st
 
     def status(self, stream=None) -> int:

@@ -101,6 +101,7 @@ typedef struct {
     int smem_bytes;    /* dynamic shared memory per CTA                                           */
     int threads;       /* threads per CTA                                                         */
     int pairs;         /* 2-SM pairs per cluster; 2: the pairs share B by TMA multicast           */
+    int b_q4_0;        /* 1: B is Q4_0 weights dequantised in shared memory (gemm_run_q4_0 only)  */
 } gemm_config_info_t;
 
 /* What gemm_run would do for a problem (pure host computation, no device needed). */
@@ -135,6 +136,33 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                        gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
                        gemm_layout_t layoutA, gemm_layout_t layoutB,
                        float alpha, float beta, const void* bias, void* stream);
+
+/* gemm_run_q4_0 - the same product with Q4_0-quantised weights as B, dequantised inside the
+ * GEMM kernel ("02 . 8m/8m(2) -- Tiled wmma f16 prefill GEMM (LANDED)": section 2.3 names the
+ * dequant-in-GEMM fused kernel as the successor of its separate dequant pass; section 3.2 gives
+ * the block format).
+ *   C (M x N) <- alpha * op(A) * W^T + beta * C + bias, W the N x K dequantised weights.
+ *   A: f16 activations, layoutA as in gemm_run, 16-byte aligned.
+ *   Bq: N rows (one per output column) of K/32 blocks of 18 bytes at a row pitch of ldbq bytes
+ *       (ldbq even, >= K/32*18); 2-byte aligned.  Block: little-endian f16 scale d, then 16 bytes
+ *       q[0..15]; weight i of the block is the low nibble of q[i], weight 16+i the high nibble;
+ *       its value is d * (nibble - 8) rounded to f16, exactly as gemm_dequant_q4_0 writes it, and
+ *       the product then runs on the f16 tensor cores with f32 accumulation.
+ *   K must be a multiple of 32 (whole blocks).  C, ldc, dtype_out, alpha, beta, bias, stream and
+ *   the returned codes are those of gemm_run.  The handle's config option must be -1 or a config
+ *   whose b_q4_0 is 1. */
+gemm_status_t gemm_run_q4_0(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                            const void* A, int64_t lda, gemm_layout_t layoutA,
+                            const void* Bq, int64_t ldbq,
+                            void* C, int64_t ldc, gemm_dtype_t dtype_out,
+                            float alpha, float beta, const void* bias, void* stream);
+
+/* gemm_dequant_q4_0 - the separate dequantisation pass of the same page (section 3.2): writes the
+ * N x K f16 weights (row n at out + n * ldo elements, ldo >= K) from Q4_0 blocks laid out as for
+ * gemm_run_q4_0, on the current device and `stream`.  K a multiple of 32; Bq and out 2-byte
+ * aligned.  Needs no handle; returns GEMM_ERR_INVALID_ARG / GEMM_ERR_ALIGNMENT / GEMM_ERR_CUDA. */
+gemm_status_t gemm_dequant_q4_0(const void* Bq, int64_t ldbq, int64_t N, int64_t K,
+                                void* out, int64_t ldo, void* stream);
 
 /* Free the handle and everything it owns (waits for its device work first).  NULL is a no-op. */
 gemm_status_t gemm_destroy(gemm_handle_t h);

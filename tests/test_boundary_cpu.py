@@ -44,7 +44,7 @@ def test_options_default(lib):
 
 def test_config_table(lib):
     n = G.gemm_num_configs()
-    assert n == 8
+    assert n == 9
     seen = set()
     for i in range(n):
         st, c = G.gemm_config_info(i)
@@ -54,9 +54,10 @@ def test_config_table(lib):
         assert c.pairs == 1 or c.cta_group == 2
         stage = (128 + c.block_n // c.cta_group) * c.block_k * 2
         assert c.smem_bytes >= c.stages * stage
-        seen.add((c.cta_group, c.pairs, c.block_n, c.block_k))
-    assert seen == {(1, 1, 128, 64), (1, 1, 256, 64), (2, 1, 128, 64), (2, 1, 256, 64), (2, 2, 256, 64),
-                    (2, 1, 256, 128), (2, 2, 256, 128), (2, 1, 512, 64)}
+        seen.add((c.cta_group, c.pairs, c.block_n, c.block_k, c.b_q4_0))
+    assert seen == {(1, 1, 128, 64, 0), (1, 1, 256, 64, 0), (2, 1, 128, 64, 0), (2, 1, 256, 64, 0),
+                    (2, 2, 256, 64, 0), (2, 1, 256, 128, 0), (2, 2, 256, 128, 0), (2, 1, 512, 64, 0),
+                    (2, 1, 256, 128, 1)}
     assert G.gemm_config_info(n)[0] == G.GEMM_ERR_UNSUPPORTED
 
 
@@ -109,9 +110,21 @@ def test_plan_degenerate(lib):
     assert st == G.GEMM_OK and p.kernels == 1
 
 
+def test_q4_0_config_is_not_a_plain_gemm_config(lib):
+    q4 = [i for i in range(G.gemm_num_configs()) if G.gemm_config_info(i)[1].b_q4_0]
+    assert q4 == [8]
+    st, p = plan(4096, 4096, 4096, dout=0, config=8)       # f16 B cannot use the Q4_0 kernel
+    assert st == G.GEMM_ERR_UNSUPPORTED
+    for shape in [(512, 512, 512), (4096, 4096, 4096), (64, 4096, 4096), (1000, 3000, 2048)]:
+        st, p = plan(*shape, dout=0)
+        assert st == G.GEMM_OK and p.config != 8
+
+
 def test_plan_tiles_and_grid(lib):
     for cfg in range(G.gemm_num_configs()):
         st, c = G.gemm_config_info(cfg)
+        if c.b_q4_0:
+            continue
         st, p = plan(4096, 4096, 4096, dout=0, config=cfg)
         assert st == G.GEMM_OK and p.config == cfg
         assert p.tiles_m == 4096 // c.block_m and p.tiles_n == 4096 // c.block_n

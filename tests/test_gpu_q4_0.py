@@ -1,0 +1,240 @@
+"""GPU parity of the Q4_0 weight path: the separate dequantisation kernel (bit-exact against the
+oracle's decode) and the GEMM whose kernel dequantises B in shared memory (against the oracle's
+dequantise-then-GEMM reference, and bit-exact against the plain GEMM on the dequantised weights)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bf16_tensor_core_gb300 import gemm as G
+from bf16_tensor_core_gb300 import workloads as W
+from gpu_cases import OR_CODE, sample_indices
+
+pytestmark = pytest.mark.gpu
+Q4_CONFIG = 8
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+
+
+def _blocks(N, K, seed, ldbq=None, scale=0.02):
+    return W.q4_0_blocks(N, K, seed, ldbq=ldbq, scale=scale)
+
+
+def _special_block_rows(K):
+    """Rows of hand-made blocks: subnormal scales, a rounding case, every nibble, negative scale."""
+    assert K % 32 == 0
+    rows = []
+    for d_bits in (0x0003, 0x03FF, 0x3C01, 0xB800, 0x3C00, 0x1400):
+        r = bytearray()
+        for b in range(K // 32):
+            r += bytes([d_bits & 0xff, d_bits >> 8]) + bytes([(i * 17 + b * 5) & 0xff for i in range(16)])
+        rows.append(np.frombuffer(bytes(r), np.uint8))
+    return torch.from_numpy(np.stack(rows))
+
+
+# ------------------------------------------------------------------ separate dequantisation
+@pytest.mark.parametrize("N,K,ldbq,ldo", [(7, 64, None, None), (70, 256, 148, 260), (33, 1024, None, 1025),
+                                          (300, 4096, None, None)])
+def test_dequant_bit_exact(N, K, ldbq, ldo):
+    _need_gpu()
+    bq = _blocks(N, K, seed=N + K, ldbq=ldbq)
+    ref = oracle.q4_0_to_f16(bq.numpy(), N, K)
+    ldo = ldo or K
+    out = torch.full((N, ldo), -1.0, dtype=torch.float16, device="cuda")
+    st = G.gemm_dequant_q4_0(bq.cuda().data_ptr(), bq.size(1), N, K, out.data_ptr(), ldo,
+                             torch.cuda.current_stream().cuda_stream)
+    assert st == G.GEMM_OK
+    torch.cuda.synchronize()
+    got = out[:, :K].cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+    if ldo > K:
+        assert torch.all(out[:, K:].cpu() == -1.0)          # padding untouched
+
+
+def test_dequant_special_blocks_bit_exact():
+    _need_gpu()
+    bq = _special_block_rows(128)
+    ref = oracle.q4_0_to_f16(bq.numpy(), bq.size(0), 128)
+    out = torch.empty(bq.size(0), 128, dtype=torch.float16, device="cuda")
+    assert G.gemm_dequant_q4_0(bq.cuda().data_ptr(), bq.size(1), bq.size(0), 128, out.data_ptr(), 128, None) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), ref)
+
+
+def test_dequant_rejects_bad_arguments():
+    _need_gpu()
+    bq = _blocks(4, 64, 1).cuda()
+    out = torch.empty(4, 64, dtype=torch.float16, device="cuda")
+    assert G.gemm_dequant_q4_0(bq.data_ptr(), 36, 4, 48, out.data_ptr(), 64, None) == G.GEMM_ERR_INVALID_ARG
+    assert G.gemm_dequant_q4_0(bq.data_ptr(), 35, 4, 64, out.data_ptr(), 64, None) == G.GEMM_ERR_INVALID_ARG
+    assert G.gemm_dequant_q4_0(bq.data_ptr() + 1, 36, 4, 64, out.data_ptr(), 64, None) == G.GEMM_ERR_ALIGNMENT
+
+
+# ------------------------------------------------------------------ fused dequant-in-GEMM
+def _case(M, N, K, seed, *, dout="f16", layoutA="row", alpha=1.0, beta=0.0, bias=False, ldbq=None, scale=0.02):
+    g = torch.Generator().manual_seed(seed)
+    A_st = (torch.rand((M, K) if layoutA == "row" else (K, M), generator=g, dtype=torch.float64) * 2 - 1).half()
+    bq = _blocks(N, K, seed + 1, ldbq=ldbq, scale=scale)
+    b = (torch.rand(N, generator=g, dtype=torch.float64) * 2 - 1).to(W.DTYPES[dout]) if bias else None
+    cin = (torch.rand((M, N), generator=g, dtype=torch.float64) * 2 - 1).to(W.DTYPES[dout]) if beta != 0 else None
+    return dict(M=M, N=N, K=K, A=A_st, bq=bq, bias=b, Cin=cin, dout=dout, layoutA=layoutA, alpha=alpha, beta=beta)
+
+
+def _run(g, c, C=None):
+    A, bq = c["A"].cuda(), c["bq"].cuda()
+    if C is None:
+        C = (c["Cin"].cuda().clone() if c["Cin"] is not None
+             else torch.full((c["M"], c["N"]), float("nan"), dtype=W.DTYPES[c["dout"]], device="cuda"))
+    g.run_q4_0(A, bq, C, N=c["N"], K=c["K"], M=c["M"], layoutA=c["layoutA"], alpha=c["alpha"], beta=c["beta"],
+               bias=c["bias"].cuda() if c["bias"] is not None else None)
+    torch.cuda.synchronize()
+    return C
+
+
+def _check(c, C, rows=None, cols=None):
+    ref = oracle.gemm_ref_q4_0(c["M"], c["N"], c["K"], c["A"], oracle.OR_ROW if c["layoutA"] == "row" else oracle.OR_COL,
+                               c["bq"].numpy(), alpha=c["alpha"], beta=c["beta"], Cin=c["Cin"],
+                               dtype_cin=OR_CODE[c["dout"]], bias=c["bias"], dtype_bias=OR_CODE[c["dout"]],
+                               rows=rows, cols=cols)
+    got = C.cpu()
+    if rows is not None:
+        got = got[torch.as_tensor(rows)]
+    if cols is not None:
+        got = got[:, torch.as_tensor(cols)]
+    got = got.double().numpy()
+    Wf = oracle.q4_0_to_f16(c["bq"].numpy(), c["N"], c["K"]).view(np.float16).astype(np.float64)
+    maxA, maxB = float(c["A"].abs().max()), float(np.abs(Wf).max())
+    cin = None
+    if c["Cin"] is not None:
+        cin = c["Cin"].double()
+        if rows is not None:
+            cin = cin[torch.as_tensor(rows)]
+        if cols is not None:
+            cin = cin[:, torch.as_tensor(cols)]
+        cin = cin.numpy()
+    bias = c["bias"].double().numpy() if c["bias"] is not None else None
+    if bias is not None and cols is not None:
+        bias = bias[np.asarray(cols)]
+    mag = oracle.epilogue_magnitude(ref, c["beta"], cin, bias)
+    rep = oracle.check(got, ref, c["K"], maxA, maxB, OR_CODE[c["dout"]], alpha=c["alpha"], epi_mag=mag)
+    assert rep["passed"], rep
+    return rep
+
+
+FUSED_CASES = [
+    dict(M=300, N=520, K=640, dout="f16", bias=True),                       # ragged tiles, K tail of 128
+    dict(M=512, N=768, K=1024, dout="f32"),
+    dict(M=257, N=300, K=2048, dout="bf16", layoutA="col"),
+    dict(M=700, N=260, K=96, dout="f32", alpha=0.5, beta=1.0),               # one partial k-tile
+    dict(M=128, N=1000, K=4096, dout="f16", ldbq=2320),                      # padded weight rows
+]
+
+
+@pytest.mark.parametrize("i", range(len(FUSED_CASES)))
+def test_fused_parity(i):
+    _need_gpu()
+    c = _case(seed=50 + i, **FUSED_CASES[i])
+    with G.Gemm(0, sync_check=1) as g:
+        C = _run(g, c)
+        assert g.last_plan()["config"] == Q4_CONFIG
+    _check(c, C)
+
+
+@pytest.mark.parametrize("sk", [0, 1])
+def test_fused_equals_plain_gemm_on_dequantised_weights(sk):
+    """Same tiles, same k order, same MMAs: only where B comes from differs, so the outputs agree
+    bit for bit with the plain GEMM (config 5, the same tile shape) on the dequantised f16 weights."""
+    _need_gpu()
+    c = _case(1000, 1500, 2048, seed=70, dout="f32", bias=True)
+    with G.Gemm(0, sync_check=1, stream_k=sk) as g:
+        C1 = _run(g, c)
+        plan = g.last_plan()
+    Wd = torch.empty(c["N"], c["K"], dtype=torch.float16, device="cuda")
+    bq = c["bq"].cuda()
+    assert G.gemm_dequant_q4_0(bq.data_ptr(), bq.size(1), c["N"], c["K"], Wd.data_ptr(), c["K"], None) == 0
+    C2 = torch.full_like(C1, float("nan"))
+    with G.Gemm(0, config=5, sync_check=1, stream_k=sk) as g:
+        g.run(c["A"].cuda(), Wd, C2, layoutB="col", bias=c["bias"].cuda())
+        p2 = g.last_plan()
+        assert (p2["stream_k"], p2["clusters"], p2["dp_tiles"]) == (plan["stream_k"], plan["clusters"], plan["dp_tiles"])
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+
+
+def test_fused_integers_exact():
+    """d = 1 and small-integer activations: every product and partial sum is an integer < 2^24."""
+    _need_gpu()
+    M, N, K = 384, 640, 1024
+    A = W.small_ints(M, K, "f16", 9)
+    g0 = torch.Generator().manual_seed(10)
+    q = torch.randint(0, 256, (N, K // 32, 16), generator=g0, dtype=torch.int64).to(torch.uint8)
+    blocks = torch.zeros(N, K // 32, 18, dtype=torch.uint8)
+    blocks[:, :, 0], blocks[:, :, 1] = 0x00, 0x3C          # d = 1.0
+    blocks[:, :, 2:] = q
+    bq = blocks.reshape(N, -1)
+    Wint = oracle.q4_0_to_f16(bq.numpy(), N, K).view(np.float16).astype(np.int64)
+    ref = torch.from_numpy(A.to(torch.int64).numpy() @ Wint.T).to(torch.float32)
+    for sk in (0, 1):
+        C = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        with G.Gemm(0, sync_check=1, stream_k=sk) as g:
+            g.run_q4_0(A.cuda(), bq.cuda(), C, N=N)
+        torch.cuda.synchronize()
+        assert torch.equal(C.cpu(), ref), sk
+
+
+def test_fused_split_k_parity():
+    """Few output tiles and long K: the schedule splits K over several clusters."""
+    _need_gpu()
+    c = _case(200, 500, 8192, seed=80, dout="f32")
+    with G.Gemm(0, sync_check=1, stream_k=1) as g:
+        C = _run(g, c)
+        plan = g.last_plan()
+    assert plan["stream_k"] == 1 and plan["clusters"] > plan["tiles_m"] * plan["tiles_n"]
+    _check(c, C)
+
+
+def test_fused_special_blocks():
+    _need_gpu()
+    M, K = 256, 128
+    bq = _special_block_rows(K)
+    A = (torch.rand(M, K, generator=torch.Generator().manual_seed(4), dtype=torch.float64) * 2 - 1).half()
+    c = dict(M=M, N=bq.size(0), K=K, A=A, bq=bq, bias=None, Cin=None, dout="f32", layoutA="row", alpha=1.0,
+             beta=0.0)
+    with G.Gemm(0, sync_check=1) as g:
+        C = _run(g, c)
+    _check(c, C)
+
+
+def test_fused_prefill_shape_sampled():
+    """The 2048 x 11008 x 4096 prefill projection with Q4_0 weights, sampled rows and columns."""
+    _need_gpu()
+    c = _case(2048, 11008, 4096, seed=90, dout="bf16", bias=True)
+    with G.Gemm(0, sync_check=1) as g:
+        C = _run(g, c)
+    rows = sample_indices(2048, 24, 1, 256)
+    cols = sample_indices(11008, 24, 2, 256)
+    _check(c, C, rows=rows)
+    _check(c, C, cols=cols)
+
+
+def test_fused_rejects_bad_arguments():
+    _need_gpu()
+    A = torch.zeros(64, 64, dtype=torch.float16, device="cuda")
+    bq = _blocks(64, 64, 3).cuda()
+    C = torch.zeros(64, 64, dtype=torch.float32, device="cuda")
+    with G.Gemm(0) as g:
+        s = torch.cuda.current_stream().cuda_stream
+        assert G.gemm_run_q4_0(g.h, 64, 64, 48, A.data_ptr(), 64, 0, bq.data_ptr(), 36, C.data_ptr(), 64, 2,
+                               1.0, 0.0, None, s) == G.GEMM_ERR_INVALID_ARG        # K not whole blocks
+        assert G.gemm_run_q4_0(g.h, 64, 64, 64, A.data_ptr(), 64, 0, bq.data_ptr(), 35, C.data_ptr(), 64, 2,
+                               1.0, 0.0, None, s) == G.GEMM_ERR_INVALID_ARG        # odd pitch
+        assert G.gemm_run_q4_0(g.h, 64, 64, 64, A.data_ptr(), 64, 0, bq.data_ptr() + 1, 36, C.data_ptr(), 64, 2,
+                               1.0, 0.0, None, s) == G.GEMM_ERR_ALIGNMENT
+    with G.Gemm(0, config=5) as g:                                                 # not a Q4_0 config
+        assert G.gemm_run_q4_0(g.h, 64, 64, 64, A.data_ptr(), 64, 0, bq.data_ptr(), 36, C.data_ptr(), 64, 2,
+                               1.0, 0.0, None, torch.cuda.current_stream().cuda_stream) == G.GEMM_ERR_UNSUPPORTED
+    with G.Gemm(0, config=Q4_CONFIG) as g:                                         # plain B on the Q4_0 config
+        assert g.run(A, A, C, check=False) == G.GEMM_ERR_UNSUPPORTED
