@@ -40,7 +40,7 @@ def _args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--workload", type=int, default=2, help="1..6 (6: Q4_0 weights through gemm_run_q4_0)")
     ap.add_argument("--config", type=int, default=-1)
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps, capped at 200")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
@@ -215,11 +215,15 @@ def oracle_block_time(w, d, rows: int, cols: int, nthreads: int) -> tuple[float,
     Cin = d["Cin"][:rows, :cols].contiguous() if d["Cin"] is not None else None
     bias = d["bias"][:cols].contiguous() if d["bias"] is not None else None
     code = {"f16": oracle.OR_F16, "bf16": oracle.OR_BF16, "f32": oracle.OR_F32}
+    la = oracle.OR_ROW if w.layoutA == "row" else oracle.OR_COL
     t0 = time.perf_counter()
-    oracle.gemm_ref(rows, cols, w.K, A, oracle.OR_ROW if w.layoutA == "row" else oracle.OR_COL, B,
-                    oracle.OR_ROW if w.layoutB == "row" else oracle.OR_COL, code[w.dtype_in], alpha=w.alpha,
-                    beta=w.beta, Cin=Cin, dtype_cin=code[w.dtype_out], bias=bias, dtype_bias=code[w.dtype_out],
-                    nthreads=nthreads)
+    if w.layoutB == "q4_0":
+        oracle.gemm_ref_q4_0(rows, cols, w.K, A, la, d["B"][:cols].numpy(), alpha=w.alpha, beta=w.beta, Cin=Cin,
+                             dtype_cin=code[w.dtype_out], bias=bias, dtype_bias=code[w.dtype_out], nthreads=nthreads)
+    else:
+        oracle.gemm_ref(rows, cols, w.K, A, la, B, oracle.OR_ROW if w.layoutB == "row" else oracle.OR_COL,
+                        code[w.dtype_in], alpha=w.alpha, beta=w.beta, Cin=Cin, dtype_cin=code[w.dtype_out],
+                        bias=bias, dtype_bias=code[w.dtype_out], nthreads=nthreads)
     dt = time.perf_counter() - t0
     return dt, 2.0 * rows * cols * w.K
 
@@ -322,9 +326,14 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
     s_handle = stream.cuda_stream
 
-    def step():
-        g.run(A, B, C, M=w.M, N=w.N, K=w.K, layoutA=w.layoutA, layoutB=w.layoutB, alpha=w.alpha, beta=w.beta,
-              bias=bias, stream=s_handle)
+    if w.layoutB == "q4_0":
+        def step():
+            g.run_q4_0(A, B, C, M=w.M, N=w.N, K=w.K, layoutA=w.layoutA, alpha=w.alpha, beta=w.beta, bias=bias,
+                       stream=s_handle)
+    else:
+        def step():
+            g.run(A, B, C, M=w.M, N=w.N, K=w.K, layoutA=w.layoutA, layoutB=w.layoutB, alpha=w.alpha,
+                  beta=w.beta, bias=bias, stream=s_handle)
 
     def barrier():
         if world > 1:

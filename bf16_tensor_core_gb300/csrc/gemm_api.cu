@@ -329,10 +329,13 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     out->raster_group = std::min(out->tiles_m, 8);
     out->tma_store = ((ldc * out_bytes) % 16 == 0) ? 1 : 0;
     out->repack_a = (lda * 2) % 16 != 0;
-    out->repack_b = b_q4 ? 0 : (ldb * 2) % 16 != 0;
+    // Q4_0 rows are read with 4-byte loads: a pitch that is not a multiple of 4 bytes is repacked
+    // (as 16-bit units) to a 16-byte pitch.
+    out->repack_b = b_q4 ? (ldb % 4 != 0) : (ldb * 2) % 16 != 0;
     int64_t ws = 0;
     if (out->repack_a) ws += round_up((la == GEMM_ROW ? M : K) * round_up(a_inner, 8) * 2, 256);
-    if (out->repack_b) ws += round_up((lb == GEMM_ROW ? K : N) * round_up(b_inner, 8) * 2, 256);
+    if (out->repack_b && b_q4) ws += round_up(N * round_up(K / 32 * 9, 8) * 2, 256);
+    else if (out->repack_b) ws += round_up((lb == GEMM_ROW ? K : N) * round_up(b_inner, 8) * 2, 256);
     if (sc.stream_k) {
         out->stream_k = 1;
         out->dp_tiles = sc.dp_tiles;
@@ -510,7 +513,7 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
 // launch.  Updates the operand pointers and leading dimensions; counts launches.
 cudaError_t repack_operands(const gemm_plan_t& plan, int64_t M, int64_t N, int64_t K, int la, int lb, void* ws,
                             const void** A, int64_t* lda, const void** B, int64_t* ldb, int num_sms,
-                            cudaStream_t s, int64_t* launches, const char** what) {
+                            cudaStream_t s, int64_t* launches, const char** what, int b_q4 = 0) {
     char* w = static_cast<char*>(ws);
     RepackJobs jobs{};
     if (plan.repack_a) {
@@ -523,7 +526,14 @@ cudaError_t repack_operands(const gemm_plan_t& plan, int64_t M, int64_t N, int64
         *lda = ld;
         w += round_up(rows * ld * 2, 256);
     }
-    if (plan.repack_b) {
+    if (plan.repack_b && b_q4) {   // Q4_0 rows (ldb in bytes, even) moved as 16-bit units
+        const int64_t cols = K / 32 * 9;
+        const int64_t ld = round_up(cols, 8);
+        jobs.job[jobs.n++] = RepackJob{static_cast<const uint16_t*>(*B), *ldb / 2, reinterpret_cast<uint16_t*>(w), ld,
+                                       N, cols};
+        *B = w;
+        *ldb = ld * 2;
+    } else if (plan.repack_b) {
         const int64_t rows = lb == GEMM_ROW ? K : N;
         const int64_t cols = lb == GEMM_ROW ? N : K;
         const int64_t ld = round_up(cols, 8);
@@ -824,6 +834,12 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
         return fail(h, GEMM_ERR_ALIGNMENT, "A must be 16-byte aligned");
     if (K > 0 && (reinterpret_cast<uintptr_t>(B) % (b_q4 ? 2 : 16)) != 0)
         return fail(h, GEMM_ERR_ALIGNMENT, b_q4 ? "Q4_0 weights must be 2-byte aligned" : "B must be 16-byte aligned");
+    if (b_q4 && K > 0 && !plan.repack_b && (reinterpret_cast<uintptr_t>(B) % 4) != 0) {
+        // The rows start 2 bytes past a 4-byte boundary: repack them like an odd pitch.
+        plan.repack_b = 1;
+        plan.workspace_bytes += round_up(N * round_up(K / 32 * 9, 8) * 2, 256);
+        plan.kernels = 2;
+    }
     DeviceGuard guard(h->device);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
@@ -843,7 +859,7 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
                                "workspace allocation");
             if (st != GEMM_OK) return st;
             cudaError_t e = repack_operands(plan, M, N, K, layoutA, layoutB, h->ws, &a_ptr, &lda_eff, &b_ptr, &ldb_eff,
-                                            h->dev.num_sms, s, &h->launches, &what);
+                                            h->dev.num_sms, s, &h->launches, &what, b_q4);
             if (e != cudaSuccess) return cuda_fail(h, what, e);
         }
         if (plan.stream_k) {

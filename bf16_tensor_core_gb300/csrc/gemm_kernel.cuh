@@ -141,9 +141,9 @@ struct TileConfig {
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kRingBytes = kStages * kStageBytes;
     // Eight epilogue warps: warps w and w+4 read the same 32 TMEM lanes and split the columns.
-    // With Q4_0 B, four of them are dequantisation warps instead and four drain all columns.
+    // With Q4_0 B, four epilogue warps drain all columns and eight dequantisation warps follow.
     static constexpr int kEpiWarps = kQ4 ? 4 : 8;
-    static constexpr int kDqWarps = kQ4 ? 4 : 0;
+    static constexpr int kDqWarps = kQ4 ? 8 : 0;
     static constexpr int kEpiCols = kBN / (kEpiWarps / 4);   // accumulator columns one warp drains
     static constexpr int kEpiBufBytes = 32 * 128;      // 32 rows x 128 bytes, one staging buffer per warp
     static constexpr int kEpiBytes = kEpiWarps * kEpiBufBytes;
@@ -549,68 +549,131 @@ __device__ __forceinline__ bool wait_flag_bounded(const unsigned* flag, unsigned
 // ---------------------------------------------------------------- Q4_0 B operand
 // Block format ("02 . 8m/8m(2) -- Tiled wmma f16 prefill GEMM", section 3.2): an f16 scale d and
 // 16 bytes q; weight i is the low nibble of q[i], weight 16+i its high nibble, value d * (q - 8)
-// rounded to f16.  Four blocks (128 K) of one B row per stage.
-struct Q4Row {
-    uint32_t d[4];      // f16 scale bits of each block (0: out of range, all weights 0)
-    uint32_t q[4][4];   // the 16 nibble bytes of each block as four little-endian words
+// rounded to f16.  A stage covers 128 K = four blocks of each B row.  Lane l of a dequantisation
+// warp works on block l % 4 of rows (l / 4) + 8 * pass, so the four lanes of a row read its 72
+// contiguous bytes together.
+constexpr int kQ4RegStages = 2;        // stages of raw blocks held in registers (loaded this many stages early)
+
+// The lane's blocks of one stage (one per pass) exactly as loaded (rows 4-byte aligned, so a block starts 0
+// or 2 bytes past a 4-byte boundary, which is the parity of its index):
+//   even block: w[0..3] = bytes 0..15, w[4] = bytes 16..17;
+//   odd block:  w[0] = bytes 0..1 (the scale), w[1..4] = bytes 2..17 (the nibbles).
+// A block outside the matrix is all zero: scale 0, so every weight is 0.
+constexpr int kQ4Passes = 2;           // B rows per dequantisation lane per stage (8 warps x 8 rows per pass)
+
+struct Q4Raw {
+    uint32_t w[kQ4Passes][5];
 };
 
-__device__ __forceinline__ void q4_load_row(const KernelParams& p, int n, int kt, Q4Row& r) {
-    const int b0 = kt * 4;
-    const uint8_t* row = p.bq + static_cast<long long>(n) * p.ldbq;
+__device__ __forceinline__ void q4_load_raw(const KernelParams& p, const int (&rows)[kQ4Passes], int blk, Q4Raw& r) {
+    const bool odd = (blk & 1) != 0;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        if (n < p.N && b0 + b < p.kblocks) {
-            // Blocks are 18 bytes, so only 2-byte alignment is guaranteed: nine 16-bit loads.
-            const uint16_t* h = reinterpret_cast<const uint16_t*>(row + static_cast<long long>(b0 + b) * 18);
-            uint32_t v[9];
-#pragma unroll
-            for (int i = 0; i < 9; ++i) v[i] = __ldg(h + i);
-            r.d[b] = v[0];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) r.q[b][w] = v[1 + 2 * w] | (v[2 + 2 * w] << 16);
+    for (int ps = 0; ps < kQ4Passes; ++ps) {
+        if (rows[ps] < p.N && blk < p.kblocks) {
+            const uint8_t* b = p.bq + static_cast<long long>(rows[ps]) * p.ldbq + static_cast<long long>(blk) * 18;
+            if (!odd) {
+                const uint32_t* w = reinterpret_cast<const uint32_t*>(b);
+                r.w[ps][0] = __ldg(w);
+                r.w[ps][1] = __ldg(w + 1);
+                r.w[ps][2] = __ldg(w + 2);
+                r.w[ps][3] = __ldg(w + 3);
+                r.w[ps][4] = __ldg(reinterpret_cast<const uint16_t*>(b + 16));
+            } else {
+                const uint32_t* w = reinterpret_cast<const uint32_t*>(b + 2);
+                r.w[ps][0] = __ldg(reinterpret_cast<const uint16_t*>(b));
+                r.w[ps][1] = __ldg(w);
+                r.w[ps][2] = __ldg(w + 1);
+                r.w[ps][3] = __ldg(w + 2);
+                r.w[ps][4] = __ldg(w + 3);
+            }
         } else {
-            r.d[b] = 0u;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) r.q[b][w] = 0x88888888u;    // nibble 8: weight 0
+            for (int i = 0; i < 5; ++i) r.w[ps][i] = 0u;
         }
     }
 }
 
-// Two weights from the low (hi_half = 0) or high nibbles of bytes 2j and 2j+1 of word w, as f16x2
-// d * (q - 8): 0x6400 | q is the f16 1024 + q, minus 1032 is q - 8 exactly, and the product with
-// d is one correctly rounded f16 multiplication.
-__device__ __forceinline__ uint32_t q4_pair(uint32_t w, int j, bool high, __half2 d2) {
-    const uint32_t bytes = __byte_perm(w, 0u, j == 0 ? 0x4140u : 0x4342u);   // byte 2j -> [7:0], 2j+1 -> [23:16]
-    const uint32_t nib = high ? ((bytes >> 4) & 0x000F000Fu) : (bytes & 0x000F000Fu);
-    const uint32_t biased = nib | 0x64006400u;
+// d * (nibble - 8) for the nibbles of two packed bytes (in bits 0..3 and 16..19 of x, other bits
+// ignored), as f16x2: 0x6400 | q is the f16 1024 + q, minus 1032 is q - 8 exactly, and the product
+// with d is one correctly rounded f16 multiplication.
+__device__ __forceinline__ uint32_t q4_two(uint32_t x, __half2 d2) {
+    const uint32_t biased = (x & 0x000F000Fu) | 0x64006400u;
     __half2 h = *reinterpret_cast<const __half2*>(&biased);
     h = __hsub2(h, __half2half2(__ushort_as_half(static_cast<unsigned short>(0x6408u))));   // - 1032
     h = __hmul2(h, d2);
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Write row `row` (0..127) of the stage's K-major, 128-byte-swizzled B tile: 128 K = two 64-wide
-// chunks of 128 bytes; block b covers 16-byte pieces 4*(b%2)..+3 of chunk b/2.
-__device__ __forceinline__ void q4_store_row(uint32_t sb, int row, const Q4Row& r, uint32_t chunk_bytes) {
+// The lane's blocks converted to f16, ready to store: per pass 16 words = four 16-byte pieces
+// (piece 0 holds weights 0..7, the low nibbles of bytes 0..7; piece 1 weights 8..15; pieces 2
+// and 3 the high nibbles of the same bytes, weights 16..31).
+struct Q4Half {
+    uint32_t v[kQ4Passes][16];
+};
+
+__device__ __forceinline__ void q4_convert(const Q4Raw& r, bool odd, Q4Half& h) {
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(r.d[b])));
-        const uint32_t base = sb + static_cast<uint32_t>(b >> 1) * chunk_bytes + static_cast<uint32_t>(row) * 128u;
+    for (int ps = 0; ps < kQ4Passes; ++ps) {
+        uint32_t dbits, q[4];
+        if (!odd) {
+            dbits = r.w[ps][0] & 0xffffu;
+            q[0] = __byte_perm(r.w[ps][0], r.w[ps][1], 0x5432u);
+            q[1] = __byte_perm(r.w[ps][1], r.w[ps][2], 0x5432u);
+            q[2] = __byte_perm(r.w[ps][2], r.w[ps][3], 0x5432u);
+            q[3] = __byte_perm(r.w[ps][3], r.w[ps][4], 0x5432u);
+        } else {
+            dbits = r.w[ps][0];
+            q[0] = r.w[ps][1];
+            q[1] = r.w[ps][2];
+            q[2] = r.w[ps][3];
+            q[3] = r.w[ps][4];
+        }
+        const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(dbits)));
 #pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
-            // pieces 0,1: weights 0..15 = low nibbles of q[0..15]; pieces 2,3: weights 16..31 = high nibbles.
-            const bool high = pc >= 2;
-            const int w0 = (pc & 1) * 2;          // q words holding bytes 8*(pc&1) .. +7
-            const uint32_t x0 = q4_pair(r.q[b][w0], 0, high, d2);
-            const uint32_t x1 = q4_pair(r.q[b][w0], 1, high, d2);
-            const uint32_t x2 = q4_pair(r.q[b][w0 + 1], 0, high, d2);
-            const uint32_t x3 = q4_pair(r.q[b][w0 + 1], 1, high, d2);
-            const uint32_t piece = static_cast<uint32_t>(4 * (b & 1) + pc) ^ (static_cast<uint32_t>(row) & 7u);
-            st_shared_v4(base + piece * 16u, x0, x1, x2, x3);
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t sh = q[i] >> 4;   // byte k's high nibble now in its low nibble
+            h.v[ps][2 * i] = q4_two(__byte_perm(q[i], 0u, 0x4140u), d2);
+            h.v[ps][2 * i + 1] = q4_two(__byte_perm(q[i], 0u, 0x4342u), d2);
+            h.v[ps][8 + 2 * i] = q4_two(__byte_perm(sh, 0u, 0x4140u), d2);
+            h.v[ps][8 + 2 * i + 1] = q4_two(__byte_perm(sh, 0u, 0x4342u), d2);
         }
     }
 }
+
+// Write the converted blocks into the stage's K-major, 128-byte-swizzled B tile: row `row0 + 8 *
+// pass` (0..127), block b (0..3) = 32 K = 16-byte pieces 4*(b%2)..+3 of the 64-wide chunk b/2.
+__device__ __forceinline__ void q4_store(uint32_t sb, int row0, int b, const Q4Half& h, uint32_t chunk_bytes) {
+#pragma unroll
+    for (int ps = 0; ps < kQ4Passes; ++ps) {
+        const int row = row0 + 8 * ps;
+        const uint32_t base = sb + static_cast<uint32_t>(b >> 1) * chunk_bytes + static_cast<uint32_t>(row) * 128u;
+        const uint32_t sw = static_cast<uint32_t>(row) & 7u;
+        const uint32_t pb = 4u * static_cast<uint32_t>(b & 1);
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc)
+            st_shared_v4(base + (((pb + static_cast<uint32_t>(pc)) ^ sw) * 16u), h.v[ps][4 * pc], h.v[ps][4 * pc + 1],
+                         h.v[ps][4 * pc + 2], h.v[ps][4 * pc + 3]);
+    }
+}
+
+// A walk over one cluster's (unit, k-tile) stages in the order every role uses.
+struct StageWalk {
+    UnitIter units;
+    Unit u;
+    int kt;
+    bool valid;
+    __device__ __forceinline__ void init(const KernelParams& p, int cluster, int num_clusters) {
+        units.init(p, cluster, num_clusters);
+        valid = units.next(p, u);
+        kt = valid ? u.k0 : 0;
+    }
+    __device__ __forceinline__ void advance(const KernelParams& p) {
+        if (++kt >= u.k1) {
+            valid = units.next(p, u);
+            kt = valid ? u.k0 : 0;
+        }
+    }
+};
 
 // ---------------------------------------------------------------- the kernel
 // kPairs == 2 (with kCtaGroup == 2): a 4-CTA cluster of two 2-SM pairs stacked along M.  Both pairs
@@ -658,9 +721,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (threadIdx.x == 0) {
         s_abort = 0;
         for (int s = 0; s < kStages; ++s) {
-            // The producer's arrive (with the TMA byte count), plus one arrive per dequantisation
-            // warp of every CTA of the pair when B is dequantised in shared memory.
-            mbar_init(smem_u32(&bar_full[s]), 1 + Cfg::kDqWarps * kCtaGroup);
+            // The producer's arrive (with the TMA byte count), plus one arrive from the dequantisation
+            // warps of every CTA of the pair when B is dequantised in shared memory.
+            mbar_init(smem_u32(&bar_full[s]), 1 + (kQ4 ? kCtaGroup : 0));
             mbar_init(smem_u32(&bar_empty[s]), kPairs);   // one commit from each pair that reads the slot
         }
         for (int b = 0; b < 2; ++b) {
@@ -941,50 +1004,89 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         __syncwarp();
     } else if constexpr (kQ4) {
         // ------------------------------------------------------------ Q4_0 dequantisation warps
-        // Lane `row` of warp dw owns B row dw * 32 + lane of this CTA's 128 (one output column n).
-        // Raw blocks of the next stage are loaded while the current one waits for its slot.
-        const int row = (warp - 2 - Cfg::kEpiWarps) * 32 + lane;
-        UnitIter units;
-        units.init(p, cluster_id, num_clusters);
-        Unit u;
-        bool valid = units.next(p, u);
-        int kt = valid ? u.k0 : 0;
-        auto row_of = [&](const Unit& uu) {
-            int mb, nb;
-            tile_coords(p, uu.tile, mb, nb);
-            return nb * kBN + static_cast<int>(prank) * Cfg::kBNC + row;
+        // Warp dw covers B rows dw * 16 .. +15 of this CTA's 128 (output columns); lane l takes block
+        // l % 4 of rows dw * 16 + l / 4 + 8 * pass.  Two walks over the same stages: `conv` is the
+        // next stage to store, `load` runs kQ4RegStages further ahead filling raw register buffers.
+        // (An L2 prefetch walk further ahead was measured to slow the loop down.)  Each stage is converted
+        // into registers while the MMA still works on earlier stages; once its slot is free only the
+        // shared-memory stores, a fence, a barrier among the four warps and one arrive remain.
+        static_assert(Cfg::kDqWarps * 8 * kQ4Passes == Cfg::kBNC, "every B row of the CTA has one lane group");
+        const int dw = warp - 2 - Cfg::kEpiWarps;
+        const int row0 = dw * 8 * kQ4Passes + (lane >> 2);
+        const int bl = lane & 3;
+        // The rows of a unit change only with its tile: keep the last tile's answer.
+        int memo_tile = -1, memo_n0 = 0;
+        auto rows_of = [&](const Unit& uu, int (&rows)[kQ4Passes]) {
+            if (uu.tile != memo_tile) {
+                int mb, nb;
+                tile_coords(p, uu.tile, mb, nb);
+                memo_tile = uu.tile;
+                memo_n0 = nb * kBN + static_cast<int>(prank) * Cfg::kBNC + row0;
+            }
+#pragma unroll
+            for (int ps = 0; ps < kQ4Passes; ++ps) rows[ps] = memo_n0 + 8 * ps;
         };
-        Q4Row cur, nxt;
-        int cur_tile = valid ? u.tile : 0;
-        if (valid) q4_load_row(p, row_of(u), kt, cur);
+        StageWalk conv, load;
+        conv.init(p, cluster_id, num_clusters);
+        load.init(p, cluster_id, num_clusters);
+        auto load_one = [&](Q4Raw& r) {
+            if (!load.valid) return;
+            int rows[kQ4Passes];
+            rows_of(load.u, rows);
+            q4_load_raw(p, rows, load.kt * 4 + bl, r);
+            load.advance(p);
+        };
+        Q4Raw r0, r1;
+        Q4Half h;
+        load_one(r0);
+        load_one(r1);
+        const bool odd = (bl & 1) != 0;
+        if (conv.valid) q4_convert(r0, odd, h);
+        load_one(r0);
         uint32_t stage = 0, phase = 0;
-        while (valid) {
-            // Advance to the next (unit, k-tile) and prefetch its raw blocks.
-            const int this_tile = cur_tile;
-            if (++kt >= u.k1) {
-                valid = units.next(p, u);
-                kt = valid ? u.k0 : 0;
+        bool ok = true;
+        // Store the converted stage, then convert the one held in `next` and refill `next`.
+        auto store_one = [&](Q4Raw& next) {
+            if (!ok || !conv.valid) return;
+            const bool got = mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, p.timeout_ns, abort_flag);
+            // Every wait above is bounded, so all four warps reach this barrier; it ANDs their
+            // outcomes so that they leave together on a failure (none is left at a barrier).
+            uint32_t all_got;
+            asm volatile("{\n\t.reg .pred pin, pout;\n\t"
+                         "setp.ne.u32 pin, %1, 0;\n\t"
+                         "bar.red.and.pred pout, 1, %2, pin;\n\t"
+                         "selp.u32 %0, 1, 0, pout;\n\t}"
+                         : "=r"(all_got) : "r"(got ? 1u : 0u), "n"(Cfg::kDqWarps * 32) : "memory");
+            if (!all_got) {
+                if (lane == 0 && !got && !*abort_flag)
+                    report_error<kClusterCtas>(p, ROLE_PRODUCER, conv.u.tile, 500 + static_cast<int>(stage), abort_flag);
+                ok = false;
+                return;
             }
-            if (valid) {
-                cur_tile = u.tile;
-                q4_load_row(p, row_of(u), kt, nxt);
-            }
-            bool ok = mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, p.timeout_ns, abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) {
-                if (lane == 0 && !*abort_flag)
-                    report_error<kClusterCtas>(p, ROLE_PRODUCER, this_tile, 500 + static_cast<int>(stage), abort_flag);
-                break;
-            }
-            q4_store_row(ring + stage * Cfg::kStageBytes + Cfg::kABytes, row, cur, Cfg::kBChunkBytes);
-            asm volatile("fence.proxy.async;" ::: "memory");   // generic writes -> the MMA's async reads
-            __syncwarp();
-            if (lane == 0) {
+            q4_store(ring + stage * Cfg::kStageBytes + Cfg::kABytes, row0, bl, h, Cfg::kBChunkBytes);
+            // This CTA's generic shared-memory writes -> the MMA's async-proxy reads.
+            fence_proxy_async_smem();
+            // The four dequantisation warps of this CTA meet (no exit path lies between the barrier
+            // above and this one); one thread arrives for all of them.
+            asm volatile("bar.sync 1, %0;" :: "n"(Cfg::kDqWarps * 32) : "memory");
+            if (dw == 0 && lane == 0) {
                 const uint32_t full_local = smem_u32(&bar_full[stage]);
-                if constexpr (kCtaGroup == 2) mbar_arrive_cluster(mapa_shared(full_local, lrank));
-                else mbar_arrive_local(full_local);
+                if constexpr (kCtaGroup == 2) {
+                    if (prank == 0) mbar_arrive_local(full_local);
+                    else mbar_arrive_cluster(mapa_shared(full_local, lrank));
+                } else {
+                    mbar_arrive_local(full_local);
+                }
             }
-            cur = nxt;
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            conv.advance(p);
+            if (conv.valid) q4_convert(next, odd, h);
+            load_one(next);
+        };
+        static_assert(kQ4RegStages == 2, "two rotating raw register buffers");
+        while (ok && conv.valid) {
+            store_one(r1);
+            store_one(r0);
         }
     }
 

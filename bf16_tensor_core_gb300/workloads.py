@@ -34,7 +34,7 @@ class Workload:
     dtype_in: str = "f16"
     dtype_out: str = "f32"
     layoutA: str = "row"        # row: M x K (K contiguous); col: stored K x M
-    layoutB: str = "row"        # row: K x N (N contiguous); col: stored N x K
+    layoutB: str = "row"        # row: K x N (N contiguous); col: stored N x K; q4_0: N rows of Q4_0 blocks
     alpha: float = 1.0
     beta: float = 0.0
     dist_a: tuple = ("uniform", -1.0, 1.0)
@@ -70,6 +70,10 @@ WORKLOADS = {
     5: Workload("gemm_8192_f16_f16", 8192, 8192, 8192, "f16", "f16", "row", "row", 1.0, 0.0,
                 ("normal_sqrtk",), ("normal_sqrtk",), None, None, _seed(5),
                 "8192^3, f16 in N(0,1)/sqrt(K), f16 out"),
+    6: Workload("prefill_2048x11008x4096_q4_0_bias", 2048, 11008, 4096, "f16", "f16", "row", "q4_0",
+                1.0, 0.0, ("normal", 1.0), ("q4_0", 0.02), ("normal", 0.02), None, _seed(6),
+                "prefill projection with Q4_0 weights (random valid blocks, |w| <= 0.04), f16 activations, "
+                "f16 out, fused per-column bias"),
 }
 
 
@@ -92,6 +96,8 @@ def stored_shape_a(w: Workload, lda: int | None = None):
 
 
 def stored_shape_b(w: Workload, ldb: int | None = None):
+    if w.layoutB == "q4_0":
+        return (w.N, ldb or w.K // 32 * Q4_0_BLOCK_BYTES)
     if w.layoutB == "row":
         return (w.K, ldb or w.N)
     return (w.N, ldb or w.K)
@@ -100,15 +106,18 @@ def stored_shape_b(w: Workload, ldb: int | None = None):
 def generate(w: Workload, *, lda=None, ldb=None, ldc=None) -> dict:
     """Draw A, B, then bias or C_in (in that order) on the CPU generator seeded with w.seed.
 
-    Returns CPU tensors in the stored layout: A, B (dtype_in), bias (N, dtype_out)
-    or None, Cin (M x ldc, dtype_out) or None.  Padding columns of a wider leading
+    Returns CPU tensors in the stored layout: A, B (dtype_in; uint8 Q4_0 blocks for layoutB
+    "q4_0"), bias (N, dtype_out) or None, Cin (M x ldc, dtype_out) or None.  Padding columns of a wider leading
     dimension are drawn too (their values never enter the product).
     """
     g = torch.Generator().manual_seed(w.seed)
     din = DTYPES[w.dtype_in]
     dout = DTYPES[w.dtype_out]
     A = _draw(stored_shape_a(w, lda), w.dist_a, w.K, g).to(din)
-    B = _draw(stored_shape_b(w, ldb), w.dist_b, w.K, g).to(din)
+    if w.layoutB == "q4_0":     # uint8 blocks from their own generator (seed + 1)
+        B = q4_0_blocks(w.N, w.K, w.seed + 1, ldbq=ldb, scale=w.dist_b[1])
+    else:
+        B = _draw(stored_shape_b(w, ldb), w.dist_b, w.K, g).to(din)
     bias = _draw((w.N,), w.dist_bias, w.K, g).to(dout) if w.dist_bias else None
     Cin = _draw((w.M, ldc or w.N), w.dist_cin, w.K, g).to(dout) if w.dist_cin else None
     return {"A": A, "B": B, "bias": bias, "Cin": Cin}

@@ -130,6 +130,7 @@ FUSED_CASES = [
     dict(M=257, N=300, K=2048, dout="bf16", layoutA="col"),
     dict(M=700, N=260, K=96, dout="f32", alpha=0.5, beta=1.0),               # one partial k-tile
     dict(M=128, N=1000, K=4096, dout="f16", ldbq=2320),                      # padded weight rows
+    dict(M=200, N=300, K=128, dout="f32", ldbq=74),                          # pitch 2 mod 4: rows repacked
 ]
 
 
@@ -162,6 +163,26 @@ def test_fused_equals_plain_gemm_on_dequantised_weights(sk):
         assert (p2["stream_k"], p2["clusters"], p2["dp_tiles"]) == (plan["stream_k"], plan["clusters"], plan["dp_tiles"])
     torch.cuda.synchronize()
     assert torch.equal(C1, C2)
+
+
+def test_fused_rows_two_bytes_past_alignment():
+    """Weights whose rows start 2 bytes past a 4-byte boundary are repacked first; same result."""
+    _need_gpu()
+    c = _case(256, 384, 1024, seed=60, dout="f32")
+    N, pitch = c["N"], c["bq"].size(1)                    # 576 bytes per row
+    store = torch.zeros(N, pitch + 4, dtype=torch.uint8)
+    store[:, 2:2 + pitch] = c["bq"]
+    dev = store.cuda()
+    view = dev[:, 2:2 + pitch]                            # data_ptr % 4 == 2, row stride pitch + 4
+    C = torch.full((c["M"], N), float("nan"), dtype=torch.float32, device="cuda")
+    with G.Gemm(0, sync_check=1) as g:
+        n0 = g.launches
+        st = G.gemm_run_q4_0(g.h, c["M"], N, c["K"], c["A"].cuda().data_ptr(), c["K"], 0, view.data_ptr(),
+                             pitch + 4, C.data_ptr(), N, 2, 1.0, 0.0, None, torch.cuda.current_stream().cuda_stream)
+        assert st == G.GEMM_OK, g.last_error()
+        assert g.last_plan()["repack_b"] == 1 and g.launches - n0 == 2
+    torch.cuda.synchronize()
+    _check(c, C)
 
 
 def test_fused_integers_exact():
@@ -238,3 +259,19 @@ def test_fused_rejects_bad_arguments():
                                1.0, 0.0, None, torch.cuda.current_stream().cuda_stream) == G.GEMM_ERR_UNSUPPORTED
     with G.Gemm(0, config=Q4_CONFIG) as g:                                         # plain B on the Q4_0 config
         assert g.run(A, A, C, check=False) == G.GEMM_ERR_UNSUPPORTED
+
+
+def test_fused_bounded_wait_expires_and_reports():
+    """Cluster 0's producer never issues the A copy of stage 3: the MMA issuer's wait runs out after
+    200 ms, the dequantisation warps leave their loop together (their per-stage barrier ANDs the
+    wait outcomes), the kernel records the timeout and returns; the next call works."""
+    _need_gpu()
+    c = _case(256, 256, 1024, seed=95, dout="f32")
+    with G.Gemm(0, timeout_ms=200, debug_skip_stage=3) as g:
+        _run(g, c)
+        st = g.status()
+        assert st == G.GEMM_ERR_TIMEOUT, G.gemm_status_string(st)
+        assert g.status() == G.GEMM_OK
+    with G.Gemm(0, sync_check=1) as g:
+        C = _run(g, c)
+    _check(c, C)
