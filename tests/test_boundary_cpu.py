@@ -50,7 +50,8 @@ def test_config_table(lib):
         st, c = G.gemm_config_info(i)
         assert st == G.GEMM_OK and c.id == i
         assert c.block_m == 128 * c.cta_group * c.pairs and c.block_k in (64, 128)
-        assert c.block_n in (128, 256, 512) and c.smem_bytes <= 232448 and c.threads == 320
+        assert c.block_n in (128, 256, 512) and c.smem_bytes <= 232448
+        assert c.threads == (448 if c.b_q4_0 else 320)        # Q4_0: 8 more dequantisation warps, 4 fewer epilogue
         assert c.pairs == 1 or c.cta_group == 2
         stage = (128 + c.block_n // c.cta_group) * c.block_k * 2
         assert c.smem_bytes >= c.stages * stage
