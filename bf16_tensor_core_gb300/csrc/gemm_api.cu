@@ -41,13 +41,14 @@ const ConfigDesc kConfigs[kNumConfigs] = {
     make_desc<2, 2, 256, 3, 128>(6),  // two pairs sharing B, 512 x 256 tile, 128-wide K stages
     make_desc<2, 1, 512, 4, 64>(7),   // 2-SM pair, 256 x 512 tile (two N=256 MMAs per K step)
     make_desc<2, 1, 256, 3, 128, true>(8),  // as 5, B dequantised from Q4_0 blocks in shared memory
+    make_desc<1, 1, 64, 4, 128>(9),   // 1 SM, 128 x 64 tile: the short side of a transposed skinny product
 };
 
 // Mainloop efficiency per config (measured k-iteration time of one long-K tile against the
 // config's tensor-core time at 1.9 GHz, cold L2, GB300): small tiles need more operand bytes per
 // flop and are bound by the TMA load rate per SM.  Config 7 is derated for its single accumulator
 // (its epilogue does not overlap the next tile).
-const double kConfigEfficiency[kNumConfigs] = {0.73, 0.78, 0.40, 0.39, 0.80, 0.85, 0.84, 0.75, 0.85};
+const double kConfigEfficiency[kNumConfigs] = {0.73, 0.78, 0.40, 0.39, 0.80, 0.85, 0.84, 0.75, 0.85, 0.40};
 
 int cluster_ctas(const ConfigDesc& d) { return d.cta_group * d.pairs; }
 int block_m(const ConfigDesc& d) { return 128 * cluster_ctas(d); }
@@ -261,13 +262,40 @@ Schedule schedule(const ConfigDesc& d, double eff, int64_t M, int64_t N, int64_t
     return best;
 }
 
+// One product as the kernels see it.  transpose() gives C^T = op(B)^T op(A)^T: M and N swap and
+// each operand's stored array is reused with the opposite layout code.  A B stored K x N (N
+// contiguous, ROW) is the M-contiguous COL operand A' of the transposed product, a B stored N x K
+// (COL) its K-contiguous ROW A'; an A stored M x K (ROW) is the COL operand B' (stored N' x K'),
+// an A stored K x M (COL) the ROW B' (stored K' x N').
+struct Problem {
+    int64_t M, N, K;
+    const void* A;
+    int64_t lda;
+    const void* B;
+    int64_t ldb;
+    int la, lb;
+};
+
+Problem transpose(const Problem& q) {
+    return Problem{q.N, q.M, q.K, q.B, q.ldb, q.A, q.lda, q.lb == GEMM_ROW ? GEMM_COL : GEMM_ROW,
+                   q.la == GEMM_ROW ? GEMM_COL : GEMM_ROW};
+}
+
+// Whether a call computes the transposed product: only on request (skinny 1), or automatically for
+// a few rows of C against many columns when the config is automatic.
+bool use_transposed(int skinny, int config, int64_t M, int64_t N, int b_q4) {
+    if (b_q4) return false;
+    if (skinny == 1) return true;
+    return skinny == -1 && config == -1 && M <= 64 && N > 64;
+}
+
 // Pure host planning: validation, config choice, grid, stream-K split and workspace.
 //   slots[c]     clusters of config c that fit on the device at once
 //   cluster_cap  optional cap on launched clusters (0 = none)
 //   b_q4         1: B is Q4_0 weights (N rows of K/32 18-byte blocks, ldb = row pitch in bytes)
 gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int din, int dout,
                         int la, int lb, float beta, const int* slots, int config, int stream_k, int cluster_cap,
-                        gemm_plan_t* out, std::string* err, int b_q4 = 0) {
+                        gemm_plan_t* out, std::string* err, int b_q4 = 0, int c_trans = 0) {
     std::memset(out, 0, sizeof(*out));
     out->config = -1;
     if (M < 0 || N < 0 || K < 0) { *err = "M, N and K must be >= 0"; return GEMM_ERR_INVALID_ARG; }
@@ -286,7 +314,8 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
             *err = "ldbq must be even and at least K/32*18 bytes"; return GEMM_ERR_INVALID_ARG;
         }
     } else if (ldb < std::max<int64_t>(1, b_inner)) { *err = "ldb too small"; return GEMM_ERR_INVALID_ARG; }
-    if (ldc < std::max<int64_t>(1, N)) { *err = "ldc too small"; return GEMM_ERR_INVALID_ARG; }
+    // (In the transposed product the kernel's rows are C's columns: C's pitch covers M here.)
+    if (ldc < std::max<int64_t>(1, c_trans ? M : N)) { *err = "ldc too small"; return GEMM_ERR_INVALID_ARG; }
     if (config < -1 || config >= kNumConfigs) { *err = "no such config"; return GEMM_ERR_UNSUPPORTED; }
     if (config >= 0 && kConfigs[config].b_q4 != b_q4) {
         *err = b_q4 ? "this config does not take Q4_0 weights" : "this config only takes Q4_0 weights";
@@ -327,7 +356,8 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     out->tiles_n = (int)((N + out->block_n - 1) / out->block_n);
     out->clusters = sc.clusters;
     out->raster_group = std::min(out->tiles_m, 8);
-    out->tma_store = ((ldc * out_bytes) % 16 == 0) ? 1 : 0;
+    out->tma_store = (!c_trans && (ldc * out_bytes) % 16 == 0) ? 1 : 0;
+    out->transposed = c_trans;
     out->repack_a = (lda * 2) % 16 != 0;
     // Q4_0 rows are read with 4-byte loads: a pitch that is not a multiple of 4 bytes is repacked
     // (as 16-bit units) to a 16-byte pitch.
@@ -390,6 +420,7 @@ struct LaunchArgs {
     unsigned epoch;
     cudaStream_t stream;
     bool force_2d;              // tuning: one 2-D box per slab even where a 3-D box would do
+    int c_trans = 0;            // the product is C^T (see Problem / transpose)
 };
 
 // Encode the tensor maps, fill the kernel parameters and launch the planned config.
@@ -448,7 +479,7 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
     if (st != GEMM_OK) return st;
     const int eb = elt_bytes(a.dout);
     const bool c_aligned = (reinterpret_cast<uintptr_t>(a.C) % 16) == 0 && (a.ldc * eb) % 16 == 0;
-    const int use_tma_store = (plan.tma_store && c_aligned) ? 1 : 0;
+    const int use_tma_store = (plan.tma_store && c_aligned && !a.c_trans) ? 1 : 0;
     if (use_tma_store) {
         *what = "tensor map of C";
         const CUtensorMapDataType tcd = a.dout == GEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -484,6 +515,7 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
     p.alpha = a.alpha;
     p.beta = a.beta;
     p.use_tma_store = use_tma_store;
+    p.c_trans = a.c_trans;
     p.c_vec_ok = c_aligned ? 1 : 0;
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
@@ -618,6 +650,7 @@ const void* config_kernel(int id, int out) {
         case 6: return cfg6_kernel(out);
         case 7: return cfg7_kernel(out);
         case 8: return cfg8_kernel(out);
+        case 9: return cfg9_kernel(out);
         default: return nullptr;
     }
 }
@@ -648,6 +681,7 @@ cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, c
         case 6: return cfg6_launch(out, lc, a, b, c, p);
         case 7: return cfg7_launch(out, lc, a, b, c, p);
         case 8: return cfg8_launch(out, lc, a, b, c, p);
+        case 9: return cfg9_launch(out, lc, a, b, c, p);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -667,6 +701,7 @@ void gemm_options_default(gemm_options_t* opt) {
     opt->max_clusters = 0;
     opt->debug_skip_stage = -1;
     opt->stream_k = -1;
+    opt->skinny = -1;
 }
 
 const char* gemm_status_string(gemm_status_t s) {
@@ -713,8 +748,12 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
         slots[c] = d.cta_group == 1 ? num_sms : max_clusters / d.pairs;
     }
     std::string err;
-    return plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, slots, config, stream_k, 0,
-                     out, &err);
+    gemm_status_t st = plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, slots, config,
+                                 stream_k, 0, out, &err);
+    if (st != GEMM_OK || M == 0 || N == 0 || K == 0 || !use_transposed(-1, config, M, N, 0)) return st;
+    const Problem q = transpose(Problem{M, N, K, nullptr, lda, nullptr, ldb, layoutA, layoutB});
+    return plan_impl(q.M, q.N, K, q.lda, q.ldb, ldc, dtype_in, dtype_out, q.la, q.lb, beta, slots, config, stream_k, 0,
+                     out, &err, 0, 1);
 }
 
 gemm_status_t gemm_create(gemm_handle_t* out, int device, const gemm_options_t* opt) {
@@ -840,6 +879,15 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
         plan.workspace_bytes += round_up(N * round_up(K / 32 * 9, 8) * 2, 256);
         plan.kernels = 2;
     }
+    // The product the kernels compute: C itself, or C^T for a few rows of C against many columns.
+    Problem q{M, N, K, A, lda, B, ldb, layoutA, layoutB};
+    const bool trans = K > 0 && use_transposed(h->opt.skinny, h->opt.config, M, N, b_q4);
+    if (trans) {
+        q = transpose(q);
+        st = plan_impl(q.M, q.N, K, q.lda, q.ldb, ldc, dtype_in, dtype_out, q.la, q.lb, beta, h->dev.slots,
+                       h->opt.config, h->opt.stream_k, h->opt.max_clusters, &plan, &err, 0, 1);
+        if (st != GEMM_OK) return fail(h, st, err);
+    }
     DeviceGuard guard(h->device);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
@@ -850,15 +898,15 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
         if (e != cudaSuccess) return cuda_fail(h, "scale/bias kernel launch", e);
         h->launches += 1;
     } else {
-        const void* a_ptr = A;
-        const void* b_ptr = B;
-        int64_t lda_eff = lda, ldb_eff = ldb;
+        const void* a_ptr = q.A;
+        const void* b_ptr = q.B;
+        int64_t lda_eff = q.lda, ldb_eff = q.ldb;
         const char* what = "";
         if (plan.repack_a || plan.repack_b) {
             st = ensure_buffer(h, &h->ws, &h->ws_bytes, (size_t)(plan.workspace_bytes - plan.sk_partial_bytes),
                                "workspace allocation");
             if (st != GEMM_OK) return st;
-            cudaError_t e = repack_operands(plan, M, N, K, layoutA, layoutB, h->ws, &a_ptr, &lda_eff, &b_ptr, &ldb_eff,
+            cudaError_t e = repack_operands(plan, q.M, q.N, K, q.la, q.lb, h->ws, &a_ptr, &lda_eff, &b_ptr, &ldb_eff,
                                             h->dev.num_sms, s, &h->launches, &what, b_q4);
             if (e != cudaSuccess) return cuda_fail(h, what, e);
         }
@@ -869,10 +917,10 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
             if (st != GEMM_OK) return st;
             if (++h->epoch == 0) ++h->epoch;
         }
-        LaunchArgs la{&plan, M, N, K, a_ptr, lda_eff, b_ptr, ldb_eff, C, ldc, dtype_in, dtype_out, layoutA, layoutB,
+        LaunchArgs la{&plan, q.M, q.N, K, a_ptr, lda_eff, b_ptr, ldb_eff, C, ldc, dtype_in, dtype_out, q.la, q.lb,
                       alpha, beta, bias, h->d_status, (unsigned long long)h->opt.timeout_ms * 1000000ull,
                       h->opt.debug_skip_stage, h->opt.raster_group, h->sk_part, h->sk_flags, h->epoch, s,
-                      h->force_2d};
+                      h->force_2d, trans ? 1 : 0};
         TmapFn tmap = [h](const TmapDesc& desc, CUtensorMap* m) { return get_tmap_cached(h, desc, m); };
         cudaError_t ce = cudaSuccess;
         st = launch_planned(la, tmap, &what, &ce);

@@ -48,6 +48,8 @@ struct KernelParams {
     const void* bias;          // N elements of the output type, or nullptr
     float alpha, beta;
     int use_tma_store;         // write C with TMA tensor stores (with beta != 0, C_in boxes arrive by TMA loads)
+    int c_trans;               // the kernel computes C^T: its element (i, j) is C[j * ldc + i]; the bias is
+                               // indexed by i (direct stores only)
     int c_vec_ok;              // C rows may be accessed with 16-byte vectors
     unsigned long long* status;
     unsigned long long timeout_ns;
@@ -251,6 +253,20 @@ __device__ __forceinline__ void epilogue_math(const KernelParams& p, const uint3
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= p.alpha;
     }
+    if (p.c_trans) {
+        if (p.beta != 0.0f && row < p.M) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (col0 + i < p.N)
+                    v[i] = fmaf(p.beta, load_out<kOut>(p.C, static_cast<long long>(col0 + i) * p.ldc + row), v[i]);
+        }
+        if (p.bias != nullptr && row < p.M) {
+            const float b = load_out<kOut>(p.bias, row);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += b;
+        }
+        return;
+    }
     if (p.beta != 0.0f && row < p.M) {
         const long long base = static_cast<long long>(row) * p.ldc + col0;
         if (p.c_vec_ok && col0 + 32 <= p.N) {
@@ -285,6 +301,18 @@ __device__ __forceinline__ void epilogue_math(const KernelParams& p, const uint3
 template <int kOut>
 __device__ __forceinline__ void store_row_direct(const KernelParams& p, const float (&v)[32], int row, int col0) {
     if (row >= p.M) return;
+    if (p.c_trans) {   // column `row` of C: for each j the lanes of a warp write consecutive addresses
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if (col0 + i < p.N) {
+                const long long idx = static_cast<long long>(col0 + i) * p.ldc + row;
+                if constexpr (kOut == OUT_F32) static_cast<float*>(p.C)[idx] = v[i];
+                else if constexpr (kOut == OUT_F16) static_cast<__half*>(p.C)[idx] = __float2half_rn(v[i]);
+                else static_cast<__nv_bfloat16*>(p.C)[idx] = __float2bfloat16_rn(v[i]);
+            }
+        }
+        return;
+    }
     const long long base = static_cast<long long>(row) * p.ldc + col0;
     if (p.c_vec_ok && col0 + 32 <= p.N) {
         if constexpr (kOut == OUT_F32) {
@@ -337,7 +365,7 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
 // Stream-K partials.  Inside one CTA's slot the data of epilogue warp ew (its 32 rows x kCols
 // columns) is one contiguous block [kCols / 4 column quads][32 lanes][4 f32]: a warp store of one
 // quad is 512 contiguous bytes, and 64 columns (8 KB) are one contiguous piece.
-constexpr uint32_t kFixPieceBytes = 64 * 32 * 4;   // 64 columns x 32 rows of f32
+constexpr uint32_t kFixPieceBytes = 64 * 32 * 4;   // at most 64 columns x 32 rows of f32 per piece
 constexpr int kFixBufs = 3;                        // pieces in flight per warp
 
 // Head fix-up: add the partials of `count` consecutive clusters (slots `stride` floats apart,
@@ -348,16 +376,18 @@ template <int kCols>
 __device__ __forceinline__ bool head_fixup(uint32_t tbase, int lane, const float* first, int count, size_t stride,
                                            uint32_t region, uint32_t bar0, uint64_t timeout_ns,
                                            const volatile int* abort_flag) {
-    static_assert(kCols % 64 == 0, "whole 64-column pieces");
-    constexpr int kPieces = kCols / 64;
+    constexpr int kPieceCols = kCols < 64 ? kCols : 64;
+    static_assert(kPieceCols % 32 == 0 && kCols % kPieceCols == 0, "whole pieces of 32 or 64 columns");
+    constexpr int kPieces = kCols / kPieceCols;
+    constexpr uint32_t kPieceBytes = kPieceCols * 32 * 4;
     const int n = count * kPieces;
     auto issue = [&](int i) {
         const int src = i / kPieces;
         const int pc = i - src * kPieces;
         const uint32_t b = static_cast<uint32_t>(i % kFixBufs);
-        mbar_arrive_expect_tx(bar0 + 8u * b, kFixPieceBytes);
-        bulk_load_g2s(region + b * kFixPieceBytes, first + static_cast<size_t>(src) * stride + pc * (64 * 32),
-                      kFixPieceBytes, bar0 + 8u * b);
+        mbar_arrive_expect_tx(bar0 + 8u * b, kPieceBytes);
+        bulk_load_g2s(region + b * kFixPieceBytes, first + static_cast<size_t>(src) * stride + pc * (kPieceCols * 32),
+                      kPieceBytes, bar0 + 8u * b);
     };
     if (lane == 0) {
         fence_proxy_async_global();   // the flags were acquired by this thread in the generic proxy
@@ -370,9 +400,9 @@ __device__ __forceinline__ bool head_fixup(uint32_t tbase, int lane, const float
         bool ok = mbar_wait_bounded(bar0 + 8u * b, static_cast<uint32_t>((i / kFixBufs) & 1), timeout_ns, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) return false;
         const uint32_t buf = region + b * kFixPieceBytes;
-        const uint32_t tpiece = tbase + static_cast<uint32_t>((i % kPieces) * 64);
+        const uint32_t tpiece = tbase + static_cast<uint32_t>((i % kPieces) * kPieceCols);
 #pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
+        for (int cc = 0; cc < kPieceCols / 32; ++cc) {
             uint32_t acc[32];
             tmem_ld_32x32b_x32(tpiece + cc * 32, acc);
             tmem_wait_ld();
@@ -940,7 +970,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int mb, nb;
             tile_coords(p, u.tile, mb, nb);
             const int row0 = mb * kClusterRows + static_cast<int>(rank) * Cfg::kBM + quarter * 32;
-            if (p.beta != 0.0f && u.kind != UNIT_TAIL)
+            if (p.beta != 0.0f && u.kind != UNIT_TAIL && !p.c_trans)
                 prefetch_c_rows<kOut, Cfg::kEpiCols>(p, row0 + lane, nb * kBN + pcol0);
             bool ok = mbar_wait_bounded(smem_u32(&bar_tfull[acc]), acc_phase, p.timeout_ns, abort_flag);
             ok = __all_sync(0xffffffffu, ok);

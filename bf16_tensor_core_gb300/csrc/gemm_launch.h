@@ -20,7 +20,7 @@ struct ConfigDesc {
     int b_q4;         // 1: B is Q4_0-quantised and dequantised in shared memory by the kernel
 };
 
-constexpr int kNumConfigs = 9;
+constexpr int kNumConfigs = 10;
 constexpr int kNumOut = 3;  // OUT_F16, OUT_BF16, OUT_F32
 
 // Static description of config `id` (nullptr if out of range).
@@ -61,6 +61,10 @@ cudaError_t cfg7_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap
 
 const void* cfg8_kernel(int out);
 cudaError_t cfg8_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
+                        const CUtensorMap& c, const KernelParams& p);
+
+const void* cfg9_kernel(int out);
+cudaError_t cfg9_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& c, const KernelParams& p);
 
 // Auxiliary kernels (gemm_aux.cu).

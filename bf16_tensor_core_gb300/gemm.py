@@ -27,7 +27,7 @@ LAYOUT_CODES = {"row": GEMM_ROW, "col": GEMM_COL}
 class gemm_options_t(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_int), ("config", ctypes.c_int), ("timeout_ms", ctypes.c_int),
                 ("sync_check", ctypes.c_int), ("raster_group", ctypes.c_int), ("max_clusters", ctypes.c_int),
-                ("debug_skip_stage", ctypes.c_int), ("stream_k", ctypes.c_int)]
+                ("debug_skip_stage", ctypes.c_int), ("stream_k", ctypes.c_int), ("skinny", ctypes.c_int)]
 
 
 class gemm_config_info_t(ctypes.Structure):
@@ -43,7 +43,8 @@ class gemm_plan_t(ctypes.Structure):
                 ("tiles_m", ctypes.c_int), ("tiles_n", ctypes.c_int), ("clusters", ctypes.c_int),
                 ("raster_group", ctypes.c_int), ("tma_store", ctypes.c_int), ("repack_a", ctypes.c_int),
                 ("repack_b", ctypes.c_int), ("workspace_bytes", ctypes.c_int64), ("kernels", ctypes.c_int),
-                ("stream_k", ctypes.c_int), ("dp_tiles", ctypes.c_int), ("sk_partial_bytes", ctypes.c_int64)]
+                ("stream_k", ctypes.c_int), ("dp_tiles", ctypes.c_int), ("sk_partial_bytes", ctypes.c_int64),
+                ("transposed", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -88,6 +88,9 @@ typedef struct {
     int debug_skip_stage; /* TEST ONLY: the producer of cluster 0 never issues this k-stage,
                              so the MMA issuer's bounded wait expires (-1 = off)              */
     int stream_k;         /* tail-wave balancing: -1 automatic, 0 off, 1 whenever possible   */
+    int skinny;           /* computing C^T = op(B)^T op(A)^T (few rows of C become the short
+                             tile side): -1 automatic (M <= 64 < N, with config -1), 0 never,
+                             1 always                                                          */
 } gemm_options_t;
 
 /* Description of a kernel configuration. */
@@ -119,6 +122,9 @@ typedef struct {
     int stream_k;          /* 1: the last wave(s) are split evenly by k-iterations          */
     int dp_tiles;          /* tiles walked whole before the stream-K region                 */
     int64_t sk_partial_bytes; /* part of workspace_bytes holding stream-K f32 partials      */
+    int transposed;        /* 1: the kernel computes C^T = op(B)^T op(A)^T; tiles_m, tiles_n,
+                              block_m, block_n and repack_a/_b then describe that product
+                              (its rows are C's columns) and C is written by direct stores    */
 } gemm_plan_t;
 
 /* Fill *opt with defaults (config -1, timeout 2000 ms, no sync check, automatic raster). */

@@ -44,13 +44,13 @@ def test_options_default(lib):
 
 def test_config_table(lib):
     n = G.gemm_num_configs()
-    assert n == 9
+    assert n == 10
     seen = set()
     for i in range(n):
         st, c = G.gemm_config_info(i)
         assert st == G.GEMM_OK and c.id == i
         assert c.block_m == 128 * c.cta_group * c.pairs and c.block_k in (64, 128)
-        assert c.block_n in (128, 256, 512) and c.smem_bytes <= 232448
+        assert c.block_n in (64, 128, 256, 512) and c.smem_bytes <= 232448
         assert c.threads == (448 if c.b_q4_0 else 320)        # Q4_0: 8 more dequantisation warps, 4 fewer epilogue
         assert c.pairs == 1 or c.cta_group == 2
         stage = (128 + c.block_n // c.cta_group) * c.block_k * 2
@@ -58,7 +58,7 @@ def test_config_table(lib):
         seen.add((c.cta_group, c.pairs, c.block_n, c.block_k, c.b_q4_0))
     assert seen == {(1, 1, 128, 64, 0), (1, 1, 256, 64, 0), (2, 1, 128, 64, 0), (2, 1, 256, 64, 0),
                     (2, 2, 256, 64, 0), (2, 1, 256, 128, 0), (2, 2, 256, 128, 0), (2, 1, 512, 64, 0),
-                    (2, 1, 256, 128, 1)}
+                    (2, 1, 256, 128, 1), (1, 1, 64, 128, 0)}
     assert G.gemm_config_info(n)[0] == G.GEMM_ERR_UNSUPPORTED
 
 
@@ -93,7 +93,7 @@ def plan(M, N, K, lda=None, ldb=None, ldc=None, din=0, dout=2, la=0, lb=0, beta=
     (dict(M=4, N=9, K=8, lb=1, ldb=7), G.GEMM_ERR_INVALID_ARG),  # ldb < K for B stored N x K
     (dict(M=4, N=9, K=8, ldc=8), G.GEMM_ERR_INVALID_ARG),
     (dict(M=2 ** 31, N=4, K=4), G.GEMM_ERR_INVALID_ARG),
-    (dict(M=4, N=4, K=4, config=9), G.GEMM_ERR_UNSUPPORTED),
+    (dict(M=4, N=4, K=4, config=10), G.GEMM_ERR_UNSUPPORTED),
     (dict(M=4, N=4, K=4, sms=0), G.GEMM_ERR_INVALID_ARG),
     (dict(M=4, N=4, K=4), G.GEMM_OK),
 ])
@@ -119,6 +119,23 @@ def test_q4_0_config_is_not_a_plain_gemm_config(lib):
     for shape in [(512, 512, 512), (4096, 4096, 4096), (64, 4096, 4096), (1000, 3000, 2048)]:
         st, p = plan(*shape, dout=0)
         assert st == G.GEMM_OK and p.config != 8
+
+
+def test_plan_skinny_products_are_transposed(lib):
+    # A few rows of C against many columns: the kernel computes C^T with C's columns as its rows.
+    for M in (1, 16, 64):
+        st, p = plan(M, 4096, 4096, dout=0)
+        assert st == G.GEMM_OK and p.transposed == 1
+        assert p.tiles_m == 4096 // p.block_m and p.tiles_n == 1 and p.tma_store == 0
+    st, p = plan(65, 4096, 4096, dout=0)                  # more rows: the plain product
+    assert p.transposed == 0
+    st, p = plan(16, 64, 4096, dout=0)                    # nothing to gain with 64 columns
+    assert p.transposed == 0
+    st, p = plan(16, 4096, 4096, dout=0, config=5)        # a forced config keeps the plain product
+    assert p.transposed == 0 and p.config == 5
+    # operand checks still refer to the caller's arrays
+    st, p = plan(16, 4096, 4096, ldb=100)
+    assert st == G.GEMM_ERR_INVALID_ARG
 
 
 def test_plan_tiles_and_grid(lib):

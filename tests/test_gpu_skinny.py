@@ -1,0 +1,107 @@
+"""GPU parity of skinny products (few rows of C against many columns), computed as C^T =
+op(B)^T op(A)^T so that C's columns fill the long side of the tile ("Matrix Multiplication: The
+Operation Behind Modern AI", section "The shape a language model actually runs": an M x 4096 by
+4096 x 4096 product with M from 1 to 64)."""
+import pytest
+import torch
+
+from bf16_tensor_core_gb300 import gemm as G
+from bf16_tensor_core_gb300 import workloads as W
+from gpu_cases import alloc_c, compare, device_inputs, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+
+
+def _check(w, **opts):
+    d = W.generate(w)
+    dd = device_inputs(d)
+    C = alloc_c(w, d)
+    with G.Gemm(0, sync_check=1, **opts) as g:
+        run_gpu(g, w, dd, C)
+        plan = g.last_plan()
+    torch.cuda.synchronize()
+    rep = compare(w, d, C)
+    assert rep["passed"], rep
+    return plan, C
+
+
+CASES = [
+    dict(M=1, N=4096, K=4096, dtype_out="f16", layoutB="col"),            # one token, weights N x K
+    dict(M=7, N=3000, K=2048, dtype_out="f32", layoutB="row", bias=True),
+    dict(M=16, N=4100, K=1000, dtype_out="bf16", dtype_in="bf16", layoutB="col", bias=True),
+    dict(M=33, N=1000, K=512, dtype_out="f32", layoutA="col", alpha=0.5, beta=1.0),
+    dict(M=64, N=4096, K=4096, dtype_out="f16", layoutB="col"),
+    dict(M=64, N=520, K=200, dtype_out="f32", layoutA="col", layoutB="row", bias=True, alpha=-2.0, beta=0.25),
+]
+
+
+@pytest.mark.parametrize("i", range(len(CASES)))
+def test_skinny_parity_automatic(i):
+    _need_gpu()
+    c = dict(CASES[i])
+    w = W.problem(c.pop("M"), c.pop("N"), c.pop("K"), seed=300 + i, **c)
+    plan, _ = _check(w)
+    assert plan["transposed"] == 1 and plan["tma_store"] == 0
+
+
+@pytest.mark.parametrize("i", [1, 3, 5])
+def test_skinny_off_gives_the_plain_product(i):
+    _need_gpu()
+    c = dict(CASES[i])
+    w = W.problem(c.pop("M"), c.pop("N"), c.pop("K"), seed=400 + i, **c)
+    plan, _ = _check(w, skinny=0)
+    assert plan["transposed"] == 0
+
+
+@pytest.mark.parametrize("cfg", [0, 2, 5, 9])
+def test_transposed_product_on_any_shape_and_config(cfg):
+    """skinny=1 forces the transposed product (and a config) on an ordinary shape."""
+    _need_gpu()
+    w = W.problem(300, 260, 700, dtype_out="f32", bias=True, alpha=0.5, beta=1.0, seed=500 + cfg)
+    plan, _ = _check(w, skinny=1, config=cfg)
+    assert plan["transposed"] == 1 and plan["config"] == cfg
+
+
+def test_skinny_split_k_and_fixup():
+    """64 x 4096 x 4096: 32 tiles of C^T on 152 SMs, so K is split over several CTAs per tile."""
+    _need_gpu()
+    w = W.problem(64, 4096, 4096, dtype_out="f32", layoutB="col", seed=601)
+    plan, _ = _check(w, stream_k=1)
+    assert plan["transposed"] == 1 and plan["stream_k"] == 1 and plan["clusters"] > plan["tiles_m"] * plan["tiles_n"]
+
+
+def test_skinny_integers_equal_plain_product():
+    """Small integers: the transposed and the plain product are both exact, hence equal."""
+    _need_gpu()
+    M, N, K = 24, 2048, 1536
+    A = W.small_ints(M, K, "f16", 31).cuda()
+    B = W.small_ints(N, K, "f16", 32).cuda()               # stored N x K
+    ref = (A.cpu().to(torch.int64) @ B.cpu().to(torch.int64).t()).to(torch.float32)
+    outs = []
+    for skinny in (0, 1):
+        C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        with G.Gemm(0, sync_check=1, skinny=skinny) as g:
+            g.run(A, B, C, layoutB="col")
+            assert g.last_plan()["transposed"] == skinny
+        outs.append(C.cpu())
+    assert torch.equal(outs[0], ref) and torch.equal(outs[1], ref)
+
+
+def test_skinny_ldc_wider_than_n_leaves_padding():
+    _need_gpu()
+    w = W.problem(5, 700, 256, dtype_out="f16", layoutB="col", seed=602)
+    d = W.generate(w)
+    dd = device_inputs(d)
+    C = torch.full((5, 720), -7.0, dtype=torch.float16, device="cuda")
+    with G.Gemm(0, sync_check=1) as g:
+        g.run(dd["A"], dd["B"], C, M=5, N=700, K=256, layoutB="col")
+        assert g.last_plan()["transposed"] == 1
+    torch.cuda.synchronize()
+    assert torch.all(C[:, 700:].cpu() == -7.0)
+    rep = compare(w, d, C[:, :700].contiguous())
+    assert rep["passed"], rep
