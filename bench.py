@@ -40,7 +40,8 @@ def _args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2, help="1..6 (6: Q4_0 weights through gemm_run_q4_0)")
+    ap.add_argument("--workload", type=int, default=2,
+                    help="1..8 (6: Q4_0 weights through gemm_run_q4_0; 7, 8: decode shapes, HBM-bound)")
     ap.add_argument("--config", type=int, default=-1)
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps, capped at 200")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
@@ -198,6 +199,19 @@ class ClockSampler:
         reasons = sorted({n for r in sel for n, v in zip(names, r[6:10]) if v.strip().lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(sel)}
+
+
+def algorithmic_bytes(w) -> int:
+    """Least traffic of one product: read A and B once, write C once (and read C_in, bias)."""
+    ein = 2
+    eout = 4 if w.dtype_out == "f32" else 2
+    b_bytes = w.N * (w.K // 32) * 18 if w.layoutB == "q4_0" else w.K * w.N * ein
+    n = w.M * w.K * ein + b_bytes + w.M * w.N * eout
+    if w.beta != 0.0:
+        n += w.M * w.N * eout
+    if w.dist_bias is not None:
+        n += w.N * eout
+    return n
 
 
 def _cpu_cores() -> int:
@@ -433,14 +447,23 @@ def run_ours(args, rank, world, local):
         return
     peaks, src = _peaks()
     peak = float(peaks.get("bf16_tflops", 1900.0))
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
     achieved = w.flops / (ms_per_step / 1e3) / 1e12
     traffic, traffic_src = _traffic(w.name)
     n_sms = torch.cuda.get_device_properties(local).multi_processor_count
-    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": traffic,
-            "peak_source": f"{src}: cuBLAS bf16 burst (f16 and bf16 share the dense tensor rate)",
-            "kernel": "gb300::gemm_tc_kernel", "algorithmic_flops_per_launch": w.flops,
-            "avg_launch_ms": ms_per_step}
+    alg_bytes = algorithmic_bytes(w)
+    if w.flops / alg_bytes < peak * 1e12 / (hbm * 1e9):      # below the ridge: the stream of bytes bounds it
+        gbs = alg_bytes / (ms_per_step / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": traffic,
+                "peak_source": f"{src}: STREAM-style copy", "kernel": "gb300::gemm_tc_kernel",
+                "algorithmic_bytes_per_launch": alg_bytes, "algorithmic_flops_per_launch": w.flops,
+                "avg_launch_ms": ms_per_step}
+    else:
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": traffic,
+                "peak_source": f"{src}: cuBLAS bf16 burst (f16 and bf16 share the dense tensor rate)",
+                "kernel": "gb300::gemm_tc_kernel", "algorithmic_flops_per_launch": w.flops,
+                "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_ms": ms_per_step}
     if traffic is not None:
         roof["traffic_source"] = traffic_src
     if clocks.get("sm_mhz"):

@@ -70,6 +70,12 @@ WORKLOADS = {
     5: Workload("gemm_8192_f16_f16", 8192, 8192, 8192, "f16", "f16", "row", "row", 1.0, 0.0,
                 ("normal_sqrtk",), ("normal_sqrtk",), None, None, _seed(5),
                 "8192^3, f16 in N(0,1)/sqrt(K), f16 out"),
+    7: Workload("decode_1x4096x4096_f16", 1, 4096, 4096, "f16", "f16", "row", "col", 1.0, 0.0,
+                ("normal", 1.0), ("normal", 0.02), None, None, _seed(7),
+                "one token through a 4096 x 4096 f16 weight stored N x K (HBM-bound, intensity ~1 FLOP/B)"),
+    8: Workload("decode_64x4096x4096_f16", 64, 4096, 4096, "f16", "f16", "row", "col", 1.0, 0.0,
+                ("normal", 1.0), ("normal", 0.02), None, None, _seed(8),
+                "64 tokens through a 4096 x 4096 f16 weight stored N x K (HBM-bound)"),
     6: Workload("prefill_2048x11008x4096_q4_0_bias", 2048, 11008, 4096, "f16", "f16", "row", "q4_0",
                 1.0, 0.0, ("normal", 1.0), ("q4_0", 0.02), ("normal", 0.02), None, _seed(6),
                 "prefill projection with Q4_0 weights (random valid blocks, |w| <= 0.04), f16 activations, "

@@ -5,7 +5,7 @@ Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 shares no code with it.
 """
 from .oracle import (  # noqa: F401
-    OR_F16, OR_BF16, OR_F32, OR_ROW, OR_COL,
+    OR_F16, OR_BF16, OR_F32, OR_E4M3, OR_E5M2, OR_ROW, OR_COL, decode_e4m3, decode_e5m2,
     build, lib_path, decode_f16, decode_bf16, decode_f32,
     gemm_ref, ulp_out, tolerance, check, error_metrics, epilogue_magnitude, num_cpus, decode,
     f64_to_f16_bits, q4_0_to_f16, gemm_ref_q4_0,

@@ -31,8 +31,8 @@
 #include <string.h>
 #include <unistd.h>
 
-/* dtype codes used by the oracle's own interface */
-enum { OR_F16 = 0, OR_BF16 = 1, OR_F32 = 2 };
+/* dtype codes used by the oracle's own interface (E4M3 and E5M2 are inputs only) */
+enum { OR_F16 = 0, OR_BF16 = 1, OR_F32 = 2, OR_E4M3 = 3, OR_E5M2 = 4 };
 /* layout codes: A ROW = M x K with K contiguous, A COL = stored K x M (M contiguous);
  *               B ROW = K x N with N contiguous, B COL = stored N x K (K contiguous). */
 enum { OR_ROW = 0, OR_COL = 1 };
@@ -85,9 +85,39 @@ double oracle_f32_to_f64(uint32_t w) {
     return sign ? -v : v;
 }
 
+/* 8-bit floats, from the OCP "8-bit floating point" definitions (the FP8 formats of the tensor
+ * cores the matrix-multiplication page mentions):
+ *   E4M3: 1 sign, 4 exponent (bias 7), 3 fraction bits; exponent field 0 is subnormal
+ *         (frac * 2^-9); no infinities; S.1111.111 is NaN, so the largest value is 448.
+ *   E5M2: 1 sign, 5 exponent (bias 15), 2 fraction bits; IEEE-754 style: exponent 0 is
+ *         subnormal (frac * 2^-16), exponent 31 is infinity (frac 0) or NaN. */
+double oracle_e4m3_to_f64(uint8_t b) {
+    const unsigned sign = (b >> 7) & 1u;
+    const unsigned expo = (b >> 3) & 0xfu;
+    const unsigned frac = b & 0x7u;
+    double v;
+    if (expo == 0xf && frac == 0x7) return NAN;
+    if (expo == 0) v = ldexp((double)frac, -9);                        /* frac * 2^(1-7-3) */
+    else v = ldexp((double)(frac | 0x8u), (int)expo - 10);             /* (8 + frac) * 2^(e-7-3) */
+    return sign ? -v : v;
+}
+
+double oracle_e5m2_to_f64(uint8_t b) {
+    const unsigned sign = (b >> 7) & 1u;
+    const unsigned expo = (b >> 2) & 0x1fu;
+    const unsigned frac = b & 0x3u;
+    double v;
+    if (expo == 0) v = ldexp((double)frac, -16);                       /* frac * 2^(1-15-2) */
+    else if (expo == 0x1f) v = frac ? NAN : INFINITY;
+    else v = ldexp((double)(frac | 0x4u), (int)expo - 17);             /* (4 + frac) * 2^(e-15-2) */
+    return sign ? -v : v;
+}
+
 static double load_elem(const void* base, int64_t idx, int dtype) {
     if (dtype == OR_F16) return oracle_f16_to_f64(((const uint16_t*)base)[idx]);
     if (dtype == OR_BF16) return oracle_bf16_to_f64(((const uint16_t*)base)[idx]);
+    if (dtype == OR_E4M3) return oracle_e4m3_to_f64(((const uint8_t*)base)[idx]);
+    if (dtype == OR_E5M2) return oracle_e5m2_to_f64(((const uint8_t*)base)[idx]);
     return oracle_f32_to_f64(((const uint32_t*)base)[idx]);
 }
 

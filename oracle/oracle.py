@@ -31,6 +31,7 @@ from pathlib import Path
 import numpy as np
 
 OR_F16, OR_BF16, OR_F32 = 0, 1, 2
+OR_E4M3, OR_E5M2 = 3, 4          # 8-bit float inputs (OCP FP8 formats)
 OR_ROW, OR_COL = 0, 1
 
 _HERE = Path(__file__).resolve().parent
@@ -100,9 +101,14 @@ def _as_raw(x, dtype_code: int) -> np.ndarray:
         if dtype_code in (OR_F16, OR_BF16):
             import torch
             return t.view(torch.int16).numpy().view(np.uint16)
+        if dtype_code in (OR_E4M3, OR_E5M2):
+            import torch
+            return t.view(torch.uint8).numpy()
         return t.numpy().astype(np.float32, copy=False)
     a = np.ascontiguousarray(x)
-    if dtype_code in (OR_F16, OR_BF16):
+    if dtype_code in (OR_E4M3, OR_E5M2):
+        assert a.dtype == np.uint8, "8-bit float inputs are passed as uint8 bit patterns"
+    elif dtype_code in (OR_F16, OR_BF16):
         if a.dtype == np.float16:
             a = a.view(np.uint16)
         assert a.dtype == np.uint16, "half inputs are passed as uint16 bit patterns"
@@ -134,6 +140,14 @@ def decode_f32(x) -> np.ndarray:
 
 def decode(x, code: int) -> np.ndarray:
     return _decode(x, code)
+
+
+def decode_e4m3(x) -> np.ndarray:
+    return _decode(x, OR_E4M3)
+
+
+def decode_e5m2(x) -> np.ndarray:
+    return _decode(x, OR_E5M2)
 
 
 def gemm_ref(M, N, K, A, layoutA, B, layoutB, dtype_in, *, alpha=1.0, beta=0.0,

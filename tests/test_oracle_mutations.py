@@ -23,9 +23,10 @@ sys.path[:0] = [{root!r}, {tests!r}]
 import oracle.oracle as om
 import test_oracle_pins as P
 import test_oracle_q4_0 as Q
+import test_oracle_fp8 as F8
 om._lib = om.configure(ctypes.CDLL({lib!r}))
 caught = []
-for pin in P.PINS + Q.PINS:
+for pin in P.PINS + Q.PINS + F8.PINS:
     try:
         pin()
     except Exception:
@@ -62,6 +63,12 @@ MUTANTS = {
     "f16_ties_away": ("return fmod(f, 2.0) == 0.0 ? f : f + 1.0;", "return f + 1.0;"),
     "f16_subnormal_scale": ("rne(ldexp(a, 24))", "rne(ldexp(a, 23))"),
     "f16_exponent_bias_enc": ("(((e + 15) << 10)", "(((e + 14) << 10)"),
+    # 8-bit floats
+    "e4m3_bias_8": ("(int)expo - 10);             /* (8 + frac)", "(int)expo - 11);             /* (8 + frac)"),
+    "e4m3_no_nan": ("if (expo == 0xf && frac == 0x7) return NAN;", "(void)0;"),
+    "e4m3_subnormal_scale": ("ldexp((double)frac, -9);", "ldexp((double)frac, -10);"),
+    "e5m2_frac_bits": ("const unsigned frac = b & 0x3u;", "const unsigned frac = b & 0x7u;"),
+    "e5m2_no_inf": ("else if (expo == 0x1f) v = frac ? NAN : INFINITY;", "else if (expo == 0x1f) v = NAN;"),
 }
 
 
