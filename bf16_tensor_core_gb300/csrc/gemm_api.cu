@@ -25,10 +25,10 @@ using namespace gb300;
 namespace {
 
 // ---------------------------------------------------------------- configuration table
-template <int CG, int PAIRS, int BN, int ST, int BK, bool Q4 = false>
+template <int CG, int PAIRS, int BN, int ST, int BK, bool Q4 = false, int ELT = 2>
 constexpr ConfigDesc make_desc(int id) {
-    return ConfigDesc{id, CG, PAIRS, BN, BK, ST, TileConfig<CG, BN, ST, BK, Q4>::kSmemBytes,
-                      TileConfig<CG, BN, ST, BK, Q4>::kThreads, Q4 ? 1 : 0};
+    return ConfigDesc{id, CG, PAIRS, BN, BK, ST, TileConfig<CG, BN, ST, BK, Q4, ELT>::kSmemBytes,
+                      TileConfig<CG, BN, ST, BK, Q4, ELT>::kThreads, Q4 ? 1 : 0, ELT};
 }
 
 const ConfigDesc kConfigs[kNumConfigs] = {
@@ -42,13 +42,17 @@ const ConfigDesc kConfigs[kNumConfigs] = {
     make_desc<2, 1, 512, 4, 64>(7),   // 2-SM pair, 256 x 512 tile (two N=256 MMAs per K step)
     make_desc<2, 1, 256, 3, 128, true>(8),  // as 5, B dequantised from Q4_0 blocks in shared memory
     make_desc<1, 1, 64, 4, 128>(9),   // 1 SM, 128 x 64 tile: the short side of a transposed skinny product
+    make_desc<2, 1, 256, 3, 256, false, 1>(10),  // 8-bit inputs: 2-SM pair, 256 x 256 tile, BK 256
+    make_desc<1, 1, 64, 4, 256, false, 1>(11),   // 8-bit inputs: 1 SM, 128 x 64 tile (transposed skinny)
+    make_desc<1, 1, 128, 6, 128, false, 1>(12),  // 8-bit inputs: 1 SM, 128 x 128 tile
 };
 
 // Mainloop efficiency per config (measured k-iteration time of one long-K tile against the
 // config's tensor-core time at 1.9 GHz, cold L2, GB300): small tiles need more operand bytes per
 // flop and are bound by the TMA load rate per SM.  Config 7 is derated for its single accumulator
 // (its epilogue does not overlap the next tile).
-const double kConfigEfficiency[kNumConfigs] = {0.73, 0.78, 0.40, 0.39, 0.80, 0.85, 0.84, 0.75, 0.85, 0.40};
+const double kConfigEfficiency[kNumConfigs] = {0.73, 0.78, 0.40, 0.39, 0.80, 0.85, 0.84, 0.75, 0.85, 0.40,
+                                                0.85, 0.40, 0.40};
 
 int cluster_ctas(const ConfigDesc& d) { return d.cta_group * d.pairs; }
 int block_m(const ConfigDesc& d) { return 128 * cluster_ctas(d); }
@@ -68,7 +72,8 @@ int read_fault_env() {
     return f;
 }
 
-int elt_bytes(int dt) { return dt == GEMM_F32 ? 4 : 2; }
+int elt_bytes(int dt) { return dt == GEMM_F32 ? 4 : (dt == GEMM_E4M3 || dt == GEMM_E5M2) ? 1 : 2; }
+bool is_f8(int dt) { return dt == GEMM_E4M3 || dt == GEMM_E5M2; }
 int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
 // What a device offers each config: SM count, co-resident clusters, the tensor-map encoder.
@@ -301,9 +306,15 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     if (M < 0 || N < 0 || K < 0) { *err = "M, N and K must be >= 0"; return GEMM_ERR_INVALID_ARG; }
     const int64_t kMaxDim = (int64_t)1 << 31;
     if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) { *err = "M, N and K must be < 2^31"; return GEMM_ERR_INVALID_ARG; }
-    if (din != GEMM_F16 && din != GEMM_BF16) { *err = "dtype_in must be GEMM_F16 or GEMM_BF16"; return GEMM_ERR_INVALID_ARG; }
+    if (din != GEMM_F16 && din != GEMM_BF16 && !is_f8(din)) {
+        *err = "dtype_in must be GEMM_F16, GEMM_BF16, GEMM_E4M3 or GEMM_E5M2"; return GEMM_ERR_INVALID_ARG;
+    }
     if (dout != GEMM_F16 && dout != GEMM_BF16 && dout != GEMM_F32) { *err = "dtype_out must be F16, BF16 or F32"; return GEMM_ERR_INVALID_ARG; }
     if ((la != GEMM_ROW && la != GEMM_COL) || (lb != GEMM_ROW && lb != GEMM_COL)) { *err = "layout must be GEMM_ROW or GEMM_COL"; return GEMM_ERR_INVALID_ARG; }
+    const int in_bytes = elt_bytes(din);
+    if (is_f8(din) && (la != GEMM_ROW || lb != GEMM_COL)) {
+        *err = "8-bit inputs need K-major operands (layoutA GEMM_ROW, layoutB GEMM_COL)"; return GEMM_ERR_UNSUPPORTED;
+    }
     const int64_t a_inner = la == GEMM_ROW ? K : M;
     const int64_t b_inner = lb == GEMM_ROW ? N : K;
     if (lda < std::max<int64_t>(1, a_inner)) { *err = "lda too small"; return GEMM_ERR_INVALID_ARG; }
@@ -321,6 +332,9 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
         *err = b_q4 ? "this config does not take Q4_0 weights" : "this config only takes Q4_0 weights";
         return GEMM_ERR_UNSUPPORTED;
     }
+    if (config >= 0 && kConfigs[config].in_bytes != in_bytes) {
+        *err = "this config is built for another input width"; return GEMM_ERR_UNSUPPORTED;
+    }
     if (stream_k < -1 || stream_k > 1) { *err = "stream_k must be -1, 0 or 1"; return GEMM_ERR_INVALID_ARG; }
     if (M == 0 || N == 0) { out->kernels = 0; return GEMM_OK; }
     if (K == 0) { out->kernels = 1; return GEMM_OK; }
@@ -336,7 +350,7 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
         double best_us = 1e300;
         for (int c = 0; c < kNumConfigs; ++c) {
             const int s = slots_of(c);
-            if (s <= 0 || kConfigs[c].b_q4 != b_q4) continue;
+            if (s <= 0 || kConfigs[c].b_q4 != b_q4 || kConfigs[c].in_bytes != in_bytes) continue;
             const Schedule sc = schedule(kConfigs[c], kConfigEfficiency[c], M, N, K, s, stream_k, out_bytes, beta);
             if (sc.est_us < best_us * (1.0 - 1e-9)) { best_us = sc.est_us; best = c; }
         }
@@ -356,16 +370,25 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     out->tiles_n = (int)((N + out->block_n - 1) / out->block_n);
     out->clusters = sc.clusters;
     out->raster_group = std::min(out->tiles_m, 8);
-    out->tma_store = (!c_trans && (ldc * out_bytes) % 16 == 0) ? 1 : 0;
+    // TMA stores move 128-byte rows: each epilogue warp must drain whole ones (a 64-wide tile with
+    // 16-bit output does not: its eight warps take 32 columns each).
+    const int warp_cols = d.block_n / (d.b_q4 ? 1 : 2);
+    out->tma_store = (!c_trans && (ldc * out_bytes) % 16 == 0 && warp_cols * out_bytes >= 128) ? 1 : 0;
     out->transposed = c_trans;
-    out->repack_a = (lda * 2) % 16 != 0;
     // Q4_0 rows are read with 4-byte loads: a pitch that is not a multiple of 4 bytes is repacked
     // (as 16-bit units) to a 16-byte pitch.
-    out->repack_b = b_q4 ? (ldb % 4 != 0) : (ldb * 2) % 16 != 0;
+    out->repack_b = b_q4 ? (ldb % 4 != 0) : (ldb * in_bytes) % 16 != 0;
+    out->repack_a = (lda * in_bytes) % 16 != 0;
+    // The repack moves 16-bit units: an 8-bit operand needs an even pitch and an even row.
+    if (is_f8(din) && ((out->repack_a && (lda % 2 || a_inner % 2)) || (out->repack_b && (ldb % 2 || b_inner % 2)))) {
+        *err = "8-bit operands with an odd pitch or odd K whose pitch is not a multiple of 16 bytes";
+        return GEMM_ERR_UNSUPPORTED;
+    }
+    const int64_t unit = 16 / in_bytes;      // elements per 16 bytes
     int64_t ws = 0;
-    if (out->repack_a) ws += round_up((la == GEMM_ROW ? M : K) * round_up(a_inner, 8) * 2, 256);
+    if (out->repack_a) ws += round_up((la == GEMM_ROW ? M : K) * round_up(a_inner, unit) * in_bytes, 256);
     if (out->repack_b && b_q4) ws += round_up(N * round_up(K / 32 * 9, 8) * 2, 256);
-    else if (out->repack_b) ws += round_up((lb == GEMM_ROW ? K : N) * round_up(b_inner, 8) * 2, 256);
+    else if (out->repack_b) ws += round_up((lb == GEMM_ROW ? K : N) * round_up(b_inner, unit) * in_bytes, 256);
     if (sc.stream_k) {
         out->stream_k = 1;
         out->dp_tiles = sc.dp_tiles;
@@ -379,7 +402,8 @@ gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
 uint32_t make_idesc(int din, int a_mn, int b_mn, int mma_m, int mma_n) {
     // tcgen05 instruction descriptor, kind::f16: D f32 (bits 4-5 = 1); A/B format 0 f16, 1 bf16
     // (bits 7-9, 10-12); A/B major 0 K, 1 MN (bits 15, 16); N >> 3 (bits 17-22); M >> 4 (24-28).
-    const uint32_t fmt = din == GEMM_BF16 ? 1u : 0u;
+    // kind::f16: 0 f16, 1 bf16; kind::f8f6f4: 0 E4M3, 1 E5M2 (same fields)
+    const uint32_t fmt = (din == GEMM_BF16 || din == GEMM_E5M2) ? 1u : 0u;
     return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
            ((uint32_t)(mma_n >> 3) << 17) | ((uint32_t)(mma_m >> 4) << 24);
 }
@@ -427,14 +451,17 @@ struct LaunchArgs {
 gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char** what, cudaError_t* cuda_err) {
     const gemm_plan_t& plan = *a.plan;
     const ConfigDesc* d = config_desc(plan.config);
-    const CUtensorMapDataType tin =
-        a.din == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType tin = is_f8(a.din) ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                    : a.din == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint64_t ib = (uint64_t)elt_bytes(a.din);
+    const uint32_t ce = (uint32_t)(128 / ib);     // K elements of one 128-byte swizzle span
     // B columns one TMA box covers: a CTA's share of one MMA's N, split once more between the
     // pairs of a multicast cluster.
     const int mma_n = std::min(d->block_n, 256);
     const uint32_t b_box_n = (uint32_t)(mma_n / d->cta_group / d->pairs);
     const uint32_t bk = (uint32_t)d->block_k;
-    const uint32_t kchunks = bk / 64;
+    const uint32_t kchunks = bk / ce;
     const uint64_t M = (uint64_t)a.M, N = (uint64_t)a.N, K = (uint64_t)a.K;
     CUtensorMap ta, tb, tc;
     std::memset(&tc, 0, sizeof(tc));
@@ -445,11 +472,11 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
     *what = "tensor map of A";
     gemm_status_t st = GEMM_ERR_CUDA;
     if (a.la == GEMM_ROW) {  // K-major
-        if (allow_3d && K % 64 == 0) {
-            st = tmap(tmap3d(a.A, tin, 64, M, K / 64, (uint64_t)a.lda * 2, 128, 64, 128, kchunks), &ta);
+        if (allow_3d && K % ce == 0) {
+            st = tmap(tmap3d(a.A, tin, ce, M, K / ce, (uint64_t)a.lda * ib, 128, ce, 128, kchunks), &ta);
             a_3d = st == GEMM_OK;
         }
-        if (!a_3d) st = tmap(tmap2d(a.A, tin, K, M, (uint64_t)a.lda * 2, 64, 128), &ta);
+        if (!a_3d) st = tmap(tmap2d(a.A, tin, K, M, (uint64_t)a.lda * ib, ce, 128), &ta);
     } else {                 // M-major
         if (allow_3d && M % 64 == 0) {
             st = tmap(tmap3d(a.A, tin, 64, K, M / 64, (uint64_t)a.lda * 2, 128, 64, bk, 2), &ta);
@@ -470,11 +497,11 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
         }
         if (!b_3d) st = tmap(tmap2d(a.B, tin, N, K, (uint64_t)a.ldb * 2, 64, bk), &tb);
     } else {                 // K-major
-        if (allow_3d && d->pairs == 1 && d->block_n <= 256 && K % 64 == 0) {
-            st = tmap(tmap3d(a.B, tin, 64, N, K / 64, (uint64_t)a.ldb * 2, 128, 64, b_box_n, kchunks), &tb);
+        if (allow_3d && d->pairs == 1 && d->block_n <= 256 && K % ce == 0) {
+            st = tmap(tmap3d(a.B, tin, ce, N, K / ce, (uint64_t)a.ldb * ib, 128, ce, b_box_n, kchunks), &tb);
             b_3d = st == GEMM_OK;
         }
-        if (!b_3d) st = tmap(tmap2d(a.B, tin, K, N, (uint64_t)a.ldb * 2, 64, b_box_n), &tb);
+        if (!b_3d) st = tmap(tmap2d(a.B, tin, K, N, (uint64_t)a.ldb * ib, ce, b_box_n), &tb);
     }
     if (st != GEMM_OK) return st;
     const int eb = elt_bytes(a.dout);
@@ -545,17 +572,20 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
 // launch.  Updates the operand pointers and leading dimensions; counts launches.
 cudaError_t repack_operands(const gemm_plan_t& plan, int64_t M, int64_t N, int64_t K, int la, int lb, void* ws,
                             const void** A, int64_t* lda, const void** B, int64_t* ldb, int num_sms,
-                            cudaStream_t s, int64_t* launches, const char** what, int b_q4 = 0) {
+                            cudaStream_t s, int64_t* launches, const char** what, int b_q4 = 0,
+                            int in_bytes = 2) {
     char* w = static_cast<char*>(ws);
     RepackJobs jobs{};
+    // 8-bit operands (in_bytes 1) move as pairs: their pitch and row length are even (checked by the plan).
+    const int64_t pair = in_bytes == 1 ? 2 : 1;
     if (plan.repack_a) {
         const int64_t rows = la == GEMM_ROW ? M : K;
-        const int64_t cols = la == GEMM_ROW ? K : M;
+        const int64_t cols = (la == GEMM_ROW ? K : M) / pair;
         const int64_t ld = round_up(cols, 8);
-        jobs.job[jobs.n++] = RepackJob{static_cast<const uint16_t*>(*A), *lda, reinterpret_cast<uint16_t*>(w), ld,
-                                       rows, cols};
+        jobs.job[jobs.n++] = RepackJob{static_cast<const uint16_t*>(*A), *lda / pair, reinterpret_cast<uint16_t*>(w),
+                                       ld, rows, cols};
         *A = w;
-        *lda = ld;
+        *lda = ld * pair;
         w += round_up(rows * ld * 2, 256);
     }
     if (plan.repack_b && b_q4) {   // Q4_0 rows (ldb in bytes, even) moved as 16-bit units
@@ -567,12 +597,12 @@ cudaError_t repack_operands(const gemm_plan_t& plan, int64_t M, int64_t N, int64
         *ldb = ld * 2;
     } else if (plan.repack_b) {
         const int64_t rows = lb == GEMM_ROW ? K : N;
-        const int64_t cols = lb == GEMM_ROW ? N : K;
+        const int64_t cols = (lb == GEMM_ROW ? N : K) / pair;
         const int64_t ld = round_up(cols, 8);
-        jobs.job[jobs.n++] = RepackJob{static_cast<const uint16_t*>(*B), *ldb, reinterpret_cast<uint16_t*>(w), ld,
-                                       rows, cols};
+        jobs.job[jobs.n++] = RepackJob{static_cast<const uint16_t*>(*B), *ldb / pair, reinterpret_cast<uint16_t*>(w),
+                                       ld, rows, cols};
         *B = w;
-        *ldb = ld;
+        *ldb = ld * pair;
     }
     if (jobs.n == 0) return cudaSuccess;
     *what = "repack of the operands";
@@ -651,6 +681,9 @@ const void* config_kernel(int id, int out) {
         case 7: return cfg7_kernel(out);
         case 8: return cfg8_kernel(out);
         case 9: return cfg9_kernel(out);
+        case 10: return cfg10_kernel(out);
+        case 11: return cfg11_kernel(out);
+        case 12: return cfg12_kernel(out);
         default: return nullptr;
     }
 }
@@ -682,6 +715,9 @@ cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, c
         case 7: return cfg7_launch(out, lc, a, b, c, p);
         case 8: return cfg8_launch(out, lc, a, b, c, p);
         case 9: return cfg9_launch(out, lc, a, b, c, p);
+        case 10: return cfg10_launch(out, lc, a, b, c, p);
+        case 11: return cfg11_launch(out, lc, a, b, c, p);
+        case 12: return cfg12_launch(out, lc, a, b, c, p);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -733,6 +769,7 @@ gemm_status_t gemm_config_info(int id, gemm_config_info_t* out) {
     out->threads = d->threads;
     out->pairs = d->pairs;
     out->b_q4_0 = d->b_q4;
+    out->in_bytes = d->in_bytes;
     return GEMM_OK;
 }
 
@@ -907,7 +944,7 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
                                "workspace allocation");
             if (st != GEMM_OK) return st;
             cudaError_t e = repack_operands(plan, q.M, q.N, K, q.la, q.lb, h->ws, &a_ptr, &lda_eff, &b_ptr, &ldb_eff,
-                                            h->dev.num_sms, s, &h->launches, &what, b_q4);
+                                            h->dev.num_sms, s, &h->launches, &what, b_q4, elt_bytes(dtype_in));
             if (e != cudaSuccess) return cuda_fail(h, what, e);
         }
         if (plan.stream_k) {
@@ -1067,7 +1104,7 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     int64_t lda_eff = lda, ldb_eff = ldb, launches = 0;
     const char* what = "";
     if (repack_operands(plan, M, N, K, layoutA, layoutB, nd.scratch, &a_ptr, &lda_eff, &b_ptr, &ldb_eff,
-                        nd.info.num_sms, s, &launches, &what) != cudaSuccess)
+                        nd.info.num_sms, s, &launches, &what, 0, elt_bytes(dtype_in)) != cudaSuccess)
         return GEMM_ERR_CUDA;
     LaunchArgs la{&plan, M, N, K, a_ptr, lda_eff, b_ptr, ldb_eff, C, ldc, dtype_in, dtype_out, layoutA, layoutB,
                   alpha, beta, bias, nd.status, 2000ull * 1000000ull, -1, 0, nullptr, nullptr, 0, s, false};

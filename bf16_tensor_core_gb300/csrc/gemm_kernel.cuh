@@ -129,14 +129,18 @@ struct UnitIter {
     }
 };
 
-template <int kCtaGroup, int kBN, int kStages, int kBKc = 64, bool kQ4 = false>
+template <int kCtaGroup, int kBN, int kStages, int kBKc = 64, bool kQ4 = false, int kElt = 2>
 struct TileConfig {
     static constexpr int kBM = 128;                    // rows per CTA (TMEM lanes)
-    static constexpr int kBK = kBKc;                   // K per stage: 64 or 128
-    static constexpr int kKChunks = kBK / 64;          // 64-wide K chunks (one 128-byte swizzle span each)
+    static constexpr int kBK = kBKc;                   // K per stage
+    static constexpr int kEltBytes = kElt;             // 2: f16 / bf16 inputs, 1: 8-bit floats
+    static constexpr int kKChunkElems = 128 / kElt;    // K elements of one 128-byte swizzle span
+    static constexpr int kKChunks = kBK / kKChunkElems;   // swizzle-span-wide K chunks per stage
+    static constexpr int kKPerMma = 32 / kElt;         // K of one tcgen05.mma: 16 (kind::f16), 32 (kind::f8f6f4)
+    static constexpr int kMmasPerStage = kBK / kKPerMma;
     static constexpr int kBNC = kBN / kCtaGroup;       // B columns each CTA loads
-    static constexpr int kABytes = kBM * kBK * 2;      // 16 or 32 KB
-    static constexpr int kBBytes = kBNC * kBK * 2;
+    static constexpr int kABytes = kBM * kBK * kElt;   // 16 or 32 KB
+    static constexpr int kBBytes = kBNC * kBK * kElt;
     static constexpr int kAChunkBytes = kBM * 128;     // one 64-wide K chunk of a K-major A tile
     static constexpr int kBChunkBytes = kBNC * 128;    // one 64-wide K chunk of a K-major B tile
     static constexpr int kSlabBytes = kBK * 128;       // one 64-wide MN slab of an MN-major tile
@@ -160,7 +164,8 @@ struct TileConfig {
                                      : (kAccBufs * kBN <= 128) ? 128 : (kAccBufs * kBN <= 256) ? 256 : 512;
     static_assert(kBN % 64 == 0 && kBN <= 512, "BN must be a multiple of 64, at most 512");
     static_assert(kBN <= 256 || kBN % 256 == 0, "BN above 256 must be a multiple of 256");
-    static_assert(kBK == 64 || kBK == 128, "BK must be 64 or 128");
+    static_assert(kBK * kElt == 128 || kBK * kElt == 256, "a stage is one or two 128-byte swizzle spans of K");
+    static_assert(kElt == 2 || !kQ4, "Q4_0 weights dequantise to f16");
     static_assert(kHalfCols % 64 == 0, "each CTA loads whole 64-column B slabs");
     static_assert(kSmemBytes <= 232448 - 512, "shared memory budget");
     static_assert(!kQ4 || (kBNC == 128 && kBK == 128 && kNHalves == 1),
@@ -243,8 +248,9 @@ __device__ __forceinline__ void epilogue_math_cin(const KernelParams& p, const u
     }
 }
 
-// v[0..31] = alpha * acc + beta * C_in + bias for columns col0 .. col0+31 of `row`.
-template <int kOut>
+// v[0..31] = alpha * acc + beta * C_in + bias for columns col0 .. col0+31 of `row` (kTrans: of the
+// transposed product, whose element (row, col) is C[col * ldc + row] and whose bias follows `row`).
+template <int kOut, bool kTrans = false>
 __device__ __forceinline__ void epilogue_math(const KernelParams& p, const uint32_t (&acc)[32], float (&v)[32],
                                               int row, int col0) {
 #pragma unroll
@@ -253,7 +259,7 @@ __device__ __forceinline__ void epilogue_math(const KernelParams& p, const uint3
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= p.alpha;
     }
-    if (p.c_trans) {
+    if constexpr (kTrans) {
         if (p.beta != 0.0f && row < p.M) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -298,10 +304,10 @@ __device__ __forceinline__ void epilogue_math(const KernelParams& p, const uint3
 }
 
 // Masked direct stores of 32 values of one row.
-template <int kOut>
+template <int kOut, bool kTrans = false>
 __device__ __forceinline__ void store_row_direct(const KernelParams& p, const float (&v)[32], int row, int col0) {
     if (row >= p.M) return;
-    if (p.c_trans) {   // column `row` of C: for each j the lanes of a warp write consecutive addresses
+    if constexpr (kTrans) {   // column `row` of C: for each j the lanes of a warp write consecutive addresses
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             if (col0 + i < p.N) {
@@ -433,7 +439,7 @@ __device__ __forceinline__ bool head_fixup(uint32_t tbase, int lane, const float
 //   With beta != 0 on the TMA path, each box of C_in is first TMA-loaded into the warp's staging
 //   buffer (completing on cin_bar; *cin_uses counts this warp's loads for the barrier parity), read
 //   back row per lane, and the result overwrites it in place before the TMA store.
-template <int kOut, int kCols>
+template <int kOut, int kCols, bool kTrans = false>
 __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUtensorMap* tmC, uint32_t tbase,
                                               int row0, int col_base, int lane, uint32_t stage_buf,
                                               float* out_part, uint32_t cin_bar, uint32_t* cin_uses,
@@ -454,9 +460,11 @@ __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUten
         }
         return true;
     }
-    if (p.use_tma_store) {
-        // A chunk is one 128-byte line per row: 64 columns of a 16-bit type, 32 of f32.
-        constexpr int kChunk = (kOut == OUT_F32) ? 32 : 64;
+    // A chunk is one 128-byte line per row: 64 columns of a 16-bit type, 32 of f32.  A warp whose
+    // columns do not fill whole chunks (a 64-wide tile with 16-bit output) uses direct stores.
+    constexpr int kChunk = (kOut == OUT_F32) ? 32 : 64;
+    constexpr bool kWholeBoxes = kCols % kChunk == 0;
+    if (kWholeBoxes && !kTrans && p.use_tma_store) {
         const bool warp_rows_in = row0 < p.M;
         const uint32_t row_addr = stage_buf + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll 1
@@ -543,8 +551,8 @@ __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUten
             tmem_wait_ld();
             if (col0 >= p.N) continue;
             float v[32];
-            epilogue_math<kOut>(p, acc, v, row, col0);
-            store_row_direct<kOut>(p, v, row, col0);
+            epilogue_math<kOut, kTrans>(p, acc, v, row, col0);
+            store_row_direct<kOut, kTrans>(p, v, row, col0);
         }
     }
     return true;
@@ -711,11 +719,12 @@ struct StageWalk {
 // matching CTA of the other pair: the cluster reads B from L2 once for 512 output rows.
 // kQ4: B is Q4_0-quantised; dequantisation warps (after the epilogue warps) write each stage's
 // B tile into shared memory instead of the producer's TMA copies.
-template <int kCtaGroup, int kPairs, int kBN, int kStages, int kBK, int kOut, bool kQ4 = false>
-__global__ void __launch_bounds__(TileConfig<kCtaGroup, kBN, kStages, kBK, kQ4>::kThreads, 1)
+// kElt == 1: 8-bit float operands (E4M3 / E5M2), both K-major, multiplied by kind::f8f6f4 MMAs.
+template <int kCtaGroup, int kPairs, int kBN, int kStages, int kBK, int kOut, bool kQ4 = false, int kElt = 2>
+__global__ void __launch_bounds__(TileConfig<kCtaGroup, kBN, kStages, kBK, kQ4, kElt>::kThreads, kQ4 ? 1 : 0)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
-    using Cfg = TileConfig<kCtaGroup, kBN, kStages, kBK, kQ4>;
+    using Cfg = TileConfig<kCtaGroup, kBN, kStages, kBK, kQ4, kElt>;
     static_assert(!kQ4 || kPairs == 1, "Q4_0 B is built for one 2-SM pair per cluster");
     static_assert(kPairs == 1 || kCtaGroup == 2, "pairs of CTAs need cta_group::2");
     static_assert(kPairs == 1 || Cfg::kNHalves == 1, "B multicast is built for one MMA per K step");
@@ -819,8 +828,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                 load3(sa, &tmA, 0, m0, kt * Cfg::kKChunks);   // box {64, 128 M, K chunks}
                             } else {
 #pragma unroll
-                                for (int c = 0; c < Cfg::kKChunks; ++c)  // box {64 K, 128 M} per K chunk
-                                    load(sa + static_cast<uint32_t>(c * Cfg::kAChunkBytes), &tmA, k0 + 64 * c, m0);
+                                for (int c = 0; c < Cfg::kKChunks; ++c)  // box {one swizzle span of K, 128 M} per chunk
+                                    load(sa + static_cast<uint32_t>(c * Cfg::kAChunkBytes), &tmA, k0 + Cfg::kKChunkElems * c, m0);
                             }
                         } else {
                             if (p.a_3d) {
@@ -843,9 +852,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                         load3(sb, &tmB, 0, nh, kt * Cfg::kKChunks);
                                     } else {
 #pragma unroll
-                                        for (int c = 0; c < Cfg::kKChunks; ++c)  // box {64 K, kHalfCols N} per K chunk
+                                        for (int c = 0; c < Cfg::kKChunks; ++c)  // box {one span of K, kHalfCols N} per chunk
                                             load(sb + static_cast<uint32_t>(c * Cfg::kBChunkBytes + h * Cfg::kHalfCols * 128),
-                                                 &tmB, k0 + 64 * c, nh);
+                                                 &tmB, k0 + Cfg::kKChunkElems * c, nh);
                                     }
                                 } else {
                                     const uint32_t dh = sb + static_cast<uint32_t>(h * (Cfg::kHalfCols / 64) * Cfg::kSlabBytes);
@@ -870,7 +879,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                                 for (int c = 0; c < Cfg::kKChunks; ++c)
                                     tma_load_2d_pair_mc(db + static_cast<uint32_t>(c * Cfg::kBChunkBytes), &tmB,
-                                                        k0 + 64 * c, nb0, full_bar, mc);
+                                                        k0 + Cfg::kKChunkElems * c, nb0, full_bar, mc);
                             } else {
                                 // slabs [pair * kPart / 64, +kPart / 64): box {64 N, BK K}
                                 const uint32_t db = sb + pair * static_cast<uint32_t>((kPart / 64) * Cfg::kSlabBytes);
@@ -895,9 +904,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // bytes apart (SBO); a K=16 step is +2048 bytes.
             const uint32_t a_lbo = p.a_mn ? static_cast<uint32_t>(Cfg::kSlabBytes) : 16u;
             const uint32_t b_lbo = p.b_mn ? static_cast<uint32_t>(Cfg::kSlabBytes) : 16u;
-            uint64_t a_koff[Cfg::kBK / 16], b_koff[Cfg::kBK / 16], b_hoff[Cfg::kNHalves];
+            // (An MMA covers 32 bytes of K in either input width, so 4 MMAs span one 128-byte chunk.)
+            uint64_t a_koff[Cfg::kMmasPerStage], b_koff[Cfg::kMmasPerStage], b_hoff[Cfg::kNHalves];
 #pragma unroll
-            for (int k = 0; k < Cfg::kBK / 16; ++k) {
+            for (int k = 0; k < Cfg::kMmasPerStage; ++k) {
                 a_koff[k] = (p.a_mn ? 2048u * k : static_cast<uint32_t>((k >> 2) * Cfg::kAChunkBytes + (k & 3) * 32)) >> 4;
                 b_koff[k] = (p.b_mn ? 2048u * k : static_cast<uint32_t>((k >> 2) * Cfg::kBChunkBytes + (k & 3) * 32)) >> 4;
             }
@@ -935,11 +945,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const uint64_t ad = a_desc0 + stage * stage_step;
                     const uint64_t bd = b_desc0 + stage * stage_step;
 #pragma unroll
-                    for (int k = 0; k < Cfg::kBK / 16; ++k)
+                    for (int k = 0; k < Cfg::kMmasPerStage; ++k)
 #pragma unroll
-                        for (int h = 0; h < Cfg::kNHalves; ++h)
-                            mma_f16<kCtaGroup>(d_tmem + static_cast<uint32_t>(h * Cfg::kMmaN), ad + a_koff[k],
-                                               bd + b_hoff[h] + b_koff[k], p.idesc, (kt > u.k0 || k > 0) ? 1u : 0u);
+                        for (int h = 0; h < Cfg::kNHalves; ++h) {
+                            const uint32_t dt = d_tmem + static_cast<uint32_t>(h * Cfg::kMmaN);
+                            const uint32_t accum = (kt > u.k0 || k > 0) ? 1u : 0u;
+                            if constexpr (kElt == 1) mma_f8<kCtaGroup>(dt, ad + a_koff[k], bd + b_hoff[h] + b_koff[k], p.idesc, accum);
+                            else mma_f16<kCtaGroup>(dt, ad + a_koff[k], bd + b_hoff[h] + b_koff[k], p.idesc, accum);
+                        }
                     mma_commit<kCtaGroup>(smem_u32(&bar_empty[stage]), all_mask);  // slot free in every CTA it feeds
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
@@ -1009,8 +1022,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     break;
                 }
             }
-            if (!epilogue_tile<kOut, Cfg::kEpiCols>(p, &tmC, tbase, row0, nb * kBN + pcol0, lane, stage_buf, out_part,
-                                                    smem_u32(&bar_cin[ew]), &cin_uses, abort_flag)) {
+            bool drained;
+            if (!kQ4 && p.c_trans)     // (the transposed product never takes Q4_0 weights)
+                drained = epilogue_tile<kOut, Cfg::kEpiCols, !kQ4>(p, &tmC, tbase, row0, nb * kBN + pcol0, lane, stage_buf,
+                                                                   out_part, smem_u32(&bar_cin[ew]), &cin_uses, abort_flag);
+            else
+                drained = epilogue_tile<kOut, Cfg::kEpiCols>(p, &tmC, tbase, row0, nb * kBN + pcol0, lane, stage_buf,
+                                                             out_part, smem_u32(&bar_cin[ew]), &cin_uses, abort_flag);
+            if (!drained) {
                 if (lane == 0 && !*abort_flag)
                     report_error<kClusterCtas>(p, ROLE_EPILOGUE, u.tile, 400 + quarter, abort_flag);
                 break;

@@ -18,9 +18,10 @@ struct ConfigDesc {
     int smem_bytes;
     int threads;
     int b_q4;         // 1: B is Q4_0-quantised and dequantised in shared memory by the kernel
+    int in_bytes;     // operand element size: 2 (f16 / bf16) or 1 (8-bit floats)
 };
 
-constexpr int kNumConfigs = 10;
+constexpr int kNumConfigs = 13;
 constexpr int kNumOut = 3;  // OUT_F16, OUT_BF16, OUT_F32
 
 // Static description of config `id` (nullptr if out of range).
@@ -66,6 +67,16 @@ cudaError_t cfg8_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap
 const void* cfg9_kernel(int out);
 cudaError_t cfg9_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& c, const KernelParams& p);
+
+const void* cfg10_kernel(int out);
+cudaError_t cfg10_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
+                         const CUtensorMap& c, const KernelParams& p);
+const void* cfg11_kernel(int out);
+cudaError_t cfg11_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
+                         const CUtensorMap& c, const KernelParams& p);
+const void* cfg12_kernel(int out);
+cudaError_t cfg12_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
+                         const CUtensorMap& c, const KernelParams& p);
 
 // Auxiliary kernels (gemm_aux.cu).
 struct RepackJob {

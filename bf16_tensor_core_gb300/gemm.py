@@ -15,12 +15,12 @@ _PKG = Path(__file__).resolve().parent
 LIB_PATH = _PKG / "libgemm_gb300.so"
 HEADER = _PKG.parent / "include" / "gemm.h"
 
-GEMM_F16, GEMM_BF16, GEMM_F32 = 0, 1, 2
+GEMM_F16, GEMM_BF16, GEMM_F32, GEMM_E4M3, GEMM_E5M2 = 0, 1, 2, 3, 4
 GEMM_ROW, GEMM_COL = 0, 1
 GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ALIGNMENT = 0, 1, 2, 3
 GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, GEMM_ERR_OOM = 4, 5, 6
 
-DTYPE_CODES = {"f16": GEMM_F16, "bf16": GEMM_BF16, "f32": GEMM_F32}
+DTYPE_CODES = {"f16": GEMM_F16, "bf16": GEMM_BF16, "f32": GEMM_F32, "e4m3": GEMM_E4M3, "e5m2": GEMM_E5M2}
 LAYOUT_CODES = {"row": GEMM_ROW, "col": GEMM_COL}
 
 
@@ -34,7 +34,7 @@ class gemm_config_info_t(ctypes.Structure):
     _fields_ = [("id", ctypes.c_int), ("cta_group", ctypes.c_int), ("block_m", ctypes.c_int),
                 ("block_n", ctypes.c_int), ("block_k", ctypes.c_int), ("stages", ctypes.c_int),
                 ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int), ("pairs", ctypes.c_int),
-                ("b_q4_0", ctypes.c_int)]
+                ("b_q4_0", ctypes.c_int), ("in_bytes", ctypes.c_int)]
 
 
 class gemm_plan_t(ctypes.Structure):
@@ -190,7 +190,8 @@ def gemm_dequant_q4_0(Bq, ldbq, N, K, out, ldo, stream) -> int:
 # ------------------------------------------------------------------ torch convenience wrapper
 def _torch_code(t) -> int:
     import torch
-    return {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16, torch.float32: GEMM_F32}[t.dtype]
+    return {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16, torch.float32: GEMM_F32,
+            torch.float8_e4m3fn: GEMM_E4M3, torch.float8_e5m2: GEMM_E5M2}[t.dtype]
 
 
 def _ld(t) -> int:

@@ -22,7 +22,8 @@ from dataclasses import dataclass, field, replace
 
 import torch
 
-DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+          "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 
 
 @dataclass(frozen=True)
@@ -70,6 +71,10 @@ WORKLOADS = {
     5: Workload("gemm_8192_f16_f16", 8192, 8192, 8192, "f16", "f16", "row", "row", 1.0, 0.0,
                 ("normal_sqrtk",), ("normal_sqrtk",), None, None, _seed(5),
                 "8192^3, f16 in N(0,1)/sqrt(K), f16 out"),
+    9: Workload("gemm_4096_e4m3_f16", 4096, 4096, 4096, "e4m3", "f16", "row", "col", 1.0, 0.0,
+                ("normal", 1.0), ("normal", 1.0), None, None, _seed(9),
+                "4096^3 with E4M3 inputs drawn N(0,1) and rounded to E4M3, K-major A and B (B stored N x K), "
+                "f16 out"),
     7: Workload("decode_1x4096x4096_f16", 1, 4096, 4096, "f16", "f16", "row", "col", 1.0, 0.0,
                 ("normal", 1.0), ("normal", 0.02), None, None, _seed(7),
                 "one token through a 4096 x 4096 f16 weight stored N x K (HBM-bound, intensity ~1 FLOP/B)"),

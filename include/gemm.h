@@ -24,7 +24,12 @@
  *            by alpha:  C_ij = alpha * S_ij + beta * C_ij + bias_j.
  *   beta == 0: C is not read (NaN in C does not propagate).
  *   K == 0:   C = beta * C + bias.   M == 0 or N == 0: no-op.
- *   dtype_in in {GEMM_F16, GEMM_BF16} (A and B share it);
+ *   dtype_in in {GEMM_F16, GEMM_BF16} (A and B share it), or the 8-bit floats
+ *   GEMM_E4M3 / GEMM_E5M2 (OCP FP8 formats; the matrix-multiplication page's
+ *   closing caveat names FP8 tensor cores).  8-bit inputs are multiplied by
+ *   kind::f8f6f4 MMAs with f32 accumulation and need K-major operands:
+ *   layoutA GEMM_ROW and layoutB GEMM_COL (else GEMM_ERR_UNSUPPORTED); an odd
+ *   byte pitch or odd K with an unaligned pitch is GEMM_ERR_UNSUPPORTED too.
  *   dtype_out in {GEMM_F32, GEMM_F16, GEMM_BF16}; the output is rounded to
  *   nearest-even from the f32 epilogue value.
  *
@@ -64,7 +69,7 @@ extern "C" {
 
 typedef struct gemm_ctx* gemm_handle_t; /* opaque, owned by the library */
 
-typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_F32 = 2 } gemm_dtype_t;
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_F32 = 2, GEMM_E4M3 = 3, GEMM_E5M2 = 4 } gemm_dtype_t;
 typedef enum { GEMM_ROW = 0, GEMM_COL = 1 } gemm_layout_t;
 
 typedef enum {
@@ -105,6 +110,7 @@ typedef struct {
     int threads;       /* threads per CTA                                                         */
     int pairs;         /* 2-SM pairs per cluster; 2: the pairs share B by TMA multicast           */
     int b_q4_0;        /* 1: B is Q4_0 weights dequantised in shared memory (gemm_run_q4_0 only)  */
+    int in_bytes;      /* operand element size: 2 (f16 / bf16) or 1 (E4M3 / E5M2)                */
 } gemm_config_info_t;
 
 /* What gemm_run would do for a problem (pure host computation, no device needed). */

@@ -8,7 +8,8 @@ import oracle
 from bf16_tensor_core_gb300 import gemm as G
 from bf16_tensor_core_gb300 import workloads as W
 
-OR_CODE = {"f16": oracle.OR_F16, "bf16": oracle.OR_BF16, "f32": oracle.OR_F32}
+OR_CODE = {"f16": oracle.OR_F16, "bf16": oracle.OR_BF16, "f32": oracle.OR_F32, "e4m3": oracle.OR_E4M3,
+           "e5m2": oracle.OR_E5M2}
 OR_LAYOUT = {"row": oracle.OR_ROW, "col": oracle.OR_COL}
 
 
@@ -49,8 +50,8 @@ def compare(w: W.Workload, d: dict, C_out: torch.Tensor, rows=None, cols=None) -
     if cols is not None:
         got = got[:, torch.as_tensor(cols, dtype=torch.long)]
     got = got.to(torch.float64).numpy()
-    maxA = float(d["A"].abs().max()) if w.K > 0 else 0.0
-    maxB = float(d["B"].abs().max()) if w.K > 0 else 0.0
+    maxA = float(d["A"].float().abs().max()) if w.K > 0 else 0.0
+    maxB = float(d["B"].float().abs().max()) if w.K > 0 else 0.0
     cin = None
     if d["Cin"] is not None and w.beta != 0.0:
         cin = d["Cin"][:, : w.N]

@@ -44,21 +44,23 @@ def test_options_default(lib):
 
 def test_config_table(lib):
     n = G.gemm_num_configs()
-    assert n == 10
+    assert n == 13
     seen = set()
     for i in range(n):
         st, c = G.gemm_config_info(i)
         assert st == G.GEMM_OK and c.id == i
-        assert c.block_m == 128 * c.cta_group * c.pairs and c.block_k in (64, 128)
+        assert c.block_m == 128 * c.cta_group * c.pairs and c.block_k in (64, 128, 256)
         assert c.block_n in (64, 128, 256, 512) and c.smem_bytes <= 232448
         assert c.threads == (448 if c.b_q4_0 else 320)        # Q4_0: 8 more dequantisation warps, 4 fewer epilogue
         assert c.pairs == 1 or c.cta_group == 2
-        stage = (128 + c.block_n // c.cta_group) * c.block_k * 2
+        stage = (128 + c.block_n // c.cta_group) * c.block_k * c.in_bytes
+        assert c.block_k * c.in_bytes in (128, 256)                  # one or two 128-byte swizzle spans of K
         assert c.smem_bytes >= c.stages * stage
-        seen.add((c.cta_group, c.pairs, c.block_n, c.block_k, c.b_q4_0))
-    assert seen == {(1, 1, 128, 64, 0), (1, 1, 256, 64, 0), (2, 1, 128, 64, 0), (2, 1, 256, 64, 0),
-                    (2, 2, 256, 64, 0), (2, 1, 256, 128, 0), (2, 2, 256, 128, 0), (2, 1, 512, 64, 0),
-                    (2, 1, 256, 128, 1), (1, 1, 64, 128, 0)}
+        seen.add((c.cta_group, c.pairs, c.block_n, c.block_k, c.b_q4_0, c.in_bytes))
+    assert seen == {(1, 1, 128, 64, 0, 2), (1, 1, 256, 64, 0, 2), (2, 1, 128, 64, 0, 2), (2, 1, 256, 64, 0, 2),
+                    (2, 2, 256, 64, 0, 2), (2, 1, 256, 128, 0, 2), (2, 2, 256, 128, 0, 2), (2, 1, 512, 64, 0, 2),
+                    (2, 1, 256, 128, 1, 2), (1, 1, 64, 128, 0, 2),
+                    (2, 1, 256, 256, 0, 1), (1, 1, 64, 256, 0, 1), (1, 1, 128, 128, 0, 1)}
     assert G.gemm_config_info(n)[0] == G.GEMM_ERR_UNSUPPORTED
 
 
@@ -93,7 +95,7 @@ def plan(M, N, K, lda=None, ldb=None, ldc=None, din=0, dout=2, la=0, lb=0, beta=
     (dict(M=4, N=9, K=8, lb=1, ldb=7), G.GEMM_ERR_INVALID_ARG),  # ldb < K for B stored N x K
     (dict(M=4, N=9, K=8, ldc=8), G.GEMM_ERR_INVALID_ARG),
     (dict(M=2 ** 31, N=4, K=4), G.GEMM_ERR_INVALID_ARG),
-    (dict(M=4, N=4, K=4, config=10), G.GEMM_ERR_UNSUPPORTED),
+    (dict(M=4, N=4, K=4, config=13), G.GEMM_ERR_UNSUPPORTED),
     (dict(M=4, N=4, K=4, sms=0), G.GEMM_ERR_INVALID_ARG),
     (dict(M=4, N=4, K=4), G.GEMM_OK),
 ])
@@ -138,10 +140,27 @@ def test_plan_skinny_products_are_transposed(lib):
     assert st == G.GEMM_ERR_INVALID_ARG
 
 
+def test_plan_8bit_inputs(lib):
+    E4M3, E5M2 = G.GEMM_E4M3, G.GEMM_E5M2
+    st, p = plan(4096, 4096, 4096, din=E4M3, dout=0, lb=1)
+    assert st == G.GEMM_OK and G.gemm_config_info(p.config)[1].in_bytes == 1 and p.block_k == 256
+    st, p = plan(4096, 4096, 4096, din=E5M2, dout=2, lb=1)
+    assert st == G.GEMM_OK and G.gemm_config_info(p.config)[1].in_bytes == 1
+    assert plan(256, 256, 256, din=E4M3, lb=0)[0] == G.GEMM_ERR_UNSUPPORTED      # B must be K-major
+    assert plan(256, 256, 256, din=E4M3, la=1, lb=1)[0] == G.GEMM_ERR_UNSUPPORTED
+    assert plan(256, 256, 256, din=E4M3, lb=1, config=5)[0] == G.GEMM_ERR_UNSUPPORTED   # 16-bit config
+    assert plan(256, 256, 256, din=0, lb=1, config=10)[0] == G.GEMM_ERR_UNSUPPORTED     # 8-bit config
+    st, p = plan(300, 300, 1000, din=E4M3, lb=1, lda=1000, ldb=1000)   # 1000-byte rows: repacked as pairs
+    assert st == G.GEMM_OK and p.repack_a == 1 and p.repack_b == 1
+    assert plan(300, 300, 999, din=E4M3, lb=1, lda=999, ldb=999)[0] == G.GEMM_ERR_UNSUPPORTED  # odd rows
+    st, p = plan(16, 4096, 4096, din=E4M3, lb=1)                       # skinny 8-bit: transposed, K-major
+    assert st == G.GEMM_OK and p.transposed == 1 and G.gemm_config_info(p.config)[1].in_bytes == 1
+
+
 def test_plan_tiles_and_grid(lib):
     for cfg in range(G.gemm_num_configs()):
         st, c = G.gemm_config_info(cfg)
-        if c.b_q4_0:
+        if c.b_q4_0 or c.in_bytes != 2:
             continue
         st, p = plan(4096, 4096, 4096, dout=0, config=cfg)
         assert st == G.GEMM_OK and p.config == cfg
