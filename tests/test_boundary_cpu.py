@@ -167,7 +167,8 @@ def test_plan_tiles_and_grid(lib):
         assert p.tiles_m == 4096 // c.block_m and p.tiles_n == 4096 // c.block_n
         slots = 152 // (c.cta_group * c.pairs)
         assert p.clusters == min(p.tiles_m * p.tiles_n, slots)
-        assert p.tma_store == 1 and p.kernels == 1
+        # f16 output: TMA stores need each epilogue warp to drain whole 128-byte rows (64 columns)
+        assert p.tma_store == (1 if c.block_n // 2 >= 64 else 0) and p.kernels == 1
         assert p.workspace_bytes == p.sk_partial_bytes
     st, p = plan(1000, 3000, 2050, config=1)
     assert (p.tiles_m, p.tiles_n) == (4, 12)           # partial last tiles: 1000 = 3*256 + 232, 3000 = 11*256 + 184
