@@ -203,7 +203,7 @@ class ClockSampler:
 
 def algorithmic_bytes(w) -> int:
     """Least traffic of one product: read A and B once, write C once (and read C_in, bias)."""
-    ein = 2
+    ein = 1 if w.dtype_in in ("e4m3", "e5m2") else 2
     eout = 4 if w.dtype_out == "f32" else 2
     b_bytes = w.N * (w.K // 32) * 18 if w.layoutB == "q4_0" else w.K * w.N * ein
     n = w.M * w.K * ein + b_bytes + w.M * w.N * eout
@@ -447,6 +447,10 @@ def run_ours(args, rank, world, local):
         return
     peaks, src = _peaks()
     peak = float(peaks.get("bf16_tflops", 1900.0))
+    peak_note = "cuBLAS bf16 burst (f16 and bf16 share the dense tensor rate)"
+    if w.dtype_in in ("e4m3", "e5m2"):       # the FP8 rate: the measured 16-bit peak x the nominal 4.5 / 2.25
+        peak *= 2.0
+        peak_note = "cuBLAS bf16 burst x 2 (nominal dense FP8 / bf16 rate 4.5 / 2.25 PFLOP/s)"
     hbm = float(peaks.get("hbm_gbs", 6800.0))
     achieved = w.flops / (ms_per_step / 1e3) / 1e12
     traffic, traffic_src = _traffic(w.name)
@@ -461,13 +465,13 @@ def run_ours(args, rank, world, local):
     else:
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": traffic,
-                "peak_source": f"{src}: cuBLAS bf16 burst (f16 and bf16 share the dense tensor rate)",
+                "peak_source": f"{src}: {peak_note}",
                 "kernel": "gb300::gemm_tc_kernel", "algorithmic_flops_per_launch": w.flops,
                 "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_ms": ms_per_step}
     if traffic is not None:
         roof["traffic_source"] = traffic_src
     if clocks.get("sm_mhz"):
-        clk_peak = 8192.0 * n_sms * clocks["sm_mhz"] * 1e6 / 1e12
+        clk_peak = 8192.0 * n_sms * clocks["sm_mhz"] * 1e6 / 1e12 * (2.0 if w.dtype_in in ("e4m3", "e5m2") else 1.0)
         roof["clock_roofline_tflops"] = clk_peak
         roof["frac_of_clock_roofline"] = achieved / clk_peak
         roof["clock_roofline_note"] = "8192 dense f16 FLOP/clk/SM x SMs x median SM clock in the timed window"
