@@ -286,6 +286,21 @@ Problem transpose(const Problem& q) {
                    q.la == GEMM_ROW ? GEMM_COL : GEMM_ROW};
 }
 
+// Whether the CUDA-core kernel can take a product: a few rows of C, 16-bit operands, A row-major and
+// B stored N x K, both with 16-byte row pitches, K a multiple of 8.
+bool gemv_applies(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int din, int la, int lb, int b_q4) {
+    return !b_q4 && (din == GEMM_F16 || din == GEMM_BF16) && M >= 1 && M <= kGemvMaxM && N >= 1 && K >= 8 &&
+           la == GEMM_ROW && lb == GEMM_COL && K % 8 == 0 && (lda * 2) % 16 == 0 && (ldb * 2) % 16 == 0 &&
+           K < (1LL << 30);
+}
+
+// Whether a call takes the CUDA-core kernel: on request (skinny 2) or automatically.
+bool use_gemv(int skinny, int config, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int din, int la,
+              int lb, int b_q4) {
+    if (skinny == 2) return true;
+    return skinny == -1 && config == -1 && N > 64 && gemv_applies(M, N, K, lda, ldb, din, la, lb, b_q4);
+}
+
 // Whether a call computes the transposed product: only on request (skinny 1), or automatically for
 // a few rows of C against many columns when the config is automatic.
 bool use_transposed(int skinny, int config, int64_t M, int64_t N, int b_q4) {
@@ -787,7 +802,15 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     std::string err;
     gemm_status_t st = plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, slots, config,
                                  stream_k, 0, out, &err);
-    if (st != GEMM_OK || M == 0 || N == 0 || K == 0 || !use_transposed(-1, config, M, N, 0)) return st;
+    if (st != GEMM_OK || M == 0 || N == 0 || K == 0) return st;
+    if (use_gemv(-1, config, M, N, K, lda, ldb, dtype_in, layoutA, layoutB, 0)) {
+        std::memset(out, 0, sizeof(*out));
+        out->config = -1;
+        out->kernels = 1;
+        out->gemv = 1;
+        return GEMM_OK;
+    }
+    if (!use_transposed(-1, config, M, N, 0)) return st;
     const Problem q = transpose(Problem{M, N, K, nullptr, lda, nullptr, ldb, layoutA, layoutB});
     return plan_impl(q.M, q.N, K, q.lda, q.ldb, ldc, dtype_in, dtype_out, q.la, q.lb, beta, slots, config, stream_k, 0,
                      out, &err, 0, 1);
@@ -915,6 +938,26 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
         plan.repack_b = 1;
         plan.workspace_bytes += round_up(N * round_up(K / 32 * 9, 8) * 2, 256);
         plan.kernels = 2;
+    }
+    if (K > 0 && use_gemv(h->opt.skinny, h->opt.config, M, N, K, lda, ldb, dtype_in, layoutA, layoutB, b_q4)) {
+        if (!gemv_applies(M, N, K, lda, ldb, dtype_in, layoutA, layoutB, b_q4) ||
+            (reinterpret_cast<uintptr_t>(B) % 16) != 0)
+            return fail(h, GEMM_ERR_UNSUPPORTED, "the CUDA-core small-M kernel does not take this product");
+        DeviceGuard guard(h->device);
+        if (h->faults & FAULT_LAUNCH) return fail(h, GEMM_ERR_CUDA, "kernel launch: forced failure (GEMM_TEST_FAIL=launch)");
+        GemvParams gp{A, lda * 2, B, ldb * 2, C, ldc, bias, alpha, beta, (int)M, (int)N, (int)K};
+        const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
+        cudaError_t e = launch_gemv(out_kind, dtype_in == GEMM_BF16, gp, h->dev.num_sms, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(h, "small-M kernel launch", e);
+        h->launches += 1;
+        gemm_plan_t gplan{};
+        gplan.config = -1;
+        gplan.kernels = 1;
+        gplan.gemv = 1;
+        h->last_plan = gplan;
+        h->has_plan = true;
+        if (h->opt.sync_check) return gemm_get_device_status(h, stream);
+        return GEMM_OK;
     }
     // The product the kernels compute: C itself, or C^T for a few rows of C against many columns.
     Problem q{M, N, K, A, lda, B, ldb, layoutA, layoutB};

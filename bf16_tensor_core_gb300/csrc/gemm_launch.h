@@ -78,6 +78,21 @@ const void* cfg12_kernel(int out);
 cudaError_t cfg12_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
                          const CUtensorMap& c, const KernelParams& p);
 
+// Few rows of C against weights stored N x K (gemm_gemv.cu): CUDA-core kernel for M <= kGemvMaxM.
+constexpr int kGemvMaxM = 8;
+struct GemvParams {
+    const void* A;           // M x K row-major, 16-bit, 16-byte aligned, row pitch lda_bytes (multiple of 16)
+    long long lda_bytes;
+    const void* W;           // N x K, K contiguous, 16-byte aligned, row pitch ldw_bytes (multiple of 16)
+    long long ldw_bytes;
+    void* C;                 // M x N row-major, ldc elements
+    long long ldc;
+    const void* bias;
+    float alpha, beta;
+    int M, N, K;             // K a multiple of 8
+};
+cudaError_t launch_gemv(int out, bool bf16, const GemvParams& p, int num_sms, cudaStream_t stream);
+
 // Auxiliary kernels (gemm_aux.cu).
 struct RepackJob {
     const uint16_t* src;   // rows x cols elements at pitch lds (2-byte aligned)

@@ -93,9 +93,11 @@ typedef struct {
     int debug_skip_stage; /* TEST ONLY: the producer of cluster 0 never issues this k-stage,
                              so the MMA issuer's bounded wait expires (-1 = off)              */
     int stream_k;         /* tail-wave balancing: -1 automatic, 0 off, 1 whenever possible   */
-    int skinny;           /* computing C^T = op(B)^T op(A)^T (few rows of C become the short
-                             tile side): -1 automatic (M <= 64 < N, with config -1), 0 never,
-                             1 always                                                          */
+    int skinny;           /* products with few rows of C: -1 automatic (config -1 only): the
+                             CUDA-core kernel for M <= 8 with B stored N x K (16-bit, K a
+                             multiple of 8, 16-byte row pitch), else C^T = op(B)^T op(A)^T
+                             for M <= 64 < N; 0 never; 1 always C^T; 2 always the CUDA-core
+                             kernel (GEMM_ERR_UNSUPPORTED where it does not apply)            */
 } gemm_options_t;
 
 /* Description of a kernel configuration. */
@@ -131,6 +133,8 @@ typedef struct {
     int transposed;        /* 1: the kernel computes C^T = op(B)^T op(A)^T; tiles_m, tiles_n,
                               block_m, block_n and repack_a/_b then describe that product
                               (its rows are C's columns) and C is written by direct stores    */
+    int gemv;              /* 1: the CUDA-core kernel for a few rows of C (no tensor cores, no
+                              tiles; config is -1)                                             */
 } gemm_plan_t;
 
 /* Fill *opt with defaults (config -1, timeout 2000 ms, no sync check, automatic raster). */

@@ -123,6 +123,19 @@ def test_q4_0_config_is_not_a_plain_gemm_config(lib):
         assert st == G.GEMM_OK and p.config != 8
 
 
+def test_plan_few_rows_use_the_cuda_core_kernel(lib):
+    # M <= 8, B stored N x K with a 16-byte pitch, K a multiple of 8: the CUDA-core kernel.
+    for M in (1, 5, 8):
+        st, p = plan(M, 4096, 4096, dout=0, lb=1)
+        assert st == G.GEMM_OK and p.gemv == 1 and p.config == -1 and p.kernels == 1
+    assert plan(9, 4096, 4096, dout=0, lb=1)[1].gemv == 0                 # 9 rows: tensor cores
+    assert plan(4, 4096, 4096, dout=0, lb=0)[1].gemv == 0                 # B stored K x N
+    assert plan(4, 4096, 4100, dout=0, lb=1)[1].gemv == 0                 # K not a multiple of 8
+    assert plan(4, 4096, 4096, dout=0, lb=1, ldb=4100)[1].gemv == 0       # pitch not 16-byte aligned
+    assert plan(4, 4096, 4096, din=G.GEMM_E4M3, dout=0, lb=1)[1].gemv == 0   # 8-bit inputs: tensor cores
+    assert plan(4, 4096, 4096, dout=0, lb=1, config=9)[1].gemv == 0       # a forced config
+
+
 def test_plan_skinny_products_are_transposed(lib):
     # A few rows of C against many columns: the kernel computes C^T with C's columns as its rows.
     for M in (1, 16, 64):

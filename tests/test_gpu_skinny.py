@@ -46,7 +46,8 @@ def test_skinny_parity_automatic(i):
     c = dict(CASES[i])
     w = W.problem(c.pop("M"), c.pop("N"), c.pop("K"), seed=300 + i, **c)
     plan, _ = _check(w)
-    assert plan["transposed"] == 1 and plan["tma_store"] == 0
+    # M <= 8 with A row-major and B stored N x K takes the CUDA-core kernel, otherwise C^T
+    assert (plan["transposed"] == 1 and plan["tma_store"] == 0) or plan["gemv"] == 1
 
 
 @pytest.mark.parametrize("i", [1, 3, 5])
@@ -98,10 +99,87 @@ def test_skinny_ldc_wider_than_n_leaves_padding():
     d = W.generate(w)
     dd = device_inputs(d)
     C = torch.full((5, 720), -7.0, dtype=torch.float16, device="cuda")
+    for skinny in (1, 2):                                  # the transposed product and the CUDA-core kernel
+        C.fill_(-7.0)
+        with G.Gemm(0, sync_check=1, skinny=skinny) as g:
+            g.run(dd["A"], dd["B"], C, M=5, N=700, K=256, layoutB="col")
+            assert g.last_plan()["transposed" if skinny == 1 else "gemv"] == 1
+        torch.cuda.synchronize()
+        assert torch.all(C[:, 700:].cpu() == -7.0)
+        rep = compare(w, d, C[:, :700].contiguous())
+        assert rep["passed"], rep
+
+
+# ------------------------------------------------------------------ CUDA-core kernel, M <= 8
+GEMV_CASES = [
+    dict(M=1, N=4096, K=4096, dtype_out="f16"),
+    dict(M=2, N=4097, K=1000, dtype_out="f32", bias=True),                  # N tail (4-row groups), K = 8 * 125
+    dict(M=3, N=300, K=72, dtype_out="bf16", dtype_in="bf16", alpha=0.5, beta=1.0),
+    dict(M=5, N=1000, K=2048, dtype_out="f32", bias=True, alpha=-1.5, beta=0.25),
+    dict(M=8, N=4096, K=4096, dtype_out="f16", bias=True),
+    dict(M=8, N=11008, K=4096, dtype_out="bf16", dtype_in="bf16"),
+    dict(M=7, N=65, K=16384, dtype_out="f32"),                               # long K
+]
+
+
+@pytest.mark.parametrize("i", range(len(GEMV_CASES)))
+def test_small_m_cuda_core_parity(i):
+    _need_gpu()
+    c = dict(GEMV_CASES[i])
+    w = W.problem(c.pop("M"), c.pop("N"), c.pop("K"), layoutB="col", seed=800 + i, **c)
+    plan, _ = _check(w)
+    assert plan["gemv"] == 1
+
+
+def test_small_m_with_a_stored_k_by_m_takes_the_transposed_product():
+    _need_gpu()
+    w = W.problem(5, 1000, 2048, dtype_out="f32", layoutA="col", layoutB="col", bias=True, seed=820)
+    plan, _ = _check(w)
+    assert plan["gemv"] == 0 and plan["transposed"] == 1
+
+
+def test_small_m_padded_pitches():
+    """B rows at a pitch wider than K (16-byte multiple), C with ldc > N: padding never touched."""
+    _need_gpu()
+    M, N, K = 6, 700, 512
+    g0 = torch.Generator().manual_seed(77)
+    A = (torch.rand(M, K, generator=g0, dtype=torch.float64) * 2 - 1).half()
+    Bs = (torch.rand(N, K + 24, generator=g0, dtype=torch.float64) * 2 - 1).half()
+    Bs[:, K:] = float("nan")                                                # must never be read
+    C = torch.full((M, N + 9), -3.0, dtype=torch.float32, device="cuda")
     with G.Gemm(0, sync_check=1) as g:
-        g.run(dd["A"], dd["B"], C, M=5, N=700, K=256, layoutB="col")
-        assert g.last_plan()["transposed"] == 1
+        g.run(A.cuda(), Bs.cuda(), C, M=M, N=N, K=K, layoutB="col")
+        assert g.last_plan()["gemv"] == 1
     torch.cuda.synchronize()
-    assert torch.all(C[:, 700:].cpu() == -7.0)
-    rep = compare(w, d, C[:, :700].contiguous())
-    assert rep["passed"], rep
+    ref = A.double() @ Bs[:, :K].double().t()
+    got = C[:, :N].cpu().double()
+    assert torch.all(C[:, N:].cpu() == -3.0)
+    assert float((got - ref).abs().max()) <= 1e-4 * K
+
+
+def test_small_m_integers_equal_tensor_core_paths():
+    _need_gpu()
+    M, N, K = 8, 3000, 2048
+    A = W.small_ints(M, K, "f16", 51).cuda()
+    B = W.small_ints(N, K, "f16", 52).cuda()                                # stored N x K
+    ref = (A.cpu().to(torch.int64) @ B.cpu().to(torch.int64).t()).to(torch.float32)
+    for skinny in (2, 1, 0):
+        C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        with G.Gemm(0, sync_check=1, skinny=skinny) as g:
+            g.run(A, B, C, layoutB="col")
+            plan = g.last_plan()
+        assert plan["gemv"] == (1 if skinny == 2 else 0)
+        torch.cuda.synchronize()
+        assert torch.equal(C.cpu(), ref), skinny
+
+
+def test_small_m_forced_where_it_does_not_apply():
+    _need_gpu()
+    A = torch.zeros(4, 4096, dtype=torch.float16, device="cuda")
+    B = torch.zeros(4096, 4096, dtype=torch.float16, device="cuda")
+    C = torch.zeros(4, 4096, dtype=torch.float32, device="cuda")
+    with G.Gemm(0, skinny=2) as g:
+        assert g.run(A, B, C, layoutB="row", check=False) == G.GEMM_ERR_UNSUPPORTED   # B stored K x N
+        A16 = torch.zeros(16, 4096, dtype=torch.float16, device="cuda")
+        C16 = torch.zeros(16, 4096, dtype=torch.float32, device="cuda")
+        assert g.run(A16, B, C16, layoutB="col", check=False) == G.GEMM_ERR_UNSUPPORTED  # M > 8
