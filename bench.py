@@ -201,6 +201,23 @@ class ClockSampler:
                 "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(sel)}
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (all ranks call it; one process: the value itself)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(flops_per_step: float, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job TFLOP/s of `world` independent replicas, each running `steps` steps, timed by the
+    slowest rank (weak scaling: the work per rank is fixed)."""
+    return world * flops_per_step * steps / max_seconds / 1e12
+
+
 def algorithmic_bytes(w) -> int:
     """Least traffic of one product: read A and B once, write C once (and read C_in, bias)."""
     ein = 1 if w.dtype_in in ("e4m3", "e5m2") else 2
@@ -394,12 +411,8 @@ def run_ours(args, rank, world, local):
     if st != G.GEMM_OK:
         raise RuntimeError(f"timed run failed: {g.last_error()}")
     times_ms = np.array([e0.elapsed_time(e1) for e0, e1 in evs])
-    total_s = float(times_ms.sum()) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
-    value = world * w.flops * args.steps / total_s / 1e12
+    total_s = max_over_ranks(float(times_ms.sum()) / 1e3, world, dev)
+    value = replica_throughput(w.flops, args.steps, world, total_s)
     ms_per_step = total_s / args.steps * 1e3
 
     # end to end through the public call with host buffers
@@ -434,12 +447,8 @@ def run_ours(args, rank, world, local):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        t_e2e = e0.elapsed_time(e1) / 1e3
-        if world > 1:
-            t = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_e2e = float(t.item())
-        e2e = {"value": world * w.flops * n_e2e / t_e2e / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+        e2e = {"value": replica_throughput(w.flops, n_e2e, world, t_e2e), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "note": "pinned host A, B (and C_in) copied in, gemm_run, C copied out, every step"}
 
