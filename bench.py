@@ -1,6 +1,6 @@
 """Benchmark of the GB300 dense GEMM: one JSON line on rank 0.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 1..5]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 1..10]
 
 A step is one gemm_run (the whole hot path: tensor maps, TMA ring, tcgen05 MMAs, epilogue)
 over the workload's seeded synthetic inputs.  Default workload: 4096^3, f16 in, f32
@@ -41,7 +41,7 @@ def _args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2,
-                    help="1..8 (6: Q4_0 weights through gemm_run_q4_0; 7, 8: decode shapes, HBM-bound)")
+                    help="1..10 (6, 10: Q4_0 weights through gemm_run_q4_0; 7, 8, 10: decode shapes, HBM-bound)")
     ap.add_argument("--config", type=int, default=-1)
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps, capped at 200")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
@@ -465,18 +465,26 @@ def run_ours(args, rank, world, local):
     traffic, traffic_src = _traffic(w.name)
     n_sms = torch.cuda.get_device_properties(local).multi_processor_count
     alg_bytes = algorithmic_bytes(w)
+    if plan.get("gemv"):
+        kernel = "gb300::gemv_q4_0_kernel" if w.layoutB == "q4_0" else "gb300::gemv_kernel"
+    else:
+        kernel = "gb300::gemm_tc_kernel"
     if w.flops / alg_bytes < peak * 1e12 / (hbm * 1e9):      # below the ridge: the stream of bytes bounds it
         gbs = alg_bytes / (ms_per_step / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": traffic,
-                "peak_source": f"{src}: STREAM-style copy", "kernel": "gb300::gemm_tc_kernel",
+                "peak_source": f"{src}: STREAM-style copy", "kernel": kernel,
                 "algorithmic_bytes_per_launch": alg_bytes, "algorithmic_flops_per_launch": w.flops,
                 "avg_launch_ms": ms_per_step}
     else:
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": traffic,
                 "peak_source": f"{src}: {peak_note}",
-                "kernel": "gb300::gemm_tc_kernel", "algorithmic_flops_per_launch": w.flops,
+                "kernel": kernel, "algorithmic_flops_per_launch": w.flops,
                 "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_ms": ms_per_step}
+    if plan.get("kernels", 1) > 1:
+        roof["launches_per_step"] = plan["kernels"]
+        roof["note"] = ("avg_launch_ms is the whole step (every launch of the call), so achieved is a lower "
+                        "bound for the dominant kernel")
     if traffic is not None:
         roof["traffic_source"] = traffic_src
     if clocks.get("sm_mhz"):
@@ -491,7 +499,9 @@ def run_ours(args, rank, world, local):
             "config": _config_dict(w, args, {"kernel_config": plan.get("config", args.config),
                                              "plan": {k: plan[k] for k in ("block_m", "block_n", "block_k", "stages",
                                                                            "tiles_m", "tiles_n", "clusters",
-                                                                           "stream_k", "dp_tiles") if k in plan},
+                                                                           "stream_k", "dp_tiles", "transposed", "gemv",
+                                                                           "q4_dequant", "kernels")
+                                                      if k in plan},
                                              "timing": "CUDA events around each gemm_run on its stream"}),
             "roofline": roof, "clocks": clocks, "gpu_launches": launches, "e2e": e2e}
     if world == 1 and not args.no_cpu_baseline:

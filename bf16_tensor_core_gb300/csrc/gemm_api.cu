@@ -50,8 +50,9 @@ const ConfigDesc kConfigs[kNumConfigs] = {
 // Mainloop efficiency per config (measured k-iteration time of one long-K tile against the
 // config's tensor-core time at 1.9 GHz, cold L2, GB300): small tiles need more operand bytes per
 // flop and are bound by the TMA load rate per SM.  Config 7 is derated for its single accumulator
-// (its epilogue does not overlap the next tile).
-const double kConfigEfficiency[kNumConfigs] = {0.73, 0.78, 0.40, 0.39, 0.80, 0.85, 0.84, 0.75, 0.85, 0.40,
+// (its epilogue does not overlap the next tile); config 8 runs at the rate of its dequantisation
+// warps (2048 x 11008 x 4096 in 288 us), not of its MMAs.
+const double kConfigEfficiency[kNumConfigs] = {0.73, 0.78, 0.40, 0.39, 0.80, 0.85, 0.84, 0.75, 0.28, 0.40,
                                                 0.85, 0.40, 0.40};
 
 int cluster_ctas(const ConfigDesc& d) { return d.cta_group * d.pairs; }
@@ -188,6 +189,8 @@ struct gemm_ctx {
     unsigned* sk_flags = nullptr;   // zeroed at creation; stream-K flags carry the launch epoch
     float* sk_part = nullptr;       // stream-K partials (grown on demand)
     size_t sk_part_bytes = 0;
+    void* q4_ws = nullptr;          // f16 weights of the separate Q4_0 dequantisation pass (grown on demand)
+    size_t q4_ws_bytes = 0;
     unsigned epoch = 0;
     gemm_plan_t last_plan{};        // plan of the last successful gemm_run
     bool has_plan = false;
@@ -307,6 +310,84 @@ bool use_transposed(int skinny, int config, int64_t M, int64_t N, int b_q4) {
     if (b_q4) return false;
     if (skinny == 1) return true;
     return skinny == -1 && config == -1 && M <= 64 && N > 64;
+}
+
+// How gemm_run_q4_0 computes a product.
+enum Q4Route {
+    Q4_FUSED = 0,       // the tensor-core kernel with dequantisation warps (config 8)
+    Q4_GEMV = 1,        // the CUDA-core kernel that dequantises as it multiplies (M <= 8)
+    Q4_TWO_PASS = 2,    // the separate dequantisation pass into the handle's workspace, then the f16 GEMM
+};
+
+constexpr double kDequantBytesPerUs = 3.7e6;          // measured rate of the separate pass (read + write)
+
+bool q4_gemv_applies(int64_t M, int64_t lda, int la) {
+    return M >= 1 && M <= kGemvMaxM && la == GEMM_ROW && (lda * 2) % 16 == 0;
+}
+
+// Estimated time of the separate pass over N x K weights (18 bytes read and 64 written per block).
+double q4_dequant_us(int64_t N, int64_t K) {
+    return kLaunchUs + static_cast<double>(N) * (K / 32) * (18 + 64) / kDequantBytesPerUs;
+}
+
+Schedule plan_schedule(const gemm_plan_t& pl, int64_t M, int64_t N, int64_t K, const int* slots, int cluster_cap,
+                       int stream_k, int dout, float beta) {
+    int s = slots[pl.config];
+    if (cluster_cap > 0) s = std::min(s, cluster_cap);
+    return schedule(kConfigs[pl.config], kConfigEfficiency[pl.config], M, N, K, s, stream_k, elt_bytes(dout), beta);
+}
+
+gemm_status_t plan_impl(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int din, int dout,
+                        int la, int lb, float beta, const int* slots, int config, int stream_k, int cluster_cap,
+                        gemm_plan_t* out, std::string* err, int b_q4, int c_trans);
+
+// The route of a Q4_0 product and its plan (the fused kernel's, or the f16 GEMM's after the
+// separate pass).  config >= 0 without Q4_0 weights asks for the separate pass and that config;
+// skinny 2 asks for the CUDA-core kernel.  Automatically: the CUDA-core kernel for M <= 8, else
+// the faster of the fused kernel and the separate pass by the time model (the fused kernel
+// dequantises B once per row of output tiles, the pass once in all).
+gemm_status_t plan_q4(int64_t M, int64_t N, int64_t K, int64_t lda, int la, int64_t ldbq, int64_t ldc, int dout,
+                      float beta, const int* slots, int config, int stream_k, int skinny, int cluster_cap,
+                      gemm_plan_t* out, std::string* err, Q4Route* route) {
+    *route = Q4_FUSED;
+    const bool two_pass_cfg = config >= 0 && config < kNumConfigs && !kConfigs[config].b_q4;
+    gemm_status_t st = plan_impl(M, N, K, lda, ldbq, ldc, GEMM_F16, dout, la, GEMM_COL, beta, slots,
+                                 two_pass_cfg ? -1 : config, stream_k, cluster_cap, out, err, 1, 0);
+    if (st != GEMM_OK || M == 0 || N == 0 || K == 0) return st;
+    if (skinny < -1 || skinny > 2) { *err = "skinny must be -1, 0, 1 or 2"; return GEMM_ERR_INVALID_ARG; }
+    if (skinny == 2 || (skinny == -1 && config == -1 && q4_gemv_applies(M, lda, la))) {
+        if (!q4_gemv_applies(M, lda, la)) {
+            *err = "the CUDA-core Q4_0 kernel takes M <= 8 row-major f16 activations with a 16-byte pitch";
+            return GEMM_ERR_UNSUPPORTED;
+        }
+        std::memset(out, 0, sizeof(*out));
+        out->config = -1;
+        out->kernels = 1;
+        out->gemv = 1;
+        *route = Q4_GEMV;
+        return GEMM_OK;
+    }
+    bool two_pass = two_pass_cfg;
+    gemm_plan_t f16plan;
+    if (two_pass || (config == -1 && M > 64)) {
+        st = plan_impl(M, N, K, lda, K, ldc, GEMM_F16, dout, la, GEMM_COL, beta, slots, two_pass_cfg ? config : -1,
+                       stream_k, cluster_cap, &f16plan, err, 0, 0);
+        if (st != GEMM_OK) return st;
+        if (!two_pass) {
+            const double fused = plan_schedule(*out, M, N, K, slots, cluster_cap, stream_k, dout, beta).est_us;
+            const double sep = q4_dequant_us(N, K) +
+                               plan_schedule(f16plan, M, N, K, slots, cluster_cap, stream_k, dout, beta).est_us;
+            two_pass = sep < fused;
+        }
+    }
+    if (two_pass) {
+        *out = f16plan;
+        out->q4_dequant = 1;
+        out->kernels += 1;
+        out->workspace_bytes += round_up(N * K * 2, 256);
+        *route = Q4_TWO_PASS;
+    }
+    return GEMM_OK;
 }
 
 // Pure host planning: validation, config choice, grid, stream-K split and workspace.
@@ -871,6 +952,7 @@ gemm_status_t gemm_destroy(gemm_handle_t h) {
         if (h->d_status) cudaFree(h->d_status);
         if (h->sk_flags) cudaFree(h->sk_flags);
         if (h->sk_part) cudaFree(h->sk_part);
+        if (h->q4_ws) cudaFree(h->q4_ws);
     }
     delete h;
     return GEMM_OK;
@@ -1028,8 +1110,65 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
 gemm_status_t gemm_run_q4_0(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                             gemm_layout_t layoutA, const void* Bq, int64_t ldbq, void* C, int64_t ldc,
                             gemm_dtype_t dtype_out, float alpha, float beta, const void* bias, void* stream) {
-    return run_impl(h, M, N, K, A, lda, Bq, ldbq, C, ldc, GEMM_F16, dtype_out, layoutA, GEMM_COL, alpha, beta, bias,
-                    stream, 1);
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    h->err.clear();
+    gemm_plan_t plan;
+    std::string err;
+    Q4Route route;
+    gemm_status_t st = plan_q4(M, N, K, lda, layoutA, ldbq, ldc, dtype_out, beta, h->dev.slots, h->opt.config,
+                               h->opt.stream_k, h->opt.skinny, h->opt.max_clusters, &plan, &err, &route);
+    if (st != GEMM_OK) return fail(h, st, err);
+    if (route == Q4_FUSED || M == 0 || N == 0 || K == 0)
+        return run_impl(h, M, N, K, A, lda, Bq, ldbq, C, ldc, GEMM_F16, dtype_out, layoutA, GEMM_COL, alpha, beta,
+                        bias, stream, 1);
+    if (!C) return fail(h, GEMM_ERR_INVALID_ARG, "C is NULL");
+    if (!A || !Bq) return fail(h, GEMM_ERR_INVALID_ARG, "A or B is NULL");
+    if ((reinterpret_cast<uintptr_t>(A) % 16) != 0) return fail(h, GEMM_ERR_ALIGNMENT, "A must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(Bq) % 2) != 0)
+        return fail(h, GEMM_ERR_ALIGNMENT, "Q4_0 weights must be 2-byte aligned");
+    DeviceGuard guard(h->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (h->faults & FAULT_LAUNCH) return fail(h, GEMM_ERR_CUDA, "kernel launch: forced failure (GEMM_TEST_FAIL=launch)");
+    if (route == Q4_GEMV) {
+        GemvParams gp{A, lda * 2, Bq, ldbq, C, ldc, bias, alpha, beta, (int)M, (int)N, (int)K};
+        const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
+        cudaError_t e = launch_gemv_q4_0(out_kind, gp, s);
+        if (e != cudaSuccess) return cuda_fail(h, "Q4_0 small-M kernel launch", e);
+        h->launches += 1;
+        h->last_plan = plan;
+        h->has_plan = true;
+        if (h->opt.sync_check) return gemm_get_device_status(h, stream);
+        return GEMM_OK;
+    }
+    // The separate pass writes the N x K f16 weights (pitch K) that the f16 GEMM then reads.
+    st = ensure_buffer(h, &h->q4_ws, &h->q4_ws_bytes, (size_t)round_up(N * K * 2, 256), "dequantised weights");
+    if (st != GEMM_OK) return st;
+    cudaError_t e = launch_dequant_q4_0(Bq, ldbq, N, K, h->q4_ws, K, h->dev.num_sms, s);
+    if (e != cudaSuccess) return cuda_fail(h, "Q4_0 dequantisation launch", e);
+    h->launches += 1;
+    st = run_impl(h, M, N, K, A, lda, h->q4_ws, K, C, ldc, GEMM_F16, dtype_out, layoutA, GEMM_COL, alpha, beta, bias,
+                  stream, 0);
+    if (st != GEMM_OK) return st;
+    h->last_plan.q4_dequant = 1;
+    h->last_plan.kernels += 1;
+    h->last_plan.workspace_bytes += round_up(N * K * 2, 256);
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_q4_0(int64_t M, int64_t N, int64_t K, int64_t lda, gemm_layout_t layoutA, int64_t ldbq,
+                             int64_t ldc, gemm_dtype_t dtype_out, float beta, int num_sms, int max_clusters,
+                             int config, int stream_k, gemm_plan_t* out) {
+    if (!out || num_sms <= 0) return GEMM_ERR_INVALID_ARG;
+    if (max_clusters <= 0) max_clusters = num_sms / 2;
+    int slots[kNumConfigs];
+    for (int c = 0; c < kNumConfigs; ++c) {
+        const ConfigDesc& d = kConfigs[c];
+        slots[c] = d.cta_group == 1 ? num_sms : max_clusters / d.pairs;
+    }
+    std::string err;
+    Q4Route route;
+    return plan_q4(M, N, K, lda, layoutA, ldbq, ldc, dtype_out, beta, slots, config, stream_k, -1, 0, out, &err,
+                   &route);
 }
 
 gemm_status_t gemm_dequant_q4_0(const void* Bq, int64_t ldbq, int64_t N, int64_t K, void* out, int64_t ldo,

@@ -46,6 +46,25 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
     return v;
 }
 
+// Read-only loads that stay in L1: the five loads of one 18-byte block (and of the warp's 576
+// contiguous bytes) hit the same lines.
+__device__ __forceinline__ uint32_t ldg_nc_u32(const uint32_t* p) { return __ldg(p); }
+__device__ __forceinline__ uint32_t ldg_nc_u16(const uint8_t* p) {
+    return __ldg(reinterpret_cast<const unsigned short*>(p));
+}
+
+// The f32 epilogue of element (m, n): alpha * s + beta * C_in + bias, rounded to the output type.
+template <int kOut>
+__device__ __forceinline__ void store_gemv_out(const GemvParams& p, int m, int n, float s) {
+    const long long idx = static_cast<long long>(m) * p.ldc + n;
+    float v = p.alpha * s;
+    if (p.beta != 0.0f) v = fmaf(p.beta, load_out<kOut>(p.C, idx), v);
+    if (p.bias != nullptr) v += load_out<kOut>(p.bias, n);
+    if constexpr (kOut == OUT_F32) static_cast<float*>(p.C)[idx] = v;
+    else if constexpr (kOut == OUT_F16) static_cast<__half*>(p.C)[idx] = __float2half_rn(v);
+    else static_cast<__nv_bfloat16*>(p.C)[idx] = __float2bfloat16_rn(v);
+}
+
 // kM rows of C; kOut: output type; kBf16: bf16 operands (else f16).
 template <int kM, int kOut, bool kBf16>
 __global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(GemvParams p) {
@@ -111,15 +130,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(GemvParams p) {
         float s = 0.0f;
 #pragma unroll
         for (int w = 0; w < kGemvWarps; ++w) s += part[w][r][m];
-        if (n < p.N) {
-            const long long idx = static_cast<long long>(m) * p.ldc + n;
-            float v = p.alpha * s;
-            if (p.beta != 0.0f) v = fmaf(p.beta, load_out<kOut>(p.C, idx), v);
-            if (p.bias != nullptr) v += load_out<kOut>(p.bias, n);
-            if constexpr (kOut == OUT_F32) static_cast<float*>(p.C)[idx] = v;
-            else if constexpr (kOut == OUT_F16) static_cast<__half*>(p.C)[idx] = __float2half_rn(v);
-            else static_cast<__nv_bfloat16*>(p.C)[idx] = __float2bfloat16_rn(v);
-        }
+        if (n < p.N) store_gemv_out<kOut>(p, m, n, s);
     }
 }
 
@@ -145,7 +156,165 @@ cudaError_t launch_out(const GemvParams& p, bool bf16, int blocks, cudaStream_t 
     }
 }
 
+// ---------------------------------------------------------------- Q4_0 weights
+// The same product with W given as Q4_0 blocks ("02 . 8m/8m(2) -- Tiled wmma f16 prefill GEMM",
+// section 3.2: per 32 weights an f16 scale d and 16 bytes q, weight i the low nibble of q[i] and
+// weight 16+i its high nibble, value d * (q - 8) rounded to f16).  At decode the weights are read
+// once at 4.5 bits each, so the kernel streams the blocks and multiplies as it dequantises: a CTA
+// owns kQ4Rows weight rows; thread t takes blocks t, t + kQ4Threads, ... of all of them (a warp's
+// loads of one row cover 576 contiguous bytes), dequantises each block exactly as the tensor-core
+// path does (f16 1024 + q, minus 1032, times d, one rounding) and accumulates a * w in f32.
+constexpr int kQ4Rows = 4;           // weight rows per CTA
+constexpr int kQ4Threads = 128;      // threads per CTA (they split the blocks of a row)
+
+// One 18-byte block at byte address b (2-byte aligned): the scale bits and the 16 nibble bytes as
+// four words.  The loads are 4-byte ones placed by the block's alignment.
+struct Q4Block {
+    uint32_t d;
+    uint32_t q[4];
+};
+
+__device__ __forceinline__ Q4Block q4_block_load(const uint8_t* b) {
+    Q4Block r;
+    if ((reinterpret_cast<uintptr_t>(b) & 2u) == 0) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(b);
+        const uint32_t w0 = ldg_nc_u32(w), w1 = ldg_nc_u32(w + 1), w2 = ldg_nc_u32(w + 2), w3 = ldg_nc_u32(w + 3);
+        const uint32_t w4 = ldg_nc_u16(b + 16);
+        r.d = w0 & 0xffffu;
+        r.q[0] = __byte_perm(w0, w1, 0x5432u);
+        r.q[1] = __byte_perm(w1, w2, 0x5432u);
+        r.q[2] = __byte_perm(w2, w3, 0x5432u);
+        r.q[3] = __byte_perm(w3, w4, 0x5432u);
+    } else {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(b + 2);
+        r.d = ldg_nc_u16(b);
+        r.q[0] = ldg_nc_u32(w);
+        r.q[1] = ldg_nc_u32(w + 1);
+        r.q[2] = ldg_nc_u32(w + 2);
+        r.q[3] = ldg_nc_u32(w + 3);
+    }
+    return r;
+}
+
+// The block's 32 weights as f16 pairs: word j holds weights 2j (low half) and 2j + 1.
+__device__ __forceinline__ void q4_block_weights(const Q4Block& b, uint32_t (&v)[16]) {
+    const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(b.d)));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t hi = b.q[i] >> 4;
+        v[2 * i] = q4_two(__byte_perm(b.q[i], 0u, 0x4140u), d2);
+        v[2 * i + 1] = q4_two(__byte_perm(b.q[i], 0u, 0x4342u), d2);
+        v[8 + 2 * i] = q4_two(__byte_perm(hi, 0u, 0x4140u), d2);
+        v[8 + 2 * i + 1] = q4_two(__byte_perm(hi, 0u, 0x4342u), d2);
+    }
+}
+
+// acc + a.lo * w.lo + a.hi * w.hi, each product exact (two f16 values) and each sum rounded in f32.
+__device__ __forceinline__ float fma2_f16_f32(uint32_t a2, uint32_t w2, float acc) {
+    asm("{\n\t.reg .b16 al, ah, wl, wh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, wl, %0;\n\t"
+        "fma.rn.f32.f16 %0, ah, wh, %0;\n\t}"
+        : "+f"(acc) : "r"(a2), "r"(w2));
+    return acc;
+}
+
+template <int kM, int kOut>
+__global__ void __launch_bounds__(kQ4Threads) gemv_q4_0_kernel(GemvParams p) {
+    constexpr int kWarps = kQ4Threads / 32;
+    __shared__ float part[kWarps][kQ4Rows][kM];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * kQ4Rows;
+    const int nblk = p.K / 32;
+    const uint8_t* Bq = static_cast<const uint8_t*>(p.W);
+    const uint8_t* A = static_cast<const uint8_t*>(p.A);
+    float acc[kQ4Rows][kM];
+#pragma unroll
+    for (int r = 0; r < kQ4Rows; ++r)
+#pragma unroll
+        for (int m = 0; m < kM; ++m) acc[r][m] = 0.0f;
+    for (int b = threadIdx.x; b < nblk; b += kQ4Threads) {
+        // All rows' loads first, then the arithmetic; rows past N are zero blocks (scale 0).
+        Q4Block raw[kQ4Rows];
+#pragma unroll
+        for (int r = 0; r < kQ4Rows; ++r) {
+            if (n0 + r < p.N) raw[r] = q4_block_load(Bq + static_cast<long long>(n0 + r) * p.ldw_bytes + 18LL * b);
+            else raw[r] = Q4Block{0u, {0u, 0u, 0u, 0u}};
+        }
+        uint32_t w[kQ4Rows][16];
+#pragma unroll
+        for (int r = 0; r < kQ4Rows; ++r) q4_block_weights(raw[r], w[r]);
+#pragma unroll
+        for (int m = 0; m < kM; ++m) {
+            const uint4* ap = reinterpret_cast<const uint4*>(A + static_cast<long long>(m) * p.lda_bytes + 64LL * b);
+#pragma unroll
+            for (int pc = 0; pc < 4; ++pc) {
+                const uint4 a = __ldg(ap + pc);
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int r = 0; r < kQ4Rows; ++r) acc[r][m] = fma2_f16_f32(aw[j], w[r][4 * pc + j], acc[r][m]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kQ4Rows; ++r)
+#pragma unroll
+        for (int m = 0; m < kM; ++m) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc[r][m] += __shfl_xor_sync(0xffffffffu, acc[r][m], off);
+            if (lane == 0) part[warp][r][m] = acc[r][m];
+        }
+    __syncthreads();
+    if (threadIdx.x < kQ4Rows * kM) {
+        const int r = threadIdx.x / kM, m = threadIdx.x - (threadIdx.x / kM) * kM;
+        const int n = n0 + r;
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s += part[w][r][m];
+        if (n < p.N) store_gemv_out<kOut>(p, m, n, s);
+    }
+}
+
+template <int kM, int kOut>
+cudaError_t launch_q4_m(const GemvParams& p, int blocks, cudaStream_t s) {
+    gemv_q4_0_kernel<kM, kOut><<<blocks, kQ4Threads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int kOut>
+cudaError_t launch_q4_out(const GemvParams& p, int blocks, cudaStream_t s) {
+    switch (p.M) {
+        case 1: return launch_q4_m<1, kOut>(p, blocks, s);
+        case 2: return launch_q4_m<2, kOut>(p, blocks, s);
+        case 3: return launch_q4_m<3, kOut>(p, blocks, s);
+        case 4: return launch_q4_m<4, kOut>(p, blocks, s);
+        case 5: return launch_q4_m<5, kOut>(p, blocks, s);
+        case 6: return launch_q4_m<6, kOut>(p, blocks, s);
+        case 7: return launch_q4_m<7, kOut>(p, blocks, s);
+        case 8: return launch_q4_m<8, kOut>(p, blocks, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_gemv_q4_0(int out, const GemvParams& p, cudaStream_t stream) {
+    if (p.M < 1 || p.M > kGemvMaxM || p.N <= 0 || p.K <= 0 || p.K % 32 != 0 || p.ldw_bytes % 2 != 0 ||
+        p.ldw_bytes < p.K / 32 * 18 || (reinterpret_cast<uintptr_t>(p.W) & 1u) != 0 || p.lda_bytes % 16 != 0 ||
+        (reinterpret_cast<uintptr_t>(p.A) & 15u) != 0)
+        return cudaErrorInvalidValue;
+    const long long blocks = (p.N + kQ4Rows - 1) / kQ4Rows;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    switch (out) {
+        case OUT_F16: return launch_q4_out<OUT_F16>(p, static_cast<int>(blocks), stream);
+        case OUT_BF16: return launch_q4_out<OUT_BF16>(p, static_cast<int>(blocks), stream);
+        case OUT_F32: return launch_q4_out<OUT_F32>(p, static_cast<int>(blocks), stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_gemv(int out, bool bf16, const GemvParams& p, int num_sms, cudaStream_t stream) {
     (void)num_sms;

@@ -44,7 +44,7 @@ class gemm_plan_t(ctypes.Structure):
                 ("raster_group", ctypes.c_int), ("tma_store", ctypes.c_int), ("repack_a", ctypes.c_int),
                 ("repack_b", ctypes.c_int), ("workspace_bytes", ctypes.c_int64), ("kernels", ctypes.c_int),
                 ("stream_k", ctypes.c_int), ("dp_tiles", ctypes.c_int), ("sk_partial_bytes", ctypes.c_int64),
-                ("transposed", ctypes.c_int), ("gemv", ctypes.c_int)]
+                ("transposed", ctypes.c_int), ("gemv", ctypes.c_int), ("q4_dequant", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -86,6 +86,9 @@ def load_library(path: Path | str | None = None):
     lib.gemm_plan.argtypes = [i64, i64, i64, i64, i64, i64, ci, ci, ci, ci, cf, ci, ci, ci, ci,
                               ctypes.POINTER(gemm_plan_t)]
     lib.gemm_plan.restype = ci
+    lib.gemm_plan_q4_0.argtypes = [i64, i64, i64, i64, ci, i64, i64, ci, cf, ci, ci, ci, ci,
+                                   ctypes.POINTER(gemm_plan_t)]
+    lib.gemm_plan_q4_0.restype = ci
     lib.gemm_num_configs.argtypes = []
     lib.gemm_num_configs.restype = ci
     lib.gemm_config_info.argtypes = [ci, ctypes.POINTER(gemm_config_info_t)]
@@ -151,6 +154,14 @@ def gemm_plan(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, bet
     p = gemm_plan_t()
     st = load_library().gemm_plan(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, num_sms,
                                   max_clusters, config, stream_k, ctypes.byref(p))
+    return st, p
+
+
+def gemm_plan_q4_0(M, N, K, lda, layoutA, ldbq, ldc, dtype_out, beta=0.0, num_sms=152, max_clusters=0, config=-1,
+                   stream_k=-1) -> tuple[int, gemm_plan_t]:
+    p = gemm_plan_t()
+    st = load_library().gemm_plan_q4_0(M, N, K, lda, layoutA, ldbq, ldc, dtype_out, beta, num_sms, max_clusters, config,
+                                       stream_k, ctypes.byref(p))
     return st, p
 
 

@@ -85,6 +85,9 @@ WORKLOADS = {
                 1.0, 0.0, ("normal", 1.0), ("q4_0", 0.02), ("normal", 0.02), None, _seed(6),
                 "prefill projection with Q4_0 weights (random valid blocks, |w| <= 0.04), f16 activations, "
                 "f16 out, fused per-column bias"),
+    10: Workload("decode_1x4096x4096_q4_0", 1, 4096, 4096, "f16", "f16", "row", "q4_0", 1.0, 0.0,
+                 ("normal", 1.0), ("q4_0", 0.02), None, None, _seed(10),
+                 "one token through a 4096 x 4096 weight in Q4_0 blocks (4.5 bits per weight, HBM-bound)"),
 }
 
 

@@ -135,6 +135,9 @@ typedef struct {
                               (its rows are C's columns) and C is written by direct stores    */
     int gemv;              /* 1: the CUDA-core kernel for a few rows of C (no tensor cores, no
                               tiles; config is -1)                                             */
+    int q4_dequant;        /* 1 (gemm_run_q4_0): the Q4_0 weights are first dequantised by the
+                              separate pass into the handle's workspace; the other fields
+                              describe the f16 GEMM that follows (kernels counts both)         */
 } gemm_plan_t;
 
 /* Fill *opt with defaults (config -1, timeout 2000 ms, no sync check, automatic raster). */
@@ -153,10 +156,19 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                        gemm_layout_t layoutA, gemm_layout_t layoutB,
                        float alpha, float beta, const void* bias, void* stream);
 
-/* gemm_run_q4_0 - the same product with Q4_0-quantised weights as B, dequantised inside the
- * GEMM kernel ("02 . 8m/8m(2) -- Tiled wmma f16 prefill GEMM (LANDED)": section 2.3 names the
- * dequant-in-GEMM fused kernel as the successor of its separate dequant pass; section 3.2 gives
- * the block format).
+/* gemm_run_q4_0 - the same product with Q4_0-quantised weights as B ("02 . 8m/8m(2) -- Tiled
+ * wmma f16 prefill GEMM (LANDED)": section 3.2 gives the block format and the separate dequant
+ * pass, section 2.3 names the dequant-in-GEMM fused kernel as its successor).  One of three routes:
+ *   - fused: the tensor-core kernel whose dequantisation warps write each B stage into shared
+ *     memory (config 8);
+ *   - small M: a CUDA-core kernel that dequantises each block in registers as it multiplies
+ *     (M <= 8, A row-major with a 16-byte pitch; automatic, or the handle's skinny option 2);
+ *   - separate pass: gemm_dequant_q4_0 into a workspace the handle owns (N*K*2 bytes, grown on
+ *     demand) followed by the f16 GEMM on it (chosen when the time model says it is faster, or
+ *     when the handle's config option names a config without Q4_0 weights, which then runs the
+ *     f16 GEMM).
+ * Every route computes the same value per element: the dequantised weight rounded to f16, times
+ * the f16 activation, summed in f32.
  *   C (M x N) <- alpha * op(A) * W^T + beta * C + bias, W the N x K dequantised weights.
  *   A: f16 activations, layoutA as in gemm_run, 16-byte aligned.
  *   Bq: N rows (one per output column) of K/32 blocks of 18 bytes at a row pitch of ldbq bytes
@@ -165,8 +177,8 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
  *       its value is d * (nibble - 8) rounded to f16, exactly as gemm_dequant_q4_0 writes it, and
  *       the product then runs on the f16 tensor cores with f32 accumulation.
  *   K must be a multiple of 32 (whole blocks).  C, ldc, dtype_out, alpha, beta, bias, stream and
- *   the returned codes are those of gemm_run.  The handle's config option must be -1 or a config
- *   whose b_q4_0 is 1. */
+ *   the returned codes are those of gemm_run (GEMM_ERR_UNSUPPORTED for skinny 2 where the
+ *   small-M kernel does not apply). */
 gemm_status_t gemm_run_q4_0(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                             const void* A, int64_t lda, gemm_layout_t layoutA,
                             const void* Bq, int64_t ldbq,
@@ -202,6 +214,12 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
                         gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
                         gemm_layout_t layoutA, gemm_layout_t layoutB, float beta,
                         int num_sms, int max_clusters, int config, int stream_k, gemm_plan_t* out);
+
+/* The same for gemm_run_q4_0 (automatic skinny option): the plan's gemv, q4_dequant or neither
+ * field says which of the three routes the call takes. */
+gemm_status_t gemm_plan_q4_0(int64_t M, int64_t N, int64_t K, int64_t lda, gemm_layout_t layoutA,
+                             int64_t ldbq, int64_t ldc, gemm_dtype_t dtype_out, float beta,
+                             int num_sms, int max_clusters, int config, int stream_k, gemm_plan_t* out);
 
 /* Number of kernel configurations and their descriptions (ids 0 .. gemm_num_configs()-1). */
 int gemm_num_configs(void);

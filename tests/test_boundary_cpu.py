@@ -123,6 +123,51 @@ def test_q4_0_config_is_not_a_plain_gemm_config(lib):
         assert st == G.GEMM_OK and p.config != 8
 
 
+def plan_q4(M, N, K, *, lda=None, la=0, ldbq=None, dout=2, config=-1, sk=-1, sms=152):
+    lda = lda if lda is not None else (K if la == 0 else M)
+    ldbq = ldbq if ldbq is not None else K // 32 * 18
+    return G.gemm_plan_q4_0(M, N, K, max(lda, 1), la, ldbq, max(N, 1), dout, 0.0, sms, 0, config, sk)
+
+
+def test_q4_0_routes(lib):
+    """gemm_run_q4_0: the CUDA-core kernel for M <= 8 (row-major A), the fused kernel for a few
+    output-tile rows, the separate pass + f16 GEMM once the fused kernel would dequantise B for
+    many tile rows (it does so once per row of output tiles)."""
+    for M in (1, 8):
+        st, p = plan_q4(M, 4096, 4096)
+        assert st == G.GEMM_OK and p.gemv == 1 and p.q4_dequant == 0 and p.config == -1 and p.kernels == 1
+    st, p = plan_q4(4, 4096, 4096, la=1)                   # column-major A: not the CUDA-core kernel
+    assert st == G.GEMM_OK and p.gemv == 0 and p.config == 8
+    for M in (9, 64, 256):
+        st, p = plan_q4(M, 11008, 4096)
+        assert st == G.GEMM_OK and p.gemv == 0 and p.q4_dequant == 0 and p.config == 8 and p.kernels == 1
+    for M in (1024, 2048, 8192):
+        st, p = plan_q4(M, 11008, 4096, dout=1)
+        assert st == G.GEMM_OK and p.q4_dequant == 1 and p.config not in (-1, 8) and p.kernels == 2
+        assert p.workspace_bytes >= 11008 * 4096 * 2
+
+
+def test_q4_0_route_by_config(lib):
+    st, p = plan_q4(2048, 11008, 4096, config=8)            # the fused kernel on request
+    assert st == G.GEMM_OK and p.config == 8 and p.q4_dequant == 0
+    st, p = plan_q4(64, 4096, 4096, config=5)               # a plain config: separate pass + that config
+    assert st == G.GEMM_OK and p.config == 5 and p.q4_dequant == 1 and p.kernels == 2
+    st, p = plan_q4(1, 4096, 4096, config=8)                # an explicit config overrides the small-M kernel
+    assert st == G.GEMM_OK and p.config == 8 and p.gemv == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=64, N=64, K=48), G.GEMM_ERR_INVALID_ARG),                 # K not whole blocks
+    (dict(M=64, N=64, K=64, ldbq=35), G.GEMM_ERR_INVALID_ARG),        # odd pitch
+    (dict(M=64, N=64, K=64, ldbq=34), G.GEMM_ERR_INVALID_ARG),        # pitch below K/32*18
+    (dict(M=64, N=64, K=64, config=99), G.GEMM_ERR_UNSUPPORTED),
+    (dict(M=0, N=64, K=64), G.GEMM_OK),
+])
+def test_q4_0_plan_validation(lib, kw, status):
+    st, _ = plan_q4(**kw)
+    assert st == status
+
+
 def test_plan_few_rows_use_the_cuda_core_kernel(lib):
     # M <= 8, B stored N x K with a 16-byte pitch, K a multiple of 8: the CUDA-core kernel.
     for M in (1, 5, 8):

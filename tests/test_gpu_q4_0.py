@@ -1,6 +1,8 @@
 """GPU parity of the Q4_0 weight path: the separate dequantisation kernel (bit-exact against the
-oracle's decode) and the GEMM whose kernel dequantises B in shared memory (against the oracle's
-dequantise-then-GEMM reference, and bit-exact against the plain GEMM on the dequantised weights)."""
+oracle's decode) and the three routes of gemm_run_q4_0 -- the GEMM whose kernel dequantises B in
+shared memory, the CUDA-core kernel for M <= 8, and the separate pass followed by the f16 GEMM --
+against the oracle's dequantise-then-GEMM reference (and, where the arithmetic is the same, bit for
+bit against the plain GEMM on the dequantised weights)."""
 import numpy as np
 import pytest
 import torch
@@ -138,7 +140,7 @@ FUSED_CASES = [
 def test_fused_parity(i):
     _need_gpu()
     c = _case(seed=50 + i, **FUSED_CASES[i])
-    with G.Gemm(0, sync_check=1) as g:
+    with G.Gemm(0, sync_check=1, config=Q4_CONFIG) as g:
         C = _run(g, c)
         assert g.last_plan()["config"] == Q4_CONFIG
     _check(c, C)
@@ -150,14 +152,15 @@ def test_fused_equals_plain_gemm_on_dequantised_weights(sk):
     bit for bit with the plain GEMM (config 5, the same tile shape) on the dequantised f16 weights."""
     _need_gpu()
     c = _case(1000, 1500, 2048, seed=70, dout="f32", bias=True)
-    with G.Gemm(0, sync_check=1, stream_k=sk) as g:
+    # 24 tiles on at most 48 clusters: both configs take the same split whatever their time models say.
+    with G.Gemm(0, sync_check=1, stream_k=sk, config=Q4_CONFIG, max_clusters=48) as g:
         C1 = _run(g, c)
         plan = g.last_plan()
     Wd = torch.empty(c["N"], c["K"], dtype=torch.float16, device="cuda")
     bq = c["bq"].cuda()
     assert G.gemm_dequant_q4_0(bq.data_ptr(), bq.size(1), c["N"], c["K"], Wd.data_ptr(), c["K"], None) == 0
     C2 = torch.full_like(C1, float("nan"))
-    with G.Gemm(0, config=5, sync_check=1, stream_k=sk) as g:
+    with G.Gemm(0, config=5, sync_check=1, stream_k=sk, max_clusters=48) as g:
         g.run(c["A"].cuda(), Wd, C2, layoutB="col", bias=c["bias"].cuda())
         p2 = g.last_plan()
         assert (p2["stream_k"], p2["clusters"], p2["dp_tiles"]) == (plan["stream_k"], plan["clusters"], plan["dp_tiles"])
@@ -175,7 +178,7 @@ def test_fused_rows_two_bytes_past_alignment():
     dev = store.cuda()
     view = dev[:, 2:2 + pitch]                            # data_ptr % 4 == 2, row stride pitch + 4
     C = torch.full((c["M"], N), float("nan"), dtype=torch.float32, device="cuda")
-    with G.Gemm(0, sync_check=1) as g:
+    with G.Gemm(0, sync_check=1, config=Q4_CONFIG) as g:
         n0 = g.launches
         st = G.gemm_run_q4_0(g.h, c["M"], N, c["K"], c["A"].cuda().data_ptr(), c["K"], 0, view.data_ptr(),
                              pitch + 4, C.data_ptr(), N, 2, 1.0, 0.0, None, torch.cuda.current_stream().cuda_stream)
@@ -200,7 +203,7 @@ def test_fused_integers_exact():
     ref = torch.from_numpy(A.to(torch.int64).numpy() @ Wint.T).to(torch.float32)
     for sk in (0, 1):
         C = torch.empty(M, N, dtype=torch.float32, device="cuda")
-        with G.Gemm(0, sync_check=1, stream_k=sk) as g:
+        with G.Gemm(0, sync_check=1, stream_k=sk, config=Q4_CONFIG) as g:
             g.run_q4_0(A.cuda(), bq.cuda(), C, N=N)
         torch.cuda.synchronize()
         assert torch.equal(C.cpu(), ref), sk
@@ -210,7 +213,7 @@ def test_fused_split_k_parity():
     """Few output tiles and long K: the schedule splits K over several clusters."""
     _need_gpu()
     c = _case(200, 500, 8192, seed=80, dout="f32")
-    with G.Gemm(0, sync_check=1, stream_k=1) as g:
+    with G.Gemm(0, sync_check=1, stream_k=1, config=Q4_CONFIG) as g:
         C = _run(g, c)
         plan = g.last_plan()
     assert plan["stream_k"] == 1 and plan["clusters"] > plan["tiles_m"] * plan["tiles_n"]
@@ -224,7 +227,7 @@ def test_fused_special_blocks():
     A = (torch.rand(M, K, generator=torch.Generator().manual_seed(4), dtype=torch.float64) * 2 - 1).half()
     c = dict(M=M, N=bq.size(0), K=K, A=A, bq=bq, bias=None, Cin=None, dout="f32", layoutA="row", alpha=1.0,
              beta=0.0)
-    with G.Gemm(0, sync_check=1) as g:
+    with G.Gemm(0, sync_check=1, config=Q4_CONFIG) as g:
         C = _run(g, c)
     _check(c, C)
 
@@ -233,7 +236,7 @@ def test_fused_prefill_shape_sampled():
     """The 2048 x 11008 x 4096 prefill projection with Q4_0 weights, sampled rows and columns."""
     _need_gpu()
     c = _case(2048, 11008, 4096, seed=90, dout="bf16", bias=True)
-    with G.Gemm(0, sync_check=1) as g:
+    with G.Gemm(0, sync_check=1, config=Q4_CONFIG) as g:
         C = _run(g, c)
     rows = sample_indices(2048, 24, 1, 256)
     cols = sample_indices(11008, 24, 2, 256)
@@ -254,7 +257,7 @@ def test_fused_rejects_bad_arguments():
                                1.0, 0.0, None, s) == G.GEMM_ERR_INVALID_ARG        # odd pitch
         assert G.gemm_run_q4_0(g.h, 64, 64, 64, A.data_ptr(), 64, 0, bq.data_ptr() + 1, 36, C.data_ptr(), 64, 2,
                                1.0, 0.0, None, s) == G.GEMM_ERR_ALIGNMENT
-    with G.Gemm(0, config=5) as g:                                                 # not a Q4_0 config
+    with G.Gemm(0, skinny=2) as g:                                                 # small-M kernel, M > 8
         assert G.gemm_run_q4_0(g.h, 64, 64, 64, A.data_ptr(), 64, 0, bq.data_ptr(), 36, C.data_ptr(), 64, 2,
                                1.0, 0.0, None, torch.cuda.current_stream().cuda_stream) == G.GEMM_ERR_UNSUPPORTED
     with G.Gemm(0, config=Q4_CONFIG) as g:                                         # plain B on the Q4_0 config
@@ -267,7 +270,7 @@ def test_fused_bounded_wait_expires_and_reports():
     wait outcomes), the kernel records the timeout and returns; the next call works."""
     _need_gpu()
     c = _case(256, 256, 1024, seed=95, dout="f32")
-    with G.Gemm(0, timeout_ms=200, debug_skip_stage=3) as g:
+    with G.Gemm(0, timeout_ms=200, debug_skip_stage=3, config=Q4_CONFIG, stream_k=0) as g:   # 8 stages per tile
         _run(g, c)
         st = g.status()
         assert st == G.GEMM_ERR_TIMEOUT, G.gemm_status_string(st)
@@ -275,3 +278,124 @@ def test_fused_bounded_wait_expires_and_reports():
     with G.Gemm(0, sync_check=1) as g:
         C = _run(g, c)
     _check(c, C)
+
+
+# ------------------------------------------------------------------ CUDA-core kernel, M <= 8
+GEMV_CASES = [
+    dict(M=1, N=4096, K=4096, dout="f16"),
+    dict(M=1, N=11008, K=4096, dout="bf16", bias=True),
+    dict(M=2, N=37, K=32, dout="f32"),                                      # one block per row
+    dict(M=3, N=1001, K=11008, dout="f32", alpha=0.5, beta=1.0),            # several blocks per thread
+    dict(M=5, N=6, K=96, dout="f16", bias=True),
+    dict(M=7, N=130, K=4128, dout="bf16", ldbq=2330),                       # pitch 2 mod 4: rows alternate alignment
+    dict(M=8, N=515, K=2048, dout="f32", bias=True, alpha=2.0, beta=-1.0),
+    dict(M=4, N=64, K=640, dout="f16", layoutA="row"),
+]
+
+
+@pytest.mark.parametrize("i", range(len(GEMV_CASES)))
+def test_small_m_parity(i):
+    _need_gpu()
+    c = _case(seed=200 + i, **GEMV_CASES[i])
+    with G.Gemm(0, sync_check=1) as g:
+        n0 = g.launches
+        C = _run(g, c)
+        plan = g.last_plan()
+        assert plan["gemv"] == 1 and plan["config"] == -1 and g.launches - n0 == 1
+    _check(c, C)
+
+
+def test_small_m_rows_two_bytes_past_alignment():
+    """The CUDA-core kernel reads blocks at any 2-byte alignment (no repack)."""
+    _need_gpu()
+    c = _case(3, 300, 1024, seed=210, dout="f32")
+    N, pitch = c["N"], c["bq"].size(1)
+    store = torch.zeros(N, pitch + 4, dtype=torch.uint8)
+    store[:, 2:2 + pitch] = c["bq"]
+    view = store.cuda()[:, 2:2 + pitch]
+    C = torch.full((c["M"], N), float("nan"), dtype=torch.float32, device="cuda")
+    with G.Gemm(0, sync_check=1) as g:
+        n0 = g.launches
+        st = G.gemm_run_q4_0(g.h, c["M"], N, c["K"], c["A"].cuda().data_ptr(), c["K"], 0, view.data_ptr(),
+                             pitch + 4, C.data_ptr(), N, 2, 1.0, 0.0, None, torch.cuda.current_stream().cuda_stream)
+        assert st == G.GEMM_OK, g.last_error()
+        assert g.last_plan()["gemv"] == 1 and g.launches - n0 == 1
+    torch.cuda.synchronize()
+    _check(c, C)
+
+
+def test_small_m_integers_exact():
+    """d = 1, small-integer activations: every product and f32 partial sum is an exact integer."""
+    _need_gpu()
+    M, N, K = 8, 333, 2048
+    A = W.small_ints(M, K, "f16", 19)
+    g0 = torch.Generator().manual_seed(20)
+    q = torch.randint(0, 256, (N, K // 32, 16), generator=g0, dtype=torch.int64).to(torch.uint8)
+    blocks = torch.zeros(N, K // 32, 18, dtype=torch.uint8)
+    blocks[:, :, 0], blocks[:, :, 1] = 0x00, 0x3C
+    blocks[:, :, 2:] = q
+    bq = blocks.reshape(N, -1)
+    Wint = oracle.q4_0_to_f16(bq.numpy(), N, K).view(np.float16).astype(np.int64)
+    ref = torch.from_numpy(A.to(torch.int64).numpy() @ Wint.T).to(torch.float32)
+    C = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    with G.Gemm(0, sync_check=1) as g:
+        g.run_q4_0(A.cuda(), bq.cuda(), C, N=N)
+        assert g.last_plan()["gemv"] == 1
+    torch.cuda.synchronize()
+    assert torch.equal(C.cpu(), ref)
+
+
+def test_small_m_special_blocks():
+    _need_gpu()
+    K = 128
+    bq = _special_block_rows(K)
+    A = (torch.rand(4, K, generator=torch.Generator().manual_seed(21), dtype=torch.float64) * 2 - 1).half()
+    c = dict(M=4, N=bq.size(0), K=K, A=A, bq=bq, bias=None, Cin=None, dout="f32", layoutA="row", alpha=1.0,
+             beta=0.0)
+    with G.Gemm(0, sync_check=1) as g:
+        C = _run(g, c)
+        assert g.last_plan()["gemv"] == 1
+    _check(c, C)
+
+
+def test_small_m_column_major_a_takes_the_fused_kernel():
+    """The CUDA-core kernel wants row-major activations; a column-major A goes to the fused kernel."""
+    _need_gpu()
+    c = _case(4, 300, 512, seed=220, dout="f32", layoutA="col")
+    with G.Gemm(0, sync_check=1) as g:
+        C = _run(g, c)
+        assert g.last_plan()["gemv"] == 0 and g.last_plan()["config"] == Q4_CONFIG
+    _check(c, C)
+
+
+# ------------------------------------------------------------------ separate pass + f16 GEMM
+def test_separate_pass_route_chosen_for_the_prefill_shape():
+    _need_gpu()
+    c = _case(2048, 11008, 4096, seed=230, dout="bf16", bias=True)
+    with G.Gemm(0, sync_check=1) as g:
+        n0 = g.launches
+        C = _run(g, c)
+        plan = g.last_plan()
+        assert plan["q4_dequant"] == 1 and plan["config"] != Q4_CONFIG and g.launches - n0 == 2
+    _check(c, C, rows=sample_indices(2048, 24, 3, 256))
+    _check(c, C, cols=sample_indices(11008, 24, 4, 256))
+
+
+@pytest.mark.parametrize("cfg", [1, 5])
+def test_separate_pass_equals_plain_gemm_on_dequantised_weights(cfg):
+    """A config without Q4_0 weights asks for the separate pass: the result is the plain GEMM on the
+    dequantised weights with that config, bit for bit."""
+    _need_gpu()
+    c = _case(700, 900, 1024, seed=240, dout="f32", bias=True, alpha=0.75, beta=0.5)
+    with G.Gemm(0, sync_check=1, config=cfg) as g:
+        C1 = _run(g, c)
+        assert g.last_plan()["q4_dequant"] == 1 and g.last_plan()["config"] == cfg
+    Wd = torch.empty(c["N"], c["K"], dtype=torch.float16, device="cuda")
+    bq = c["bq"].cuda()
+    assert G.gemm_dequant_q4_0(bq.data_ptr(), bq.size(1), c["N"], c["K"], Wd.data_ptr(), c["K"], None) == 0
+    C2 = c["Cin"].cuda().clone()
+    with G.Gemm(0, sync_check=1, config=cfg) as g:
+        g.run(c["A"].cuda(), Wd, C2, layoutB="col", bias=c["bias"].cuda(), alpha=c["alpha"], beta=c["beta"])
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+    _check(c, C1)
