@@ -301,7 +301,10 @@ cudaError_t launch_q4_out(const GemvParams& p, int blocks, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_gemv_q4_0(int out, const GemvParams& p, cudaStream_t stream) {
+cudaError_t gemv_prepare() { return cudaSuccess; }   // the small-M kernels use static shared memory only
+
+cudaError_t launch_gemv_q4_0(int out, const GemvParams& p, int num_sms, cudaStream_t stream) {
+    (void)num_sms;
     if (p.M < 1 || p.M > kGemvMaxM || p.N <= 0 || p.K <= 0 || p.K % 32 != 0 || p.ldw_bytes % 2 != 0 ||
         p.ldw_bytes < p.K / 32 * 18 || (reinterpret_cast<uintptr_t>(p.W) & 1u) != 0 || p.lda_bytes % 16 != 0 ||
         (reinterpret_cast<uintptr_t>(p.A) & 15u) != 0)

@@ -290,6 +290,9 @@ GEMV_CASES = [
     dict(M=7, N=130, K=4128, dout="bf16", ldbq=2330),                       # pitch 2 mod 4: rows alternate alignment
     dict(M=8, N=515, K=2048, dout="f32", bias=True, alpha=2.0, beta=-1.0),
     dict(M=4, N=64, K=640, dout="f16", layoutA="row"),
+    dict(M=1, N=3, K=8192, dout="f32"),                                     # two pieces per row, few rows
+    dict(M=2, N=2000, K=4096, dout="f16", ldbq=2320, bias=True),            # padded 16-byte pitch
+    dict(M=6, N=777, K=12288, dout="bf16", alpha=0.25, beta=0.5),
 ]
 
 

@@ -119,7 +119,18 @@ GEMV_CASES = [
     dict(M=8, N=4096, K=4096, dtype_out="f16", bias=True),
     dict(M=8, N=11008, K=4096, dtype_out="bf16", dtype_in="bf16"),
     dict(M=7, N=65, K=16384, dtype_out="f32"),                               # long K
+    dict(M=4, N=151, K=1032, dtype_out="f16", bias=True),                    # fewer rows than SMs, K = 1024 + 8
+    dict(M=1, N=20000, K=520, dtype_out="bf16", dtype_in="bf16"),           # many short rows per CTA
 ]
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 4096), (3, 2, 8), (8, 17, 5000), (2, 5, 1024)])
+def test_small_m_forced_tiny_n(M, N, K):
+    """skinny 2 takes the CUDA-core kernel for any N: a row's pieces spread over many warps."""
+    _need_gpu()
+    w = W.problem(M, N, K, dtype_out="f32", layoutB="col", bias=True, seed=850 + M + N)
+    plan, _ = _check(w, skinny=2)
+    assert plan["gemv"] == 1
 
 
 @pytest.mark.parametrize("i", range(len(GEMV_CASES)))
