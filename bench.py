@@ -67,26 +67,32 @@ def _peaks() -> tuple[dict, str]:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def _kernel_hash() -> str:
-    """Hash of the GEMM kernel's own sources (the kernel template, its PTX wrappers, its TUs)."""
+def _kernel_hash(kernel: str = "gb300::gemm_tc_kernel") -> str:
+    """Hash of one kernel's own sources: the tensor-core kernel (its template, PTX wrappers and
+    TUs) or the small-M CUDA-core kernels (their file and the helpers they include)."""
     h = hashlib.sha256()
     csrc = ROOT / "bf16_tensor_core_gb300" / "csrc"
-    for f in [csrc / "gemm_kernel.cuh", csrc / "ptx_sm103.cuh", *sorted(csrc.glob("gemm_cfg*.cu"))]:
+    if kernel.startswith("gb300::gemv"):
+        files = [csrc / "gemm_gemv.cu", csrc / "gemm_kernel.cuh", csrc / "ptx_sm103.cuh"]
+    else:
+        files = [csrc / "gemm_kernel.cuh", csrc / "ptx_sm103.cuh", *sorted(csrc.glob("gemm_cfg*.cu"))]
+    for f in files:
         h.update(f.name.encode())
         h.update(f.read_bytes())
     return h.hexdigest()[:16]
 
 
-def _traffic(workload_name: str):
-    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+def _traffic(workload_name: str, kernel: str, config: int):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if it was
+    taken on that kernel and config with the current sources (else None)."""
     p = ROOT / "profiles" / "traffic.json"
     if not p.exists():
         return None, None
     try:
         d = json.loads(p.read_text())
         e = d.get(workload_name)
-        if e and e.get("kernel_hash") == _kernel_hash():
+        if (e and e.get("kernel") == kernel and e.get("config", -1) == config
+                and e.get("kernel_hash") == _kernel_hash(kernel)):
             return e.get("dram_bytes_per_launch"), e.get("source")
     except Exception:
         pass
@@ -462,13 +468,13 @@ def run_ours(args, rank, world, local):
         peak_note = "cuBLAS bf16 burst x 2 (nominal dense FP8 / bf16 rate 4.5 / 2.25 PFLOP/s)"
     hbm = float(peaks.get("hbm_gbs", 6800.0))
     achieved = w.flops / (ms_per_step / 1e3) / 1e12
-    traffic, traffic_src = _traffic(w.name)
     n_sms = torch.cuda.get_device_properties(local).multi_processor_count
     alg_bytes = algorithmic_bytes(w)
     if plan.get("gemv"):
         kernel = "gb300::gemv_q4_0_kernel" if w.layoutB == "q4_0" else "gb300::gemv_kernel"
     else:
         kernel = "gb300::gemm_tc_kernel"
+    traffic, traffic_src = _traffic(w.name, kernel, plan.get("config", -1))
     if w.flops / alg_bytes < peak * 1e12 / (hbm * 1e9):      # below the ridge: the stream of bytes bounds it
         gbs = alg_bytes / (ms_per_step / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": traffic,

@@ -121,11 +121,66 @@ __global__ void __launch_bounds__(256) dequant_q4_0_kernel(const uint8_t* __rest
     }
 }
 
+// The same pass for 16-byte aligned rows and output (the common case): warp w takes 32 consecutive
+// blocks of one row at a time (576 bytes in, 2 KB out).  The input arrives with 16-byte loads into
+// shared memory, lane l dequantises block l there (f16 1024 + q, minus 1032, times d: one rounding,
+// the same value as above), and the 2 KB leave as 16-byte stores that cover it contiguously.
+constexpr int kDqWarpsPerCta = 8;
+constexpr int kDqStagePitch = 80;     // bytes per block in the staging buffer (64 + 16: no bank conflicts)
+
+__global__ void __launch_bounds__(kDqWarpsPerCta * 32) dequant_q4_0_rows_kernel(const uint8_t* __restrict__ bq,
+                                                                                 long long ldbq, long long N,
+                                                                                 int nblocks, __half* __restrict__ out,
+                                                                                 long long ldo) {
+    __shared__ __align__(16) uint8_t raw[kDqWarpsPerCta][576];
+    __shared__ __align__(16) uint8_t stage[kDqWarpsPerCta][32 * kDqStagePitch];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gpr = (nblocks + 31) / 32;                    // groups of 32 blocks per row
+    const long long groups = N * gpr;
+    const uint32_t raw_s = static_cast<uint32_t>(__cvta_generic_to_shared(raw[warp]));
+    for (long long g = static_cast<long long>(blockIdx.x) * kDqWarpsPerCta + warp; g < groups;
+         g += static_cast<long long>(gridDim.x) * kDqWarpsPerCta) {
+        const long long n = g / gpr;
+        const int b0 = static_cast<int>(g - n * gpr) * 32;
+        const int nb = min(32, nblocks - b0);
+        const uint8_t* src = bq + n * ldbq + 18LL * b0;
+        const int bytes = 18 * nb;
+        const int full = bytes & ~15;
+        for (int off = 16 * lane; off < full; off += 512)
+            *reinterpret_cast<uint4*>(&raw[warp][off]) = __ldg(reinterpret_cast<const uint4*>(src + off));
+        for (int off = full + 2 * lane; off < bytes; off += 64)
+            *reinterpret_cast<uint16_t*>(&raw[warp][off]) = __ldg(reinterpret_cast<const uint16_t*>(src + off));
+        __syncwarp();
+        if (lane < nb) {
+            uint32_t v[16];
+            q4_block_weights(q4_block_shared(raw_s, lane), v);
+            uint4* st = reinterpret_cast<uint4*>(&stage[warp][lane * kDqStagePitch]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) st[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+        __syncwarp();
+        uint4* dst = reinterpret_cast<uint4*>(out + n * ldo + 32LL * b0);
+        for (int i = lane; i < 4 * nb; i += 32)
+            dst[i] = *reinterpret_cast<const uint4*>(&stage[warp][(i >> 2) * kDqStagePitch + (i & 3) * 16]);
+        __syncwarp();
+    }
+}
+
 cudaError_t launch_dequant_q4_0(const void* bq, long long ldbq, long long N, long long K, void* out, long long ldo,
                                 int num_sms, cudaStream_t stream) {
     const long long nblocks = K / 32;
     const long long total = N * nblocks;
     if (total <= 0) return cudaSuccess;
+    if ((reinterpret_cast<uintptr_t>(bq) & 15u) == 0 && ldbq % 16 == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0 &&
+        ldo % 8 == 0 && nblocks < (1LL << 30)) {
+        const long long groups = N * ((nblocks + 31) / 32);
+        long long ctas = (groups + kDqWarpsPerCta - 1) / kDqWarpsPerCta;
+        const long long cap = static_cast<long long>(num_sms > 0 ? num_sms : 152) * 8;
+        if (ctas > cap) ctas = cap;
+        dequant_q4_0_rows_kernel<<<static_cast<unsigned>(ctas), kDqWarpsPerCta * 32, 0, stream>>>(
+            static_cast<const uint8_t*>(bq), ldbq, N, static_cast<int>(nblocks), static_cast<__half*>(out), ldo);
+        return cudaGetLastError();
+    }
     long long blocks = (total + 255) / 256;
     const long long cap = static_cast<long long>(num_sms > 0 ? num_sms : 152) * 8;
     if (blocks > cap) blocks = cap;

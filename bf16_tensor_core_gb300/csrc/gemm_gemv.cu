@@ -46,13 +46,6 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
     return v;
 }
 
-// Read-only loads that stay in L1: the five loads of one 18-byte block (and of the warp's 576
-// contiguous bytes) hit the same lines.
-__device__ __forceinline__ uint32_t ldg_nc_u32(const uint32_t* p) { return __ldg(p); }
-__device__ __forceinline__ uint32_t ldg_nc_u16(const uint8_t* p) {
-    return __ldg(reinterpret_cast<const unsigned short*>(p));
-}
-
 // The f32 epilogue of element (m, n): alpha * s + beta * C_in + bias, rounded to the output type.
 template <int kOut>
 __device__ __forceinline__ void store_gemv_out(const GemvParams& p, int m, int n, float s) {
@@ -167,48 +160,6 @@ cudaError_t launch_out(const GemvParams& p, bool bf16, int blocks, cudaStream_t 
 constexpr int kQ4Rows = 4;           // weight rows per CTA
 constexpr int kQ4Threads = 128;      // threads per CTA (they split the blocks of a row)
 
-// One 18-byte block at byte address b (2-byte aligned): the scale bits and the 16 nibble bytes as
-// four words.  The loads are 4-byte ones placed by the block's alignment.
-struct Q4Block {
-    uint32_t d;
-    uint32_t q[4];
-};
-
-__device__ __forceinline__ Q4Block q4_block_load(const uint8_t* b) {
-    Q4Block r;
-    if ((reinterpret_cast<uintptr_t>(b) & 2u) == 0) {
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(b);
-        const uint32_t w0 = ldg_nc_u32(w), w1 = ldg_nc_u32(w + 1), w2 = ldg_nc_u32(w + 2), w3 = ldg_nc_u32(w + 3);
-        const uint32_t w4 = ldg_nc_u16(b + 16);
-        r.d = w0 & 0xffffu;
-        r.q[0] = __byte_perm(w0, w1, 0x5432u);
-        r.q[1] = __byte_perm(w1, w2, 0x5432u);
-        r.q[2] = __byte_perm(w2, w3, 0x5432u);
-        r.q[3] = __byte_perm(w3, w4, 0x5432u);
-    } else {
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(b + 2);
-        r.d = ldg_nc_u16(b);
-        r.q[0] = ldg_nc_u32(w);
-        r.q[1] = ldg_nc_u32(w + 1);
-        r.q[2] = ldg_nc_u32(w + 2);
-        r.q[3] = ldg_nc_u32(w + 3);
-    }
-    return r;
-}
-
-// The block's 32 weights as f16 pairs: word j holds weights 2j (low half) and 2j + 1.
-__device__ __forceinline__ void q4_block_weights(const Q4Block& b, uint32_t (&v)[16]) {
-    const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(b.d)));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t hi = b.q[i] >> 4;
-        v[2 * i] = q4_two(__byte_perm(b.q[i], 0u, 0x4140u), d2);
-        v[2 * i + 1] = q4_two(__byte_perm(b.q[i], 0u, 0x4342u), d2);
-        v[8 + 2 * i] = q4_two(__byte_perm(hi, 0u, 0x4140u), d2);
-        v[8 + 2 * i + 1] = q4_two(__byte_perm(hi, 0u, 0x4342u), d2);
-    }
-}
-
 // acc + a.lo * w.lo + a.hi * w.hi, each product exact (two f16 values) and each sum rounded in f32.
 __device__ __forceinline__ float fma2_f16_f32(uint32_t a2, uint32_t w2, float acc) {
     asm("{\n\t.reg .b16 al, ah, wl, wh;\n\t"
@@ -239,7 +190,7 @@ __global__ void __launch_bounds__(kQ4Threads) gemv_q4_0_kernel(GemvParams p) {
         Q4Block raw[kQ4Rows];
 #pragma unroll
         for (int r = 0; r < kQ4Rows; ++r) {
-            if (n0 + r < p.N) raw[r] = q4_block_load(Bq + static_cast<long long>(n0 + r) * p.ldw_bytes + 18LL * b);
+            if (n0 + r < p.N) raw[r] = q4_block_global(Bq + static_cast<long long>(n0 + r) * p.ldw_bytes + 18LL * b);
             else raw[r] = Q4Block{0u, {0u, 0u, 0u, 0u}};
         }
         uint32_t w[kQ4Rows][16];

@@ -39,7 +39,8 @@ def _special_block_rows(K):
 
 # ------------------------------------------------------------------ separate dequantisation
 @pytest.mark.parametrize("N,K,ldbq,ldo", [(7, 64, None, None), (70, 256, 148, 260), (33, 1024, None, 1025),
-                                          (300, 4096, None, None)])
+                                          (300, 4096, None, None), (45, 1056, 608, 1064), (3, 32, 32, 40),
+                                          (129, 8192, 4624, None)])
 def test_dequant_bit_exact(N, K, ldbq, ldo):
     _need_gpu()
     bq = _blocks(N, K, seed=N + K, ldbq=ldbq)
