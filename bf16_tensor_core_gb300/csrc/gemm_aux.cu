@@ -10,6 +10,7 @@
 
 #include "gemm_kernel.cuh"
 #include "gemm_launch.h"
+#include "q4_block.cuh"
 
 namespace gb300 {
 
