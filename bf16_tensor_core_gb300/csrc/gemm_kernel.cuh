@@ -588,8 +588,8 @@ __device__ __forceinline__ bool wait_flag_bounded(const unsigned* flag, unsigned
 // Block format ("02 . 8m/8m(2) -- Tiled wmma f16 prefill GEMM", section 3.2): an f16 scale d and
 // 16 bytes q; weight i is the low nibble of q[i], weight 16+i its high nibble, value d * (q - 8)
 // rounded to f16.  A stage covers 128 K = four blocks of each B row.  Lane l of a dequantisation
-// warp works on block l % 4 of rows (l / 4) + 8 * pass, so the four lanes of a row read its 72
-// contiguous bytes together.
+// warp works on block l / 8 of rows (l % 8) + 8 * pass, so a warp's loads cover the 72 contiguous
+// stage bytes of eight rows and each 8-lane phase of its stores one K chunk of eight rows.
 constexpr int kQ4RegStages = 2;        // stages of raw blocks held in registers (loaded this many stages early)
 
 // The lane's blocks of one stage (one per pass) exactly as loaded (rows 4-byte aligned, so a block starts 0
@@ -1061,8 +1061,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // shared-memory stores, a fence, a barrier among the four warps and one arrive remain.
         static_assert(Cfg::kDqWarps * 8 * kQ4Passes == Cfg::kBNC, "every B row of the CTA has one lane group");
         const int dw = warp - 2 - Cfg::kEpiWarps;
-        const int row0 = dw * 8 * kQ4Passes + (lane >> 2);
-        const int bl = lane & 3;
+        // Lanes 8j..8j+7 take block j of eight consecutive rows: each 8-lane phase of a 16-byte
+        // shared store then covers eight rows of one K chunk, whose swizzled pieces are all distinct.
+        const int row0 = dw * 8 * kQ4Passes + (lane & 7);
+        const int bl = lane >> 3;
         // The rows of a unit change only with its tile: keep the last tile's answer.
         int memo_tile = -1, memo_n0 = 0;
         auto rows_of = [&](const Unit& uu, int (&rows)[kQ4Passes]) {
