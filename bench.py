@@ -247,8 +247,9 @@ def _cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
-def oracle_block_time(w, d, rows: int, cols: int, nthreads: int) -> tuple[float, float]:
-    """Time the oracle on the block C[0:rows, 0:cols] (full K).  Returns (seconds, flops)."""
+def oracle_block_time(w, d, rows: int, cols: int, nthreads: int, want=None) -> tuple[float, float]:
+    """Time the oracle on the block C[0:rows, 0:cols] (full K).  Returns (seconds, flops); the block
+    itself goes to want["ref"] when a dict is passed."""
     import oracle
     A = d["A"][:rows] if w.layoutA == "row" else d["A"][:, :rows].contiguous()
     B = d["B"][:, :cols].contiguous() if w.layoutB == "row" else d["B"][:cols]
@@ -258,28 +259,63 @@ def oracle_block_time(w, d, rows: int, cols: int, nthreads: int) -> tuple[float,
     la = oracle.OR_ROW if w.layoutA == "row" else oracle.OR_COL
     t0 = time.perf_counter()
     if w.layoutB == "q4_0":
-        oracle.gemm_ref_q4_0(rows, cols, w.K, A, la, d["B"][:cols].numpy(), alpha=w.alpha, beta=w.beta, Cin=Cin,
-                             dtype_cin=code[w.dtype_out], bias=bias, dtype_bias=code[w.dtype_out], nthreads=nthreads)
+        ref = oracle.gemm_ref_q4_0(rows, cols, w.K, A, la, d["B"][:cols].numpy(), alpha=w.alpha, beta=w.beta,
+                                   Cin=Cin, dtype_cin=code[w.dtype_out], bias=bias, dtype_bias=code[w.dtype_out],
+                                   nthreads=nthreads)
     else:
-        oracle.gemm_ref(rows, cols, w.K, A, la, B, oracle.OR_ROW if w.layoutB == "row" else oracle.OR_COL,
-                        code[w.dtype_in], alpha=w.alpha, beta=w.beta, Cin=Cin, dtype_cin=code[w.dtype_out],
-                        bias=bias, dtype_bias=code[w.dtype_out], nthreads=nthreads)
+        ref = oracle.gemm_ref(rows, cols, w.K, A, la, B, oracle.OR_ROW if w.layoutB == "row" else oracle.OR_COL,
+                              _oracle_code(w.dtype_in),
+                              alpha=w.alpha, beta=w.beta, Cin=Cin, dtype_cin=code[w.dtype_out], bias=bias,
+                              dtype_bias=code[w.dtype_out], nthreads=nthreads)
     dt = time.perf_counter() - t0
+    if want is not None:
+        want["ref"] = ref
     return dt, 2.0 * rows * cols * w.K
 
 
-def cpu_baseline(w, d, budget_s: float) -> dict:
+def _oracle_code(dtype: str) -> int:
+    import oracle
+    return {"f16": oracle.OR_F16, "bf16": oracle.OR_BF16, "f32": oracle.OR_F32, "e4m3": oracle.OR_E4M3,
+            "e5m2": oracle.OR_E5M2}[dtype]
+
+
+def check_rows(w, d, ref, got) -> dict:
+    """The GPU's rows 0..r-1 of C (all columns) against the oracle's, with the tests' element bound."""
+    import numpy as np
+    import torch
+
+    import oracle
+    rows = ref.shape[0]
+    got = got.to(torch.float64).numpy()
+    maxA = float(d["A"].float().abs().max()) if w.K > 0 else 0.0
+    if w.layoutB == "q4_0":
+        Wf = oracle.q4_0_to_f16(d["B"].numpy(), w.N, w.K).view(np.float16).astype(np.float64)
+        maxB = float(np.abs(Wf).max())
+    else:
+        maxB = float(d["B"].float().abs().max()) if w.K > 0 else 0.0
+    cin = d["Cin"][:rows].to(torch.float64).numpy() if (d["Cin"] is not None and w.beta != 0.0) else None
+    bias = d["bias"].to(torch.float64).numpy() if d["bias"] is not None else None
+    mag = oracle.epilogue_magnitude(ref, w.beta, cin, bias)
+    rep = oracle.check(got, ref, w.K, maxA, maxB, _oracle_code(w.dtype_out), alpha=w.alpha, epi_mag=mag)
+    return {"rows": rows, "passed": bool(rep["passed"]), "n": rep["n"], "n_bad": rep["n_bad"],
+            "max_abs_err": float(rep.get("max_abs_err", float("nan"))),
+            "worst_err_over_bound": float(rep.get("worst_ratio", float("nan")))}
+
+
+def cpu_baseline(w, d, budget_s: float, gpu_rows=None) -> dict:
     """The oracle as it stands, all host cores, on a bounded block of the workload: whole rows of C
     (all columns, full K), grown until the block takes about half the budget; when even all of C
-    takes less, the whole product is repeated to fill the budget."""
+    takes less, the whole product is repeated to fill the budget.  With gpu_rows(r) (the GPU's
+    first r rows of C from one fresh step), the same block is also checked element by element."""
     cores = _cpu_cores()
     rows, cols = min(w.M, cores), w.N
-    dt, fl = oracle_block_time(w, d, rows, cols, cores)
+    want = {}
+    dt, fl = oracle_block_time(w, d, rows, cols, cores, want)
     while dt < budget_s / 2 and rows < w.M:
         grow = max(2, int(budget_s / 2 / max(dt, 1e-3)))
         rows = min(w.M, rows * grow)
         rows = max(cores, rows - rows % cores) if rows < w.M else rows
-        dt, fl = oracle_block_time(w, d, rows, cols, cores)
+        dt, fl = oracle_block_time(w, d, rows, cols, cores, want)
     reps, total_s, total_fl = 1, dt, fl
     while total_s < budget_s / 2:
         dt, fl = oracle_block_time(w, d, rows, cols, cores)
@@ -287,8 +323,11 @@ def cpu_baseline(w, d, budget_s: float) -> dict:
     what = (f"rows 0..{rows - 1} of {w.M}" if rows < w.M else f"all {w.M} rows") + f" x all {cols} columns, full K={w.K}"
     if reps > 1:
         what += f", {reps} passes"
-    return {"value": total_fl / total_s / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{what}; {total_s:.1f} s on {cores} threads", "seconds": total_s}
+    out = {"value": total_fl / total_s / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+           "sample": f"{what}; {total_s:.1f} s on {cores} threads", "seconds": total_s}
+    if gpu_rows is not None:
+        out["check"] = check_rows(w, d, want["ref"], gpu_rows(rows))
+    return out
 
 
 def _workload(args):
@@ -592,7 +631,13 @@ def run_ours(args, rank, world, local):
                         "note": "rank 0's per-step CUDA-event times in the timed region (cold L2)"},
             "sustained": sustained}
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, d, args.cpu_seconds)
+        def gpu_rows(r):
+            if Cin_host is not None:
+                C.copy_(Cin_host.to(dev))
+            step()
+            torch.cuda.synchronize()
+            return C[:r].cpu()
+        line["cpu_baseline"] = cpu_baseline(w, d, args.cpu_seconds, gpu_rows)
     print(json.dumps(line), flush=True)
 
 
