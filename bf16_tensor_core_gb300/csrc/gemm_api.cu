@@ -51,8 +51,8 @@ const ConfigDesc kConfigs[kNumConfigs] = {
 // config's tensor-core time at 1.9 GHz, cold L2, GB300): small tiles need more operand bytes per
 // flop and are bound by the TMA load rate per SM.  Config 7 is derated for its single accumulator
 // (its epilogue does not overlap the next tile); config 8 runs at the rate of its dequantisation
-// warps (2048 x 11008 x 4096 in 288 us), not of its MMAs.
-const double kConfigEfficiency[kNumConfigs] = {0.73, 0.78, 0.40, 0.39, 0.80, 0.85, 0.84, 0.75, 0.28, 0.40,
+// warps (2048 x 11008 x 4096 in 260 us), not of its MMAs.
+const double kConfigEfficiency[kNumConfigs] = {0.73, 0.78, 0.40, 0.39, 0.80, 0.85, 0.84, 0.75, 0.31, 0.40,
                                                 0.85, 0.40, 0.40};
 
 int cluster_ctas(const ConfigDesc& d) { return d.cta_group * d.pairs; }
@@ -126,10 +126,6 @@ gemm_status_t query_device(int dev, bool force_optin_failure, DevInfo* info) {
             }
         }
         info->slots[c] = n;
-    }
-    if (gemv_prepare() != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_CUDA;
     }
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -988,10 +984,10 @@ gemm_status_t gemm_get_device_status(gemm_handle_t h, void* stream) {
     const unsigned role = (unsigned)((word >> 8) & 0xff);
     const unsigned stage = (unsigned)((word >> 16) & 0xffff);
     const unsigned tile = (unsigned)(word >> 32);
-    static const char* roles[] = {"?", "producer", "mma", "epilogue", "weight stream"};
+    static const char* roles[] = {"?", "producer", "mma", "epilogue"};
     char buf[256];
     std::snprintf(buf, sizeof(buf), "device wait expired: code %u role %s tile %u stage %u", code,
-                  roles[role < 5 ? role : 0], tile, stage);
+                  roles[role < 4 ? role : 0], tile, stage);
     h->err = buf;
     return GEMM_ERR_TIMEOUT;
 }
@@ -1031,8 +1027,7 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
             return fail(h, GEMM_ERR_UNSUPPORTED, "the CUDA-core small-M kernel does not take this product");
         DeviceGuard guard(h->device);
         if (h->faults & FAULT_LAUNCH) return fail(h, GEMM_ERR_CUDA, "kernel launch: forced failure (GEMM_TEST_FAIL=launch)");
-        GemvParams gp{A, lda * 2, B, ldb * 2, C, ldc, bias, alpha, beta, (int)M, (int)N, (int)K, h->d_status,
-                      (unsigned long long)h->opt.timeout_ms * 1000000ull};
+        GemvParams gp{A, lda * 2, B, ldb * 2, C, ldc, bias, alpha, beta, (int)M, (int)N, (int)K};
         const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
         cudaError_t e = launch_gemv(out_kind, dtype_in == GEMM_BF16, gp, h->dev.num_sms, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(h, "small-M kernel launch", e);
@@ -1135,8 +1130,7 @@ gemm_status_t gemm_run_q4_0(gemm_handle_t h, int64_t M, int64_t N, int64_t K, co
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (h->faults & FAULT_LAUNCH) return fail(h, GEMM_ERR_CUDA, "kernel launch: forced failure (GEMM_TEST_FAIL=launch)");
     if (route == Q4_GEMV) {
-        GemvParams gp{A, lda * 2, Bq, ldbq, C, ldc, bias, alpha, beta, (int)M, (int)N, (int)K, h->d_status,
-                      (unsigned long long)h->opt.timeout_ms * 1000000ull};
+        GemvParams gp{A, lda * 2, Bq, ldbq, C, ldc, bias, alpha, beta, (int)M, (int)N, (int)K};
         const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
         cudaError_t e = launch_gemv_q4_0(out_kind, gp, h->dev.num_sms, s);
         if (e != cudaSuccess) return cuda_fail(h, "Q4_0 small-M kernel launch", e);

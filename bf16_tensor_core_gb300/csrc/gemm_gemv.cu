@@ -253,8 +253,6 @@ cudaError_t launch_q4_out(const GemvParams& p, int blocks, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t gemv_prepare() { return cudaSuccess; }   // the small-M kernels use static shared memory only
-
 cudaError_t launch_gemv_q4_0(int out, const GemvParams& p, int num_sms, cudaStream_t stream) {
     (void)num_sms;
     if (p.M < 1 || p.M > kGemvMaxM || p.N <= 0 || p.K <= 0 || p.K % 32 != 0 || p.ldw_bytes % 2 != 0 ||

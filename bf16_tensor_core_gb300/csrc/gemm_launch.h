@@ -90,15 +90,11 @@ struct GemvParams {
     const void* bias;
     float alpha, beta;
     int M, N, K;             // K a multiple of 8
-    unsigned long long* status;       // device status word (unused: these kernels never wait)
-    unsigned long long timeout_ns;
 };
 cudaError_t launch_gemv(int out, bool bf16, const GemvParams& p, int num_sms, cudaStream_t stream);
 // The same with W given as Q4_0 blocks: W = the block rows (2-byte aligned), ldw_bytes = their even
 // pitch (>= K/32*18), K a multiple of 32, A f16 with a 16-byte aligned base and pitch.
 cudaError_t launch_gemv_q4_0(int out, const GemvParams& p, int num_sms, cudaStream_t stream);
-// Per-device preparation of the small-M kernels (at handle creation).
-cudaError_t gemv_prepare();
 
 // Auxiliary kernels (gemm_aux.cu).
 struct RepackJob {
