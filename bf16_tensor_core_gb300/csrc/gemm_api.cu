@@ -224,6 +224,14 @@ constexpr double kLaunchUs = 2.0;                     // prologue and pipeline f
 constexpr double kStreamKUs = 4.5;                    // measured fixed cost of a stream-K schedule (partial
                                                       // stores, flag release and acquire, the extra unit)
 constexpr int kMaxSplit = 8;                          // clusters sharing one tile (split-K)
+// Stream-K ranges start at staggered k offsets, so concurrent clusters share few operand lines in
+// L2.  Once A and B together fill most of L2 those iterations come largely from DRAM and run slower
+// than data-parallel ones.  Splitting only the partial last wave then beats splitting a wave and a
+// half (GB300, f16: 4096 x 4096 x 16384 324 vs 386 us, 4096 x 4096 x 8192 176 vs 188 us, 8192^3 625
+// vs 628 us), while 4096^3, whose operands fit, keeps the longer ranges (88 vs 92 us).  A factor of
+// 1.2 on the stream-K iterations, over the fixed stream-K cost, reproduces those choices.
+constexpr double kL2FitBytes = 80.0e6;
+constexpr double kSkIterSlowdown = 1.2;
 
 Schedule schedule(const ConfigDesc& d, double eff, int64_t M, int64_t N, int64_t K, int P, int stream_k,
                   int out_bytes, float beta) {
@@ -238,6 +246,8 @@ Schedule schedule(const ConfigDesc& d, double eff, int64_t M, int64_t N, int64_t
     best.clusters = (int)std::min<int64_t>(T, P);
     best.est_us = kLaunchUs + (double)((T + P - 1) / P) * kt * t_iter + t_epi;
     if (stream_k == 0 || kt < 2) return best;
+    const double operand_bytes = ((double)M * K + (double)K * N) * d.in_bytes;
+    const double sk_slow = operand_bytes > kL2FitBytes ? kSkIterSlowdown : 1.0;
     auto consider = [&](int C, int64_t dp_tiles) {
         const int64_t sk_iters = (T - dp_tiles) * kt;
         const int64_t base = sk_iters / C, extra = sk_iters % C;
@@ -257,12 +267,15 @@ Schedule schedule(const ConfigDesc& d, double eff, int64_t M, int64_t N, int64_t
         s.clusters = C;
         s.stream_k = 1;
         s.dp_tiles = (int)dp_tiles;
-        s.est_us = kLaunchUs + kStreamKUs + (double)(dp_tiles / C) * kt * t_iter + per * t_iter + (1 + srcs) * t_part +
-                   t_epi;
+        s.est_us = kLaunchUs + kStreamKUs + (double)(dp_tiles / C) * kt * t_iter + per * t_iter * sk_slow +
+                   (1 + srcs) * t_part + t_epi;
         if (stream_k == 1 ? (!best.stream_k || s.est_us < best.est_us) : s.est_us < best.est_us * 0.99) best = s;
     };
     if (T > P) {
-        if (T % P != 0) consider(P, (T / P - 1) * P);      // the last wave and a half split K-wise
+        if (T % P != 0) {
+            consider(P, (T / P - 1) * P);   // the last wave and a half split K-wise: long ranges, few partials
+            consider(P, (T / P) * P);       // only the partial last wave: short ranges, more partials per tile
+        }
     } else {
         for (int64_t split = 2; split <= kMaxSplit; ++split)  // fewer tiles than clusters: split K
             consider((int)std::min<int64_t>(P, T * split), 0);
