@@ -267,8 +267,11 @@ Schedule schedule(const ConfigDesc& d, double eff, int64_t M, int64_t N, int64_t
         s.clusters = C;
         s.stream_k = 1;
         s.dp_tiles = (int)dp_tiles;
-        s.est_us = kLaunchUs + kStreamKUs + (double)(dp_tiles / C) * kt * t_iter + per * t_iter * sk_slow +
-                   (1 + srcs) * t_part + t_epi;
+        // The fix-up, costed as one head reading every other part's partial.  (A clean split runs as a
+        // reduce-scatter, which moves less per SM; the planner keeps the head's cost for it, measured
+        // to choose no worse than before on the small-M and long-K shapes.)
+        const double fix = (1 + srcs) * t_part;
+        s.est_us = kLaunchUs + kStreamKUs + (double)(dp_tiles / C) * kt * t_iter + per * t_iter * sk_slow + fix + t_epi;
         if (stream_k == 1 ? (!best.stream_k || s.est_us < best.est_us) : s.est_us < best.est_us * 0.99) best = s;
     };
     if (T > P) {
@@ -556,6 +559,16 @@ struct LaunchArgs {
     int c_trans = 0;            // the product is C^T (see Problem / transpose)
 };
 
+// Whether a stream-K schedule splits every tile over the same number S of consecutive clusters with
+// equal k ranges, S dividing the config's epilogue warp count (8, or 4 with Q4_0 B): the kernel then
+// reduces the partials as a reduce-scatter (each part finishes 1/S of the tile's epilogue blocks)
+// instead of through one head per tile.
+bool rs_split(int64_t dp_tiles, int64_t clusters, int64_t tiles, int64_t k_tiles, int epi_warps) {
+    if (dp_tiles != 0 || tiles <= 0 || clusters % tiles != 0) return false;
+    const int64_t S = clusters / tiles;
+    return S >= 2 && epi_warps % S == 0 && k_tiles % S == 0;
+}
+
 // Encode the tensor maps, fill the kernel parameters and launch the planned config.
 gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char** what, cudaError_t* cuda_err) {
     const gemm_plan_t& plan = *a.plan;
@@ -665,6 +678,8 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
         p.sk_partials = a.sk_partials;
         p.sk_flags = a.sk_flags;
         p.epoch = a.epoch;
+        const int S = plan.clusters / p.num_tiles;   // whole tiles split over S clusters each: reduce-scatter
+        if (rs_split(plan.dp_tiles, plan.clusters, p.num_tiles, p.k_tiles, d->b_q4 ? 4 : 8)) p.sk_rs = S;
     }
     *what = "GEMM kernel launch";
     cudaError_t e = config_launch(plan.config, a.dout == GEMM_F32 ? OUT_F32 : (a.dout == GEMM_F16 ? OUT_F16 : OUT_BF16),

@@ -69,6 +69,13 @@ struct KernelParams {
     float* sk_partials;        // [cluster][cta rank][BN / 4][128 rows][4] f32
     unsigned* sk_flags;        // [cluster][cta rank][epilogue warp]
     unsigned epoch;            // launch counter of the handle, never 0
+    // Split K as a reduce-scatter (sk_rs = S dividing the epilogue warp count, with sk_enabled, no whole
+    // tiles and every tile split over exactly S consecutive clusters with equal k ranges): part r of a
+    // tile owns the blocks (32 rows x the warp's columns) of epilogue warps ew with ew * S / warps == r.
+    // A warp whose block another part owns writes its partial and raises its flag; an owning warp waits
+    // for the S - 1 flags of the same warp in the tile's other parts, adds their partials and stores its
+    // block of C.  So every part moves (S - 1) / S of a tile instead of one head reading all S - 1.
+    int sk_rs;
     // Q4_0 B (kernels built with kQ4): N rows of K/32 blocks of 18 bytes at pitch ldbq bytes.
     const uint8_t* bq;
     long long ldbq;
@@ -375,21 +382,23 @@ constexpr uint32_t kFixPieceBytes = 64 * 32 * 4;   // at most 64 columns x 32 ro
 constexpr int kFixBufs = 3;                        // pieces in flight per warp
 
 // Head fix-up: add the partials of `count` consecutive clusters (slots `stride` floats apart,
-// `first` already at this warp's block) into this warp's accumulator columns in TMEM, in cluster
-// order.  The head is always its cluster's last unit, so the operand ring is idle: each warp stages
-// pieces through its own kFixBufs x 8 KB of it with bulk copies, kFixBufs in flight.
+// `first` already at this warp's block; slot `hole`, if given, is skipped) into this warp's
+// accumulator columns in TMEM, in cluster order.  The head is always its cluster's last unit, so the
+// operand ring is idle: each warp stages pieces through its own kFixBufs x 8 KB of it with bulk
+// copies, kFixBufs in flight.
 template <int kCols>
 __device__ __forceinline__ bool head_fixup(uint32_t tbase, int lane, const float* first, int count, size_t stride,
                                            uint32_t region, uint32_t bar0, uint64_t timeout_ns,
-                                           const volatile int* abort_flag) {
+                                           const volatile int* abort_flag, int hole = 1 << 30) {
     constexpr int kPieceCols = kCols < 64 ? kCols : 64;
     static_assert(kPieceCols % 32 == 0 && kCols % kPieceCols == 0, "whole pieces of 32 or 64 columns");
     constexpr int kPieces = kCols / kPieceCols;
     constexpr uint32_t kPieceBytes = kPieceCols * 32 * 4;
     const int n = count * kPieces;
     auto issue = [&](int i) {
-        const int src = i / kPieces;
-        const int pc = i - src * kPieces;
+        const int j = i / kPieces;
+        const int pc = i - j * kPieces;
+        const int src = j + (j >= hole ? 1 : 0);   // sources skip slot `hole` (the caller's own)
         const uint32_t b = static_cast<uint32_t>(i % kFixBufs);
         mbar_arrive_expect_tx(bar0 + 8u * b, kPieceBytes);
         bulk_load_g2s(region + b * kFixPieceBytes, first + static_cast<size_t>(src) * stride + pc * (kPieceCols * 32),
@@ -996,7 +1005,35 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    acc * static_cast<uint32_t>(Cfg::kAccCols) + static_cast<uint32_t>(pcol0);
             float* out_part = nullptr;
-            if (u.kind == UNIT_TAIL) {
+            if (p.sk_rs > 1 && u.kind != UNIT_FULL) {
+                // Reduce-scatter split (one unit per cluster, parts of a tile in consecutive clusters).
+                const int S = p.sk_rs;
+                const int r = cluster_id % S;
+                if (ew * S / Cfg::kEpiWarps != r) {
+                    out_part = p.sk_partials + static_cast<size_t>(cluster_id) * slot_floats + warp_block;
+                } else {
+                    const int c0 = cluster_id - r;
+                    bool ready = true;
+                    for (int src = c0; src < c0 + S; ++src) {
+                        if (src == cluster_id) continue;
+                        const unsigned* flag =
+                            p.sk_flags + (static_cast<size_t>(src) * kClusterCtas + rank) * Cfg::kEpiWarps + ew;
+                        if (lane == 0 && ready) ready = wait_flag_bounded(flag, p.epoch, p.timeout_ns, abort_flag);
+                    }
+                    ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+                    if (ready) {
+                        ready = head_fixup<Cfg::kEpiCols>(
+                            tbase, lane, p.sk_partials + static_cast<size_t>(c0) * slot_floats + warp_block, S - 1,
+                            slot_floats, ring + static_cast<uint32_t>(ew) * kFixBufs * kFixPieceBytes,
+                            smem_u32(&bar_fix[ew * kFixBufs]), p.timeout_ns, abort_flag, r);
+                    }
+                    if (!ready) {
+                        if (lane == 0 && !*abort_flag)
+                            report_error<kClusterCtas>(p, ROLE_EPILOGUE, u.tile, 300 + quarter, abort_flag);
+                        break;
+                    }
+                }
+            } else if (u.kind == UNIT_TAIL) {
                 out_part = p.sk_partials + static_cast<size_t>(cluster_id) * slot_floats + warp_block;
             } else if (u.kind == UNIT_HEAD) {
                 // The rest of this tile, [k1, k_tiles), is the first unit of each following cluster
@@ -1040,7 +1077,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const uint32_t te = smem_u32(&bar_tempty[acc]);
                 if constexpr (kCtaGroup == 2) mbar_arrive_cluster(mapa_shared(te, lrank));
                 else mbar_arrive_local(te);
-                if (u.kind == UNIT_TAIL) {
+                if (out_part != nullptr) {
                     // Every lane's partial stores precede this release (warp barrier, then fence).
                     __threadfence();
                     st_release_gpu(p.sk_flags + (static_cast<size_t>(cluster_id) * kClusterCtas + rank) * Cfg::kEpiWarps + ew,

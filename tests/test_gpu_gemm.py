@@ -272,8 +272,9 @@ def test_optin_fault_fails_create(monkeypatch):
 @pytest.mark.parametrize("cfg", CONFIGS)
 def test_bounded_wait_expires_and_reports(handles, cfg):
     """The producer of cluster 0 never issues stage 3, so the MMA issuer's wait runs out after
-    200 ms; the kernel records the timeout, frees its TMEM and returns; the next call works."""
-    g = G.Gemm(0, config=cfg, timeout_ms=200, debug_skip_stage=3)
+    200 ms; the kernel records the timeout, frees its TMEM and returns; the next call works.  (No
+    split: with K split over clusters, cluster 0 might not reach stage 3.)"""
+    g = G.Gemm(0, config=cfg, timeout_ms=200, debug_skip_stage=3, stream_k=0)
     w = W.problem(256, 256, 1024, seed=21)
     d = W.generate(w)
     dd = device_inputs(d)
@@ -354,6 +355,86 @@ def _plan_for(w, cfg, sk):
                        w.N, G.DTYPE_CODES[w.dtype_in], G.DTYPE_CODES[w.dtype_out], G.LAYOUT_CODES[w.layoutA],
                        G.LAYOUT_CODES[w.layoutB], w.beta, torch.cuda.get_device_properties(0).multi_processor_count,
                        0, cfg, sk)
+
+
+# Every tile split over the same number S of consecutive clusters with equal k ranges: the partials
+# meet as a reduce-scatter, each part finishing 1/S of the tile's epilogue blocks (S = 2, 4, 8).
+RS_CASES = [
+    (9, 0, dict(M=300, N=200, K=2048, dtype_out="f16", bias=True)),                       # S = 4, ragged tiles
+    (9, 0, dict(M=1000, N=130, K=4096, dtype_out="f32", layoutB="col", alpha=0.5, beta=1.0)),   # S = 4, C_in
+    (9, 0, dict(M=520, N=264, K=1536, dtype_out="bf16", dtype_in="bf16")),                # S = 4
+    (9, 0, dict(M=1000, N=128, K=8192, dtype_out="f32", layoutB="col", beta=1.0)),        # S = 8, C_in
+    (2, 0, dict(M=256, N=256, K=4096, dtype_out="f32", bias=True, layoutA="col")),        # S = 8
+    (5, 12, dict(M=640, N=512, K=2048, dtype_out="f16", bias=True)),                      # 2-SM pairs, S = 2
+    (5, 24, dict(M=640, N=512, K=2048, dtype_out="f32", beta=1.0)),                       # 2-SM pairs, S = 4
+    (5, 0, dict(M=600, N=700, K=3000, dtype_out="bf16", dtype_in="bf16", layoutA="col")),  # S = 4, K tail
+    (12, 0, dict(M=256, N=256, K=8192, dtype_in="e4m3", layoutB="col", dtype_out="f16")),  # FP8, S = 8
+]
+
+
+def _rs_plan(w, cfg, mc):
+    st, plan = G.gemm_plan(w.M, w.N, w.K, w.K if w.layoutA == "row" else w.M, w.N if w.layoutB == "row" else w.K,
+                           w.N, G.DTYPE_CODES[w.dtype_in], G.DTYPE_CODES[w.dtype_out], G.LAYOUT_CODES[w.layoutA],
+                           G.LAYOUT_CODES[w.layoutB], w.beta, torch.cuda.get_device_properties(0).multi_processor_count,
+                           mc, cfg, 1)
+    assert st == G.GEMM_OK
+    tiles = plan.tiles_m * plan.tiles_n
+    k_tiles = -(-w.K // plan.block_k)
+    split = plan.clusters // tiles
+    assert plan.stream_k == 1 and plan.dp_tiles == 0 and plan.clusters == tiles * split
+    assert split in (2, 4, 8) and k_tiles % split == 0, (split, k_tiles)
+    return plan
+
+
+@pytest.mark.parametrize("i", range(len(RS_CASES)))
+def test_split_k_reduce_scatter_parity(i):
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    cfg, mc, c = RS_CASES[i]
+    c = dict(c)
+    w = W.problem(c.pop("M"), c.pop("N"), c.pop("K"), seed=260 + i, **c)
+    _rs_plan(w, cfg, mc)
+    with G.Gemm(0, config=cfg, stream_k=1, max_clusters=mc, sync_check=1) as g:
+        for _ in range(2):                                      # the second launch runs with the next epoch
+            _run_check(g, w)
+
+
+@pytest.mark.parametrize("cfg,mc,M,N,K", [(9, 0, 300, 200, 2048), (5, 24, 640, 512, 2048), (2, 0, 256, 256, 4096)])
+def test_split_k_reduce_scatter_integers_exact(cfg, mc, M, N, K):
+    """Small integers: every part's sum and their total are exact, in any order of addition."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    _rs_plan(W.problem(M, N, K), cfg, mc)
+    A = W.small_ints(M, K, "f16", 40 + cfg).cuda()
+    B = W.small_ints(K, N, "f16", 41 + cfg).cuda()
+    ref = (A.cpu().to(torch.int64) @ B.cpu().to(torch.int64)).to(torch.float32)
+    for sk in (1, 0):
+        C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        with G.Gemm(0, config=cfg, stream_k=sk, max_clusters=mc, sync_check=1) as g:
+            g.run(A, B, C)
+        torch.cuda.synchronize()
+        assert torch.equal(C.cpu(), ref), sk
+
+
+def test_split_k_reduce_scatter_bounded_wait():
+    """Cluster 0 (part 0 of tile 0) never receives its second stage: its MMA wait runs out, so its
+    partials are never written, and the owning warps of tile 0's other three parts give up on their
+    flags after 200 ms.  The timeout is reported and the next call works."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    w = W.problem(300, 200, 2048, dtype_out="f16", bias=True, seed=270)
+    _rs_plan(w, 9, 0)
+    d = W.generate(w)
+    dd = device_inputs(d)
+    C = alloc_c(w, d)
+    g = G.Gemm(0, config=9, stream_k=1, timeout_ms=200, debug_skip_stage=1)
+    run_gpu(g, w, dd, C)
+    st = g.status()
+    assert st == G.GEMM_ERR_TIMEOUT, G.gemm_status_string(st)
+    assert g.status() == G.GEMM_OK
+    g.close()
+    with G.Gemm(0, config=9, stream_k=1, sync_check=1) as g2:
+        _run_check(g2, w)
 
 
 @pytest.mark.parametrize("cfg", CONFIGS)

@@ -221,6 +221,19 @@ def test_fused_split_k_parity():
     _check(c, C)
 
 
+def test_fused_split_k_reduce_scatter_parity():
+    """Two tiles split four ways each (eight clusters): the four epilogue warps of a tile are shared out
+    among its parts, one each."""
+    _need_gpu()
+    c = _case(256, 512, 4096, seed=81, dout="f16", bias=True)
+    with G.Gemm(0, sync_check=1, stream_k=1, config=Q4_CONFIG, max_clusters=8) as g:
+        C = _run(g, c)
+        plan = g.last_plan()
+    assert plan["stream_k"] == 1 and plan["dp_tiles"] == 0
+    assert plan["clusters"] == 4 * plan["tiles_m"] * plan["tiles_n"] == 8
+    _check(c, C)
+
+
 def test_fused_special_blocks():
     _need_gpu()
     M, K = 256, 128
