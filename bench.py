@@ -47,6 +47,8 @@ def _args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--context-cublas", action="store_true",
+                    help="also time torch.matmul (cuBLAS) on the same inputs and protocol, as context")
     ap.add_argument("--sustained-seconds", type=float, default=4.0,
                     help="back-to-back steps (warm L2) after the timed region, to expose power or thermal limits; "
                          "0 skips them")
@@ -93,10 +95,11 @@ def _traffic(workload_name: str, kernel: str, config: int):
         return None, None
     try:
         d = json.loads(p.read_text())
-        e = d.get(workload_name)
-        if (e and e.get("kernel") == kernel and e.get("config", -1) == config
-                and e.get("kernel_hash") == _kernel_hash(kernel)):
-            return e.get("dram_bytes_per_launch"), e.get("source")
+        entries = d.get(workload_name) or []
+        for e in entries if isinstance(entries, list) else [entries]:   # one entry per kernel and config
+            if (e.get("kernel") == kernel and e.get("config", -1) == config
+                    and e.get("kernel_hash") == _kernel_hash(kernel)):
+                return e.get("dram_bytes_per_launch"), e.get("source")
     except Exception:
         pass
     return None, None
@@ -328,6 +331,42 @@ def cpu_baseline(w, d, budget_s: float, gpu_rows=None) -> dict:
     if gpu_rows is not None:
         out["check"] = check_rows(w, d, want["ref"], gpu_rows(rows))
     return out
+
+
+def cublas_context(w, A, B, bias, C, flush, steps, warmup, stream):
+    """torch.matmul / torch.addmm (cuBLAS) on the same device inputs, timed like our arm (L2 flushed,
+    CUDA events around each call).  Context only: None where torch has no single call for the product
+    (Q4_0 or 8-bit inputs, an output type other than the inputs')."""
+    import numpy as np
+    import torch
+    if w.layoutB == "q4_0" or w.dtype_in not in ("f16", "bf16") or w.dtype_out != w.dtype_in:
+        return None
+    a = A if w.layoutA == "row" else A.t()
+    b = B if w.layoutB == "row" else B.t()
+    a, b = a[: w.M, : w.K], b[: w.K, : w.N]
+    out = torch.empty(w.M, w.N, dtype=C.dtype, device=C.device)
+    cin = C[: w.M, : w.N].clone() if w.beta != 0.0 else None
+    if cin is not None:
+        call = lambda: torch.addmm(cin, a, b, beta=w.beta, alpha=w.alpha, out=out)
+    elif bias is not None:
+        call = lambda: torch.addmm(bias, a, b, alpha=w.alpha, out=out)
+    else:
+        call = lambda: torch.mm(a, b, out=out) if w.alpha == 1.0 else torch.addmm(out, a, b, beta=0.0, alpha=w.alpha, out=out)
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            flush.zero_()
+            call()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            call()
+            e1.record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+    return {"value": w.flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "call": "torch.addmm" if (cin is not None or bias is not None or w.alpha != 1.0) else "torch.mm",
+            "note": "cuBLAS through torch on the same inputs and timing protocol; context, not a baseline"}
 
 
 def _workload(args):
@@ -630,6 +669,8 @@ def run_ours(args, rank, world, local):
                         "best_value": w.flops / (float(times_ms.min()) / 1e3) / 1e12,
                         "note": "rank 0's per-step CUDA-event times in the timed region (cold L2)"},
             "sustained": sustained}
+    if args.context_cublas:
+        line["context_cublas"] = cublas_context(w, A, B, bias, C, flush, args.steps, args.warmup, stream)
     if world == 1 and not args.no_cpu_baseline:
         def gpu_rows(r):
             if Cin_host is not None:
