@@ -666,6 +666,7 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
     p.use_tma_store = use_tma_store;
     p.c_trans = a.c_trans;
     p.c_vec_ok = c_aligned ? 1 : 0;
+    p.bias_vec_ok = (a.bias != nullptr && (reinterpret_cast<uintptr_t>(a.bias) % 16) == 0) ? 1 : 0;
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
     p.debug_skip_stage = a.debug_skip_stage;

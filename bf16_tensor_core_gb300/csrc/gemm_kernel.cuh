@@ -51,6 +51,7 @@ struct KernelParams {
     int c_trans;               // the kernel computes C^T: its element (i, j) is C[j * ldc + i]; the bias is
                                // indexed by i (direct stores only)
     int c_vec_ok;              // C rows may be accessed with 16-byte vectors
+    int bias_vec_ok;           // the bias is 16-byte aligned: 32 of its values load as 16-byte vectors
     unsigned long long* status;
     unsigned long long timeout_ns;
     long long debug_skip_stage;  // test only: cluster 0's producer never issues this stage
@@ -236,6 +237,44 @@ __device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
     }
 }
 
+// v[i] += bias[col0 + i] for the columns inside C.  col0 is a multiple of 32 and the same for every lane,
+// so with a 16-byte aligned bias the 32 values arrive as broadcast 16-byte loads.
+template <int kOut>
+__device__ __forceinline__ void add_bias(const KernelParams& p, float (&v)[32], int col0) {
+    if (p.bias == nullptr) return;
+    if (!p.bias_vec_ok || col0 + 32 > p.N) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (col0 + i < p.N) v[i] += load_out<kOut>(p.bias, col0 + i);
+        return;
+    }
+    if constexpr (kOut == OUT_F32) {
+        const float4* b4 = reinterpret_cast<const float4*>(static_cast<const float*>(p.bias) + col0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 b = __ldg(b4 + j);
+            v[4 * j + 0] += b.x;
+            v[4 * j + 1] += b.y;
+            v[4 * j + 2] += b.z;
+            v[4 * j + 3] += b.w;
+        }
+    } else {
+        const uint4* b4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.bias) + col0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 b = __ldg(b4 + j);
+            const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                float lo, hi;
+                unpack2<kOut>(w[h], lo, hi);
+                v[8 * j + 2 * h] += lo;
+                v[8 * j + 2 * h + 1] += hi;
+            }
+        }
+    }
+}
+
 // v[0..31] = alpha * acc + beta * cin + bias for columns col0 .. col0+31, C_in already in registers.
 template <int kOut>
 __device__ __forceinline__ void epilogue_math_cin(const KernelParams& p, const uint32_t (&acc)[32], float (&v)[32],
@@ -248,11 +287,7 @@ __device__ __forceinline__ void epilogue_math_cin(const KernelParams& p, const u
     }
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = fmaf(p.beta, cin[i], v[i]);
-    if (p.bias != nullptr) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (col0 + i < p.N) v[i] += load_out<kOut>(p.bias, col0 + i);
-    }
+    add_bias<kOut>(p, v, col0);
 }
 
 // v[0..31] = alpha * acc + beta * C_in + bias for columns col0 .. col0+31 of `row` (kTrans: of the
@@ -303,11 +338,7 @@ __device__ __forceinline__ void epilogue_math(const KernelParams& p, const uint3
                 if (col0 + i < p.N) v[i] = fmaf(p.beta, load_out<kOut>(p.C, base + i), v[i]);
         }
     }
-    if (p.bias != nullptr) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (col0 + i < p.N) v[i] += load_out<kOut>(p.bias, col0 + i);
-    }
+    add_bias<kOut>(p, v, col0);
 }
 
 // Masked direct stores of 32 values of one row.

@@ -357,6 +357,30 @@ def _plan_for(w, cfg, sk):
                        0, cfg, sk)
 
 
+@pytest.mark.parametrize("dout,cfg", [("bf16", 5), ("f32", 9), ("f16", 2)])
+def test_bias_unaligned_matches_aligned(dout, cfg):
+    """A bias one element past a 16-byte boundary takes the scalar loads, an aligned one the 16-byte
+    vector loads; both add the same values, so C is bit-identical and matches the oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    w = W.problem(300, 520, 256, dtype_in="bf16" if dout == "bf16" else "f16", dtype_out=dout, bias=True,
+                  seed=280 + cfg)
+    d = W.generate(w)
+    dd = device_inputs(d)
+    store = torch.empty(w.N + 8, dtype=W.DTYPES[dout], device="cuda")
+    store[1:w.N + 1].copy_(dd["bias"])
+    outs = []
+    for bias in (dd["bias"], store[1:w.N + 1]):
+        C = alloc_c(w, d)
+        with G.Gemm(0, config=cfg, sync_check=1) as g:
+            g.run(dd["A"], dd["B"], C, M=w.M, N=w.N, K=w.K, bias=bias)
+        torch.cuda.synchronize()
+        rep = compare(w, d, C)
+        assert rep["passed"], rep
+        outs.append(C)
+    assert torch.equal(outs[0], outs[1])
+
+
 # Every tile split over the same number S of consecutive clusters with equal k ranges: the partials
 # meet as a reduce-scatter, each part finishing 1/S of the tile's epilogue blocks (S = 2, 4, 8).
 RS_CASES = [
