@@ -1,0 +1,72 @@
+"""Host-side logic of bench.py that needs no GPU: the algorithmic byte counts behind the roofline and
+the lookup of the committed DRAM traffic, which must be withdrawn once the kernel's sources change."""
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from bf16_tensor_core_gb300 import workloads as W  # noqa: E402
+
+
+# Least traffic of one product, worked out by hand from each workload's shapes: A and B read once,
+# C written once, C_in read when beta != 0, the bias read once (element sizes 2 for f16/bf16,
+# 4 for f32, 1 for E4M3, 18 bytes per 32 Q4_0 weights).
+@pytest.mark.parametrize("wid, want", [
+    (1, 512 * 512 * 2 * 2 + 512 * 512 * 4),                                  # 2,097,152
+    (2, 3 * 4096 * 4096 * 2),                                                 # 100,663,296
+    (3, 2048 * 4096 * 2 + 4096 * 11008 * 2 + 2048 * 11008 * 2 + 11008 * 2),  # 152,065,536
+    (4, 1000 * 2050 * 2 + 2050 * 3000 * 2 + 2 * 1000 * 3000 * 4),            # 40,400,000
+    (5, 3 * 8192 * 8192 * 2),                                                 # 402,653,184
+    (6, 2048 * 4096 * 2 + 11008 * 128 * 18 + 2048 * 11008 * 2 + 11008 * 2),
+    (7, 4096 * 2 + 4096 * 4096 * 2 + 4096 * 2),
+    (9, 2 * 4096 * 4096 + 4096 * 4096 * 2),
+    (10, 4096 * 2 + 4096 * 128 * 18 + 4096 * 2),
+])
+def test_algorithmic_bytes(wid, want):
+    assert bench.algorithmic_bytes(W.WORKLOADS[wid]) == want
+
+
+def test_algorithmic_bytes_of_the_gate_workload_match_its_flop_ratio():
+    w = W.WORKLOADS[2]
+    flops = 2 * w.M * w.N * w.K
+    assert round(flops / bench.algorithmic_bytes(w)) == 1365
+
+
+def _entries():
+    d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    for name, v in d.items():
+        for e in (v if isinstance(v, list) else [v]):
+            yield name, e
+
+
+def test_traffic_file_entries_are_complete():
+    names = {w.name for w in W.WORKLOADS.values()}
+    for name, e in _entries():
+        assert name in names, name
+        assert e["kernel"] in ("gb300::gemm_tc_kernel", "gb300::gemv_kernel", "gb300::gemv_q4_0_kernel")
+        assert e["dram_bytes_per_launch"] == e["dram_bytes_read"] + e["dram_bytes_write"]
+        assert e["gpu_time_ns"] > 0 and len(e["kernel_hash"]) == 16
+        # The capture command runs committed files only, with the clocks left alone.
+        assert "bench.py" in e["source"] and "--clock-control none" in e["source"]
+
+
+def test_traffic_is_reported_only_for_the_current_kernel_sources(monkeypatch):
+    name, e = next((n, e) for n, e in _entries() if n == "gemm_4096_f16_f16")
+    real = bench._kernel_hash
+    monkeypatch.setattr(bench, "_kernel_hash", lambda kernel="gb300::gemm_tc_kernel": e["kernel_hash"])
+    got, src = bench._traffic(name, e["kernel"], e["config"])
+    assert got == e["dram_bytes_per_launch"] and "ncu" in src
+    # Another config of the same kernel, or changed sources, has no figure.
+    assert bench._traffic(name, e["kernel"], e["config"] + 1) == (None, None)
+    monkeypatch.setattr(bench, "_kernel_hash", lambda kernel="gb300::gemm_tc_kernel": "0" * 16)
+    assert bench._traffic(name, e["kernel"], e["config"]) == (None, None)
+    monkeypatch.setattr(bench, "_kernel_hash", real)
+
+
+def test_kernel_hash_depends_on_the_kernel_family():
+    assert bench._kernel_hash("gb300::gemm_tc_kernel") != bench._kernel_hash("gb300::gemv_kernel")
+    assert bench._kernel_hash("gb300::gemv_kernel") == bench._kernel_hash("gb300::gemv_q4_0_kernel")
