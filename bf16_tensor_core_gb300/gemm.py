@@ -111,7 +111,7 @@ def load_library(path: Path | str | None = None):
 def header_functions() -> list[str]:
     """Names of the functions declared in include/gemm.h."""
     text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
-    return sorted(set(re.findall(r"\b(gemm_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(gemm_[a-z0-9_]+)\s*\(", text)))
 
 
 # ------------------------------------------------------------------ one-to-one forwarders

@@ -28,6 +28,42 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) <= exported
 
 
+def _header_prototypes():
+    """Each declared function's parameter types, parsed from include/gemm.h (comments removed)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", G.HEADER.read_text(), flags=re.S)
+    protos = {}
+    for m in re.finditer(r"\b(gemm_[a-z_0-9]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = " ".join(m.group(2).split())
+        protos[m.group(1)] = [] if params in ("", "void") else [q.strip() for q in params.split(",")]
+    return protos
+
+
+def _ctypes_kind(param: str):
+    """The ctypes type a C parameter must be marshalled as (pointers and handles as void*)."""
+    if "*" in param or param.startswith("gemm_handle_t"):
+        return "ptr"
+    if param.startswith("int64_t"):
+        return ctypes.c_int64
+    if param.startswith("float"):
+        return ctypes.c_float
+    return ctypes.c_int    # int and the enums
+
+
+def test_bindings_match_the_header(lib):
+    protos = _header_prototypes()
+    assert set(protos) == set(G.header_functions())
+    for name, params in protos.items():
+        argtypes = getattr(lib, name).argtypes
+        assert argtypes is not None and len(argtypes) == len(params), name
+        for param, t in zip(params, argtypes):
+            want = _ctypes_kind(param)
+            if want == "ptr":
+                assert t is ctypes.c_void_p or hasattr(t, "_type_") and issubclass(t, ctypes._Pointer), (name, param)
+            else:
+                assert t is want, (name, param, t)
+
+
 def test_status_strings(lib):
     for code, name in [(0, "GEMM_OK"), (1, "GEMM_ERR_INVALID_ARG"), (2, "GEMM_ERR_UNSUPPORTED"),
                        (3, "GEMM_ERR_ALIGNMENT"), (4, "GEMM_ERR_CUDA"), (5, "GEMM_ERR_TIMEOUT"),
