@@ -393,3 +393,37 @@ def test_stream_k_schedule_covers_every_k_iteration_once(T, P, KT, dp):
             if kind == "tail":
                 assert c > 0
     assert len(cover) == T * KT
+
+
+# The plan of every bench workload on a 152-SM GB300, as the measurements and profiles quote it:
+# (config, stream_k, dp_tiles, clusters, transposed, gemv, q4_dequant, kernels).
+WORKLOAD_PLANS = {
+    1: (9, 0, 0, 32, 0, 0, 0, 1),        # 512^3: 128 x 64 tiles on single SMs
+    2: (5, 1, 152, 76, 0, 0, 0, 1),      # 4096^3: two whole waves, then the wave and a half split K-wise
+    3: (5, 0, 0, 76, 0, 0, 0, 1),        # prefill bf16 + bias: data-parallel
+    4: (5, 0, 0, 48, 0, 0, 0, 2),        # ragged: both operands repacked to 16-byte pitches, then the product
+    5: (5, 1, 988, 76, 0, 0, 0, 1),      # 8192^3: only the partial last wave split
+    6: (5, 0, 0, 76, 0, 0, 1, 2),        # prefill Q4_0: the separate dequantisation pass, then config 5
+    7: (-1, 0, 0, 0, 0, 1, 0, 1),        # decode M = 1: the CUDA-core kernel
+    8: (9, 1, 0, 128, 1, 0, 0, 1),       # decode M = 64: transposed product, split-K over 128 SMs
+    9: (10, 1, 152, 76, 0, 0, 0, 1),     # 4096^3 E4M3
+    10: (-1, 0, 0, 0, 0, 1, 0, 1),       # decode M = 1 with Q4_0 weights: the CUDA-core kernel
+}
+
+
+@pytest.mark.parametrize("wid", sorted(WORKLOAD_PLANS))
+def test_bench_workload_plans(lib, wid):
+    from bf16_tensor_core_gb300 import workloads as W
+    w = W.WORKLOADS[wid]
+    la = G.LAYOUT_CODES[w.layoutA]
+    lda = w.K if w.layoutA == "row" else w.M
+    if w.layoutB == "q4_0":
+        st, p = G.gemm_plan_q4_0(w.M, w.N, w.K, lda, la, w.K // 32 * 18, w.N, G.DTYPE_CODES[w.dtype_out], beta=w.beta)
+    else:
+        ldb = w.N if w.layoutB == "row" else w.K
+        st, p = G.gemm_plan(w.M, w.N, w.K, lda, ldb, w.N, G.DTYPE_CODES[w.dtype_in], G.DTYPE_CODES[w.dtype_out],
+                            la, G.LAYOUT_CODES[w.layoutB], beta=w.beta)
+    assert st == G.GEMM_OK
+    got = (p.config, p.stream_k, p.dp_tiles, p.clusters, p.transposed, p.gemv, p.q4_dequant, p.kernels)
+    assert got == WORKLOAD_PLANS[wid], (w.name, got)
+    assert (p.repack_a, p.repack_b) == ((1, 1) if wid == 4 else (0, 0))
