@@ -70,3 +70,29 @@ def test_traffic_is_reported_only_for_the_current_kernel_sources(monkeypatch):
 def test_kernel_hash_depends_on_the_kernel_family():
     assert bench._kernel_hash("gb300::gemm_tc_kernel") != bench._kernel_hash("gb300::gemv_kernel")
     assert bench._kernel_hash("gb300::gemv_kernel") == bench._kernel_hash("gb300::gemv_q4_0_kernel")
+
+
+@pytest.mark.parametrize("wid", [1, 3, 4])
+def test_check_rows_accepts_the_rounded_oracle_and_rejects_a_planted_error(wid):
+    """The bench's in-line parity check: the oracle's own rows rounded to the output type pass; the
+    same rows with one element moved by 10 bounds, or one NaN, fail."""
+    import torch
+    w = W.WORKLOADS[wid]
+    w = W.with_changes(w, M=16, N=min(w.N, 96), K=min(w.K, 256))
+    d = W.generate(w)
+    rows = 8
+    want = {}
+    bench.oracle_block_time(w, d, rows, w.N, 2, want)
+    ref = want["ref"]
+    got = torch.from_numpy(ref.copy()).to(W.DTYPES[w.dtype_out])
+    rep = bench.check_rows(w, d, ref, got)
+    assert rep["passed"] and rep["n"] == rows * w.N and rep["n_bad"] == 0
+    # The stated bound, 1e-4 * K * max|A| * max|B| (scaled by |alpha| > 1), plus a margin of 1 for the
+    # output rounding and epilogue terms; the planted error is ten times that.
+    bound = 1e-4 * w.K * float(d["A"].float().abs().max()) * float(d["B"].float().abs().max())
+    bad = got.clone().to(torch.float64)
+    bad[3, 5] += 10.0 * (bound * max(1.0, abs(w.alpha)) + 1.0)
+    assert not bench.check_rows(w, d, ref, bad.to(W.DTYPES[w.dtype_out]))["passed"]
+    nan = got.clone()
+    nan[0, 0] = float("nan")
+    assert not bench.check_rows(w, d, ref, nan)["passed"]
