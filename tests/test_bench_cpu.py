@@ -96,3 +96,32 @@ def test_check_rows_accepts_the_rounded_oracle_and_rejects_a_planted_error(wid):
     nan = got.clone()
     nan[0, 0] = float("nan")
     assert not bench.check_rows(w, d, ref, nan)["passed"]
+
+
+def test_nvml_summary_decodes_reasons_inside_the_window():
+    s = bench.NvmlSampler.__new__(bench.NvmlSampler)     # no NVML here: fill the samples by hand
+    s.max_mhz = 2070
+    # (time, SM MHz, watts, reason bits): 0x4 software power cap, 0x8 hardware slowdown (outside the window),
+    # 0x40 hardware thermal slowdown, 0x1 idle (not a reported reason)
+    s.rows = [(0.5, 1000, 100.0, 0x8), (1.0, 2070, 900.0, 0x0), (1.5, 1900, 1390.0, 0x4), (2.0, 1800, 1300.0, 0x41),
+              (3.5, 500, 50.0, 0x8)]
+    c = s.summarize(1.0, 2.0)
+    assert c["samples"] == 3 and c["sm_mhz"] == 1900 and c["sm_max_mhz"] == 2070 and c["power_w_max"] == 1390.0
+    assert c["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert s.summarize(5.0, 6.0)["samples"] == 0
+
+
+def test_nvidia_smi_summary_reads_the_active_reasons():
+    import datetime
+    t = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    def row(sec, mhz, hw, hwt, swt, cap):
+        ts = (t + datetime.timedelta(seconds=sec)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return [ts, "0", str(mhz), "2070", "700.5", "0x0", hw, hwt, swt, cap]
+    rows = [row(0, 2070, "Not Active", "Not Active", "Not Active", "Not Active"),
+            row(1, 1500, "Not Active", "Not Active", "Not Active", "Active"),
+            row(2, 1400, "Active", "Not Active", "Not Active", "Not Active"),
+            row(9, 300, "Not Active", "Active", "Active", "Not Active")]
+    t0 = t.timestamp() - 0.5
+    c = bench.ClockSampler.summarize(rows, t0, t0 + 3.0)
+    assert c["samples"] == 3 and c["sm_mhz"] == 1500 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["hw_slowdown", "sw_power_cap"]
