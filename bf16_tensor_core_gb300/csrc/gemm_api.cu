@@ -25,37 +25,34 @@ using namespace gb300;
 namespace {
 
 // ---------------------------------------------------------------- configuration table
-template <int CG, int PAIRS, int BN, int ST, int BK, bool Q4 = false, int ELT = 2>
+template <int CG, int BN, int ST, int BK, bool Q4 = false, int ELT = 2>
 constexpr ConfigDesc make_desc(int id) {
-    return ConfigDesc{id, CG, PAIRS, BN, BK, ST, TileConfig<CG, BN, ST, BK, Q4, ELT>::kSmemBytes,
+    return ConfigDesc{id, CG, BN, BK, ST, TileConfig<CG, BN, ST, BK, Q4, ELT>::kSmemBytes,
                       TileConfig<CG, BN, ST, BK, Q4, ELT>::kThreads, Q4 ? 1 : 0, ELT};
 }
 
 const ConfigDesc kConfigs[kNumConfigs] = {
-    make_desc<1, 1, 256, 4, 64>(0),   // 1 SM, 128 x 256 tile
-    make_desc<2, 1, 256, 6, 64>(1),   // 2-SM pair, 256 x 256 tile
-    make_desc<1, 1, 128, 6, 64>(2),   // 1 SM, 128 x 128 tile
-    make_desc<2, 1, 128, 8, 64>(3),   // 2-SM pair, 256 x 128 tile
-    make_desc<2, 2, 256, 6, 64>(4),   // two 2-SM pairs sharing B by multicast, 512 x 256 tile
-    make_desc<2, 1, 256, 3, 128>(5),  // 2-SM pair, 256 x 256 tile, 128-wide K stages
-    make_desc<2, 2, 256, 3, 128>(6),  // two pairs sharing B, 512 x 256 tile, 128-wide K stages
-    make_desc<2, 1, 512, 4, 64>(7),   // 2-SM pair, 256 x 512 tile (two N=256 MMAs per K step)
-    make_desc<2, 1, 256, 3, 128, true>(8),  // as 5, B dequantised from Q4_0 blocks in shared memory
-    make_desc<1, 1, 64, 4, 128>(9),   // 1 SM, 128 x 64 tile: the short side of a transposed skinny product
-    make_desc<2, 1, 256, 3, 256, false, 1>(10),  // 8-bit inputs: 2-SM pair, 256 x 256 tile, BK 256
-    make_desc<1, 1, 64, 4, 256, false, 1>(11),   // 8-bit inputs: 1 SM, 128 x 64 tile (transposed skinny)
-    make_desc<1, 1, 128, 6, 128, false, 1>(12),  // 8-bit inputs: 1 SM, 128 x 128 tile
+    make_desc<1, 256, 4, 64>(0),   // 1 SM, 128 x 256 tile
+    make_desc<2, 256, 6, 64>(1),   // 2-SM pair, 256 x 256 tile
+    make_desc<1, 128, 6, 64>(2),   // 1 SM, 128 x 128 tile
+    make_desc<2, 128, 8, 64>(3),   // 2-SM pair, 256 x 128 tile
+    make_desc<2, 256, 3, 128>(4),  // 2-SM pair, 256 x 256 tile, 128-wide K stages
+    make_desc<2, 512, 4, 64>(5),   // 2-SM pair, 256 x 512 tile (two N=256 MMAs per K step)
+    make_desc<2, 256, 3, 128, true>(6),  // as 4, B dequantised from Q4_0 blocks in shared memory
+    make_desc<1, 64, 4, 128>(7),   // 1 SM, 128 x 64 tile: the short side of a transposed skinny product
+    make_desc<2, 256, 3, 256, false, 1>(8),  // 8-bit inputs: 2-SM pair, 256 x 256 tile, BK 256
+    make_desc<1, 64, 4, 256, false, 1>(9),   // 8-bit inputs: 1 SM, 128 x 64 tile (transposed skinny)
+    make_desc<1, 128, 6, 128, false, 1>(10), // 8-bit inputs: 1 SM, 128 x 128 tile
 };
 
 // Mainloop efficiency per config (measured k-iteration time of one long-K tile against the
 // config's tensor-core time at 1.9 GHz, cold L2, GB300): small tiles need more operand bytes per
-// flop and are bound by the TMA load rate per SM.  Config 7 is derated for its single accumulator
-// (its epilogue does not overlap the next tile); config 8 runs at the rate of its dequantisation
+// flop and are bound by the TMA load rate per SM.  Config 5 is derated for its single accumulator
+// (its epilogue does not overlap the next tile); config 6 runs at the rate of its dequantisation
 // warps (2048 x 11008 x 4096 in 260 us), not of its MMAs.
-const double kConfigEfficiency[kNumConfigs] = {0.73, 0.78, 0.40, 0.39, 0.80, 0.85, 0.84, 0.75, 0.31, 0.40,
-                                                0.85, 0.40, 0.40};
+const double kConfigEfficiency[kNumConfigs] = {0.73, 0.78, 0.40, 0.39, 0.85, 0.75, 0.31, 0.40, 0.85, 0.40, 0.40};
 
-int cluster_ctas(const ConfigDesc& d) { return d.cta_group * d.pairs; }
+int cluster_ctas(const ConfigDesc& d) { return d.cta_group; }
 int block_m(const ConfigDesc& d) { return 128 * cluster_ctas(d); }
 
 enum FaultSite { FAULT_NONE = 0, FAULT_OPTIN = 1, FAULT_TMAP = 2, FAULT_LAUNCH = 4, FAULT_ALLOC = 8 };
@@ -330,7 +327,7 @@ bool use_transposed(int skinny, int config, int64_t M, int64_t N, int b_q4) {
 
 // How gemm_run_q4_0 computes a product.
 enum Q4Route {
-    Q4_FUSED = 0,       // the tensor-core kernel with dequantisation warps (config 8)
+    Q4_FUSED = 0,       // the tensor-core kernel with dequantisation warps (config 6)
     Q4_GEMV = 1,        // the CUDA-core kernel that dequantises as it multiplies (M <= 8)
     Q4_TWO_PASS = 2,    // the separate dequantisation pass into the handle's workspace, then the f16 GEMM
 };
@@ -578,10 +575,9 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const uint64_t ib = (uint64_t)elt_bytes(a.din);
     const uint32_t ce = (uint32_t)(128 / ib);     // K elements of one 128-byte swizzle span
-    // B columns one TMA box covers: a CTA's share of one MMA's N, split once more between the
-    // pairs of a multicast cluster.
+    // B columns one TMA box covers: a CTA's share of one MMA's N.
     const int mma_n = std::min(d->block_n, 256);
-    const uint32_t b_box_n = (uint32_t)(mma_n / d->cta_group / d->pairs);
+    const uint32_t b_box_n = (uint32_t)(mma_n / d->cta_group);
     const uint32_t bk = (uint32_t)d->block_k;
     const uint32_t kchunks = bk / ce;
     const uint64_t M = (uint64_t)a.M, N = (uint64_t)a.N, K = (uint64_t)a.K;
@@ -613,13 +609,13 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
         std::memset(&tb, 0, sizeof(tb));
         st = GEMM_OK;
     } else if (a.lb == GEMM_ROW) {  // N-major
-        if (allow_3d && d->pairs == 1 && N % 64 == 0) {
+        if (allow_3d && N % 64 == 0) {
             st = tmap(tmap3d(a.B, tin, 64, K, N / 64, (uint64_t)a.ldb * 2, 128, 64, bk, b_box_n / 64), &tb);
             b_3d = st == GEMM_OK;
         }
         if (!b_3d) st = tmap(tmap2d(a.B, tin, N, K, (uint64_t)a.ldb * 2, 64, bk), &tb);
     } else {                 // K-major
-        if (allow_3d && d->pairs == 1 && d->block_n <= 256 && K % ce == 0) {
+        if (allow_3d && d->block_n <= 256 && K % ce == 0) {
             st = tmap(tmap3d(a.B, tin, ce, N, K / ce, (uint64_t)a.ldb * ib, 128, ce, b_box_n, kchunks), &tb);
             b_3d = st == GEMM_OK;
         }
@@ -807,8 +803,6 @@ const void* config_kernel(int id, int out) {
         case 8: return cfg8_kernel(out);
         case 9: return cfg9_kernel(out);
         case 10: return cfg10_kernel(out);
-        case 11: return cfg11_kernel(out);
-        case 12: return cfg12_kernel(out);
         default: return nullptr;
     }
 }
@@ -841,8 +835,6 @@ cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, c
         case 8: return cfg8_launch(out, lc, a, b, c, p);
         case 9: return cfg9_launch(out, lc, a, b, c, p);
         case 10: return cfg10_launch(out, lc, a, b, c, p);
-        case 11: return cfg11_launch(out, lc, a, b, c, p);
-        case 12: return cfg12_launch(out, lc, a, b, c, p);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -892,7 +884,6 @@ gemm_status_t gemm_config_info(int id, gemm_config_info_t* out) {
     out->stages = d->stages;
     out->smem_bytes = d->smem_bytes;
     out->threads = d->threads;
-    out->pairs = d->pairs;
     out->b_q4_0 = d->b_q4;
     out->in_bytes = d->in_bytes;
     return GEMM_OK;
@@ -907,7 +898,7 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ld
     int slots[kNumConfigs];
     for (int c = 0; c < kNumConfigs; ++c) {
         const ConfigDesc& d = kConfigs[c];
-        slots[c] = d.cta_group == 1 ? num_sms : max_clusters / d.pairs;
+        slots[c] = d.cta_group == 1 ? num_sms : max_clusters;
     }
     std::string err;
     gemm_status_t st = plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, slots, config,
@@ -1192,7 +1183,7 @@ gemm_status_t gemm_plan_q4_0(int64_t M, int64_t N, int64_t K, int64_t lda, gemm_
     int slots[kNumConfigs];
     for (int c = 0; c < kNumConfigs; ++c) {
         const ConfigDesc& d = kConfigs[c];
-        slots[c] = d.cta_group == 1 ? num_sms : max_clusters / d.pairs;
+        slots[c] = d.cta_group == 1 ? num_sms : max_clusters;
     }
     std::string err;
     Q4Route route;
@@ -1323,4 +1314,31 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     TmapFn tmap = [enc](const TmapDesc& desc, CUtensorMap* m) { return encode_tmap(enc, desc, m); };
     cudaError_t ce = cudaSuccess;
     return launch_planned(la, tmap, &what, &ce);
+}
+
+extern "C" gemm_status_t gemm_noalloc_get_device_status(void* stream) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kNoallocMaxDevices) return GEMM_ERR_UNSUPPORTED;
+    NoallocDevice& nd = g_noalloc_dev[dev];
+    std::call_once(nd.once, noalloc_setup, dev, std::ref(nd));
+    if (nd.setup_status != GEMM_OK) return nd.setup_status;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    unsigned long long word = 0;
+    if (cudaMemcpy(&word, nd.status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (word == 0) return GEMM_OK;
+    if (cudaMemset(nd.status, 0, sizeof(word)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_ERR_TIMEOUT;
 }

@@ -1,4 +1,4 @@
-// Kernel configuration 1: cta_group::2, 1 pair(s) per cluster, output tile 256 x 256, BK 64, 6-stage ring.
+// Kernel configuration 1: cta_group::2 (2-SM pair), output tile 256 x 256, BK 64, 6-stage ring.
 #include "gemm_kernel.cuh"
 #include "gemm_launch.h"
 
@@ -6,9 +6,9 @@ namespace gb300 {
 
 const void* cfg1_kernel(int out) {
     switch (out) {
-        case OUT_F16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 1, 256, 6, 64, OUT_F16>);
-        case OUT_BF16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 1, 256, 6, 64, OUT_BF16>);
-        case OUT_F32: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 1, 256, 6, 64, OUT_F32>);
+        case OUT_F16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 256, 6, 64, OUT_F16>);
+        case OUT_BF16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 256, 6, 64, OUT_BF16>);
+        case OUT_F32: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 256, 6, 64, OUT_F32>);
         default: return nullptr;
     }
 }
@@ -16,9 +16,9 @@ const void* cfg1_kernel(int out) {
 cudaError_t cfg1_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& c, const KernelParams& p) {
     switch (out) {
-        case OUT_F16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 1, 256, 6, 64, OUT_F16>, a, b, c, p);
-        case OUT_BF16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 1, 256, 6, 64, OUT_BF16>, a, b, c, p);
-        case OUT_F32: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 1, 256, 6, 64, OUT_F32>, a, b, c, p);
+        case OUT_F16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 256, 6, 64, OUT_F16>, a, b, c, p);
+        case OUT_BF16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 256, 6, 64, OUT_BF16>, a, b, c, p);
+        case OUT_F32: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 256, 6, 64, OUT_F32>, a, b, c, p);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -1,4 +1,5 @@
-// Kernel configuration 6: cta_group::2, 2 pair(s) per cluster, output tile 512 x 256, BK 128, 3-stage ring.
+// Kernel configuration 6: cta_group::2 (2-SM pair), output tile 256 x 256, BK 128, 3-stage ring,
+// B dequantised from Q4_0 blocks in shared memory.
 #include "gemm_kernel.cuh"
 #include "gemm_launch.h"
 
@@ -6,9 +7,9 @@ namespace gb300 {
 
 const void* cfg6_kernel(int out) {
     switch (out) {
-        case OUT_F16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 2, 256, 3, 128, OUT_F16>);
-        case OUT_BF16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 2, 256, 3, 128, OUT_BF16>);
-        case OUT_F32: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 2, 256, 3, 128, OUT_F32>);
+        case OUT_F16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 256, 3, 128, OUT_F16, true>);
+        case OUT_BF16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 256, 3, 128, OUT_BF16, true>);
+        case OUT_F32: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 256, 3, 128, OUT_F32, true>);
         default: return nullptr;
     }
 }
@@ -16,9 +17,9 @@ const void* cfg6_kernel(int out) {
 cudaError_t cfg6_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& c, const KernelParams& p) {
     switch (out) {
-        case OUT_F16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 2, 256, 3, 128, OUT_F16>, a, b, c, p);
-        case OUT_BF16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 2, 256, 3, 128, OUT_BF16>, a, b, c, p);
-        case OUT_F32: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 2, 256, 3, 128, OUT_F32>, a, b, c, p);
+        case OUT_F16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 256, 3, 128, OUT_F16, true>, a, b, c, p);
+        case OUT_BF16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 256, 3, 128, OUT_BF16, true>, a, b, c, p);
+        case OUT_F32: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 256, 3, 128, OUT_F32, true>, a, b, c, p);
         default: return cudaErrorInvalidValue;
     }
 }

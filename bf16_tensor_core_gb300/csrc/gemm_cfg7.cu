@@ -1,4 +1,5 @@
-// Kernel configuration 7: cta_group::2, 1 pair(s) per cluster, output tile 256 x 512, BK 64, 4-stage ring.
+// Kernel configuration 7: cta_group::1, output tile 128 x 64, BK 128, 4-stage ring
+// (the short side of a transposed skinny product).
 #include "gemm_kernel.cuh"
 #include "gemm_launch.h"
 
@@ -6,9 +7,9 @@ namespace gb300 {
 
 const void* cfg7_kernel(int out) {
     switch (out) {
-        case OUT_F16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 1, 512, 4, 64, OUT_F16>);
-        case OUT_BF16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 1, 512, 4, 64, OUT_BF16>);
-        case OUT_F32: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 1, 512, 4, 64, OUT_F32>);
+        case OUT_F16: return reinterpret_cast<const void*>(&gemm_tc_kernel<1, 64, 4, 128, OUT_F16>);
+        case OUT_BF16: return reinterpret_cast<const void*>(&gemm_tc_kernel<1, 64, 4, 128, OUT_BF16>);
+        case OUT_F32: return reinterpret_cast<const void*>(&gemm_tc_kernel<1, 64, 4, 128, OUT_F32>);
         default: return nullptr;
     }
 }
@@ -16,9 +17,9 @@ const void* cfg7_kernel(int out) {
 cudaError_t cfg7_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& c, const KernelParams& p) {
     switch (out) {
-        case OUT_F16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 1, 512, 4, 64, OUT_F16>, a, b, c, p);
-        case OUT_BF16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 1, 512, 4, 64, OUT_BF16>, a, b, c, p);
-        case OUT_F32: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 1, 512, 4, 64, OUT_F32>, a, b, c, p);
+        case OUT_F16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<1, 64, 4, 128, OUT_F16>, a, b, c, p);
+        case OUT_BF16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<1, 64, 4, 128, OUT_BF16>, a, b, c, p);
+        case OUT_F32: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<1, 64, 4, 128, OUT_F32>, a, b, c, p);
         default: return cudaErrorInvalidValue;
     }
 }

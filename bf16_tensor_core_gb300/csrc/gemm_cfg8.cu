@@ -1,5 +1,4 @@
-// Kernel configuration 8: cta_group::2, 1 pair per cluster, output tile 256 x 256, BK 128, 3-stage ring,
-// B dequantised from Q4_0 blocks in shared memory.
+// Kernel configuration 8: cta_group::2 (2-SM pair), output tile 256 x 256, 8-bit inputs, BK 256, 3-stage ring.
 #include "gemm_kernel.cuh"
 #include "gemm_launch.h"
 
@@ -7,9 +6,9 @@ namespace gb300 {
 
 const void* cfg8_kernel(int out) {
     switch (out) {
-        case OUT_F16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 1, 256, 3, 128, OUT_F16, true>);
-        case OUT_BF16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 1, 256, 3, 128, OUT_BF16, true>);
-        case OUT_F32: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 1, 256, 3, 128, OUT_F32, true>);
+        case OUT_F16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 256, 3, 256, OUT_F16, false, 1>);
+        case OUT_BF16: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 256, 3, 256, OUT_BF16, false, 1>);
+        case OUT_F32: return reinterpret_cast<const void*>(&gemm_tc_kernel<2, 256, 3, 256, OUT_F32, false, 1>);
         default: return nullptr;
     }
 }
@@ -17,9 +16,9 @@ const void* cfg8_kernel(int out) {
 cudaError_t cfg8_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& c, const KernelParams& p) {
     switch (out) {
-        case OUT_F16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 1, 256, 3, 128, OUT_F16, true>, a, b, c, p);
-        case OUT_BF16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 1, 256, 3, 128, OUT_BF16, true>, a, b, c, p);
-        case OUT_F32: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 1, 256, 3, 128, OUT_F32, true>, a, b, c, p);
+        case OUT_F16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 256, 3, 256, OUT_F16, false, 1>, a, b, c, p);
+        case OUT_BF16: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 256, 3, 256, OUT_BF16, false, 1>, a, b, c, p);
+        case OUT_F32: return cudaLaunchKernelEx(&lc, &gemm_tc_kernel<2, 256, 3, 256, OUT_F32, false, 1>, a, b, c, p);
         default: return cudaErrorInvalidValue;
     }
 }

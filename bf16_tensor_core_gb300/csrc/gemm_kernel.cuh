@@ -754,23 +754,18 @@ struct StageWalk {
 };
 
 // ---------------------------------------------------------------- the kernel
-// kPairs == 2 (with kCtaGroup == 2): a 4-CTA cluster of two 2-SM pairs stacked along M.  Both pairs
-// need the same B columns, so each pair loads half of every B stage and multicasts it to the
-// matching CTA of the other pair: the cluster reads B from L2 once for 512 output rows.
+// kCtaGroup == 2: a cluster is one 2-SM pair; rank 0 issues the MMAs for both CTAs.
 // kQ4: B is Q4_0-quantised; dequantisation warps (after the epilogue warps) write each stage's
 // B tile into shared memory instead of the producer's TMA copies.
 // kElt == 1: 8-bit float operands (E4M3 / E5M2), both K-major, multiplied by kind::f8f6f4 MMAs.
-template <int kCtaGroup, int kPairs, int kBN, int kStages, int kBK, int kOut, bool kQ4 = false, int kElt = 2>
+template <int kCtaGroup, int kBN, int kStages, int kBK, int kOut, bool kQ4 = false, int kElt = 2>
 __global__ void __launch_bounds__(TileConfig<kCtaGroup, kBN, kStages, kBK, kQ4, kElt>::kThreads, kQ4 ? 1 : 0)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
     using Cfg = TileConfig<kCtaGroup, kBN, kStages, kBK, kQ4, kElt>;
-    static_assert(!kQ4 || kPairs == 1, "Q4_0 B is built for one 2-SM pair per cluster");
-    static_assert(kPairs == 1 || kCtaGroup == 2, "pairs of CTAs need cta_group::2");
-    static_assert(kPairs == 1 || Cfg::kNHalves == 1, "B multicast is built for one MMA per K step");
     static_assert(Cfg::kRingBytes >= Cfg::kEpiWarps * kFixBufs * static_cast<int>(kFixPieceBytes),
                   "the head fix-up stages its pieces in the operand ring");
-    constexpr int kClusterCtas = kCtaGroup * kPairs;
+    constexpr int kClusterCtas = kCtaGroup;
     constexpr int kClusterRows = Cfg::kBM * kClusterCtas;      // output rows of one cluster tile
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[kStages];
@@ -786,11 +781,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = (kClusterCtas > 1) ? cluster_ctarank() : 0u;
-    const uint32_t prank = rank & static_cast<uint32_t>(kCtaGroup - 1);   // rank within the 2-SM pair
-    const uint32_t pair = rank / kCtaGroup;                                // which pair of the cluster
-    const uint32_t lrank = rank - prank;                                   // MMA-issuing CTA of my pair
-    const uint16_t pair_mask = static_cast<uint16_t>(((1u << kCtaGroup) - 1u) << lrank);
-    const uint16_t all_mask = static_cast<uint16_t>((1u << kClusterCtas) - 1u);
+    const uint32_t prank = rank;                                           // rank within the 2-SM pair
+    const uint32_t lrank = 0;                                              // MMA-issuing CTA of the pair
     const int cluster_id = blockIdx.x / kClusterCtas;
     const int num_clusters = gridDim.x / kClusterCtas;
     const uint32_t ring = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -803,7 +795,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // The producer's arrive (with the TMA byte count), plus one arrive from the dequantisation
             // warps of every CTA of the pair when B is dequantised in shared memory.
             mbar_init(smem_u32(&bar_full[s]), 1 + (kQ4 ? kCtaGroup : 0));
-            mbar_init(smem_u32(&bar_empty[s]), kPairs);   // one commit from each pair that reads the slot
+            mbar_init(smem_u32(&bar_empty[s]), 1);        // one commit from the pair's MMA issuer
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bar_tfull[b]), 1);
@@ -840,7 +832,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 int mb, nb;
                 tile_coords(p, u.tile, mb, nb);
                 const int m0 = mb * kClusterRows + static_cast<int>(rank) * Cfg::kBM;
-                const int n0 = nb * kBN + static_cast<int>(prank) * Cfg::kBNC;   // (kNHalves == 1)
                 for (int kt = u.k0; kt < u.k1; ++kt) {
                     if (!mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, p.timeout_ns, abort_flag)) {
                         if (!*abort_flag) report_error<kClusterCtas>(p, ROLE_PRODUCER, u.tile, static_cast<int>(stage), abort_flag);
@@ -881,7 +872,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         }
                         if constexpr (kQ4) {
                             // B arrives from the dequantisation warps.
-                        } else if constexpr (kPairs == 1) {
+                        } else {
                             // For each MMA N half h the CTA holds columns
                             // [nb*BN + h*kMmaN + prank*kHalfCols, +kHalfCols).
 #pragma unroll
@@ -906,27 +897,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                             load(dh + static_cast<uint32_t>(j * Cfg::kSlabBytes), &tmB, nh + 64 * j, k0);
                                     }
                                 }
-                            }
-                        } else {
-                            // This pair loads part `pair` of the CTA's B columns and multicasts it to
-                            // the CTA with the same rank-in-pair in every pair of the cluster.
-                            constexpr int kPart = Cfg::kBNC / kPairs;     // B columns per part
-                            const uint16_t mc = static_cast<uint16_t>(((1u << prank) | (1u << (prank + 2))));
-                            const int nb0 = n0 + kPart * static_cast<int>(pair);
-                            if (!p.b_mn) {
-                                // rows [pair * kPart, +kPart) of every K chunk: box {64 K, kPart N}
-                                const uint32_t db = sb + pair * static_cast<uint32_t>(kPart * 128);
-#pragma unroll
-                                for (int c = 0; c < Cfg::kKChunks; ++c)
-                                    tma_load_2d_pair_mc(db + static_cast<uint32_t>(c * Cfg::kBChunkBytes), &tmB,
-                                                        k0 + Cfg::kKChunkElems * c, nb0, full_bar, mc);
-                            } else {
-                                // slabs [pair * kPart / 64, +kPart / 64): box {64 N, BK K}
-                                const uint32_t db = sb + pair * static_cast<uint32_t>((kPart / 64) * Cfg::kSlabBytes);
-#pragma unroll
-                                for (int j = 0; j < kPart / 64; ++j)
-                                    tma_load_2d_pair_mc(db + static_cast<uint32_t>(j * Cfg::kSlabBytes), &tmB,
-                                                        nb0 + 64 * j, k0, full_bar, mc);
                             }
                         }
                     }
@@ -993,16 +963,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             if constexpr (kElt == 1) mma_f8<kCtaGroup>(dt, ad + a_koff[k], bd + b_hoff[h] + b_koff[k], p.idesc, accum);
                             else mma_f16<kCtaGroup>(dt, ad + a_koff[k], bd + b_hoff[h] + b_koff[k], p.idesc, accum);
                         }
-                    mma_commit<kCtaGroup>(smem_u32(&bar_empty[stage]), all_mask);  // slot free in every CTA it feeds
+                    mma_commit_pair<kCtaGroup>(smem_u32(&bar_empty[stage]), 1u);  // slot free in both CTAs
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                mma_commit<kCtaGroup>(smem_u32(&bar_tfull[acc]), pair_mask);  // accumulator ready
+                mma_commit_pair<kCtaGroup>(smem_u32(&bar_tfull[acc]), 1u);  // accumulator ready
                 if (++acc == static_cast<uint32_t>(Cfg::kAccBufs)) { acc = 0; acc_phase ^= 1u; }
             }
             // Drain: every MMA this thread issued has completed once bar_drain flips.  This wait
             // ignores the abort flag (only the time limit ends it): TMEM is freed after it.
-            mma_commit<kCtaGroup>(smem_u32(&bar_drain), pair_mask);
+            mma_commit_pair<kCtaGroup>(smem_u32(&bar_drain), 1u);
             volatile int never = 0;
             mbar_wait_bounded(smem_u32(&bar_drain), 0u, p.timeout_ns, &never);
         }

@@ -11,7 +11,6 @@ struct KernelParams;
 struct ConfigDesc {
     int id;
     int cta_group;
-    int pairs;        // 2-SM pairs per cluster (2: B multicast between the pairs)
     int block_n;
     int block_k;      // K per pipeline stage (64 or 128)
     int stages;
@@ -21,7 +20,7 @@ struct ConfigDesc {
     int in_bytes;     // operand element size: 2 (f16 / bf16) or 1 (8-bit floats)
 };
 
-constexpr int kNumConfigs = 13;
+constexpr int kNumConfigs = 11;
 constexpr int kNumOut = 3;  // OUT_F16, OUT_BF16, OUT_F32
 
 // Static description of config `id` (nullptr if out of range).
@@ -59,23 +58,14 @@ cudaError_t cfg6_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap
 const void* cfg7_kernel(int out);
 cudaError_t cfg7_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& c, const KernelParams& p);
-
 const void* cfg8_kernel(int out);
 cudaError_t cfg8_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& c, const KernelParams& p);
-
 const void* cfg9_kernel(int out);
 cudaError_t cfg9_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
                         const CUtensorMap& c, const KernelParams& p);
-
 const void* cfg10_kernel(int out);
 cudaError_t cfg10_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
-                         const CUtensorMap& c, const KernelParams& p);
-const void* cfg11_kernel(int out);
-cudaError_t cfg11_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
-                         const CUtensorMap& c, const KernelParams& p);
-const void* cfg12_kernel(int out);
-cudaError_t cfg12_launch(int out, const cudaLaunchConfig_t& lc, const CUtensorMap& a, const CUtensorMap& b,
                          const CUtensorMap& c, const KernelParams& p);
 
 // Few rows of C against weights stored N x K (gemm_gemv.cu): CUDA-core kernel for M <= kGemvMaxM.

@@ -126,17 +126,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
                  : "memory");
 }
 
-// Same as tma_load_2d_pair, multicast: the box lands at the same shared-memory offset in every
-// CTA of `cta_mask`, and each destination's bytes complete on the barrier at `bar`'s offset in
-// the even (MMA-issuing) CTA of that destination's pair.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
-                                                    uint32_t bar, uint16_t cta_mask) {
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-                 ".cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;"
-                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask)
-                 : "memory");
-}
-
 // 3-D tiled loads (one box spanning several 64-element slabs of a 2-D matrix viewed in 3-D).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,
                                             uint32_t bar) {
@@ -259,17 +248,26 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
     }
 }
 
-// Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
-// kCtaGroup == 2: the arrive goes to the barrier at the same offset in every CTA of `cta_mask`.
+// Arrive once on the barrier at shared::cluster address `bar` when every tcgen05 operation this
+// thread issued so far has completed.  With cta_group::2 the barrier may sit in either CTA of the
+// pair (a mapa address for the peer); a pair that needs both CTAs signalled issues two commits.
 template <int kCtaGroup>
-__device__ __forceinline__ void mma_commit(uint32_t bar, uint16_t cta_mask = 0x3) {
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
     if constexpr (kCtaGroup == 1) {
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                      :: "r"(bar) : "memory");
     } else {
-        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-                     " [%0], %1;" :: "r"(bar), "h"(cta_mask) : "memory");
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                     :: "r"(bar) : "memory");
     }
+}
+
+// Signal the barrier at shared-memory offset `bar` in this CTA and, for a 2-SM pair, the barrier at
+// the same offset in CTA `peer` of the cluster: one plain commit each.
+template <int kCtaGroup>
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint32_t peer) {
+    mma_commit<kCtaGroup>(bar);
+    if constexpr (kCtaGroup == 2) mma_commit<kCtaGroup>(mapa_shared(bar, peer));
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives TMEM lane (base + t).

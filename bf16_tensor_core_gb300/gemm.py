@@ -33,8 +33,8 @@ class gemm_options_t(ctypes.Structure):
 class gemm_config_info_t(ctypes.Structure):
     _fields_ = [("id", ctypes.c_int), ("cta_group", ctypes.c_int), ("block_m", ctypes.c_int),
                 ("block_n", ctypes.c_int), ("block_k", ctypes.c_int), ("stages", ctypes.c_int),
-                ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int), ("pairs", ctypes.c_int),
-                ("b_q4_0", ctypes.c_int), ("in_bytes", ctypes.c_int)]
+                ("smem_bytes", ctypes.c_int), ("threads", ctypes.c_int), ("b_q4_0", ctypes.c_int),
+                ("in_bytes", ctypes.c_int)]
 
 
 class gemm_plan_t(ctypes.Structure):
@@ -99,6 +99,8 @@ def load_library(path: Path | str | None = None):
     lib.gemm_last_plan.restype = ci
     lib.gemm_run_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ci, ci, ci, ci, cf, cf, vp, vp]
     lib.gemm_run_noalloc.restype = ci
+    lib.gemm_noalloc_get_device_status.argtypes = [vp]
+    lib.gemm_noalloc_get_device_status.restype = ci
     lib.gemm_run_q4_0.argtypes = [vp, i64, i64, i64, vp, i64, ci, vp, i64, vp, i64, ci, cf, cf, vp, vp]
     lib.gemm_run_q4_0.restype = ci
     lib.gemm_dequant_q4_0.argtypes = [vp, i64, i64, i64, vp, i64, vp]
@@ -187,6 +189,10 @@ def gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, dtype_in, dtype_out, layou
                      alpha, beta, bias, stream) -> int:
     return load_library().gemm_run_noalloc(M, N, K, A, lda, B, ldb, C, ldc, dtype_in, dtype_out, layoutA,
                                            layoutB, alpha, beta, bias, stream)
+
+
+def gemm_noalloc_get_device_status(stream=None) -> int:
+    return load_library().gemm_noalloc_get_device_status(stream)
 
 
 def gemm_run_q4_0(h, M, N, K, A, lda, layoutA, Bq, ldbq, C, ldc, dtype_out, alpha, beta, bias, stream) -> int:

@@ -104,13 +104,12 @@ typedef struct {
 typedef struct {
     int id;
     int cta_group;     /* 1: one CTA per output tile; 2: a 2-SM cluster issues cta_group::2 MMAs */
-    int block_m;       /* output-tile rows (128 * cta_group * pairs)                              */
+    int block_m;       /* output-tile rows (128 * cta_group)                                      */
     int block_n;       /* output-tile columns (= MMA N)                                           */
     int block_k;       /* K elements per pipeline stage (64 = one 128-byte swizzle span)          */
     int stages;        /* depth of the shared-memory ring                                         */
     int smem_bytes;    /* dynamic shared memory per CTA                                           */
     int threads;       /* threads per CTA                                                         */
-    int pairs;         /* 2-SM pairs per cluster; 2: the pairs share B by TMA multicast           */
     int b_q4_0;        /* 1: B is Q4_0 weights dequantised in shared memory (gemm_run_q4_0 only)  */
     int in_bytes;      /* operand element size: 2 (f16 / bf16) or 1 (E4M3 / E5M2)                */
 } gemm_config_info_t;
@@ -160,7 +159,7 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
  * wmma f16 prefill GEMM (LANDED)": section 3.2 gives the block format and the separate dequant
  * pass, section 2.3 names the dequant-in-GEMM fused kernel as its successor).  One of three routes:
  *   - fused: the tensor-core kernel whose dequantisation warps write each B stage into shared
- *     memory (config 8);
+ *     memory (config 6);
  *   - small M: a CUDA-core kernel that dequantises each block in registers as it multiplies
  *     (M <= 8, A row-major with a 16-byte pitch; automatic, or the handle's skinny option 2);
  *   - separate pass: gemm_dequant_q4_0 into a workspace the handle owns (N*K*2 bytes, grown on
@@ -256,8 +255,9 @@ gemm_status_t gemm_last_plan(gemm_handle_t h, gemm_plan_t* out);
  *     contents; this call writes every byte it later reads, so nothing has to start at zero.
  *     Calls whose work overlaps on the GPU (for example on two streams) race on the scratch:
  *     order them on one stream or with events.
- *   - Errors: there is no handle, hence no gemm_last_error text; the kernels' bounded waits
- *     record into a library-internal word that this entry point does not report.
+ *   - Errors: there is no handle, hence no gemm_last_error text.  The return code covers
+ *     validation and launch only: a bounded device wait that expires later records into a
+ *     library-internal word per device, which gemm_noalloc_get_device_status reads and clears.
  */
 gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K,
                                const void* A, int64_t lda, const void* B, int64_t ldb,
@@ -265,6 +265,13 @@ gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K,
                                gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
                                gemm_layout_t layoutA, gemm_layout_t layoutB,
                                float alpha, float beta, const void* bias, void* stream);
+
+/* gemm_noalloc_get_device_status - synchronise `stream`, then read and clear the status word that
+ * gemm_run_noalloc's kernels write on the current device when a bounded wait expires.  Returns
+ * GEMM_OK, GEMM_ERR_TIMEOUT (a wait expired since the last read: the output of that call is
+ * incomplete) or GEMM_ERR_CUDA.  Like gemm_run_noalloc it allocates nothing; its first call on a
+ * device performs the same one-time set-up. */
+gemm_status_t gemm_noalloc_get_device_status(void* stream);
 
 #ifdef __cplusplus
 }

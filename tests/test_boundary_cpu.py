@@ -80,23 +80,21 @@ def test_options_default(lib):
 
 def test_config_table(lib):
     n = G.gemm_num_configs()
-    assert n == 13
+    assert n == 11
     seen = set()
     for i in range(n):
         st, c = G.gemm_config_info(i)
         assert st == G.GEMM_OK and c.id == i
-        assert c.block_m == 128 * c.cta_group * c.pairs and c.block_k in (64, 128, 256)
+        assert c.block_m == 128 * c.cta_group and c.block_k in (64, 128, 256)
         assert c.block_n in (64, 128, 256, 512) and c.smem_bytes <= 232448
         assert c.threads == (448 if c.b_q4_0 else 320)        # Q4_0: 8 more dequantisation warps, 4 fewer epilogue
-        assert c.pairs == 1 or c.cta_group == 2
         stage = (128 + c.block_n // c.cta_group) * c.block_k * c.in_bytes
         assert c.block_k * c.in_bytes in (128, 256)                  # one or two 128-byte swizzle spans of K
         assert c.smem_bytes >= c.stages * stage
-        seen.add((c.cta_group, c.pairs, c.block_n, c.block_k, c.b_q4_0, c.in_bytes))
-    assert seen == {(1, 1, 128, 64, 0, 2), (1, 1, 256, 64, 0, 2), (2, 1, 128, 64, 0, 2), (2, 1, 256, 64, 0, 2),
-                    (2, 2, 256, 64, 0, 2), (2, 1, 256, 128, 0, 2), (2, 2, 256, 128, 0, 2), (2, 1, 512, 64, 0, 2),
-                    (2, 1, 256, 128, 1, 2), (1, 1, 64, 128, 0, 2),
-                    (2, 1, 256, 256, 0, 1), (1, 1, 64, 256, 0, 1), (1, 1, 128, 128, 0, 1)}
+        seen.add((c.cta_group, c.block_n, c.block_k, c.b_q4_0, c.in_bytes))
+    assert seen == {(1, 128, 64, 0, 2), (1, 256, 64, 0, 2), (2, 128, 64, 0, 2), (2, 256, 64, 0, 2),
+                    (2, 256, 128, 0, 2), (2, 512, 64, 0, 2), (2, 256, 128, 1, 2), (1, 64, 128, 0, 2),
+                    (2, 256, 256, 0, 1), (1, 64, 256, 0, 1), (1, 128, 128, 0, 1)}
     assert G.gemm_config_info(n)[0] == G.GEMM_ERR_UNSUPPORTED
 
 
@@ -131,7 +129,7 @@ def plan(M, N, K, lda=None, ldb=None, ldc=None, din=0, dout=2, la=0, lb=0, beta=
     (dict(M=4, N=9, K=8, lb=1, ldb=7), G.GEMM_ERR_INVALID_ARG),  # ldb < K for B stored N x K
     (dict(M=4, N=9, K=8, ldc=8), G.GEMM_ERR_INVALID_ARG),
     (dict(M=2 ** 31, N=4, K=4), G.GEMM_ERR_INVALID_ARG),
-    (dict(M=4, N=4, K=4, config=13), G.GEMM_ERR_UNSUPPORTED),
+    (dict(M=4, N=4, K=4, config=11), G.GEMM_ERR_UNSUPPORTED),
     (dict(M=4, N=4, K=4, sms=0), G.GEMM_ERR_INVALID_ARG),
     (dict(M=4, N=4, K=4), G.GEMM_OK),
 ])
@@ -151,12 +149,12 @@ def test_plan_degenerate(lib):
 
 def test_q4_0_config_is_not_a_plain_gemm_config(lib):
     q4 = [i for i in range(G.gemm_num_configs()) if G.gemm_config_info(i)[1].b_q4_0]
-    assert q4 == [8]
-    st, p = plan(4096, 4096, 4096, dout=0, config=8)       # f16 B cannot use the Q4_0 kernel
+    assert q4 == [6]
+    st, p = plan(4096, 4096, 4096, dout=0, config=6)       # f16 B cannot use the Q4_0 kernel
     assert st == G.GEMM_ERR_UNSUPPORTED
     for shape in [(512, 512, 512), (4096, 4096, 4096), (64, 4096, 4096), (1000, 3000, 2048)]:
         st, p = plan(*shape, dout=0)
-        assert st == G.GEMM_OK and p.config != 8
+        assert st == G.GEMM_OK and p.config != 6
 
 
 def plan_q4(M, N, K, *, lda=None, la=0, ldbq=None, dout=2, config=-1, sk=-1, sms=152):
@@ -173,23 +171,23 @@ def test_q4_0_routes(lib):
         st, p = plan_q4(M, 4096, 4096)
         assert st == G.GEMM_OK and p.gemv == 1 and p.q4_dequant == 0 and p.config == -1 and p.kernels == 1
     st, p = plan_q4(4, 4096, 4096, la=1)                   # column-major A: not the CUDA-core kernel
-    assert st == G.GEMM_OK and p.gemv == 0 and p.config == 8
+    assert st == G.GEMM_OK and p.gemv == 0 and p.config == 6
     for M in (9, 64, 256):
         st, p = plan_q4(M, 11008, 4096)
-        assert st == G.GEMM_OK and p.gemv == 0 and p.q4_dequant == 0 and p.config == 8 and p.kernels == 1
+        assert st == G.GEMM_OK and p.gemv == 0 and p.q4_dequant == 0 and p.config == 6 and p.kernels == 1
     for M in (1024, 2048, 8192):
         st, p = plan_q4(M, 11008, 4096, dout=1)
-        assert st == G.GEMM_OK and p.q4_dequant == 1 and p.config not in (-1, 8) and p.kernels == 2
+        assert st == G.GEMM_OK and p.q4_dequant == 1 and p.config not in (-1, 6) and p.kernels == 2
         assert p.workspace_bytes >= 11008 * 4096 * 2
 
 
 def test_q4_0_route_by_config(lib):
-    st, p = plan_q4(2048, 11008, 4096, config=8)            # the fused kernel on request
-    assert st == G.GEMM_OK and p.config == 8 and p.q4_dequant == 0
-    st, p = plan_q4(64, 4096, 4096, config=5)               # a plain config: separate pass + that config
-    assert st == G.GEMM_OK and p.config == 5 and p.q4_dequant == 1 and p.kernels == 2
-    st, p = plan_q4(1, 4096, 4096, config=8)                # an explicit config overrides the small-M kernel
-    assert st == G.GEMM_OK and p.config == 8 and p.gemv == 0
+    st, p = plan_q4(2048, 11008, 4096, config=6)            # the fused kernel on request
+    assert st == G.GEMM_OK and p.config == 6 and p.q4_dequant == 0
+    st, p = plan_q4(64, 4096, 4096, config=4)               # a plain config: separate pass + that config
+    assert st == G.GEMM_OK and p.config == 4 and p.q4_dequant == 1 and p.kernels == 2
+    st, p = plan_q4(1, 4096, 4096, config=6)                # an explicit config overrides the small-M kernel
+    assert st == G.GEMM_OK and p.config == 6 and p.gemv == 0
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -214,7 +212,7 @@ def test_plan_few_rows_use_the_cuda_core_kernel(lib):
     assert plan(4, 4096, 4100, dout=0, lb=1)[1].gemv == 0                 # K not a multiple of 8
     assert plan(4, 4096, 4096, dout=0, lb=1, ldb=4100)[1].gemv == 0       # pitch not 16-byte aligned
     assert plan(4, 4096, 4096, din=G.GEMM_E4M3, dout=0, lb=1)[1].gemv == 0   # 8-bit inputs: tensor cores
-    assert plan(4, 4096, 4096, dout=0, lb=1, config=9)[1].gemv == 0       # a forced config
+    assert plan(4, 4096, 4096, dout=0, lb=1, config=7)[1].gemv == 0       # a forced config
 
 
 def test_plan_skinny_products_are_transposed(lib):
@@ -227,8 +225,8 @@ def test_plan_skinny_products_are_transposed(lib):
     assert p.transposed == 0
     st, p = plan(16, 64, 4096, dout=0)                    # nothing to gain with 64 columns
     assert p.transposed == 0
-    st, p = plan(16, 4096, 4096, dout=0, config=5)        # a forced config keeps the plain product
-    assert p.transposed == 0 and p.config == 5
+    st, p = plan(16, 4096, 4096, dout=0, config=4)        # a forced config keeps the plain product
+    assert p.transposed == 0 and p.config == 4
     # operand checks still refer to the caller's arrays
     st, p = plan(16, 4096, 4096, ldb=100)
     assert st == G.GEMM_ERR_INVALID_ARG
@@ -242,8 +240,8 @@ def test_plan_8bit_inputs(lib):
     assert st == G.GEMM_OK and G.gemm_config_info(p.config)[1].in_bytes == 1
     assert plan(256, 256, 256, din=E4M3, lb=0)[0] == G.GEMM_ERR_UNSUPPORTED      # B must be K-major
     assert plan(256, 256, 256, din=E4M3, la=1, lb=1)[0] == G.GEMM_ERR_UNSUPPORTED
-    assert plan(256, 256, 256, din=E4M3, lb=1, config=5)[0] == G.GEMM_ERR_UNSUPPORTED   # 16-bit config
-    assert plan(256, 256, 256, din=0, lb=1, config=10)[0] == G.GEMM_ERR_UNSUPPORTED     # 8-bit config
+    assert plan(256, 256, 256, din=E4M3, lb=1, config=4)[0] == G.GEMM_ERR_UNSUPPORTED   # 16-bit config
+    assert plan(256, 256, 256, din=0, lb=1, config=8)[0] == G.GEMM_ERR_UNSUPPORTED     # 8-bit config
     st, p = plan(300, 300, 1000, din=E4M3, lb=1, lda=1000, ldb=1000)   # 1000-byte rows: repacked as pairs
     assert st == G.GEMM_OK and p.repack_a == 1 and p.repack_b == 1
     assert plan(300, 300, 999, din=E4M3, lb=1, lda=999, ldb=999)[0] == G.GEMM_ERR_UNSUPPORTED  # odd rows
@@ -259,7 +257,7 @@ def test_plan_tiles_and_grid(lib):
         st, p = plan(4096, 4096, 4096, dout=0, config=cfg)
         assert st == G.GEMM_OK and p.config == cfg
         assert p.tiles_m == 4096 // c.block_m and p.tiles_n == 4096 // c.block_n
-        slots = 152 // (c.cta_group * c.pairs)
+        slots = 152 // c.cta_group
         assert p.clusters == min(p.tiles_m * p.tiles_n, slots)
         # f16 output: TMA stores need each epilogue warp to drain whole 128-byte rows (64 columns)
         assert p.tma_store == (1 if c.block_n // 2 >= 64 else 0) and p.kernels == 1
@@ -398,15 +396,15 @@ def test_stream_k_schedule_covers_every_k_iteration_once(T, P, KT, dp):
 # The plan of every bench workload on a 152-SM GB300, as the measurements and profiles quote it:
 # (config, stream_k, dp_tiles, clusters, transposed, gemv, q4_dequant, kernels).
 WORKLOAD_PLANS = {
-    1: (9, 0, 0, 32, 0, 0, 0, 1),        # 512^3: 128 x 64 tiles on single SMs
-    2: (5, 1, 152, 76, 0, 0, 0, 1),      # 4096^3: two whole waves, then the wave and a half split K-wise
-    3: (5, 0, 0, 76, 0, 0, 0, 1),        # prefill bf16 + bias: data-parallel
-    4: (5, 0, 0, 48, 0, 0, 0, 2),        # ragged: both operands repacked to 16-byte pitches, then the product
-    5: (5, 1, 988, 76, 0, 0, 0, 1),      # 8192^3: only the partial last wave split
-    6: (5, 0, 0, 76, 0, 0, 1, 2),        # prefill Q4_0: the separate dequantisation pass, then config 5
+    1: (7, 0, 0, 32, 0, 0, 0, 1),        # 512^3: 128 x 64 tiles on single SMs
+    2: (4, 1, 152, 76, 0, 0, 0, 1),      # 4096^3: two whole waves, then the wave and a half split K-wise
+    3: (4, 0, 0, 76, 0, 0, 0, 1),        # prefill bf16 + bias: data-parallel
+    4: (4, 0, 0, 48, 0, 0, 0, 2),        # ragged: both operands repacked to 16-byte pitches, then the product
+    5: (4, 1, 988, 76, 0, 0, 0, 1),      # 8192^3: only the partial last wave split
+    6: (4, 0, 0, 76, 0, 0, 1, 2),        # prefill Q4_0: the separate dequantisation pass, then config 4
     7: (-1, 0, 0, 0, 0, 1, 0, 1),        # decode M = 1: the CUDA-core kernel
-    8: (9, 1, 0, 128, 1, 0, 0, 1),       # decode M = 64: transposed product, split-K over 128 SMs
-    9: (10, 1, 152, 76, 0, 0, 0, 1),     # 4096^3 E4M3
+    8: (7, 1, 0, 128, 1, 0, 0, 1),       # decode M = 64: transposed product, split-K over 128 SMs
+    9: (8, 1, 152, 76, 0, 0, 0, 1),      # 4096^3 E4M3
     10: (-1, 0, 0, 0, 0, 1, 0, 1),       # decode M = 1 with Q4_0 weights: the CUDA-core kernel
 }
 

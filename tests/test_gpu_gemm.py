@@ -17,7 +17,7 @@ from gpu_cases import alloc_c, compare, device_inputs, run_gpu, sample_indices
 
 pytestmark = pytest.mark.gpu
 
-CONFIGS = [0, 1, 2, 3, 4, 5, 6, 7]
+CONFIGS = [0, 1, 2, 3, 4, 5]
 
 
 @pytest.fixture(scope="module")
@@ -294,10 +294,8 @@ SK_CASES = {
     1: dict(M=2274, N=2300, K=700, dtype_out="bf16", dtype_in="bf16"),       # 9 x 9 = 81 tiles > 76
     2: dict(M=1650, N=1640, K=200, dtype_out="f32", alpha=0.5, beta=1.0),   # 13 x 13 = 169 > 152
     3: dict(M=2250, N=1250, K=450, dtype_out="f32", layoutB="col"),         # 9 x 10 = 90 > 76
-    4: dict(M=2460, N=2274, K=576, dtype_out="f16", bias=True),               # 5 x 9 = 45 > 38
-    5: dict(M=2274, N=2300, K=700, dtype_out="f32", layoutA="col"),         # 81 tiles > 76, 6 k-tiles of 128
-    6: dict(M=2460, N=2274, K=900, dtype_out="bf16", dtype_in="bf16", layoutB="col"),   # 45 tiles > 38
-    7: dict(M=2250, N=4500, K=320, dtype_out="f16", bias=True, layoutB="col"),  # 9 x 9 = 81 tiles > 76
+    4: dict(M=2274, N=2300, K=700, dtype_out="f32", layoutA="col"),         # 81 tiles > 76, 6 k-tiles of 128
+    5: dict(M=2250, N=4500, K=320, dtype_out="f16", bias=True, layoutB="col"),  # 9 x 9 = 81 tiles > 76
 }
 
 
@@ -343,10 +341,8 @@ SPLIT_CASES = {
     1: dict(M=500, N=300, K=4100, dtype_out="bf16", dtype_in="bf16"),        # 2 x 2 tiles
     2: dict(M=250, N=250, K=2500, dtype_out="f32", alpha=0.5, beta=1.0),     # 2 x 2 tiles
     3: dict(M=700, N=250, K=1500, dtype_out="f32", layoutB="col"),           # 3 x 2 tiles
-    4: dict(M=1000, N=500, K=2100, dtype_out="f16", bias=True),              # 2 x 2 tiles on 38 clusters
-    5: dict(M=600, N=700, K=3000, dtype_out="f32", layoutA="col"),           # 3 x 3 tiles, 24 k-tiles of 128
-    6: dict(M=520, N=260, K=5000, dtype_out="bf16", dtype_in="bf16", layoutB="col"),
-    7: dict(M=300, N=1000, K=2000, dtype_out="f16", bias=True, layoutA="col"),
+    4: dict(M=600, N=700, K=3000, dtype_out="f32", layoutA="col"),           # 3 x 3 tiles, 24 k-tiles of 128
+    5: dict(M=300, N=1000, K=2000, dtype_out="f16", bias=True, layoutA="col"),
 }
 
 
@@ -357,7 +353,7 @@ def _plan_for(w, cfg, sk):
                        0, cfg, sk)
 
 
-@pytest.mark.parametrize("dout,cfg", [("bf16", 5), ("f32", 9), ("f16", 2)])
+@pytest.mark.parametrize("dout,cfg", [("bf16", 4), ("f32", 7), ("f16", 2)])
 def test_bias_unaligned_matches_aligned(dout, cfg):
     """A bias one element past a 16-byte boundary takes the scalar loads, an aligned one the 16-byte
     vector loads; both add the same values, so C is bit-identical and matches the oracle."""
@@ -384,15 +380,15 @@ def test_bias_unaligned_matches_aligned(dout, cfg):
 # Every tile split over the same number S of consecutive clusters with equal k ranges: the partials
 # meet as a reduce-scatter, each part finishing 1/S of the tile's epilogue blocks (S = 2, 4, 8).
 RS_CASES = [
-    (9, 0, dict(M=300, N=200, K=2048, dtype_out="f16", bias=True)),                       # S = 4, ragged tiles
-    (9, 0, dict(M=1000, N=130, K=4096, dtype_out="f32", layoutB="col", alpha=0.5, beta=1.0)),   # S = 4, C_in
-    (9, 0, dict(M=520, N=264, K=1536, dtype_out="bf16", dtype_in="bf16")),                # S = 4
-    (9, 0, dict(M=1000, N=128, K=8192, dtype_out="f32", layoutB="col", beta=1.0)),        # S = 8, C_in
+    (7, 0, dict(M=300, N=200, K=2048, dtype_out="f16", bias=True)),                       # S = 4, ragged tiles
+    (7, 0, dict(M=1000, N=130, K=4096, dtype_out="f32", layoutB="col", alpha=0.5, beta=1.0)),   # S = 4, C_in
+    (7, 0, dict(M=520, N=264, K=1536, dtype_out="bf16", dtype_in="bf16")),                # S = 4
+    (7, 0, dict(M=1000, N=128, K=8192, dtype_out="f32", layoutB="col", beta=1.0)),        # S = 8, C_in
     (2, 0, dict(M=256, N=256, K=4096, dtype_out="f32", bias=True, layoutA="col")),        # S = 8
-    (5, 12, dict(M=640, N=512, K=2048, dtype_out="f16", bias=True)),                      # 2-SM pairs, S = 2
-    (5, 24, dict(M=640, N=512, K=2048, dtype_out="f32", beta=1.0)),                       # 2-SM pairs, S = 4
-    (5, 0, dict(M=600, N=700, K=3000, dtype_out="bf16", dtype_in="bf16", layoutA="col")),  # S = 4, K tail
-    (12, 0, dict(M=256, N=256, K=8192, dtype_in="e4m3", layoutB="col", dtype_out="f16")),  # FP8, S = 8
+    (4, 12, dict(M=640, N=512, K=2048, dtype_out="f16", bias=True)),                      # 2-SM pairs, S = 2
+    (4, 24, dict(M=640, N=512, K=2048, dtype_out="f32", beta=1.0)),                       # 2-SM pairs, S = 4
+    (4, 0, dict(M=600, N=700, K=3000, dtype_out="bf16", dtype_in="bf16", layoutA="col")),  # S = 4, K tail
+    (10, 0, dict(M=256, N=256, K=8192, dtype_in="e4m3", layoutB="col", dtype_out="f16")),  # FP8, S = 8
 ]
 
 
@@ -423,7 +419,7 @@ def test_split_k_reduce_scatter_parity(i):
             _run_check(g, w)
 
 
-@pytest.mark.parametrize("cfg,mc,M,N,K", [(9, 0, 300, 200, 2048), (5, 24, 640, 512, 2048), (2, 0, 256, 256, 4096)])
+@pytest.mark.parametrize("cfg,mc,M,N,K", [(7, 0, 300, 200, 2048), (4, 24, 640, 512, 2048), (2, 0, 256, 256, 4096)])
 def test_split_k_reduce_scatter_integers_exact(cfg, mc, M, N, K):
     """Small integers: every part's sum and their total are exact, in any order of addition."""
     if not torch.cuda.is_available():
@@ -447,17 +443,17 @@ def test_split_k_reduce_scatter_bounded_wait():
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     w = W.problem(300, 200, 2048, dtype_out="f16", bias=True, seed=270)
-    _rs_plan(w, 9, 0)
+    _rs_plan(w, 7, 0)
     d = W.generate(w)
     dd = device_inputs(d)
     C = alloc_c(w, d)
-    g = G.Gemm(0, config=9, stream_k=1, timeout_ms=200, debug_skip_stage=1)
+    g = G.Gemm(0, config=7, stream_k=1, timeout_ms=200, debug_skip_stage=1)
     run_gpu(g, w, dd, C)
     st = g.status()
     assert st == G.GEMM_ERR_TIMEOUT, G.gemm_status_string(st)
     assert g.status() == G.GEMM_OK
     g.close()
-    with G.Gemm(0, config=9, stream_k=1, sync_check=1) as g2:
+    with G.Gemm(0, config=7, stream_k=1, sync_check=1) as g2:
         _run_check(g2, w)
 
 
@@ -479,7 +475,7 @@ def test_split_k_parity(cfg):
     assert torch.equal(outs[0], outs[1])                        # partials are added in a fixed order
 
 
-@pytest.mark.parametrize("cfg", [0, 2, 5])
+@pytest.mark.parametrize("cfg", [0, 2, 4])
 def test_split_k_matches_data_parallel_on_integers(cfg):
     """Several partial sums per tile; with small integers every schedule is exact."""
     if not torch.cuda.is_available():
@@ -503,7 +499,7 @@ def test_three_d_and_two_d_tensor_maps_agree(monkeypatch):
     one-box-per-slab 2-D path bit for bit: same data in the same shared-memory layout."""
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
-    for (la, lb, cfg) in [("row", "row", 5), ("col", "col", 1), ("row", "col", 0), ("col", "row", 5)]:
+    for (la, lb, cfg) in [("row", "row", 4), ("col", "col", 1), ("row", "col", 0), ("col", "row", 4)]:
         w = W.problem(640, 768, 512, dtype_in="bf16", dtype_out="f32", layoutA=la, layoutB=lb, bias=True,
                       seed=len(la) + 3 * len(lb) + cfg)
         d = W.generate(w)
@@ -523,7 +519,7 @@ def test_three_d_and_two_d_tensor_maps_agree(monkeypatch):
 def test_last_plan_reports_the_run():
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
-    with G.Gemm(0, config=5) as g:
+    with G.Gemm(0, config=4) as g:
         assert g.last_plan() == {}
         w = W.problem(600, 700, 256, seed=3)
         d = W.generate(w)
@@ -531,5 +527,5 @@ def test_last_plan_reports_the_run():
         C = alloc_c(w, d)
         run_gpu(g, w, dd, C)
         p = g.last_plan()
-        assert p["config"] == 5 and p["block_k"] == 128 and p["tiles_m"] == 3 and p["tiles_n"] == 3
+        assert p["config"] == 4 and p["block_k"] == 128 and p["tiles_m"] == 3 and p["tiles_n"] == 3
         assert 1 <= p["clusters"] <= 9

@@ -13,7 +13,7 @@ import torch
 import oracle
 from bf16_tensor_core_gb300 import gemm as G
 from bf16_tensor_core_gb300 import workloads as W
-from gpu_cases import OR_CODE, alloc_c, device_inputs
+from gpu_cases import OR_CODE, alloc_c, compare, device_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -69,20 +69,26 @@ def test_noalloc_matches_gemm_run_on_two_calls_in_a_row(lib):
     out1, out2 = alloc_c(w1, d1), alloc_c(w2, d2)
     assert _noalloc(w1, dd1, out1, stream) == G.GEMM_OK
     assert _noalloc(w2, dd2, out2, stream) == G.GEMM_OK     # second call reuses the scratch
+    assert G.gemm_noalloc_get_device_status(stream) == G.GEMM_OK   # no bounded wait expired
     torch.cuda.synchronize()
     for w, d, got, want in ((w1, d1, out1, ref1), (w2, d2, out2, ref2)):
-        rep = _within_tolerance(w, d, got, want)
-        assert rep["passed"], (w.name, rep)
+        rep = compare(w, d, got)                             # every element against the CPU oracle
+        assert rep["passed"], (w.name, "oracle", rep)
+        rep = _within_tolerance(w, d, got, want)             # and against gemm_run's output
+        assert rep["passed"], (w.name, "gemm_run", rep)
 
 
 def test_noalloc_rejects_repack_beyond_the_scratch(lib):
     # A stored 4100 x 4100 with lda = 4100 f16 (8200-byte pitch) needs 4100 * 4104 * 2 bytes of scratch,
-    # more than the 32 MiB the entry point holds.
-    assert 4100 * 4104 * 2 > (32 << 20)
-    A = torch.zeros(64, dtype=torch.float16, device="cuda")
-    B = torch.zeros(64, dtype=torch.float16, device="cuda")
-    C = torch.zeros(64, dtype=torch.float32, device="cuda")
-    st = G.gemm_run_noalloc(4100, 64, 4100, A.data_ptr(), 4100, B.data_ptr(), 64, C.data_ptr(), 64,
+    # more than the 32 MiB the entry point holds.  A, B and C have their full sizes, so the operands a
+    # call would read and the output it would write all lie in memory the test owns.
+    M, N, K = 4100, 64, 4100
+    assert M * 4104 * 2 > (32 << 20)
+    A = torch.zeros(M, K, dtype=torch.float16, device="cuda")
+    B = torch.zeros(K, N, dtype=torch.float16, device="cuda")
+    C = torch.zeros(M, N, dtype=torch.float32, device="cuda")
+    st = G.gemm_run_noalloc(M, N, K, A.data_ptr(), K, B.data_ptr(), N, C.data_ptr(), N,
                             G.GEMM_F16, G.GEMM_F32, G.GEMM_ROW, G.GEMM_ROW, 1.0, 0.0, None,
                             torch.cuda.current_stream().cuda_stream)
     assert st == G.GEMM_ERR_UNSUPPORTED
+    assert G.gemm_noalloc_get_device_status(torch.cuda.current_stream().cuda_stream) == G.GEMM_OK
