@@ -4,10 +4,15 @@
 
 A step is one gemm_run (the whole hot path: tensor maps, TMA ring, tcgen05 MMAs, epilogue)
 over the workload's seeded synthetic inputs.  Default workload: 4096^3, f16 in, f32
-accumulate, f16 out.  Timing: CUDA events on the launching stream around every gemm_run,
-after W untimed warm-up steps, with a 256 MiB write between steps so that every step starts
-with a cold L2 (the 96 MB working set would otherwise fit in the 129 MB L2).  The K timed
-steps are bracketed by a barrier and a device synchronise; the time is the max over ranks.
+accumulate, f16 out.  Two timing protocols, both on the device with CUDA events after W untimed
+warm-up steps, the K timed steps bracketed by a barrier and a device synchronise:
+  rotate (the headline by default): inputs larger than L2.  The operands (and C) are copied into
+    enough sets that one pass over them moves more than 3 x L2, so every step reads its operands
+    from HBM; the K steps run back to back from CUDA graphs (one graph per pass over the sets),
+    with one event pair around them all, so the per-call host cost is not on the device's clock.
+  flush: a 256 MiB write before every step, each step alone between its own two events (the
+    launch latency of every step is then part of its time).
+The protocol not chosen with --l2 is measured as well and reported under other_protocol.
 Several GPUs (torchrun) run independent replicas of the same GEMM: the product has no data
 exchange, so there is no collective in the timed path (weak scaling).
 
@@ -49,6 +54,10 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--context-cublas", action="store_true",
                     help="also time torch.matmul (cuBLAS) on the same inputs and protocol, as context")
+    ap.add_argument("--l2", choices=["rotate", "flush"], default="rotate",
+                    help="headline protocol: 'rotate' runs the K steps back to back from CUDA graphs over rotating "
+                         "operand sets larger than L2 in all; 'flush' times each step alone after a 256 MiB write. "
+                         "The other protocol is always measured too and reported beside the headline.")
     ap.add_argument("--sustained-seconds", type=float, default=4.0,
                     help="back-to-back steps (warm L2) after the timed region, to expose power or thermal limits; "
                          "0 skips them")
@@ -105,6 +114,20 @@ def _traffic(workload_name: str, kernel: str, config: int):
     return None, None
 
 
+def _window(rows, ts, t0: float, t1: float, least: int = 3, reach: float = 0.02):
+    """The samples inside [t0, t1]; when fewer than `least` fall inside (a region shorter than a few
+    sampling periods), the `least` samples nearest the region's middle among those within `reach`
+    seconds of it.  Returns (rows, widened)."""
+    sel = [r for r in rows if t0 <= ts(r) <= t1]
+    if len(sel) >= least:
+        return sel, False
+    near = [r for r in rows if t0 - reach <= ts(r) <= t1 + reach]
+    if len(near) <= len(sel):
+        return sel, False
+    mid = 0.5 * (t0 + t1)
+    return sorted(near, key=lambda r: abs(ts(r) - mid))[:least], True
+
+
 class NvmlSampler:
     """SM clock, power and clock-event reasons read through NVML (read-only queries) by a thread
     polling every ~0.5 ms, so that even a timed region of a few milliseconds gets samples."""
@@ -157,12 +180,15 @@ class NvmlSampler:
             self._thread.join(timeout=2)
 
     def summarize(self, t0: float, t1: float) -> dict:
-        sel = [r for r in self.rows if t0 <= r[0] <= t1]
+        sel, widened = _window(self.rows, lambda r: r[0], t0, t1)
         if not sel:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": "nvml"}
         reasons = sorted({n for r in sel for bit, n in self.REASONS.items() if r[3] & bit})
-        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": self.max_mhz,
-                "power_w_max": max(r[2] for r in sel), "reasons": reasons, "samples": len(sel), "source": "nvml"}
+        out = {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": self.max_mhz,
+               "power_w_max": max(r[2] for r in sel), "reasons": reasons, "samples": len(sel), "source": "nvml"}
+        if widened:
+            out["window"] = "the timed region was shorter than the sampling period: the 3 samples nearest it"
+        return out
 
 
 class ClockSampler:
@@ -194,14 +220,13 @@ class ClockSampler:
 
     @staticmethod
     def summarize(rows, t0: float, t1: float) -> dict:
-        sel = []
+        stamped = []
         for r in rows:
             try:
-                ts = _dt.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                stamped.append((_dt.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp(), r))
             except ValueError:
                 continue
-            if t0 <= ts <= t1:
-                sel.append(r)
+        sel = [r for _, r in _window(stamped, lambda x: x[0], t0, t1)[0]]
         if not sel:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         sm = [float(r[2]) for r in sel if r[2].replace(".", "").isdigit()]
@@ -378,7 +403,6 @@ def _config_dict(w, args, extra=None) -> dict:
     c = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype_in": w.dtype_in, "dtype_out": w.dtype_out,
          "layoutA": w.layoutA, "layoutB": w.layoutB, "alpha": w.alpha, "beta": w.beta,
          "bias": w.dist_bias is not None, "inputs": "seeded synthetic, " + w.note,
-         "l2": f"{FLUSH_BYTES >> 20} MiB write between timed steps (cold L2 every step)",
          "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
     if extra:
         c.update(extra)
@@ -451,27 +475,61 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
     s_handle = stream.cuda_stream
 
-    if w.layoutB == "q4_0":
-        def step():
-            g.run_q4_0(A, B, C, M=w.M, N=w.N, K=w.K, layoutA=w.layoutA, alpha=w.alpha, beta=w.beta, bias=bias,
-                       stream=s_handle)
-    else:
-        def step():
-            g.run(A, B, C, M=w.M, N=w.N, K=w.K, layoutA=w.layoutA, layoutB=w.layoutB, alpha=w.alpha,
-                  beta=w.beta, bias=bias, stream=s_handle)
-
     def barrier():
         if world > 1:
             dist.barrier()
 
-    # warm-up
-    for _ in range(max(args.warmup, 3)):
+    # Rotating operand sets: S copies of the inputs (and of C), so that the set a step reads was last
+    # touched S - 1 steps earlier, with more than 3 x L2 of other traffic in between: every step reads
+    # its operands from HBM without a flush between steps.
+    l2_bytes = torch.cuda.get_device_properties(local).L2_cache_size if hasattr(
+        torch.cuda.get_device_properties(local), "L2_cache_size") else 132 << 20
+    set_bytes = algorithmic_bytes(w)
+    n_sets = max(2, min(512, -(-3 * l2_bytes // max(set_bytes, 1)) + 1))
+    sets = [dict(A=A, B=B, C=C)]
+    for _ in range(n_sets - 1):
+        sets.append(dict(A=A.clone(), B=B.clone(), C=C.clone()))
+
+    def step_on(j, st=None):
+        bs = sets[j]
+        if w.layoutB == "q4_0":
+            g.run_q4_0(bs["A"], bs["B"], bs["C"], M=w.M, N=w.N, K=w.K, layoutA=w.layoutA, alpha=w.alpha, beta=w.beta,
+                       bias=bias, stream=st)
+        else:
+            g.run(bs["A"], bs["B"], bs["C"], M=w.M, N=w.N, K=w.K, layoutA=w.layoutA, layoutB=w.layoutB,
+                  alpha=w.alpha, beta=w.beta, bias=bias, stream=st)
+
+    def step():
+        step_on(0, s_handle)
+
+    # warm-up: every set at least once (workspaces reach their size before any capture)
+    for i in range(max(args.warmup, 3, n_sets)):
         flush.zero_()
-        step()
+        step_on(i % n_sets, s_handle)
     torch.cuda.synchronize()
     st = g.status()
     if st != G.GEMM_OK:
         raise RuntimeError(f"warm-up failed: {g.last_error()}")
+
+    # One graph over all sets (a pass), one over the first K % S sets; K steps = K // S passes + the rest.
+    n_pass, n_rest = args.steps // n_sets, args.steps % n_sets
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    launches0 = g.launches
+    graph_pass = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_pass, stream=cap):
+        for j in range(n_sets):
+            step_on(j, cap.cuda_stream)
+    launches_per_step = (g.launches - launches0) / n_sets
+    graph_rest = None
+    if n_rest:
+        graph_rest = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_rest, stream=cap):
+            for j in range(n_rest):
+                step_on(j, cap.cuda_stream)
+    torch.cuda.synchronize()
+    graph_pass.replay()                       # one untimed pass on the graph path
+    torch.cuda.synchronize()
 
     uuid = str(torch.cuda.get_device_properties(local).uuid)
     dev_id = uuid if uuid.startswith("GPU-") else ("GPU-" + uuid)
@@ -480,22 +538,52 @@ def run_ours(args, rank, world, local):
     time.sleep(0.3)
     switch = sys.getswitchinterval()
     sys.setswitchinterval(0.0002)          # let the sampler thread run between launches
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    launches0 = g.launches
-    barrier()
-    torch.cuda.synchronize()
-    t_start = time.time()
-    for e0, e1 in evs:
-        flush.zero_()
-        e0.record(stream)
-        step()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    t_end = time.time()
-    launches = g.launches - launches0
+
+    def timed_rotate():
+        """K steps back to back from the graphs; events between passes give a per-pass distribution."""
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_pass + 2)]
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        with torch.cuda.stream(stream):
+            evs[0].record(stream)
+            for i in range(n_pass):
+                graph_pass.replay()
+                evs[i + 1].record(stream)
+            if graph_rest is not None:
+                graph_rest.replay()
+            evs[n_pass + 1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        t1 = time.time()
+        total_ms = evs[0].elapsed_time(evs[n_pass + 1])
+        per_step = np.array([evs[i].elapsed_time(evs[i + 1]) / n_sets for i in range(n_pass)])
+        if per_step.size == 0:                # fewer steps than operand sets: the rest graph alone
+            per_step = np.array([total_ms / args.steps])
+        return total_ms, per_step, t0, t1
+
+    def timed_flush():
+        """Each step alone between two events, after a 256 MiB write (cold L2, per-step launch cost included)."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        t1 = time.time()
+        times = np.array([e0.elapsed_time(e1) for e0, e1 in evs])
+        return float(times.sum()), times, t0, t1
+
+    first, second = (timed_rotate, timed_flush) if args.l2 == "rotate" else (timed_flush, timed_rotate)
+    total_ms, times_ms, t_start, t_end = first()
+    other_ms, other_times, o_start, o_end = second()
+    launches = int(round(launches_per_step * args.steps))
     plan = g.last_plan()
-    times_ms = np.array([e0.elapsed_time(e1) for e0, e1 in evs])
 
     # Sustained: the same step back to back (no flush, warm L2) for a few seconds, so that power or
     # thermal limits show in the clocks.  Reported beside the cold-L2 value, never as it.
@@ -520,20 +608,36 @@ def run_ours(args, rank, world, local):
     sys.setswitchinterval(switch)
     if sampler is None:
         nvml.stop()
-        clocks = nvml.summarize(t_start, t_end)
-        if sustained:
-            sustained["clocks"] = nvml.summarize(ts0, ts1)
+        summarize = nvml.summarize
     else:
         rows = sampler.stop()
-        clocks = ClockSampler.summarize(rows, t_start, t_end)
-        if sustained:
-            sustained["clocks"] = ClockSampler.summarize(rows, ts0, ts1)
+        summarize = lambda a, b: ClockSampler.summarize(rows, a, b)
+    clocks = summarize(t_start, t_end)
+    other_clocks = summarize(o_start, o_end)
+    if sustained:
+        sustained["clocks"] = summarize(ts0, ts1)
     st = g.status()
     if st != G.GEMM_OK:
         raise RuntimeError(f"timed run failed: {g.last_error()}")
-    total_s = max_over_ranks(float(times_ms.sum()) / 1e3, world, dev)
+    total_s = max_over_ranks(total_ms / 1e3, world, dev)
     value = replica_throughput(w.flops, args.steps, world, total_s)
     ms_per_step = total_s / args.steps * 1e3
+    other_s = max_over_ranks(other_ms / 1e3, world, dev)
+    l2_text = {
+        "rotate": (f"inputs larger than L2: {n_sets} rotating operand sets (A, B, C and C_in each; "
+                   f"{n_sets * set_bytes / 1e6:.0f} MB in all, over 3 x the {l2_bytes / 1e6:.0f} MB L2), no flush"),
+        "flush": f"{FLUSH_BYTES >> 20} MiB write between timed steps (cold L2 every step)"}
+    timing_text = {
+        "rotate": (f"the K steps back to back from CUDA graphs ({n_sets} steps per graph, one per operand set), "
+                   "one event pair around all of them on the launching stream"),
+        "flush": "CUDA events around each gemm_run on its stream, the flush outside them"}
+    other = "flush" if args.l2 == "rotate" else "rotate"
+    other_line = {"protocol": other, "value": replica_throughput(w.flops, args.steps, world, other_s),
+                  "unit": "TFLOP/s", "ms_per_step": other_s / args.steps * 1e3, "l2": l2_text[other],
+                  "timing": timing_text[other],
+                  "step_ms": {"mean": float(other_times.mean()), "median": float(np.median(other_times)),
+                              "best": float(other_times.min()), "p90": float(np.percentile(other_times, 90))},
+                  "clocks": other_clocks}
 
     # end to end through the public call with host buffers
     e2e = None
@@ -551,8 +655,8 @@ def run_ours(args, rank, world, local):
         # Two device buffer sets on three streams: step k copies its inputs in (H2D stream), runs
         # gemm_run on them (compute stream) and copies C out (D2H stream); events order each set's
         # reuse, so step k+1's copy-in and step k-1's copy-out overlap step k's product.
-        sets = [dict(A=A, B=B, C=C)]
-        sets.append(dict(A=torch.empty_like(A), B=torch.empty_like(B), C=torch.empty_like(C)))
+        e2e_sets = [dict(A=A, B=B, C=C)]
+        e2e_sets.append(dict(A=torch.empty_like(A), B=torch.empty_like(B), C=torch.empty_like(C)))
         C_pins = [C_pin, torch.empty_like(C_pin).pin_memory()]
         s_in, s_mm, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev = lambda: torch.cuda.Event()
@@ -569,7 +673,7 @@ def run_ours(args, rank, world, local):
             done_mm, done_out = [None, None], [None, None]
             for k in range(n):
                 j = k % 2
-                bs = sets[j]
+                bs = e2e_sets[j]
                 if done_mm[j] is not None:
                     s_in.wait_event(done_mm[j])          # set j's previous product has read A and B
                 if done_out[j] is not None:
@@ -656,18 +760,20 @@ def run_ours(args, rank, world, local):
             "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype_in, "data": "synthetic", "impl": "ours",
-            "config": _config_dict(w, args, {"kernel_config": plan.get("config", args.config),
+            "config": _config_dict(w, args, {"l2": l2_text[args.l2], "kernel_config": plan.get("config", args.config),
                                              "plan": {k: plan[k] for k in ("block_m", "block_n", "block_k", "stages",
                                                                            "tiles_m", "tiles_n", "clusters",
                                                                            "stream_k", "dp_tiles", "transposed", "gemv",
                                                                            "q4_dequant", "kernels")
                                                       if k in plan},
-                                             "timing": "CUDA events around each gemm_run on its stream"}),
+                                             "timing": timing_text[args.l2]}),
             "roofline": roof, "clocks": clocks, "gpu_launches": launches, "e2e": e2e,
             "step_ms": {"mean": float(times_ms.mean()), "median": float(np.median(times_ms)),
                         "best": float(times_ms.min()), "p90": float(np.percentile(times_ms, 90)),
                         "best_value": w.flops / (float(times_ms.min()) / 1e3) / 1e12,
-                        "note": "rank 0's per-step CUDA-event times in the timed region (cold L2)"},
+                        "note": ("rank 0's per-step times in the timed region: per graph pass / steps per pass "
+                                 "(rotate), or each step's own event pair (flush)")},
+            "other_protocol": other_line,
             "sustained": sustained}
     if args.context_cublas:
         line["context_cublas"] = cublas_context(w, A, B, bias, C, flush, args.steps, args.warmup, stream)

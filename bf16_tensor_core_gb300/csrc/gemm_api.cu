@@ -183,7 +183,7 @@ struct gemm_ctx {
     int faults = FAULT_NONE;
     bool force_2d = false;          // GEMM_TMA_RANK=2 (tuning): never use 3-D operand maps
     int64_t launches = 0;
-    unsigned* sk_flags = nullptr;   // zeroed at creation; stream-K flags carry the launch epoch
+    unsigned* sk_flags = nullptr;   // zeroed at creation; raised to the launch epoch, reset by their consumer
     float* sk_part = nullptr;       // stream-K partials (grown on demand)
     size_t sk_part_bytes = 0;
     void* q4_ws = nullptr;          // f16 weights of the separate Q4_0 dequantisation pass (grown on demand)
@@ -1000,6 +1000,10 @@ gemm_status_t gemm_get_device_status(gemm_handle_t h, void* stream) {
     if (word == 0) return GEMM_OK;
     e = cudaMemset(h->d_status, 0, sizeof(word));
     if (e != cudaSuccess) return cuda_fail(h, "clearing the status word", e);
+    // An aborted launch may leave stream-K flags raised; reset them so that no later launch (a graph
+    // replay repeats its epoch) can take one for a fresh partial.
+    e = cudaMemset(h->sk_flags, 0, (size_t)h->dev.num_sms * 8 * sizeof(unsigned));
+    if (e != cudaSuccess) return cuda_fail(h, "clearing the stream-K flags", e);
     const unsigned code = (unsigned)(word & 0xff);
     const unsigned role = (unsigned)((word >> 8) & 0xff);
     const unsigned stage = (unsigned)((word >> 16) & 0xffff);

@@ -608,6 +608,13 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* addr) {
     return v;
 }
 
+// Each stream-K flag has one consumer, which sets it back to 0 once it has the partial: the next
+// launch then finds every flag at 0 whatever its epoch, so replaying a launch with the same epoch
+// (a CUDA graph) cannot see a stale flag.
+__device__ __forceinline__ void clear_flag(unsigned* flag) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" :: "l"(flag), "r"(0u) : "memory");
+}
+
 // Bounded wait for a stream-K flag written by another cluster of this grid (all clusters are
 // co-resident: the grid never exceeds the device's active-cluster capacity).
 __device__ __forceinline__ bool wait_flag_bounded(const unsigned* flag, unsigned want, uint64_t timeout_ns,
@@ -1028,6 +1035,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                             slot_floats, ring + static_cast<uint32_t>(ew) * kFixBufs * kFixPieceBytes,
                             smem_u32(&bar_fix[ew * kFixBufs]), p.timeout_ns, abort_flag, r);
                     }
+                    if (ready && lane == 0) {
+                        for (int src = c0; src < c0 + S; ++src)
+                            if (src != cluster_id)
+                                clear_flag(p.sk_flags + (static_cast<size_t>(src) * kClusterCtas + rank) * Cfg::kEpiWarps + ew);
+                    }
                     if (!ready) {
                         if (lane == 0 && !*abort_flag)
                             report_error<kClusterCtas>(p, ROLE_EPILOGUE, u.tile, 300 + quarter, abort_flag);
@@ -1053,6 +1065,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         tbase, lane, p.sk_partials + static_cast<size_t>(cluster_id + 1) * slot_floats + warp_block, n,
                         slot_floats, ring + static_cast<uint32_t>(ew) * kFixBufs * kFixPieceBytes,
                         smem_u32(&bar_fix[ew * kFixBufs]), p.timeout_ns, abort_flag);
+                }
+                if (ready && lane == 0) {
+                    for (int src = cluster_id + 1; src < cluster_id + 1 + n; ++src)
+                        clear_flag(p.sk_flags + (static_cast<size_t>(src) * kClusterCtas + rank) * Cfg::kEpiWarps + ew);
                 }
                 if (!ready) {
                     if (lane == 0 && !*abort_flag)

@@ -49,7 +49,11 @@
  *   (cf. the prefill GEMM page, section 3.3: setting the attribute inside a
  *   graph-capture window fails silently).  A call that grows the workspace
  *   allocates device memory, so warm such shapes up before capturing a graph.
- *   A handle must not be used by two host threads at once.
+ *   Once warm, calls may be captured into a CUDA graph and the graph replayed
+ *   any number of times: the stream-K hand-off flags are reset by the kernel
+ *   that consumes them, so a replayed launch never sees a stale flag.  Calls
+ *   of one handle share its workspace, so they must not run concurrently on
+ *   several streams.  A handle must not be used by two host threads at once.
  *
  * Errors
  *   Every entry point returns a gemm_status_t; nothing calls exit or abort.

@@ -109,6 +109,11 @@ def test_nvml_summary_decodes_reasons_inside_the_window():
     assert c["samples"] == 3 and c["sm_mhz"] == 1900 and c["sm_max_mhz"] == 2070 and c["power_w_max"] == 1390.0
     assert c["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
     assert s.summarize(5.0, 6.0)["samples"] == 0
+    # A region shorter than the sampling period (a graph of a few short steps) takes the samples nearest it,
+    # within 20 ms, and says so.
+    s.rows = [(10.000, 2070, 900.0, 0x0), (10.0005, 2060, 910.0, 0x0), (10.0010, 2050, 920.0, 0x4), (10.5, 1000, 1.0, 0x8)]
+    c = s.summarize(10.0006, 10.0008)
+    assert c["samples"] == 3 and c["sm_mhz"] == 2060 and c["reasons"] == ["sw_power_cap"] and "window" in c
 
 
 def test_nvidia_smi_summary_reads_the_active_reasons():

@@ -529,3 +529,41 @@ def test_last_plan_reports_the_run():
         p = g.last_plan()
         assert p["config"] == 4 and p["block_k"] == 128 and p["tiles_m"] == 3 and p["tiles_n"] == 3
         assert 1 <= p["clusters"] <= 9
+
+
+@pytest.mark.parametrize("cfg,mc,c", [
+    (4, 0, dict(M=2274, N=2300, K=700, dtype_out="f32", layoutA="col")),             # stream-K heads
+    (4, 24, dict(M=640, N=512, K=2048, dtype_out="f32", beta=1.0)),                  # reduce-scatter, S = 4
+    (7, 0, dict(M=300, N=200, K=2048, dtype_out="f16", bias=True)),                  # reduce-scatter, S = 4
+])
+def test_graph_replay_with_stream_k_hand_off(cfg, mc, c):
+    """A captured call replayed several times, with new A each time, matches the oracle every time: the
+    hand-off flags are reset by their consumer, so a replay (same epoch) never reads a stale partial."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    c = dict(c)
+    w = W.problem(c.pop("M"), c.pop("N"), c.pop("K"), seed=900 + cfg + mc, **c)
+    ds = [W.generate(w)] + [W.generate(W.problem(w.M, w.N, w.K, seed=901 + i + cfg + mc, **c)) for i in range(3)]
+    dd = device_inputs(ds[0])
+    C = alloc_c(w, ds[0])
+    Cin = C.clone()
+    g = G.Gemm(0, config=cfg, stream_k=1, max_clusters=mc)
+    try:
+        run_gpu(g, w, dd, C)                                  # warm-up: the partial buffers are allocated here
+        torch.cuda.synchronize()
+        assert g.last_plan()["stream_k"] == 1
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run_gpu(g, w, dd, C)
+        for d in ds[1:]:
+            A = d["A"]
+            dd["A"].copy_(A.cuda())                           # new A in the captured buffer
+            C.copy_(Cin)
+            graph.replay()
+            torch.cuda.synchronize()
+            want = dict(ds[0], A=A)
+            rep = compare(w, want, C)
+            assert rep["passed"], rep
+        assert g.status() == G.GEMM_OK
+    finally:
+        g.close()
