@@ -48,6 +48,7 @@ def _args():
     ap.add_argument("--workload", type=int, default=2,
                     help="1..10 (6, 10: Q4_0 weights through gemm_run_q4_0; 7, 8, 10: decode shapes, HBM-bound)")
     ap.add_argument("--config", type=int, default=-1)
+    ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic stream serialization")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps, capped at 200")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -471,7 +472,7 @@ def run_ours(args, rank, world, local):
     C = (Cin_host.to(dev).clone() if Cin_host is not None
          else torch.empty(w.M, w.N, dtype=W.DTYPES[w.dtype_out], device=dev))
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    g = G.Gemm(local, config=args.config)
+    g = G.Gemm(local, config=args.config, pdl=0 if args.no_pdl else 1)
     stream = torch.cuda.current_stream(dev)
     s_handle = stream.cuda_stream
 

@@ -554,6 +554,7 @@ struct LaunchArgs {
     cudaStream_t stream;
     bool force_2d;              // tuning: one 2-D box per slab even where a 3-D box would do
     int c_trans = 0;            // the product is C^T (see Problem / transpose)
+    bool pdl = true;            // launch with programmatic stream serialization
 };
 
 // Whether a stream-K schedule splits every tile over the same number S of consecutive clusters with
@@ -680,7 +681,7 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
     }
     *what = "GEMM kernel launch";
     cudaError_t e = config_launch(plan.config, a.dout == GEMM_F32 ? OUT_F32 : (a.dout == GEMM_F16 ? OUT_F16 : OUT_BF16),
-                                  plan.clusters * cluster_ctas(*d), a.stream, ta, tb, tc, p);
+                                  plan.clusters * cluster_ctas(*d), a.stream, a.pdl, ta, tb, tc, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         *cuda_err = e;
@@ -693,7 +694,7 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
 // launch.  Updates the operand pointers and leading dimensions; counts launches.
 cudaError_t repack_operands(const gemm_plan_t& plan, int64_t M, int64_t N, int64_t K, int la, int lb, void* ws,
                             const void** A, int64_t* lda, const void** B, int64_t* ldb, int num_sms,
-                            cudaStream_t s, int64_t* launches, const char** what, int b_q4 = 0,
+                            cudaStream_t s, bool pdl, int64_t* launches, const char** what, int b_q4 = 0,
                             int in_bytes = 2) {
     char* w = static_cast<char*>(ws);
     RepackJobs jobs{};
@@ -727,7 +728,7 @@ cudaError_t repack_operands(const gemm_plan_t& plan, int64_t M, int64_t N, int64
     }
     if (jobs.n == 0) return cudaSuccess;
     *what = "repack of the operands";
-    cudaError_t e = launch_repack_u16(jobs, num_sms, s);
+    cudaError_t e = launch_repack_u16(jobs, num_sms, s, pdl);
     if (e != cudaSuccess) return e;
     ++*launches;
     return cudaSuccess;
@@ -807,7 +808,7 @@ const void* config_kernel(int id, int out) {
     }
 }
 
-cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, const CUtensorMap& a,
+cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, bool pdl, const CUtensorMap& a,
                           const CUtensorMap& b, const CUtensorMap& c, const KernelParams& p) {
     const ConfigDesc* d = config_desc(id);
     if (!d) return cudaErrorInvalidValue;
@@ -816,13 +817,15 @@ cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, c
     lc.blockDim = dim3((unsigned)d->threads, 1, 1);
     lc.dynamicSmemBytes = (size_t)d->smem_bytes;
     lc.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cluster_ctas(*d);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
-    lc.numAttrs = 1;
+    lc.numAttrs = pdl ? 2 : 1;
     switch (id) {
         case 0: return cfg0_launch(out, lc, a, b, c, p);
         case 1: return cfg1_launch(out, lc, a, b, c, p);
@@ -855,6 +858,7 @@ void gemm_options_default(gemm_options_t* opt) {
     opt->debug_skip_stage = -1;
     opt->stream_k = -1;
     opt->skinny = -1;
+    opt->pdl = 1;
 }
 
 const char* gemm_status_string(gemm_status_t s) {
@@ -927,7 +931,7 @@ gemm_status_t gemm_create(gemm_handle_t* out, int device, const gemm_options_t* 
         o = *opt;
     }
     if (o.config < -1 || o.config >= kNumConfigs || o.timeout_ms <= 0 || o.raster_group < 0 || o.max_clusters < 0 ||
-        o.stream_k < -1 || o.stream_k > 1)
+        o.stream_k < -1 || o.stream_k > 1 || o.pdl < 0 || o.pdl > 1)
         return GEMM_ERR_INVALID_ARG;
     int count = 0;
     cudaError_t e = cudaGetDeviceCount(&count);
@@ -1053,7 +1057,8 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
         if (h->faults & FAULT_LAUNCH) return fail(h, GEMM_ERR_CUDA, "kernel launch: forced failure (GEMM_TEST_FAIL=launch)");
         GemvParams gp{A, lda * 2, B, ldb * 2, C, ldc, bias, alpha, beta, (int)M, (int)N, (int)K};
         const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
-        cudaError_t e = launch_gemv(out_kind, dtype_in == GEMM_BF16, gp, h->dev.num_sms, static_cast<cudaStream_t>(stream));
+        cudaError_t e = launch_gemv(out_kind, dtype_in == GEMM_BF16, gp, h->dev.num_sms, static_cast<cudaStream_t>(stream),
+                                    h->opt.pdl != 0);
         if (e != cudaSuccess) return cuda_fail(h, "small-M kernel launch", e);
         h->launches += 1;
         gemm_plan_t gplan{};
@@ -1080,7 +1085,7 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
     if (h->faults & FAULT_LAUNCH) return fail(h, GEMM_ERR_CUDA, "kernel launch: forced failure (GEMM_TEST_FAIL=launch)");
 
     if (K == 0) {
-        cudaError_t e = launch_scale_bias(out_kind, C, ldc, bias, beta, M, N, h->dev.num_sms, s);
+        cudaError_t e = launch_scale_bias(out_kind, C, ldc, bias, beta, M, N, h->dev.num_sms, s, h->opt.pdl != 0);
         if (e != cudaSuccess) return cuda_fail(h, "scale/bias kernel launch", e);
         h->launches += 1;
     } else {
@@ -1093,7 +1098,8 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
                                "workspace allocation");
             if (st != GEMM_OK) return st;
             cudaError_t e = repack_operands(plan, q.M, q.N, K, q.la, q.lb, h->ws, &a_ptr, &lda_eff, &b_ptr, &ldb_eff,
-                                            h->dev.num_sms, s, &h->launches, &what, b_q4, elt_bytes(dtype_in));
+                                            h->dev.num_sms, s, h->opt.pdl != 0, &h->launches, &what, b_q4,
+                                            elt_bytes(dtype_in));
             if (e != cudaSuccess) return cuda_fail(h, what, e);
         }
         if (plan.stream_k) {
@@ -1106,7 +1112,7 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
         LaunchArgs la{&plan, q.M, q.N, K, a_ptr, lda_eff, b_ptr, ldb_eff, C, ldc, dtype_in, dtype_out, q.la, q.lb,
                       alpha, beta, bias, h->d_status, (unsigned long long)h->opt.timeout_ms * 1000000ull,
                       h->opt.debug_skip_stage, h->opt.raster_group, h->sk_part, h->sk_flags, h->epoch, s,
-                      h->force_2d, trans ? 1 : 0};
+                      h->force_2d, trans ? 1 : 0, h->opt.pdl != 0};
         TmapFn tmap = [h](const TmapDesc& desc, CUtensorMap* m) { return get_tmap_cached(h, desc, m); };
         cudaError_t ce = cudaSuccess;
         st = launch_planned(la, tmap, &what, &ce);
@@ -1156,7 +1162,7 @@ gemm_status_t gemm_run_q4_0(gemm_handle_t h, int64_t M, int64_t N, int64_t K, co
     if (route == Q4_GEMV) {
         GemvParams gp{A, lda * 2, Bq, ldbq, C, ldc, bias, alpha, beta, (int)M, (int)N, (int)K};
         const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
-        cudaError_t e = launch_gemv_q4_0(out_kind, gp, h->dev.num_sms, s);
+        cudaError_t e = launch_gemv_q4_0(out_kind, gp, h->dev.num_sms, s, h->opt.pdl != 0);
         if (e != cudaSuccess) return cuda_fail(h, "Q4_0 small-M kernel launch", e);
         h->launches += 1;
         h->last_plan = plan;
@@ -1167,7 +1173,7 @@ gemm_status_t gemm_run_q4_0(gemm_handle_t h, int64_t M, int64_t N, int64_t K, co
     // The separate pass writes the N x K f16 weights (pitch K) that the f16 GEMM then reads.
     st = ensure_buffer(h, &h->q4_ws, &h->q4_ws_bytes, (size_t)round_up(N * K * 2, 256), "dequantised weights");
     if (st != GEMM_OK) return st;
-    cudaError_t e = launch_dequant_q4_0(Bq, ldbq, N, K, h->q4_ws, K, h->dev.num_sms, s);
+    cudaError_t e = launch_dequant_q4_0(Bq, ldbq, N, K, h->q4_ws, K, h->dev.num_sms, s, h->opt.pdl != 0);
     if (e != cudaSuccess) return cuda_fail(h, "Q4_0 dequantisation launch", e);
     h->launches += 1;
     st = run_impl(h, M, N, K, A, lda, h->q4_ws, K, C, ldc, GEMM_F16, dtype_out, layoutA, GEMM_COL, alpha, beta, bias,
@@ -1208,7 +1214,7 @@ gemm_status_t gemm_dequant_q4_0(const void* Bq, int64_t ldbq, int64_t N, int64_t
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
-    cudaError_t e = launch_dequant_q4_0(Bq, ldbq, N, K, out, ldo, sms, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_dequant_q4_0(Bq, ldbq, N, K, out, ldo, sms, static_cast<cudaStream_t>(stream), true);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
@@ -1300,8 +1306,8 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int out_kind = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_F16 ? OUT_F16 : OUT_BF16);
     if (K == 0) {
-        return launch_scale_bias(out_kind, C, ldc, bias, beta, M, N, nd.info.num_sms, s) == cudaSuccess ? GEMM_OK
-                                                                                                      : GEMM_ERR_CUDA;
+        return launch_scale_bias(out_kind, C, ldc, bias, beta, M, N, nd.info.num_sms, s, true) == cudaSuccess
+                   ? GEMM_OK : GEMM_ERR_CUDA;
     }
     // Repack into the file-scope scratch.  Every byte the GEMM then reads is written by this call
     // first, so nothing in the scratch has to start at zero.
@@ -1310,7 +1316,7 @@ extern "C" gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, const
     int64_t lda_eff = lda, ldb_eff = ldb, launches = 0;
     const char* what = "";
     if (repack_operands(plan, M, N, K, layoutA, layoutB, nd.scratch, &a_ptr, &lda_eff, &b_ptr, &ldb_eff,
-                        nd.info.num_sms, s, &launches, &what, 0, elt_bytes(dtype_in)) != cudaSuccess)
+                        nd.info.num_sms, s, true, &launches, &what, 0, elt_bytes(dtype_in)) != cudaSuccess)
         return GEMM_ERR_CUDA;
     LaunchArgs la{&plan, M, N, K, a_ptr, lda_eff, b_ptr, ldb_eff, C, ldc, dtype_in, dtype_out, layoutA, layoutB,
                   alpha, beta, bias, nd.status, 2000ull * 1000000ull, -1, 0, nullptr, nullptr, 0, s, false};

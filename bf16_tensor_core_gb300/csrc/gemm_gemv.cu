@@ -63,6 +63,8 @@ __device__ __forceinline__ void store_gemv_out(const GemvParams& p, int m, int n
 template <int kM, int kOut, bool kBf16>
 __global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(GemvParams p) {
     __shared__ float part[kGemvWarps][kGemvRows][kM];
+    griddep_launch_dependents();
+    griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kGemvRows;
     const int chunks = p.K / 8;                                     // 8 values per chunk (K % 8 == 0)
@@ -129,23 +131,22 @@ __global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(GemvParams p) {
 }
 
 template <int kM, int kOut>
-cudaError_t launch_m(const GemvParams& p, bool bf16, int blocks, cudaStream_t s) {
+cudaError_t launch_m(const GemvParams& p, bool bf16, int blocks, cudaStream_t s, bool pdl) {
     auto kern = bf16 ? &gemv_kernel<kM, kOut, true> : &gemv_kernel<kM, kOut, false>;
-    kern<<<blocks, kGemvWarps * 32, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_ex(kern, dim3(blocks), dim3(kGemvWarps * 32), 0, s, pdl, p);
 }
 
 template <int kOut>
-cudaError_t launch_out(const GemvParams& p, bool bf16, int blocks, cudaStream_t s) {
+cudaError_t launch_out(const GemvParams& p, bool bf16, int blocks, cudaStream_t s, bool pdl) {
     switch (p.M) {
-        case 1: return launch_m<1, kOut>(p, bf16, blocks, s);
-        case 2: return launch_m<2, kOut>(p, bf16, blocks, s);
-        case 3: return launch_m<3, kOut>(p, bf16, blocks, s);
-        case 4: return launch_m<4, kOut>(p, bf16, blocks, s);
-        case 5: return launch_m<5, kOut>(p, bf16, blocks, s);
-        case 6: return launch_m<6, kOut>(p, bf16, blocks, s);
-        case 7: return launch_m<7, kOut>(p, bf16, blocks, s);
-        case 8: return launch_m<8, kOut>(p, bf16, blocks, s);
+        case 1: return launch_m<1, kOut>(p, bf16, blocks, s, pdl);
+        case 2: return launch_m<2, kOut>(p, bf16, blocks, s, pdl);
+        case 3: return launch_m<3, kOut>(p, bf16, blocks, s, pdl);
+        case 4: return launch_m<4, kOut>(p, bf16, blocks, s, pdl);
+        case 5: return launch_m<5, kOut>(p, bf16, blocks, s, pdl);
+        case 6: return launch_m<6, kOut>(p, bf16, blocks, s, pdl);
+        case 7: return launch_m<7, kOut>(p, bf16, blocks, s, pdl);
+        case 8: return launch_m<8, kOut>(p, bf16, blocks, s, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -176,6 +177,8 @@ template <int kM, int kOut>
 __global__ void __launch_bounds__(kQ4Threads) gemv_q4_0_kernel(GemvParams p) {
     constexpr int kWarps = kQ4Threads / 32;
     __shared__ float part[kWarps][kQ4Rows][kM];
+    griddep_launch_dependents();
+    griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kQ4Rows;
     const int nblk = p.K / 32;
@@ -231,29 +234,28 @@ __global__ void __launch_bounds__(kQ4Threads) gemv_q4_0_kernel(GemvParams p) {
 }
 
 template <int kM, int kOut>
-cudaError_t launch_q4_m(const GemvParams& p, int blocks, cudaStream_t s) {
-    gemv_q4_0_kernel<kM, kOut><<<blocks, kQ4Threads, 0, s>>>(p);
-    return cudaGetLastError();
+cudaError_t launch_q4_m(const GemvParams& p, int blocks, cudaStream_t s, bool pdl) {
+    return launch_ex(gemv_q4_0_kernel<kM, kOut>, dim3(blocks), dim3(kQ4Threads), 0, s, pdl, p);
 }
 
 template <int kOut>
-cudaError_t launch_q4_out(const GemvParams& p, int blocks, cudaStream_t s) {
+cudaError_t launch_q4_out(const GemvParams& p, int blocks, cudaStream_t s, bool pdl) {
     switch (p.M) {
-        case 1: return launch_q4_m<1, kOut>(p, blocks, s);
-        case 2: return launch_q4_m<2, kOut>(p, blocks, s);
-        case 3: return launch_q4_m<3, kOut>(p, blocks, s);
-        case 4: return launch_q4_m<4, kOut>(p, blocks, s);
-        case 5: return launch_q4_m<5, kOut>(p, blocks, s);
-        case 6: return launch_q4_m<6, kOut>(p, blocks, s);
-        case 7: return launch_q4_m<7, kOut>(p, blocks, s);
-        case 8: return launch_q4_m<8, kOut>(p, blocks, s);
+        case 1: return launch_q4_m<1, kOut>(p, blocks, s, pdl);
+        case 2: return launch_q4_m<2, kOut>(p, blocks, s, pdl);
+        case 3: return launch_q4_m<3, kOut>(p, blocks, s, pdl);
+        case 4: return launch_q4_m<4, kOut>(p, blocks, s, pdl);
+        case 5: return launch_q4_m<5, kOut>(p, blocks, s, pdl);
+        case 6: return launch_q4_m<6, kOut>(p, blocks, s, pdl);
+        case 7: return launch_q4_m<7, kOut>(p, blocks, s, pdl);
+        case 8: return launch_q4_m<8, kOut>(p, blocks, s, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_gemv_q4_0(int out, const GemvParams& p, int num_sms, cudaStream_t stream) {
+cudaError_t launch_gemv_q4_0(int out, const GemvParams& p, int num_sms, cudaStream_t stream, bool pdl) {
     (void)num_sms;
     if (p.M < 1 || p.M > kGemvMaxM || p.N <= 0 || p.K <= 0 || p.K % 32 != 0 || p.ldw_bytes % 2 != 0 ||
         p.ldw_bytes < p.K / 32 * 18 || (reinterpret_cast<uintptr_t>(p.W) & 1u) != 0 || p.lda_bytes % 16 != 0 ||
@@ -262,22 +264,22 @@ cudaError_t launch_gemv_q4_0(int out, const GemvParams& p, int num_sms, cudaStre
     const long long blocks = (p.N + kQ4Rows - 1) / kQ4Rows;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     switch (out) {
-        case OUT_F16: return launch_q4_out<OUT_F16>(p, static_cast<int>(blocks), stream);
-        case OUT_BF16: return launch_q4_out<OUT_BF16>(p, static_cast<int>(blocks), stream);
-        case OUT_F32: return launch_q4_out<OUT_F32>(p, static_cast<int>(blocks), stream);
+        case OUT_F16: return launch_q4_out<OUT_F16>(p, static_cast<int>(blocks), stream, pdl);
+        case OUT_BF16: return launch_q4_out<OUT_BF16>(p, static_cast<int>(blocks), stream, pdl);
+        case OUT_F32: return launch_q4_out<OUT_F32>(p, static_cast<int>(blocks), stream, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_gemv(int out, bool bf16, const GemvParams& p, int num_sms, cudaStream_t stream) {
+cudaError_t launch_gemv(int out, bool bf16, const GemvParams& p, int num_sms, cudaStream_t stream, bool pdl) {
     (void)num_sms;
     if (p.M < 1 || p.M > kGemvMaxM || p.N <= 0 || p.K <= 0 || p.K % 8 != 0) return cudaErrorInvalidValue;
     const long long blocks = (p.N + kGemvRows - 1) / kGemvRows;   // one row group per CTA
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     switch (out) {
-        case OUT_F16: return launch_out<OUT_F16>(p, bf16, static_cast<int>(blocks), stream);
-        case OUT_BF16: return launch_out<OUT_BF16>(p, bf16, static_cast<int>(blocks), stream);
-        case OUT_F32: return launch_out<OUT_F32>(p, bf16, static_cast<int>(blocks), stream);
+        case OUT_F16: return launch_out<OUT_F16>(p, bf16, static_cast<int>(blocks), stream, pdl);
+        case OUT_BF16: return launch_out<OUT_BF16>(p, bf16, static_cast<int>(blocks), stream, pdl);
+        case OUT_F32: return launch_out<OUT_F32>(p, bf16, static_cast<int>(blocks), stream, pdl);
         default: return cudaErrorInvalidValue;
     }
 }

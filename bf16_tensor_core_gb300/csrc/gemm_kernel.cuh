@@ -824,6 +824,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if constexpr (kClusterCtas > 1) cluster_sync();
     tc_fence_after_sync();
     const uint32_t tmem_base = s_tmem_base;
+    // The set-up above touched no global memory; everything below may read what the previous kernel
+    // on the stream wrote, or overwrite what it reads.
+    griddep_launch_dependents();
+    griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer

@@ -8,6 +8,25 @@ namespace gb300 {
 
 struct KernelParams;
 
+// Launch `kernel` with cudaLaunchKernelEx; with `pdl` the launch allows programmatic stream
+// serialization, so it may be scheduled while the previous kernel on the stream finishes (every
+// kernel here waits with griddepcontrol.wait before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                      Args&&... args) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, kernel, static_cast<KArgs>(args)...);
+}
+
 struct ConfigDesc {
     int id;
     int cta_group;
@@ -30,7 +49,7 @@ const ConfigDesc* config_desc(int id);
 const void* config_kernel(int id, int out);
 
 // Launch config `id` on `grid_ctas` CTAs (clusters of cta_group) on `stream`.
-cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, const CUtensorMap& a,
+cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, bool pdl, const CUtensorMap& a,
                           const CUtensorMap& b, const CUtensorMap& c, const KernelParams& p);
 
 // Per-config translation units.
@@ -81,10 +100,10 @@ struct GemvParams {
     float alpha, beta;
     int M, N, K;             // K a multiple of 8
 };
-cudaError_t launch_gemv(int out, bool bf16, const GemvParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_gemv(int out, bool bf16, const GemvParams& p, int num_sms, cudaStream_t stream, bool pdl);
 // The same with W given as Q4_0 blocks: W = the block rows (2-byte aligned), ldw_bytes = their even
 // pitch (>= K/32*18), K a multiple of 32, A f16 with a 16-byte aligned base and pitch.
-cudaError_t launch_gemv_q4_0(int out, const GemvParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_gemv_q4_0(int out, const GemvParams& p, int num_sms, cudaStream_t stream, bool pdl);
 
 // Auxiliary kernels (gemm_aux.cu).
 struct RepackJob {
@@ -98,10 +117,10 @@ struct RepackJobs {
     RepackJob job[2];
     int n;                 // jobs in use (0..2), all moved by one launch
 };
-cudaError_t launch_repack_u16(const RepackJobs& jobs, int num_sms, cudaStream_t stream);
+cudaError_t launch_repack_u16(const RepackJobs& jobs, int num_sms, cudaStream_t stream, bool pdl);
 cudaError_t launch_dequant_q4_0(const void* bq, long long ldbq, long long N, long long K, void* out, long long ldo,
-                                int num_sms, cudaStream_t stream);
+                                int num_sms, cudaStream_t stream, bool pdl);
 cudaError_t launch_scale_bias(int out, void* C, long long ldc, const void* bias, float beta, long long M,
-                              long long N, int num_sms, cudaStream_t stream);
+                              long long N, int num_sms, cudaStream_t stream, bool pdl);
 
 }  // namespace gb300

@@ -46,6 +46,20 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v)
     asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while the kernel before it on
+// the stream is still running.  griddep_wait() returns once every grid this one depends on has
+// completed and its memory operations are visible (at once when there is no such grid); every kernel
+// of the library calls it before its first access to global memory.  griddep_launch_dependents()
+// lets the next such kernel be scheduled (it only gets an SM as this grid's CTAs leave).
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");

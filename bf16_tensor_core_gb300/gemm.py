@@ -27,7 +27,8 @@ LAYOUT_CODES = {"row": GEMM_ROW, "col": GEMM_COL}
 class gemm_options_t(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_int), ("config", ctypes.c_int), ("timeout_ms", ctypes.c_int),
                 ("sync_check", ctypes.c_int), ("raster_group", ctypes.c_int), ("max_clusters", ctypes.c_int),
-                ("debug_skip_stage", ctypes.c_int), ("stream_k", ctypes.c_int), ("skinny", ctypes.c_int)]
+                ("debug_skip_stage", ctypes.c_int), ("stream_k", ctypes.c_int), ("skinny", ctypes.c_int),
+                ("pdl", ctypes.c_int)]
 
 
 class gemm_config_info_t(ctypes.Structure):

@@ -102,6 +102,11 @@ typedef struct {
                              multiple of 8, 16-byte row pitch), else C^T = op(B)^T op(A)^T
                              for M <= 64 < N; 0 never; 1 always C^T; 2 always the CUDA-core
                              kernel (GEMM_ERR_UNSUPPORTED where it does not apply)            */
+    int pdl;              /* 1 (default): launch with programmatic stream serialization, so a
+                             kernel's set-up (barriers, tensor memory, descriptor prefetch)
+                             overlaps the end of the kernel before it on the stream; each
+                             kernel still waits for its predecessors to complete before it
+                             touches global memory.  0: plain stream order               */
 } gemm_options_t;
 
 /* Description of a kernel configuration. */
