@@ -182,6 +182,7 @@ struct gemm_ctx {
     size_t cache_next = 0;
     int faults = FAULT_NONE;
     bool force_2d = false;          // GEMM_TMA_RANK=2 (tuning): never use 3-D operand maps
+    bool k_forward = false;         // GEMM_K_ORDER=forward (tuning): every tile walks K upwards
     int64_t launches = 0;
     unsigned* sk_flags = nullptr;   // zeroed at creation; raised to the launch epoch, reset by their consumer
     float* sk_part = nullptr;       // stream-K partials (grown on demand)
@@ -555,6 +556,7 @@ struct LaunchArgs {
     bool force_2d;              // tuning: one 2-D box per slab even where a 3-D box would do
     int c_trans = 0;            // the product is C^T (see Problem / transpose)
     bool pdl = true;            // launch with programmatic stream serialization
+    bool k_alternate = true;    // whole tiles of odd waves walk K downwards (L2 reuse between waves)
 };
 
 // Whether a stream-K schedule splits every tile over the same number S of consecutive clusters with
@@ -667,6 +669,7 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
     p.debug_skip_stage = a.debug_skip_stage;
+    p.k_alternate = a.k_alternate ? 1 : 0;
     if (plan.stream_k) {
         const long long sk_total = (long long)(p.num_tiles - plan.dp_tiles) * p.k_tiles;
         p.sk_enabled = 1;
@@ -944,6 +947,7 @@ gemm_status_t gemm_create(gemm_handle_t* out, int device, const gemm_options_t* 
     h->opt = o;
     h->faults = read_fault_env();
     if (const char* r = std::getenv("GEMM_TMA_RANK")) h->force_2d = std::atoi(r) == 2;
+    if (const char* r = std::getenv("GEMM_K_ORDER")) h->k_forward = std::string(r) == "forward";
     DeviceGuard guard(device);
     gemm_status_t st = query_device(device, (h->faults & FAULT_OPTIN) != 0, &h->dev);
     if (st != GEMM_OK) {
@@ -1112,7 +1116,7 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
         LaunchArgs la{&plan, q.M, q.N, K, a_ptr, lda_eff, b_ptr, ldb_eff, C, ldc, dtype_in, dtype_out, q.la, q.lb,
                       alpha, beta, bias, h->d_status, (unsigned long long)h->opt.timeout_ms * 1000000ull,
                       h->opt.debug_skip_stage, h->opt.raster_group, h->sk_part, h->sk_flags, h->epoch, s,
-                      h->force_2d, trans ? 1 : 0, h->opt.pdl != 0};
+                      h->force_2d, trans ? 1 : 0, h->opt.pdl != 0, !h->k_forward};
         TmapFn tmap = [h](const TmapDesc& desc, CUtensorMap* m) { return get_tmap_cached(h, desc, m); };
         cudaError_t ce = cudaSuccess;
         st = launch_planned(la, tmap, &what, &ce);

@@ -77,6 +77,9 @@ struct KernelParams {
     // for the S - 1 flags of the same warp in the tile's other parts, adds their partials and stores its
     // block of C.  So every part moves (S - 1) / S of a tile instead of one head reading all S - 1.
     int sk_rs;
+    // 1: whole tiles of odd waves walk their k-tiles from the last to the first, so the first operand
+    // slabs such a tile reads are the ones the tiles of the wave before read last (still in L2).
+    int k_alternate;
     // Q4_0 B (kernels built with kQ4): N rows of K/32 blocks of 18 bytes at pitch ldbq bytes.
     const uint8_t* bq;
     long long ldbq;
@@ -89,6 +92,9 @@ struct Unit {
     int tile;
     int k0, k1;   // k-tile range [k0, k1) of this tile computed here
     int kind;     // UNIT_FULL, UNIT_HEAD (adds the partials of the following clusters), UNIT_TAIL (writes a partial)
+    int rev;      // 1: the range is walked from k1 - 1 down to k0
+    // The k-tile of the unit's i-th stage.
+    __device__ __forceinline__ int kt_at(int i) const { return rev ? k1 - 1 - i : k0 + i; }
 };
 
 // First stream-K iteration of cluster c.
@@ -119,6 +125,7 @@ struct UnitIter {
             u.k0 = 0;
             u.k1 = p.k_tiles;
             u.kind = UNIT_FULL;
+            u.rev = p.k_alternate ? (next_dp / stride) & 1 : 0;   // the wave's parity
             next_dp += stride;
             return true;
         }
@@ -130,6 +137,7 @@ struct UnitIter {
             u.k0 = k0;
             u.k1 = k0 + static_cast<int>(seg_end - it);
             u.kind = (k0 == 0 && u.k1 == p.k_tiles) ? UNIT_FULL : (k0 == 0 ? UNIT_HEAD : UNIT_TAIL);
+            u.rev = 0;
             it = seg_end;
             return true;
         }
@@ -479,11 +487,14 @@ __device__ __forceinline__ bool head_fixup(uint32_t tbase, int lane, const float
 //   With beta != 0 on the TMA path, each box of C_in is first TMA-loaded into the warp's staging
 //   buffer (completing on cin_bar; *cin_uses counts this warp's loads for the barrier parity), read
 //   back row per lane, and the result overwrites it in place before the TMA store.
+//   cin_ring != 0 (the cluster's last unit, whose operand ring is idle): all of the warp's C_in boxes
+//   are loaded at once, each into its own 4 KB at cin_ring, and each result is stored from there, so
+//   the boxes do not wait for one another's round trips.
 template <int kOut, int kCols, bool kTrans = false>
 __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUtensorMap* tmC, uint32_t tbase,
                                               int row0, int col_base, int lane, uint32_t stage_buf,
                                               float* out_part, uint32_t cin_bar, uint32_t* cin_uses,
-                                              const volatile int* abort_flag) {
+                                              const volatile int* abort_flag, uint32_t cin_ring = 0) {
     const int row = row0 + lane;
     if (out_part != nullptr) {
         float4* dst = reinterpret_cast<float4*>(out_part);
@@ -506,13 +517,36 @@ __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUten
     constexpr bool kWholeBoxes = kCols % kChunk == 0;
     if (kWholeBoxes && !kTrans && p.use_tma_store) {
         const bool warp_rows_in = row0 < p.M;
-        const uint32_t row_addr = stage_buf + static_cast<uint32_t>(lane) * 128u;
+        constexpr int kBoxes = kCols / kChunk;
+        const bool ring_cin = cin_ring != 0 && p.beta != 0.0f && warp_rows_in;   // warp-uniform
+        if (ring_cin) {
+            int nbox = 0;
 #pragma unroll 1
-        for (int c = 0; c < kCols / kChunk; ++c) {
+            for (int c = 0; c < kBoxes; ++c) nbox += (col_base + c * kChunk < p.N) ? 1 : 0;
+            if (nbox > 0) {
+                __syncwarp();
+                if (lane == 0) {
+                    fence_proxy_async_smem();   // earlier generic reads of this region (a fix-up) precede the copies
+                    mbar_arrive_expect_tx(cin_bar, static_cast<uint32_t>(nbox) * 32u * 128u);
+#pragma unroll 1
+                    for (int c = 0; c < kBoxes; ++c)
+                        if (col_base + c * kChunk < p.N)
+                            tma_load_2d(cin_ring + static_cast<uint32_t>(c) * 4096u, tmC, col_base + c * kChunk, row0,
+                                        cin_bar);
+                }
+                const bool ok = mbar_wait_bounded(cin_bar, *cin_uses & 1u, p.timeout_ns, abort_flag);
+                ++*cin_uses;
+                if (!__all_sync(0xffffffffu, ok)) return false;
+            }
+        }
+#pragma unroll 1
+        for (int c = 0; c < kBoxes; ++c) {
             const int col0 = col_base + c * kChunk;
             const bool box_in = warp_rows_in && col0 < p.N;   // warp-uniform
             const bool with_cin = box_in && p.beta != 0.0f;
-            if (with_cin && lane == 0) {
+            const uint32_t buf = ring_cin ? cin_ring + static_cast<uint32_t>(c) * 4096u : stage_buf;
+            const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128u;
+            if (with_cin && !ring_cin && lane == 0) {
                 bulk_wait_group_read<0>();                    // the previous store has read the buffer
                 mbar_arrive_expect_tx(cin_bar, 32u * 128u);
                 tma_load_2d(stage_buf, tmC, col0, row0, cin_bar);
@@ -524,9 +558,11 @@ __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUten
             tmem_wait_ld();
             float v[32];
             if (with_cin) {
-                const bool ok = mbar_wait_bounded(cin_bar, *cin_uses & 1u, p.timeout_ns, abort_flag);
-                ++*cin_uses;
-                if (!__all_sync(0xffffffffu, ok)) return false;
+                if (!ring_cin) {
+                    const bool ok = mbar_wait_bounded(cin_bar, *cin_uses & 1u, p.timeout_ns, abort_flag);
+                    ++*cin_uses;
+                    if (!__all_sync(0xffffffffu, ok)) return false;
+                }
                 // Row `lane` of the box: 16-byte piece j sits at piece j ^ (lane & 7) (128-byte swizzle).
                 uint32_t cw[32];
 #pragma unroll
@@ -578,7 +614,7 @@ __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUten
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_store_2d(tmC, col0, row0, stage_buf);
+                tma_store_2d(tmC, col0, row0, buf);
                 bulk_commit_group();
             }
         }
@@ -745,18 +781,21 @@ __device__ __forceinline__ void q4_store(uint32_t sb, int row0, int b, const Q4H
 struct StageWalk {
     UnitIter units;
     Unit u;
-    int kt;
+    int i;        // stage index inside the unit
+    int kt;       // its k-tile
     bool valid;
     __device__ __forceinline__ void init(const KernelParams& p, int cluster, int num_clusters) {
         units.init(p, cluster, num_clusters);
         valid = units.next(p, u);
-        kt = valid ? u.k0 : 0;
+        i = 0;
+        kt = valid ? u.kt_at(0) : 0;
     }
     __device__ __forceinline__ void advance(const KernelParams& p) {
-        if (++kt >= u.k1) {
+        if (++i >= u.k1 - u.k0) {
             valid = units.next(p, u);
-            kt = valid ? u.k0 : 0;
+            i = 0;
         }
+        kt = valid ? u.kt_at(i) : 0;
     }
 };
 
@@ -843,7 +882,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 int mb, nb;
                 tile_coords(p, u.tile, mb, nb);
                 const int m0 = mb * kClusterRows + static_cast<int>(rank) * Cfg::kBM;
-                for (int kt = u.k0; kt < u.k1; ++kt) {
+                for (int i = 0; i < u.k1 - u.k0; ++i) {
+                    const int kt = u.kt_at(i);
                     if (!mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, p.timeout_ns, abort_flag)) {
                         if (!*abort_flag) report_error<kClusterCtas>(p, ROLE_PRODUCER, u.tile, static_cast<int>(stage), abort_flag);
                         ok = false;
@@ -953,7 +993,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * static_cast<uint32_t>(Cfg::kAccCols);
-                for (int kt = u.k0; kt < u.k1; ++kt) {
+                for (int i = 0; i < u.k1 - u.k0; ++i) {
                     // With dequantised B the peer CTA's warps arrive on this barrier too (release at
                     // cluster scope), so the wait acquires at cluster scope.
                     if (!mbar_wait_bounded<kQ4 && kCtaGroup == 2>(smem_u32(&bar_full[stage]), phase, p.timeout_ns,
@@ -970,7 +1010,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                         for (int h = 0; h < Cfg::kNHalves; ++h) {
                             const uint32_t dt = d_tmem + static_cast<uint32_t>(h * Cfg::kMmaN);
-                            const uint32_t accum = (kt > u.k0 || k > 0) ? 1u : 0u;
+                            const uint32_t accum = (i > 0 || k > 0) ? 1u : 0u;
                             if constexpr (kElt == 1) mma_f8<kCtaGroup>(dt, ad + a_koff[k], bd + b_hoff[h] + b_koff[k], p.idesc, accum);
                             else mma_f16<kCtaGroup>(dt, ad + a_koff[k], bd + b_hoff[h] + b_koff[k], p.idesc, accum);
                         }
@@ -997,15 +1037,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // This warp's block inside a CTA slot of the partials.
         const size_t warp_block = static_cast<size_t>(rank) * 128 * kBN + static_cast<size_t>(ew) * Cfg::kEpiCols * 32;
         uint32_t acc = 0, acc_phase = 0, cin_uses = 0;
+        // The slice of the operand ring this warp may use once the ring is idle (its cluster's last unit).
+        constexpr uint32_t kRingSlice = (static_cast<uint32_t>(Cfg::kRingBytes) / Cfg::kEpiWarps) & ~4095u;
+        constexpr int kCinBoxes = Cfg::kEpiCols / ((kOut == OUT_F32) ? 32 : 64);
+        constexpr bool kRingCin = kRingSlice >= static_cast<uint32_t>(kCinBoxes) * 4096u;
+        const uint32_t ring_slice = ring + static_cast<uint32_t>(ew) * kRingSlice;
         UnitIter units;
         units.init(p, cluster_id, num_clusters);
-        Unit u;
-        while (units.next(p, u)) {
+        Unit u, u_next;
+        bool have = units.next(p, u);
+        while (have) {
+            const bool more = units.next(p, u_next);
             int mb, nb;
             tile_coords(p, u.tile, mb, nb);
             const int row0 = mb * kClusterRows + static_cast<int>(rank) * Cfg::kBM + quarter * 32;
             if (p.beta != 0.0f && u.kind != UNIT_TAIL && !p.c_trans)
-                prefetch_c_rows<kOut, Cfg::kEpiCols>(p, row0 + lane, nb * kBN + pcol0);
+                prefetch_c_rows<kOut, Cfg::kEpiCols>(p, row0 + lane, nb * kBN + pcol0);   // C_in rows into L2
             bool ok = mbar_wait_bounded(smem_u32(&bar_tfull[acc]), acc_phase, p.timeout_ns, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
@@ -1086,7 +1133,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                                                    out_part, smem_u32(&bar_cin[ew]), &cin_uses, abort_flag);
             else
                 drained = epilogue_tile<kOut, Cfg::kEpiCols>(p, &tmC, tbase, row0, nb * kBN + pcol0, lane, stage_buf,
-                                                             out_part, smem_u32(&bar_cin[ew]), &cin_uses, abort_flag);
+                                                             out_part, smem_u32(&bar_cin[ew]), &cin_uses, abort_flag,
+                                                             (kRingCin && !more) ? ring_slice : 0u);
             if (!drained) {
                 if (lane == 0 && !*abort_flag)
                     report_error<kClusterCtas>(p, ROLE_EPILOGUE, u.tile, 400 + quarter, abort_flag);
@@ -1106,6 +1154,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
             }
             if (++acc == static_cast<uint32_t>(Cfg::kAccBufs)) { acc = 0; acc_phase ^= 1u; }
+            u = u_next;
+            have = more;
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
