@@ -64,9 +64,13 @@ template <int kM, int kOut, bool kBf16>
 __global__ void __launch_bounds__(kGemvWarps * 32) gemv_kernel(GemvParams p) {
     __shared__ float part[kGemvWarps][kGemvRows][kM];
     griddep_launch_dependents();
+    const int n0 = blockIdx.x * kGemvRows;
+    // This CTA's weight rows into L2 while the kernel before it may still run (see tma_prefetch_2d).
+    if (threadIdx.x < kGemvRows && n0 + static_cast<int>(threadIdx.x) < p.N)
+        bulk_prefetch_l2(static_cast<const uint8_t*>(p.W) + static_cast<long long>(n0 + threadIdx.x) * p.ldw_bytes,
+                         static_cast<uint32_t>(p.K) * 2u);
     griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kGemvRows;
     const int chunks = p.K / 8;                                     // 8 values per chunk (K % 8 == 0)
     const int per_warp = (chunks + kGemvWarps - 1) / kGemvWarps;
     const int c_begin = warp * per_warp;
@@ -178,10 +182,18 @@ __global__ void __launch_bounds__(kQ4Threads) gemv_q4_0_kernel(GemvParams p) {
     constexpr int kWarps = kQ4Threads / 32;
     __shared__ float part[kWarps][kQ4Rows][kM];
     griddep_launch_dependents();
-    griddep_wait();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kQ4Rows;
     const int nblk = p.K / 32;
+    // This CTA's block rows into L2 while the kernel before it may still run (see tma_prefetch_2d); a row
+    // starts at any 2-byte boundary, so the range is widened to the 16-byte granules that hold it.
+    if (threadIdx.x < kQ4Rows && n0 + static_cast<int>(threadIdx.x) < p.N) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(static_cast<const uint8_t*>(p.W) +
+                                                        static_cast<long long>(n0 + threadIdx.x) * p.ldw_bytes);
+        const uintptr_t lo = a & ~static_cast<uintptr_t>(15), hi = (a + 18ull * nblk + 15) & ~static_cast<uintptr_t>(15);
+        bulk_prefetch_l2(reinterpret_cast<const void*>(lo), static_cast<uint32_t>(hi - lo));
+    }
+    griddep_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint8_t* Bq = static_cast<const uint8_t*>(p.W);
     const uint8_t* A = static_cast<const uint8_t*>(p.A);
     float acc[kQ4Rows][kM];

@@ -835,6 +835,81 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const uint32_t epi_smem = ring + Cfg::kRingBytes;
     volatile int* abort_flag = &s_abort;
 
+    // The TMA copies of one operand stage -- k-tile kt of output tile (mb, nb) -- into sa / sb, completing on
+    // full_bar; with `prefetch` the same boxes are only brought into L2.
+    auto stage_copies = [&](int mb, int nb, int kt, uint32_t sa, uint32_t sb, uint32_t full_bar, bool prefetch) {
+        const int m0 = mb * kClusterRows + static_cast<int>(rank) * Cfg::kBM;
+        const int k0 = kt * Cfg::kBK;
+        auto load = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1) {
+            if (prefetch) tma_prefetch_2d(map, c0, c1);
+            else if constexpr (kCtaGroup == 2) tma_load_2d_pair(dst, map, c0, c1, full_bar);
+            else tma_load_2d(dst, map, c0, c1, full_bar);
+        };
+        auto load3 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2) {
+            if (prefetch) tma_prefetch_3d(map, c0, c1, c2);
+            else if constexpr (kCtaGroup == 2) tma_load_3d_pair(dst, map, c0, c1, c2, full_bar);
+            else tma_load_3d(dst, map, c0, c1, c2, full_bar);
+        };
+        if (!p.a_mn) {
+            if (p.a_3d) {
+                load3(sa, &tmA, 0, m0, kt * Cfg::kKChunks);   // box {64, 128 M, K chunks}
+            } else {
+#pragma unroll
+                for (int c = 0; c < Cfg::kKChunks; ++c)  // box {one swizzle span of K, 128 M} per chunk
+                    load(sa + static_cast<uint32_t>(c * Cfg::kAChunkBytes), &tmA, k0 + Cfg::kKChunkElems * c, m0);
+            }
+        } else {
+            if (p.a_3d) {
+                load3(sa, &tmA, 0, k0, m0 / 64);          // box {64, BK K, 2 M slabs}
+            } else {
+                load(sa, &tmA, m0, k0);                   // box {64 M, BK K} slabs
+                load(sa + static_cast<uint32_t>(Cfg::kSlabBytes), &tmA, m0 + 64, k0);
+            }
+        }
+        if constexpr (kQ4) {
+            // B arrives from the dequantisation warps.
+        } else {
+            // For each MMA N half h the CTA holds columns
+            // [nb*BN + h*kMmaN + prank*kHalfCols, +kHalfCols).
+#pragma unroll
+            for (int h = 0; h < Cfg::kNHalves; ++h) {
+                const int nh = nb * kBN + h * Cfg::kMmaN + static_cast<int>(prank) * Cfg::kHalfCols;
+                if (!p.b_mn) {
+                    if (p.b_3d) {                         // box {64, kHalfCols N, K chunks}
+                        load3(sb, &tmB, 0, nh, kt * Cfg::kKChunks);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < Cfg::kKChunks; ++c)  // box {one span of K, kHalfCols N} per chunk
+                            load(sb + static_cast<uint32_t>(c * Cfg::kBChunkBytes + h * Cfg::kHalfCols * 128),
+                                 &tmB, k0 + Cfg::kKChunkElems * c, nh);
+                    }
+                } else {
+                    const uint32_t dh = sb + static_cast<uint32_t>(h * (Cfg::kHalfCols / 64) * Cfg::kSlabBytes);
+                    if (p.b_3d) {                         // box {64, BK K, N slabs}
+                        load3(dh, &tmB, 0, k0, nh / 64);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < Cfg::kHalfCols / 64; ++j)  // box {64 N, BK K} slabs
+                            load(dh + static_cast<uint32_t>(j * Cfg::kSlabBytes), &tmB, nh + 64 * j, k0);
+                    }
+                }
+            }
+        }
+    };
+    if (threadIdx.x == 0) {
+        // The first ring of operand stages of this cluster's first unit into L2 before anything else: the
+        // kernel before this one on the stream may still be running (the waits below come later), and the
+        // loads of these stages then hit L2.
+        UnitIter first_units;
+        first_units.init(p, cluster_id, num_clusters);
+        Unit fu;
+        if (first_units.next(p, fu)) {
+            int mb, nb;
+            tile_coords(p, fu.tile, mb, nb);
+            const int n = min(kStages, fu.k1 - fu.k0);
+            for (int i = 0; i < n; ++i) stage_copies(mb, nb, fu.kt_at(i), 0u, 0u, 0u, true);
+        }
+    }
     if (threadIdx.x == 0) {
         s_abort = 0;
         for (int s = 0; s < kStages; ++s) {
@@ -881,7 +956,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             while (ok && units.next(p, u)) {
                 int mb, nb;
                 tile_coords(p, u.tile, mb, nb);
-                const int m0 = mb * kClusterRows + static_cast<int>(rank) * Cfg::kBM;
                 for (int i = 0; i < u.k1 - u.k0; ++i) {
                     const int kt = u.kt_at(i);
                     if (!mbar_wait_bounded(smem_u32(&bar_empty[stage]), phase ^ 1u, p.timeout_ns, abort_flag)) {
@@ -896,60 +970,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         if (prank == 0) mbar_arrive_expect_tx(full_local, tx_bytes);
                         const uint32_t sa = ring + stage * Cfg::kStageBytes;
                         const uint32_t sb = sa + Cfg::kABytes;
-                        const int k0 = kt * Cfg::kBK;
-                        auto load = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1) {
-                            if constexpr (kCtaGroup == 2) tma_load_2d_pair(dst, map, c0, c1, full_bar);
-                            else tma_load_2d(dst, map, c0, c1, full_bar);
-                        };
-                        auto load3 = [&](uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2) {
-                            if constexpr (kCtaGroup == 2) tma_load_3d_pair(dst, map, c0, c1, c2, full_bar);
-                            else tma_load_3d(dst, map, c0, c1, c2, full_bar);
-                        };
-                        if (!p.a_mn) {
-                            if (p.a_3d) {
-                                load3(sa, &tmA, 0, m0, kt * Cfg::kKChunks);   // box {64, 128 M, K chunks}
-                            } else {
-#pragma unroll
-                                for (int c = 0; c < Cfg::kKChunks; ++c)  // box {one swizzle span of K, 128 M} per chunk
-                                    load(sa + static_cast<uint32_t>(c * Cfg::kAChunkBytes), &tmA, k0 + Cfg::kKChunkElems * c, m0);
-                            }
-                        } else {
-                            if (p.a_3d) {
-                                load3(sa, &tmA, 0, k0, m0 / 64);          // box {64, BK K, 2 M slabs}
-                            } else {
-                                load(sa, &tmA, m0, k0);                   // box {64 M, BK K} slabs
-                                load(sa + static_cast<uint32_t>(Cfg::kSlabBytes), &tmA, m0 + 64, k0);
-                            }
-                        }
-                        if constexpr (kQ4) {
-                            // B arrives from the dequantisation warps.
-                        } else {
-                            // For each MMA N half h the CTA holds columns
-                            // [nb*BN + h*kMmaN + prank*kHalfCols, +kHalfCols).
-#pragma unroll
-                            for (int h = 0; h < Cfg::kNHalves; ++h) {
-                                const int nh = nb * kBN + h * Cfg::kMmaN + static_cast<int>(prank) * Cfg::kHalfCols;
-                                if (!p.b_mn) {
-                                    if (p.b_3d) {                         // box {64, kHalfCols N, K chunks}
-                                        load3(sb, &tmB, 0, nh, kt * Cfg::kKChunks);
-                                    } else {
-#pragma unroll
-                                        for (int c = 0; c < Cfg::kKChunks; ++c)  // box {one span of K, kHalfCols N} per chunk
-                                            load(sb + static_cast<uint32_t>(c * Cfg::kBChunkBytes + h * Cfg::kHalfCols * 128),
-                                                 &tmB, k0 + Cfg::kKChunkElems * c, nh);
-                                    }
-                                } else {
-                                    const uint32_t dh = sb + static_cast<uint32_t>(h * (Cfg::kHalfCols / 64) * Cfg::kSlabBytes);
-                                    if (p.b_3d) {                         // box {64, BK K, N slabs}
-                                        load3(dh, &tmB, 0, k0, nh / 64);
-                                    } else {
-#pragma unroll
-                                        for (int j = 0; j < Cfg::kHalfCols / 64; ++j)  // box {64 N, BK K} slabs
-                                            load(dh + static_cast<uint32_t>(j * Cfg::kSlabBytes), &tmB, nh + 64 * j, k0);
-                                    }
-                                }
-                            }
-                        }
+                        stage_copies(mb, nb, kt, sa, sb, full_bar, false);
                     }
                     ++gstage;
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }

@@ -157,6 +157,25 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
                  : "memory");
 }
 
+// The boxes a tiled load with the same coordinates would copy, brought into L2 only (no shared memory,
+// no barrier).  L2 is where every write of the device lands, so a line prefetched before the kernel
+// that writes it has finished still reads back that kernel's data.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1) : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+
+// Bring `bytes` (a multiple of 16) from the 16-byte aligned global address `src` into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                 :: "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes) : "memory");
+}
+
 // 2-D tiled store of one box from shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t c0, int32_t c1, uint32_t src) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
