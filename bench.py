@@ -49,6 +49,10 @@ def _args():
                     help="1..10 (6, 10: Q4_0 weights through gemm_run_q4_0; 7, 8, 10: decode shapes, HBM-bound)")
     ap.add_argument("--config", type=int, default=-1)
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic stream serialization")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the bench line: every 16-bit config on workloads 1-5 under the rotate protocol, "
+                         "the planner's pick marked; one JSON line per (workload, config), then a markdown table")
+    ap.add_argument("--sweep-workloads", default="1,2,3,4,5")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps, capped at 200")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -450,6 +454,90 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------------------------------ sweep
+def graph_step_us(step_on, n_sets: int, reps: int = 20) -> float:
+    """Mean device time per step of n_sets steps (one per operand set) captured in one CUDA graph and
+    replayed `reps` times back to back (the rotate protocol)."""
+    import numpy as np
+    import torch
+    stream = torch.cuda.current_stream()
+    for j in range(n_sets):
+        step_on(j, stream.cuda_stream)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for j in range(n_sets):
+            step_on(j, cap.cuda_stream)
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    evs[0].record(stream)
+    for i in range(reps):
+        graph.replay()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return float(np.mean([evs[i].elapsed_time(evs[i + 1]) * 1e3 / n_sets for i in range(reps)]))
+
+
+def run_sweep(args, local):
+    """Every 16-bit config (and the planner's automatic choice) on the chosen workloads."""
+    import torch
+
+    import __graft_entry__
+    from bf16_tensor_core_gb300 import gemm as G
+    from bf16_tensor_core_gb300 import workloads as W
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    l2 = getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 132 << 20)
+    configs = [c for c in range(G.gemm_num_configs())
+               if G.gemm_config_info(c)[1].in_bytes == 2 and not G.gemm_config_info(c)[1].b_q4_0]
+    rows = []
+    for wid in [int(x) for x in args.sweep_workloads.split(",")]:
+        w = W.WORKLOADS[wid]
+        d = W.generate(w)
+        A, B = d["A"].to(dev), d["B"].to(dev)
+        bias = d["bias"].to(dev) if d["bias"] is not None else None
+        C0 = (d["Cin"].to(dev) if d["Cin"] is not None
+              else torch.empty(w.M, w.N, dtype=W.DTYPES[w.dtype_out], device=dev))
+        n_sets = max(2, min(512, -(-3 * l2 // algorithmic_bytes(w)) + 1))
+        sets = [(A, B, C0)] + [(A.clone(), B.clone(), C0.clone()) for _ in range(n_sets - 1)]
+        for cfg in [-1] + configs:
+            g = G.Gemm(local, config=cfg)
+
+            def step_on(j, st, g=g):
+                a, b, c = sets[j]
+                g.run(a, b, c, M=w.M, N=w.N, K=w.K, layoutA=w.layoutA, layoutB=w.layoutB, alpha=w.alpha,
+                      beta=w.beta, bias=bias, stream=st)
+            us = graph_step_us(step_on, n_sets)
+            plan = g.last_plan()
+            if g.status() != G.GEMM_OK:
+                raise RuntimeError(f"sweep: {w.name} config {cfg}: {g.last_error()}")
+            g.close()
+            row = {"workload": w.name, "config": cfg, "plan_config": plan.get("config"),
+                   "stream_k": plan.get("stream_k"), "clusters": plan.get("clusters"), "us_per_step": us,
+                   "tflops": w.flops / us / 1e6, "n_sets": n_sets}
+            rows.append(row)
+            print(json.dumps(row), flush=True)
+        del sets
+        torch.cuda.empty_cache()
+    # the table: one row per workload, one column per config, the planner's pick in bold
+    names = sorted({r["workload"] for r in rows}, key=lambda n: [r["workload"] for r in rows].index(n))
+    print("| workload | " + " | ".join(f"config {c}" for c in configs) + " | planner |")
+    print("|---|" + "---|" * (len(configs) + 1))
+    for n in names:
+        auto = next(r for r in rows if r["workload"] == n and r["config"] == -1)
+        cells = []
+        for c in configs:
+            r = next(r for r in rows if r["workload"] == n and r["config"] == c)
+            cell = f"{r['us_per_step']:.1f} us ({r['tflops']:.0f})"
+            cells.append(f"**{cell}**" if c == auto["plan_config"] else cell)
+        print(f"| {n} | " + " | ".join(cells) + f" | config {auto['plan_config']}: {auto['us_per_step']:.1f} us |")
+
+
 # ------------------------------------------------------------------------------------------ ours
 def run_ours(args, rank, world, local):
     import numpy as np
@@ -797,7 +885,10 @@ def main():
         import torch.distributed as dist
         backend = "nccl" if (torch.cuda.is_available() and args.impl == "ours") else "gloo"
         dist.init_process_group(backend)
-    if args.impl == "reference":
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args, int(os.environ.get("LOCAL_RANK", "0")))
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, int(os.environ.get("LOCAL_RANK", "0")))
