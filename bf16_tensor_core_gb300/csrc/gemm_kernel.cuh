@@ -490,7 +490,9 @@ __device__ __forceinline__ bool head_fixup(uint32_t tbase, int lane, const float
 //   cin_ring != 0 (the cluster's last unit, whose operand ring is idle): all of the warp's C_in boxes
 //   are loaded at once, each into its own 4 KB at cin_ring, and each result is stored from there, so
 //   the boxes do not wait for one another's round trips.
-template <int kOut, int kCols, bool kTrans = false>
+//   kLean (a CTA of 14 warps, 128 registers each): the second 32-column half of a 16-bit box is read from
+//   TMEM only after the first half is packed, so that the two halves are never live together.
+template <int kOut, int kCols, bool kTrans = false, bool kLean = false>
 __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUtensorMap* tmC, uint32_t tbase,
                                               int row0, int col_base, int lane, uint32_t stage_buf,
                                               float* out_part, uint32_t cin_bar, uint32_t* cin_uses,
@@ -552,10 +554,20 @@ __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUten
                 tma_load_2d(stage_buf, tmC, col0, row0, cin_bar);
             }
             uint32_t words[32];
-            uint32_t acc0[32], acc1[32];
+            uint32_t acc0[32], acc1[kLean ? 1 : 32];
             tmem_ld_32x32b_x32(tbase + c * (kChunk == 32 ? 32 : 64), acc0);
-            if constexpr (kChunk == 64) tmem_ld_32x32b_x32(tbase + c * 64 + 32, acc1);
+            if constexpr (kChunk == 64 && !kLean) tmem_ld_32x32b_x32(tbase + c * 64 + 32, acc1);
             tmem_wait_ld();
+            // The second half of a 16-bit box (kLean: read into acc0 once the first half is packed).
+            auto second_half = [&]() -> const uint32_t (&)[32] {
+                if constexpr (kLean) {
+                    tmem_ld_32x32b_x32(tbase + c * 64 + 32, acc0);
+                    tmem_wait_ld();
+                    return acc0;
+                } else {
+                    return acc1;
+                }
+            };
             float v[32];
             if (with_cin) {
                 if (!ring_cin) {
@@ -585,7 +597,8 @@ __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUten
                     for (int h = 0; h < 2; ++h) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) unpack2<kOut>(cw[16 * h + i], cin[2 * i], cin[2 * i + 1]);
-                        epilogue_math_cin<kOut>(p, h == 0 ? acc0 : acc1, v, cin, col0 + 32 * h);
+                        if (h == 0) epilogue_math_cin<kOut>(p, acc0, v, cin, col0);
+                        else epilogue_math_cin<kOut>(p, second_half(), v, cin, col0 + 32);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) words[16 * h + i] = pack2<kOut>(v[2 * i], v[2 * i + 1]);
                     }
@@ -598,7 +611,7 @@ __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUten
                 } else {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) words[i] = pack2<kOut>(v[2 * i], v[2 * i + 1]);
-                    epilogue_math<kOut>(p, acc1, v, row, col0 + 32);
+                    epilogue_math<kOut>(p, second_half(), v, row, col0 + 32);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) words[16 + i] = pack2<kOut>(v[2 * i], v[2 * i + 1]);
                 }
@@ -1153,7 +1166,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 drained = epilogue_tile<kOut, Cfg::kEpiCols, !kQ4>(p, &tmC, tbase, row0, nb * kBN + pcol0, lane, stage_buf,
                                                                    out_part, smem_u32(&bar_cin[ew]), &cin_uses, abort_flag);
             else
-                drained = epilogue_tile<kOut, Cfg::kEpiCols>(p, &tmC, tbase, row0, nb * kBN + pcol0, lane, stage_buf,
+                drained = epilogue_tile<kOut, Cfg::kEpiCols, false, kQ4>(p, &tmC, tbase, row0, nb * kBN + pcol0, lane, stage_buf,
                                                              out_part, smem_u32(&bar_cin[ew]), &cin_uses, abort_flag,
                                                              (kRingCin && !more) ? ring_slice : 0u);
             if (!drained) {
