@@ -1181,8 +1181,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if constexpr (kCtaGroup == 2) mbar_arrive_cluster(mapa_shared(te, lrank));
                 else mbar_arrive_local(te);
                 if (out_part != nullptr) {
-                    // Every lane's partial stores precede this release (warp barrier, then fence).
-                    __threadfence();
+                    // Every lane's partial stores precede this release: the warp barrier above orders
+                    // them before it, and a release is cumulative.
                     st_release_gpu(p.sk_flags + (static_cast<size_t>(cluster_id) * kClusterCtas + rank) * Cfg::kEpiWarps + ew,
                                    p.epoch);
                 }

@@ -535,6 +535,7 @@ def test_last_plan_reports_the_run():
     (4, 0, dict(M=2274, N=2300, K=700, dtype_out="f32", layoutA="col")),             # stream-K heads
     (4, 24, dict(M=640, N=512, K=2048, dtype_out="f32", beta=1.0)),                  # reduce-scatter, S = 4
     (7, 0, dict(M=300, N=200, K=2048, dtype_out="f16", bias=True)),                  # reduce-scatter, S = 4
+    (7, 32, dict(M=40, N=1024, K=4096, dtype_out="f32", layoutB="col", beta=1.0)),  # C^T, reduce-scatter, S = 4
 ])
 def test_graph_replay_with_stream_k_hand_off(cfg, mc, c):
     """A captured call replayed several times, with new A each time, matches the oracle every time: the

@@ -76,6 +76,35 @@ def test_skinny_split_k_and_fixup():
     assert plan["transposed"] == 1 and plan["stream_k"] == 1 and plan["clusters"] > plan["tiles_m"] * plan["tiles_n"]
 
 
+@pytest.mark.parametrize("S", [2, 4])
+@pytest.mark.parametrize("dout,beta,bias", [("f16", 0.0, False), ("f32", 1.0, True), ("bf16", 0.0, True)])
+def test_skinny_split_reduction_is_deterministic(S, dout, beta, bias):
+    """40 x 1024 x 4096: 8 tiles of C^T, each split over S CTAs whose partial sums are reduced as a
+    reduce-scatter.  Each block is added up in a fixed order, so every run gives the same bits
+    whichever part finishes first, and the result matches the oracle."""
+    _need_gpu()
+    din = "bf16" if dout == "bf16" else "f16"
+    w = W.problem(40, 1024, 4096, dtype_in=din, dtype_out=dout, layoutB="col", bias=bias, alpha=0.75, beta=beta,
+                  seed=640 + S)
+    d = W.generate(w)
+    dd = device_inputs(d)
+    C0 = alloc_c(w, d)
+    outs = []
+    with G.Gemm(0, stream_k=1, max_clusters=8 * S) as g:
+        for _ in range(6):
+            C = C0.clone()
+            run_gpu(g, w, dd, C)
+            outs.append(C)
+        plan = g.last_plan()
+        assert g.status() == G.GEMM_OK
+    torch.cuda.synchronize()
+    assert plan["transposed"] == 1 and plan["stream_k"] == 1 and plan["clusters"] == 8 * S
+    rep = compare(w, d, outs[0])
+    assert rep["passed"], rep
+    for C in outs[1:]:
+        assert torch.equal(C, outs[0])
+
+
 def test_skinny_integers_equal_plain_product():
     """Small integers: the transposed and the plain product are both exact, hence equal."""
     _need_gpu()
