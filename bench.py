@@ -103,9 +103,14 @@ def _kernel_hash(kernel: str = "gb300::gemm_tc_kernel") -> str:
     return h.hexdigest()[:16]
 
 
-def _traffic(workload_name: str, kernel: str, config: int):
+# The schedule fields that decide which operand lines a launch reads; a traffic figure taken under
+# another schedule does not describe this launch.
+TRAFFIC_PLAN_KEYS = ("config", "clusters", "stream_k", "dp_tiles", "raster_group")
+
+
+def _traffic(workload_name: str, kernel: str, plan: dict):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if it was
-    taken on that kernel and config with the current sources (else None)."""
+    taken on that kernel, with the current sources and the same schedule (else None)."""
     p = ROOT / "profiles" / "traffic.json"
     if not p.exists():
         return None, None
@@ -113,8 +118,8 @@ def _traffic(workload_name: str, kernel: str, config: int):
         d = json.loads(p.read_text())
         entries = d.get(workload_name) or []
         for e in entries if isinstance(entries, list) else [entries]:   # one entry per kernel and config
-            if (e.get("kernel") == kernel and e.get("config", -1) == config
-                    and e.get("kernel_hash") == _kernel_hash(kernel)):
+            same_plan = all(e.get("plan", {}).get(k) == plan.get(k) for k in TRAFFIC_PLAN_KEYS)
+            if e.get("kernel") == kernel and same_plan and e.get("kernel_hash") == _kernel_hash(kernel):
                 return e.get("dram_bytes_per_launch"), e.get("source")
     except Exception:
         pass
@@ -823,7 +828,7 @@ def run_ours(args, rank, world, local):
         kernel = "gb300::gemv_q4_0_kernel" if w.layoutB == "q4_0" else "gb300::gemv_kernel"
     else:
         kernel = "gb300::gemm_tc_kernel"
-    traffic, traffic_src = _traffic(w.name, kernel, plan.get("config", -1))
+    traffic, traffic_src = _traffic(w.name, kernel, plan)
     if w.flops / alg_bytes < peak * 1e12 / (hbm * 1e9):      # below the ridge: the stream of bytes bounds it
         gbs = alg_bytes / (ms_per_step / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": traffic,
@@ -859,8 +864,8 @@ def run_ours(args, rank, world, local):
             "config": _config_dict(w, args, {"l2": l2_text[args.l2], "kernel_config": plan.get("config", args.config),
                                              "plan": {k: plan[k] for k in ("block_m", "block_n", "block_k", "stages",
                                                                            "tiles_m", "tiles_n", "clusters",
-                                                                           "stream_k", "dp_tiles", "transposed", "gemv",
-                                                                           "q4_dequant", "kernels")
+                                                                           "stream_k", "dp_tiles", "raster_group",
+                                                                           "transposed", "gemv", "q4_dequant", "kernels")
                                                       if k in plan},
                                              "timing": timing_text[args.l2]}),
             "roofline": roof, "clocks": clocks, "gpu_launches": launches, "e2e": e2e,

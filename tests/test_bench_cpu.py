@@ -50,20 +50,24 @@ def test_traffic_file_entries_are_complete():
         assert e["kernel"] in ("gb300::gemm_tc_kernel", "gb300::gemv_kernel", "gb300::gemv_q4_0_kernel")
         assert e["dram_bytes_per_launch"] == e["dram_bytes_read"] + e["dram_bytes_write"]
         assert e["gpu_time_ns"] > 0 and len(e["kernel_hash"]) == 16
+        assert set(bench.TRAFFIC_PLAN_KEYS) <= set(e["plan"]), e["plan"]
         # The capture command runs committed files only, with the clocks left alone.
         assert "bench.py" in e["source"] and "--clock-control none" in e["source"]
 
 
-def test_traffic_is_reported_only_for_the_current_kernel_sources(monkeypatch):
+def test_traffic_is_reported_only_for_the_current_kernel_sources_and_schedule(monkeypatch):
     name, e = next((n, e) for n, e in _entries() if n == "gemm_4096_f16_f16")
     real = bench._kernel_hash
     monkeypatch.setattr(bench, "_kernel_hash", lambda kernel="gb300::gemm_tc_kernel": e["kernel_hash"])
-    got, src = bench._traffic(name, e["kernel"], e["config"])
+    plan = dict(e["plan"], tiles_m=16)                   # fields outside the schedule key do not matter
+    got, src = bench._traffic(name, e["kernel"], plan)
     assert got == e["dram_bytes_per_launch"] and "ncu" in src
-    # Another config of the same kernel, or changed sources, has no figure.
-    assert bench._traffic(name, e["kernel"], e["config"] + 1) == (None, None)
+    # Another config, another schedule of the same config, or changed sources: no figure.
+    for k, v in (("config", plan["config"] + 1), ("raster_group", plan["raster_group"] + 1),
+                 ("dp_tiles", plan["dp_tiles"] + 1), ("clusters", plan["clusters"] - 1)):
+        assert bench._traffic(name, e["kernel"], dict(plan, **{k: v})) == (None, None), k
     monkeypatch.setattr(bench, "_kernel_hash", lambda kernel="gb300::gemm_tc_kernel": "0" * 16)
-    assert bench._traffic(name, e["kernel"], e["config"]) == (None, None)
+    assert bench._traffic(name, e["kernel"], plan) == (None, None)
     monkeypatch.setattr(bench, "_kernel_hash", real)
 
 

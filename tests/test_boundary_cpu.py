@@ -293,6 +293,22 @@ def test_plan_auto_choice_is_a_valid_config(lib):
         assert p.clusters >= 1 and p.raster_group >= 1 and p.raster_group <= p.tiles_m
 
 
+@pytest.mark.parametrize("M,N,K,cfg,group", [
+    (4096, 4096, 4096, 4, 8),        # 16 tile rows of 256: two groups of 8
+    (1024, 4096, 4096, 4, 4),        # 4 tile rows: one group
+    (8192, 8192, 8192, 4, 16),       # 32 tile rows: two groups of 16 (A panels 64 MiB per group)
+    (6144, 6144, 4096, 4, 12),       # 24 tile rows: two groups of 12
+    (8192, 8192, 16384, 4, 8),       # a group of 16 would hold 128 MiB of A panels: groups of 8
+    (8192, 4096, 4096, 0, 16),       # 64 tile rows of 128: four groups of 16
+])
+def test_plan_raster_group(lib, M, N, K, cfg, group):
+    """Tall products are rastered in as few groups of at most 16 tile rows as cover them (each group
+    re-reads every B panel), unless a group's A panels would outgrow half the L2."""
+    st, p = plan(M, N, K, dout=0, config=cfg)
+    assert st == G.GEMM_OK and p.config == cfg
+    assert p.raster_group == group, (M, N, K, p.tiles_m, p.raster_group)
+
+
 def test_python_binding_fails_loudly_without_library(tmp_path):
     code = ("import sys; sys.path.insert(0, %r)\n"
             "from bf16_tensor_core_gb300 import gemm\n"
