@@ -51,6 +51,8 @@ def _args():
                     help="1..10 (6, 10: Q4_0 weights through gemm_run_q4_0; 7, 8, 10: decode shapes, HBM-bound)")
     ap.add_argument("--config", type=int, default=-1)
     ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic stream serialization")
+    ap.add_argument("--raster-group", type=int, default=0,
+                    help="tile rows per raster group (the handle option; 0: the planner's)")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: every 16-bit config on workloads 1-5 under the rotate protocol, "
                          "the planner's pick marked; one JSON line per (workload, config), then a markdown table")
@@ -567,7 +569,7 @@ def run_ours(args, rank, world, local):
     C = (Cin_host.to(dev).clone() if Cin_host is not None
          else torch.empty(w.M, w.N, dtype=W.DTYPES[w.dtype_out], device=dev))
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    g = G.Gemm(local, config=args.config, pdl=0 if args.no_pdl else 1)
+    g = G.Gemm(local, config=args.config, pdl=0 if args.no_pdl else 1, raster_group=args.raster_group)
     stream = torch.cuda.current_stream(dev)
     s_handle = stream.cuda_stream
 

@@ -1041,6 +1041,12 @@ gemm_status_t gemm_get_device_status(gemm_handle_t h, void* stream) {
 
 namespace {
 
+// The handle's raster_group option, when set, replaces the planner's choice in the plan itself, so
+// that gemm_last_plan reports the group the kernel runs with.
+void apply_raster_option(const gemm_ctx* h, gemm_plan_t* plan) {
+    if (h->opt.raster_group > 0 && plan->tiles_m > 0) plan->raster_group = std::min(h->opt.raster_group, plan->tiles_m);
+}
+
 // The body of gemm_run and gemm_run_q4_0 (b_q4 = 1: B is Q4_0 weights at row pitch ldb bytes).
 gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                        int64_t ldb, void* C, int64_t ldc, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
@@ -1053,6 +1059,7 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
     gemm_status_t st = plan_impl(M, N, K, lda, ldb, ldc, dtype_in, dtype_out, layoutA, layoutB, beta, h->dev.slots,
                                  h->opt.config, h->opt.stream_k, h->opt.max_clusters, &plan, &err, b_q4);
     if (st != GEMM_OK) return fail(h, st, err);
+    apply_raster_option(h, &plan);
     if (M == 0 || N == 0) return GEMM_OK;
     if (!C) return fail(h, GEMM_ERR_INVALID_ARG, "C is NULL");
     if (K > 0 && (!A || !B)) return fail(h, GEMM_ERR_INVALID_ARG, "A or B is NULL");
@@ -1165,6 +1172,7 @@ gemm_status_t gemm_run_q4_0(gemm_handle_t h, int64_t M, int64_t N, int64_t K, co
     gemm_status_t st = plan_q4(M, N, K, lda, layoutA, ldbq, ldc, dtype_out, beta, h->dev.slots, h->opt.config,
                                h->opt.stream_k, h->opt.skinny, h->opt.max_clusters, &plan, &err, &route);
     if (st != GEMM_OK) return fail(h, st, err);
+    apply_raster_option(h, &plan);
     if (route == Q4_FUSED || M == 0 || N == 0 || K == 0)
         return run_impl(h, M, N, K, A, lda, Bq, ldbq, C, ldc, GEMM_F16, dtype_out, layoutA, GEMM_COL, alpha, beta,
                         bias, stream, 1);

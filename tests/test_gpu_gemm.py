@@ -334,6 +334,27 @@ def test_stream_k_matches_data_parallel_on_integers():
     assert torch.equal(outs[1].cpu(), ref)
 
 
+@pytest.mark.parametrize("group", [0, 1, 3, 16, 40])
+def test_raster_groups_cover_every_tile_once(group):
+    """Any raster group (the planner's, 1, one that does not divide the tile rows, or more rows than
+    there are) visits every tile exactly once: small integers give the exact product, and the plan
+    reports the group the kernel ran with."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    M, N, K = 4352, 1280, 512                       # 17 x 5 tiles of 256 x 256 on 76 clusters
+    A = W.small_ints(M, K, "f16", 7).cuda()
+    B = W.small_ints(K, N, "f16", 8).cuda()
+    C = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    with G.Gemm(0, config=4, raster_group=group, sync_check=1) as g:
+        g.run(A, B, C)
+        plan = g.last_plan()
+    torch.cuda.synchronize()
+    assert plan["tiles_m"] == 17
+    assert plan["raster_group"] == (min(group, 17) if group > 0 else 9)   # 17 rows: two groups of 9
+    ref = (A.cpu().to(torch.int64) @ B.cpu().to(torch.int64)).to(torch.float32)
+    assert torch.equal(C.cpu(), ref)
+
+
 # Fewer tiles than clusters: each tile's K range is split over several clusters and the head adds
 # every following cluster's partial (split-K).  K is long enough for several sources per tile.
 SPLIT_CASES = {
