@@ -92,7 +92,7 @@ typedef struct {
     int config;           /* -1: choose per call; else a kernel config id (gemm_config_info)  */
     int timeout_ms;       /* limit of every bounded device wait (default 2000)                */
     int sync_check;       /* 1: gemm_run synchronises the stream and reads the status word    */
-    int raster_group;     /* output-tile rows per raster group; 0 = automatic                 */
+    int raster_group;     /* output-tile rows per raster group; 0 = automatic (gemm_plan)     */
     int max_clusters;     /* cap on persistent clusters (0 = as many as fit on the device)    */
     int debug_skip_stage; /* TEST ONLY: the producer of cluster 0 never issues this k-stage,
                              so the MMA issuer's bounded wait expires (-1 = off)              */
@@ -129,7 +129,10 @@ typedef struct {
     int cta_group, block_m, block_n, block_k, stages;
     int tiles_m, tiles_n;  /* output tiles                                                  */
     int clusters;          /* persistent clusters launched (grid = clusters * cta_group)    */
-    int raster_group;      /* tile rows per raster group                                    */
+    int raster_group;      /* tile rows per raster group: up to 16 tile rows, groups of up
+                              to 8; beyond, as few groups of at most 16 as cover them
+                              while a group's A panels take at most 64 MiB, else 8.  In
+                              gemm_last_plan, the handle's raster_group option when set */
     int tma_store;         /* 1: epilogue moves C boxes by TMA (C_in loads when beta != 0,
                               then tensor stores); 0: per-row st.global / ld.global        */
     int repack_a, repack_b;/* 1: operand copied to a 16-byte pitch workspace first          */
