@@ -441,3 +441,47 @@ def test_bench_workload_plans(lib, wid):
     got = (p.config, p.stream_k, p.dp_tiles, p.clusters, p.transposed, p.gemv, p.q4_dequant, p.kernels)
     assert got == WORKLOAD_PLANS[wid], (w.name, got)
     assert (p.repack_a, p.repack_b) == ((1, 1) if wid == 4 else (0, 0))
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include "gemm.h"
+
+int main(void) {
+    gemm_options_t o;
+    gemm_plan_t p;
+    gemm_config_info_t info;
+    int n = gemm_num_configs();
+    gemm_options_default(&o);
+    if (o.config != -1) return 1;
+    if (gemm_config_info(n - 1, &info) != GEMM_OK) return 2;
+    if (gemm_plan(4096, 4096, 4096, 4096, 4096, 4096, GEMM_F16, GEMM_F16, GEMM_ROW, GEMM_ROW, 0.0f, 152, 0, -1, -1,
+                  &p) != GEMM_OK) return 3;
+    printf("configs %d plan %d tiles %d x %d status %s\n", n, p.config, p.tiles_m, p.tiles_n,
+           gemm_status_string(GEMM_ERR_ALIGNMENT));
+    return 0;
+}
+"""
+
+
+def test_header_compiles_as_c_and_links(lib, tmp_path):
+    """include/gemm.h is a plain C header: a C99 client built with gcc -Werror links against the
+    library and gets the same plan as the Python binding, using host-only entry points."""
+    import shutil
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(lib._name)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(root, "include"), str(src),
+                        "-o", str(exe), "-L", libdir, "-l:" + os.path.basename(lib._name), "-Wl,-rpath," + libdir],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    st, p = plan(4096, 4096, 4096, dout=0)
+    assert r.stdout.split()[:7] == ["configs", str(G.gemm_num_configs()), "plan", str(p.config), "tiles",
+                                    str(p.tiles_m), "x"], r.stdout
