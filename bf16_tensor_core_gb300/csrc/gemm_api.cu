@@ -78,6 +78,7 @@ int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 struct DevInfo {
     int num_sms = 0;
     int slots[kNumConfigs] = {};                 // clusters of each config that fit at once
+    int rs_slots[kNumConfigs][3] = {};           // 1-SM 64-wide configs: clusters of 2, 4, 8 CTAs that fit
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
 };
 
@@ -123,6 +124,28 @@ gemm_status_t query_device(int dev, bool force_optin_failure, DevInfo* info) {
             }
         }
         info->slots[c] = n;
+        // The split parts of a tile as one cluster (KernelParams::rs_cluster): 1-SM configs of 64-wide tiles.
+        if (d->cta_group == 1 && d->block_n == 64 && !d->b_q4) {
+            for (int i = 0; i < 3; ++i) {
+                cudaLaunchConfig_t lc = {};
+                lc.gridDim = dim3((unsigned)((info->num_sms >> (i + 1)) << (i + 1)), 1, 1);
+                lc.blockDim = dim3((unsigned)d->threads, 1, 1);
+                lc.dynamicSmemBytes = (size_t)d->smem_bytes;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 2u << i;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                lc.attrs = attr;
+                lc.numAttrs = 1;
+                int m = 0;
+                if (cudaOccupancyMaxActiveClusters(&m, config_kernel(c, OUT_F16), &lc) != cudaSuccess) {
+                    cudaGetLastError();
+                    m = 0;
+                }
+                info->rs_slots[c][i] = m;
+            }
+        }
     }
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -570,6 +593,8 @@ struct LaunchArgs {
     int c_trans = 0;            // the product is C^T (see Problem / transpose)
     bool pdl = true;            // launch with programmatic stream serialization
     bool k_alternate = true;    // whole tiles of odd waves walk K downwards (L2 reuse between waves)
+    const DevInfo* dev = nullptr;  // the device's cluster capacities (split parts as clusters); null: not used
+    int* split_cluster_out = nullptr;  // receives KernelParams::rs_cluster of the launch
 };
 
 // Whether a stream-K schedule splits every tile over the same number S of consecutive clusters with
@@ -695,9 +720,20 @@ gemm_status_t launch_planned(const LaunchArgs& a, const TmapFn& tmap, const char
         const int S = plan.clusters / p.num_tiles;   // whole tiles split over S clusters each: reduce-scatter
         if (rs_split(plan.dp_tiles, plan.clusters, p.num_tiles, p.k_tiles, d->b_q4 ? 4 : 8)) p.sk_rs = S;
     }
+    // The transposed skinny product's split parts exchange their blocks inside a thread-block cluster
+    // when every tile's cluster of S CTAs fits on the device at once.
+    int launch_cluster = cluster_ctas(*d);
+    if (p.sk_rs > 1 && a.c_trans && a.dev != nullptr && d->cta_group == 1 && d->block_n == 64 && !d->b_q4) {
+        const int i = p.sk_rs == 2 ? 0 : p.sk_rs == 4 ? 1 : p.sk_rs == 8 ? 2 : -1;
+        if (i >= 0 && a.dev->rs_slots[plan.config][i] >= p.num_tiles) {
+            p.rs_cluster = 1;
+            launch_cluster = p.sk_rs;
+        }
+    }
+    if (a.split_cluster_out) *a.split_cluster_out = p.rs_cluster;
     *what = "GEMM kernel launch";
     cudaError_t e = config_launch(plan.config, a.dout == GEMM_F32 ? OUT_F32 : (a.dout == GEMM_F16 ? OUT_F16 : OUT_BF16),
-                                  plan.clusters * cluster_ctas(*d), a.stream, a.pdl, ta, tb, tc, p);
+                                  plan.clusters * cluster_ctas(*d), launch_cluster, a.stream, a.pdl, ta, tb, tc, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         *cuda_err = e;
@@ -824,8 +860,8 @@ const void* config_kernel(int id, int out) {
     }
 }
 
-cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, bool pdl, const CUtensorMap& a,
-                          const CUtensorMap& b, const CUtensorMap& c, const KernelParams& p) {
+cudaError_t config_launch(int id, int out, int grid_ctas, int cluster, cudaStream_t stream, bool pdl,
+                          const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const KernelParams& p) {
     const ConfigDesc* d = config_desc(id);
     if (!d) return cudaErrorInvalidValue;
     cudaLaunchConfig_t lc = {};
@@ -835,7 +871,7 @@ cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, b
     lc.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cluster_ctas(*d);
+    attr[0].val.clusterDim.x = (unsigned)cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1136,7 +1172,7 @@ gemm_status_t run_impl(gemm_handle_t h, int64_t M, int64_t N, int64_t K, const v
         LaunchArgs la{&plan, q.M, q.N, K, a_ptr, lda_eff, b_ptr, ldb_eff, C, ldc, dtype_in, dtype_out, q.la, q.lb,
                       alpha, beta, bias, h->d_status, (unsigned long long)h->opt.timeout_ms * 1000000ull,
                       h->opt.debug_skip_stage, h->opt.raster_group, h->sk_part, h->sk_flags, h->epoch, s,
-                      h->force_2d, trans ? 1 : 0, h->opt.pdl != 0, !h->k_forward};
+                      h->force_2d, trans ? 1 : 0, h->opt.pdl != 0, !h->k_forward, &h->dev, &plan.split_cluster};
         TmapFn tmap = [h](const TmapDesc& desc, CUtensorMap* m) { return get_tmap_cached(h, desc, m); };
         cudaError_t ce = cudaSuccess;
         st = launch_planned(la, tmap, &what, &ce);

@@ -77,6 +77,13 @@ struct KernelParams {
     // for the S - 1 flags of the same warp in the tile's other parts, adds their partials and stores its
     // block of C.  So every part moves (S - 1) / S of a tile instead of one head reading all S - 1.
     int sk_rs;
+    // 1 (with sk_rs, 1-SM configs of 64-wide tiles, the transposed product): the S parts of a tile are the
+    // S CTAs of one thread-block cluster, and the blocks travel through distributed shared memory
+    // instead of global partials and flags.  Each owning warp arms a barrier for S - 1 blocks and tells
+    // the same warp of every other part that its slice of the (now idle) operand ring is free; each of
+    // those warps then stores its accumulator block straight into that slice (st.async, completing on
+    // the owner's barrier); the owner adds the S blocks in part order and stores its block of C.
+    int rs_cluster;
     // 1: whole tiles of odd waves walk their k-tiles from the last to the first, so the first operand
     // slabs such a tile reads are the ones the tiles of the wave before read last (still in L2).
     int k_alternate;
@@ -492,11 +499,16 @@ __device__ __forceinline__ bool head_fixup(uint32_t tbase, int lane, const float
 //   the boxes do not wait for one another's round trips.
 //   kLean (a CTA of 14 warps, 128 registers each): the second 32-column half of a 16-bit box is read from
 //   TMEM only after the first half is packed, so that the two halves are never live together.
+//   parts > 0 (transposed 32-column blocks only, KernelParams::rs_cluster): the accumulator is part `self`
+//   of the tile's `parts` partial sums and the others' blocks are in shared memory at parts_smem + 4 KB x
+//   part (slot `self` free, each block [8 column quads][32 lanes][4 f32]); the block's value is
+//   ((x_0 + x_1) + x_2) + ... in part order.
 template <int kOut, int kCols, bool kTrans = false, bool kLean = false>
 __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUtensorMap* tmC, uint32_t tbase,
                                               int row0, int col_base, int lane, uint32_t stage_buf,
                                               float* out_part, uint32_t cin_bar, uint32_t* cin_uses,
-                                              const volatile int* abort_flag, uint32_t cin_ring = 0) {
+                                              const volatile int* abort_flag, uint32_t cin_ring = 0,
+                                              uint32_t parts_smem = 0, int parts = 0, int self = 0) {
     const int row = row0 + lane;
     if (out_part != nullptr) {
         float4* dst = reinterpret_cast<float4*>(out_part);
@@ -638,6 +650,31 @@ __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUten
             uint32_t acc[32];
             tmem_ld_32x32b_x32(tbase + c * 32, acc);
             tmem_wait_ld();
+            if constexpr (kTrans && kCols == 32) {
+                if (parts > 0) {
+                    // This warp's own block joins the others at its part's slot; then the sum runs in
+                    // part order.
+                    const uint32_t own = parts_smem + static_cast<uint32_t>(self) * 4096u;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        st_shared_v4(own + static_cast<uint32_t>((q * 32 + lane) * 16), acc[4 * q], acc[4 * q + 1],
+                                     acc[4 * q + 2], acc[4 * q + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        float4 sum = ld_shared_f4(parts_smem + static_cast<uint32_t>((q * 32 + lane) * 16));
+                        for (int i = 1; i < parts; ++i) {
+                            const float4 e = ld_shared_f4(parts_smem + static_cast<uint32_t>(i) * 4096u +
+                                                          static_cast<uint32_t>((q * 32 + lane) * 16));
+                            sum.x += e.x; sum.y += e.y; sum.z += e.z; sum.w += e.w;
+                        }
+                        acc[4 * q + 0] = __float_as_uint(sum.x);
+                        acc[4 * q + 1] = __float_as_uint(sum.y);
+                        acc[4 * q + 2] = __float_as_uint(sum.z);
+                        acc[4 * q + 3] = __float_as_uint(sum.w);
+                    }
+                }
+            }
             if (col0 >= p.N) continue;
             float v[32];
             epilogue_math<kOut, kTrans>(p, acc, v, row, col0);
@@ -834,6 +871,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __shared__ __align__(8) uint64_t bar_drain;
     __shared__ __align__(8) uint64_t bar_fix[Cfg::kEpiWarps * kFixBufs];   // stream-K head fix-up pieces
     __shared__ __align__(8) uint64_t bar_cin[Cfg::kEpiWarps];              // C_in boxes (beta != 0, TMA path)
+    __shared__ __align__(8) uint64_t bar_rsx[Cfg::kEpiWarps];              // rs_cluster: blocks in / owner ready
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_abort;
 
@@ -938,6 +976,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         mbar_init(smem_u32(&bar_drain), 1);
         for (int b = 0; b < Cfg::kEpiWarps * kFixBufs; ++b) mbar_init(smem_u32(&bar_fix[b]), 1);
         for (int b = 0; b < Cfg::kEpiWarps; ++b) mbar_init(smem_u32(&bar_cin[b]), 1);
+        for (int b = 0; b < Cfg::kEpiWarps; ++b) mbar_init(smem_u32(&bar_rsx[b]), 1);
         fence_barrier_init();
     }
     if (threadIdx.x == 32) {
@@ -949,6 +988,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tc_fence_before_sync();
     __syncthreads();
     if constexpr (kClusterCtas > 1) cluster_sync();
+    else if (p.rs_cluster) cluster_sync();      // the other parts arrive on this CTA's barriers
     tc_fence_after_sync();
     const uint32_t tmem_base = s_tmem_base;
     // The set-up above touched no global memory; everything below may read what the previous kernel
@@ -1098,7 +1138,54 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    acc * static_cast<uint32_t>(Cfg::kAccCols) + static_cast<uint32_t>(pcol0);
             float* out_part = nullptr;
-            if (p.sk_rs > 1 && u.kind != UNIT_FULL) {
+            uint32_t parts_smem = 0;   // rs_cluster owner: the other parts' blocks, 4 KB per part
+            int parts = 0, self_part = 0;
+            bool sent = false;         // rs_cluster: this warp's block went to its owner; no C block here
+            if (kCtaGroup == 1 && !kQ4 && Cfg::kEpiCols == 32 && p.rs_cluster && p.sk_rs > 1 && u.kind != UNIT_FULL) {
+                // The S parts of the tile are the S CTAs of this thread-block cluster.  The owner of
+                // warp ew's block is part ew * S / warps; its owner warps take S x 4 KB each of its ring.
+                const int S = p.sk_rs;
+                const uint32_t r = cluster_ctarank();
+                const int per_owner = Cfg::kEpiWarps / S;
+                const uint32_t owner = static_cast<uint32_t>(ew / per_owner);
+                const uint32_t region = ring + static_cast<uint32_t>(ew - static_cast<int>(owner) * per_owner) *
+                                                   static_cast<uint32_t>(S) * 4096u;
+                const uint32_t bar = smem_u32(&bar_rsx[ew]);
+                bool ready;
+                if (owner == r) {
+                    if (lane == 0) {
+                        // Arm for the S - 1 blocks, then tell the same warp of every other part that
+                        // this slice of the idle ring may be written.
+                        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(S - 1) * 4096u);
+                        for (int j = 0; j < S; ++j)
+                            if (j != static_cast<int>(r)) mbar_arrive_cluster(mapa_shared(bar, static_cast<uint32_t>(j)));
+                    }
+                    ready = mbar_wait_bounded<true>(bar, 0u, p.timeout_ns, abort_flag);
+                    parts_smem = region;
+                    parts = S;
+                    self_part = static_cast<int>(r);
+                } else {
+                    // Wait for the owner's word, then store the block into its slot of the owner's slice.
+                    ready = mbar_wait_bounded<true>(bar, 0u, p.timeout_ns, abort_flag);
+                    if (__all_sync(0xffffffffu, ready)) {
+                        uint32_t a[32];
+                        tmem_ld_32x32b_x32(tbase, a);
+                        tmem_wait_ld();
+                        const uint32_t slot = region + r * 4096u + static_cast<uint32_t>(lane) * 16u;
+                        const uint32_t rbar = mapa_shared(bar, owner);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)    // [quad][lane][4 f32], as the owner reads it
+                            st_async_v4(mapa_shared(slot + static_cast<uint32_t>(q) * 512u, owner), a[4 * q], a[4 * q + 1],
+                                        a[4 * q + 2], a[4 * q + 3], rbar);
+                        sent = true;
+                    }
+                }
+                if (!__all_sync(0xffffffffu, ready)) {
+                    if (lane == 0 && !*abort_flag)
+                        report_error<kClusterCtas>(p, ROLE_EPILOGUE, u.tile, 300 + quarter, abort_flag);
+                    break;
+                }
+            } else if (p.sk_rs > 1 && u.kind != UNIT_FULL) {
                 // Reduce-scatter split (one unit per cluster, parts of a tile in consecutive clusters).
                 const int S = p.sk_rs;
                 const int r = cluster_id % S;
@@ -1162,9 +1249,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
             }
             bool drained;
-            if (!kQ4 && p.c_trans)     // (the transposed product never takes Q4_0 weights)
+            if (sent)
+                drained = true;
+            else if (!kQ4 && p.c_trans)     // (the transposed product never takes Q4_0 weights)
                 drained = epilogue_tile<kOut, Cfg::kEpiCols, !kQ4>(p, &tmC, tbase, row0, nb * kBN + pcol0, lane, stage_buf,
-                                                                   out_part, smem_u32(&bar_cin[ew]), &cin_uses, abort_flag);
+                                                                   out_part, smem_u32(&bar_cin[ew]), &cin_uses, abort_flag,
+                                                                   0u, parts_smem, parts, self_part);
             else
                 drained = epilogue_tile<kOut, Cfg::kEpiCols, false, kQ4>(p, &tmC, tbase, row0, nb * kBN + pcol0, lane, stage_buf,
                                                              out_part, smem_u32(&bar_cin[ew]), &cin_uses, abort_flag,
@@ -1292,6 +1382,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tc_fence_before_sync();
     __syncthreads();
     if constexpr (kClusterCtas > 1) cluster_sync();
+    else if (p.rs_cluster) cluster_sync();      // no part leaves while another may still write into it
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();

@@ -48,9 +48,10 @@ const ConfigDesc* config_desc(int id);
 // Kernel entry for config `id` and output type `out` (for attributes and occupancy queries).
 const void* config_kernel(int id, int out);
 
-// Launch config `id` on `grid_ctas` CTAs (clusters of cta_group) on `stream`.
-cudaError_t config_launch(int id, int out, int grid_ctas, cudaStream_t stream, bool pdl, const CUtensorMap& a,
-                          const CUtensorMap& b, const CUtensorMap& c, const KernelParams& p);
+// Launch config `id` on `grid_ctas` CTAs on `stream`, in thread-block clusters of `cluster_ctas` CTAs
+// (the config's cta_group, or the split parts of a tile for KernelParams::rs_cluster).
+cudaError_t config_launch(int id, int out, int grid_ctas, int cluster_ctas, cudaStream_t stream, bool pdl,
+                          const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const KernelParams& p);
 
 // Per-config translation units.
 const void* cfg0_kernel(int out);

@@ -46,6 +46,14 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v)
     asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
 }
 
+// 16-byte store into another CTA's shared memory (both addresses shared::cluster, from mapa); its
+// bytes complete the transaction count of the barrier `bar` in that CTA.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+                 :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar) : "memory");
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // A kernel launched with programmatic stream serialization may start while the kernel before it on
 // the stream is still running.  griddep_wait() returns once every grid this one depends on has

@@ -45,7 +45,8 @@ class gemm_plan_t(ctypes.Structure):
                 ("raster_group", ctypes.c_int), ("tma_store", ctypes.c_int), ("repack_a", ctypes.c_int),
                 ("repack_b", ctypes.c_int), ("workspace_bytes", ctypes.c_int64), ("kernels", ctypes.c_int),
                 ("stream_k", ctypes.c_int), ("dp_tiles", ctypes.c_int), ("sk_partial_bytes", ctypes.c_int64),
-                ("transposed", ctypes.c_int), ("gemv", ctypes.c_int), ("q4_dequant", ctypes.c_int)]
+                ("transposed", ctypes.c_int), ("gemv", ctypes.c_int), ("q4_dequant", ctypes.c_int),
+                ("split_cluster", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}

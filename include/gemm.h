@@ -149,6 +149,9 @@ typedef struct {
     int q4_dequant;        /* 1 (gemm_run_q4_0): the Q4_0 weights are first dequantised by the
                               separate pass into the handle's workspace; the other fields
                               describe the f16 GEMM that follows (kernels counts both)         */
+    int split_cluster;     /* 1 (gemm_last_plan only; gemm_plan, which queries no device, reports
+                              0): the split-K parts of each tile ran as one thread-block cluster
+                              and exchanged their partial sums through distributed shared memory */
 } gemm_plan_t;
 
 /* Fill *opt with defaults (config -1, timeout 2000 ms, no sync check, automatic raster). */

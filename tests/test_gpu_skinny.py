@@ -76,12 +76,23 @@ def test_skinny_split_k_and_fixup():
     assert plan["transposed"] == 1 and plan["stream_k"] == 1 and plan["clusters"] > plan["tiles_m"] * plan["tiles_n"]
 
 
-@pytest.mark.parametrize("S", [2, 4])
+def test_skinny_split_through_global_partials_without_clusters():
+    """A split of 3 parts per tile is not a reduce-scatter (3 does not divide the 8 epilogue warps), so
+    the cluster exchange does not take it: the parts hand their partial sums to the tile's head through
+    global memory."""
+    _need_gpu()
+    w = W.problem(48, 640, 4096, dtype_out="f16", layoutB="col", bias=True, seed=602)
+    plan, _ = _check(w, stream_k=1, max_clusters=15)        # 5 tiles x 3 parts: not a reduce-scatter
+    assert plan["transposed"] == 1 and plan["stream_k"] == 1 and plan["split_cluster"] == 0
+
+
+@pytest.mark.parametrize("S", [2, 4, 8])
 @pytest.mark.parametrize("dout,beta,bias", [("f16", 0.0, False), ("f32", 1.0, True), ("bf16", 0.0, True)])
 def test_skinny_split_reduction_is_deterministic(S, dout, beta, bias):
-    """40 x 1024 x 4096: 8 tiles of C^T, each split over S CTAs whose partial sums are reduced as a
-    reduce-scatter.  Each block is added up in a fixed order, so every run gives the same bits
-    whichever part finishes first, and the result matches the oracle."""
+    """40 x 1024 x 4096: 8 tiles of C^T, each split over S CTAs that form one thread-block cluster and
+    reduce their partial sums as a reduce-scatter through distributed shared memory.  Each block is
+    added up in part order, so every run gives the same bits whichever part finishes first, and the
+    result matches the oracle."""
     _need_gpu()
     din = "bf16" if dout == "bf16" else "f16"
     w = W.problem(40, 1024, 4096, dtype_in=din, dtype_out=dout, layoutB="col", bias=bias, alpha=0.75, beta=beta,
@@ -99,6 +110,7 @@ def test_skinny_split_reduction_is_deterministic(S, dout, beta, bias):
         assert g.status() == G.GEMM_OK
     torch.cuda.synchronize()
     assert plan["transposed"] == 1 and plan["stream_k"] == 1 and plan["clusters"] == 8 * S
+    assert plan["split_cluster"] == 1
     rep = compare(w, d, outs[0])
     assert rep["passed"], rep
     for C in outs[1:]:
