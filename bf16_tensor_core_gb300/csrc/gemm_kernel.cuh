@@ -421,6 +421,34 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
     return v;
 }
 
+// A warp's whole 32 x 32 block of the transposed product, 16-bit output: lane l holds v[i] =
+// C[col0 + i][row0 + l].  The block goes through the warp's staging buffer (row i of C at i * 64 bytes)
+// so that each lane then writes 16-byte pieces of C's rows instead of 32 two-byte stores.  Needs the
+// whole block inside C and 16-byte aligned C rows (row0 is a multiple of 32).
+template <int kOut>
+__device__ __forceinline__ void store_block_trans_staged(const KernelParams& p, const float (&v)[32], int row0,
+                                                         int col0, int lane, uint32_t buf) {
+    static_assert(kOut != OUT_F32, "16-bit outputs");
+    constexpr int kElt = 2;
+    constexpr int kPieces = 32 * kElt / 16;          // 16-byte pieces per row of the block
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t a = buf + static_cast<uint32_t>((i * 32 + lane) * kElt);
+        const unsigned short h = static_cast<unsigned short>(pack2<kOut>(v[i], 0.0f) & 0xffffu);
+        asm volatile("st.shared.u16 [%0], %1;" :: "r"(a), "h"(h) : "memory");
+    }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < kPieces; ++k) {
+        const int c = lane + 32 * k;
+        const int i = c / kPieces, piece = c % kPieces;
+        const float4 w = ld_shared_f4(buf + static_cast<uint32_t>(i * 32 * kElt + piece * 16));
+        char* dst = static_cast<char*>(p.C) + (static_cast<long long>(col0 + i) * p.ldc + row0) * kElt + piece * 16;
+        *reinterpret_cast<float4*>(dst) = w;
+    }
+    __syncwarp();   // the buffer is free again
+}
+
 // Stream-K partials.  Inside one CTA's slot the data of epilogue warp ew (its 32 rows x kCols
 // columns) is one contiguous block [kCols / 4 column quads][32 lanes][4 f32]: a warp store of one
 // quad is 512 contiguous bytes, and 64 columns (8 KB) are one contiguous piece.
@@ -678,6 +706,14 @@ __device__ __forceinline__ bool epilogue_tile(const KernelParams& p, const CUten
             if (col0 >= p.N) continue;
             float v[32];
             epilogue_math<kOut, kTrans>(p, acc, v, row, col0);
+            if constexpr (kTrans && kCols == 32 && kOut != OUT_F32) {
+                // The warp's whole block inside C (warp-uniform): 16-byte stores through the staging buffer
+                // (f32 rows are already written 128 bytes per warp instruction).
+                if (p.c_vec_ok && row0 + 32 <= p.M && col0 + 32 <= p.N) {
+                    store_block_trans_staged<kOut>(p, v, row0, col0, lane, stage_buf);
+                    continue;
+                }
+            }
             store_row_direct<kOut, kTrans>(p, v, row, col0);
         }
     }
