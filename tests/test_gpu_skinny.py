@@ -117,6 +117,31 @@ def test_skinny_split_reduction_is_deterministic(S, dout, beta, bias):
         assert torch.equal(C, outs[0])
 
 
+def test_skinny_cluster_split_bounded_wait():
+    """The first CTA of the first tile's cluster never receives its second stage: its MMA wait runs out,
+    so it never signals its slices free nor sends its blocks, and the other three parts of that cluster
+    give up on it after 200 ms.  The timeout is reported, every CTA leaves, and the next call works."""
+    _need_gpu()
+    w = W.problem(40, 1024, 4096, dtype_out="f16", layoutB="col", seed=650)
+    d = W.generate(w)
+    dd = device_inputs(d)
+    C = alloc_c(w, d)
+    g = G.Gemm(0, stream_k=1, max_clusters=32, timeout_ms=200, debug_skip_stage=1)
+    run_gpu(g, w, dd, C)
+    assert g.last_plan()["split_cluster"] == 1 and g.last_plan()["config"] == 7
+    st = g.status()
+    assert st == G.GEMM_ERR_TIMEOUT, G.gemm_status_string(st)
+    assert g.status() == G.GEMM_OK
+    g.close()
+    C = alloc_c(w, d)
+    with G.Gemm(0, stream_k=1, max_clusters=32, sync_check=1) as g2:
+        run_gpu(g2, w, dd, C)
+        assert g2.last_plan()["split_cluster"] == 1
+    torch.cuda.synchronize()
+    rep = compare(w, d, C)
+    assert rep["passed"], rep
+
+
 def test_skinny_integers_equal_plain_product():
     """Small integers: the transposed and the plain product are both exact, hence equal."""
     _need_gpu()
