@@ -372,40 +372,66 @@ def cpu_baseline(w, d, budget_s: float, gpu_rows=None) -> dict:
     return out
 
 
-def cublas_context(w, A, B, bias, C, flush, steps, warmup, stream):
-    """torch.matmul / torch.addmm (cuBLAS) on the same device inputs, timed like our arm (L2 flushed,
-    CUDA events around each call).  Context only: None where torch has no single call for the product
-    (Q4_0 or 8-bit inputs, an output type other than the inputs')."""
+def cublas_context(w, A, B, bias, C, flush, steps, warmup, stream, sets=None):
+    """cuBLAS through torch on the same device inputs, timed like our arm: torch.matmul / torch.addmm for
+    16-bit inputs, torch._scaled_mm (unit scales, alpha folded into A's scale) for 8-bit ones.  `value` is
+    the flush protocol (L2 flushed, CUDA events around each call); with `sets`, `rotate` is the rotate
+    protocol (the calls on the rotating operand sets captured in one CUDA graph, replayed back to back).
+    Context only: None where torch has no single call for the product (Q4_0 weights, or an output type
+    other than the inputs' for 16-bit inputs)."""
     import numpy as np
     import torch
-    if w.layoutB == "q4_0" or w.dtype_in not in ("f16", "bf16") or w.dtype_out != w.dtype_in:
+    f8 = w.dtype_in in ("e4m3", "e5m2")
+    if w.layoutB == "q4_0" or (not f8 and (w.dtype_in not in ("f16", "bf16") or w.dtype_out != w.dtype_in)):
         return None
-    a = A if w.layoutA == "row" else A.t()
-    b = B if w.layoutB == "row" else B.t()
-    a, b = a[: w.M, : w.K], b[: w.K, : w.N]
-    out = torch.empty(w.M, w.N, dtype=C.dtype, device=C.device)
-    cin = C[: w.M, : w.N].clone() if w.beta != 0.0 else None
-    if cin is not None:
-        call = lambda: torch.addmm(cin, a, b, beta=w.beta, alpha=w.alpha, out=out)
-    elif bias is not None:
-        call = lambda: torch.addmm(bias, a, b, alpha=w.alpha, out=out)
-    else:
-        call = lambda: torch.mm(a, b, out=out) if w.alpha == 1.0 else torch.addmm(out, a, b, beta=0.0, alpha=w.alpha, out=out)
-    with torch.cuda.stream(stream):
-        for _ in range(max(warmup, 3)):
-            flush.zero_()
-            call()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        for e0, e1 in evs:
-            flush.zero_()
-            e0.record(stream)
-            call()
-            e1.record(stream)
-    torch.cuda.synchronize()
+    if f8 and (w.beta != 0.0 or w.layoutA != "row" or w.layoutB != "col"):
+        return None
+
+    def make_call(A, B, C):
+        a = A if w.layoutA == "row" else A.t()
+        b = B if w.layoutB == "row" else B.t()
+        a, b = a[: w.M, : w.K], b[: w.K, : w.N]
+        if f8:                      # row-major A, column-major B (B stored N x K)
+            sa = torch.tensor(w.alpha, dtype=torch.float32, device=A.device)
+            sb = torch.tensor(1.0, dtype=torch.float32, device=A.device)
+            odt = C.dtype
+            return lambda: torch._scaled_mm(a, b, sa, sb, bias=bias, out_dtype=odt)
+        out = torch.empty(w.M, w.N, dtype=C.dtype, device=C.device)
+        cin = C[: w.M, : w.N].clone() if w.beta != 0.0 else None
+        if cin is not None:
+            return lambda: torch.addmm(cin, a, b, beta=w.beta, alpha=w.alpha, out=out)
+        if bias is not None:
+            return lambda: torch.addmm(bias, a, b, alpha=w.alpha, out=out)
+        if w.alpha == 1.0:
+            return lambda: torch.mm(a, b, out=out)
+        return lambda: torch.addmm(out, a, b, beta=0.0, alpha=w.alpha, out=out)
+
+    try:
+        call = make_call(A, B, C)
+        with torch.cuda.stream(stream):
+            for _ in range(max(warmup, 3)):
+                flush.zero_()
+                call()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for e0, e1 in evs:
+                flush.zero_()
+                e0.record(stream)
+                call()
+                e1.record(stream)
+        torch.cuda.synchronize()
+    except (RuntimeError, TypeError) as e:       # e.g. no 8-bit matmul for this device in this torch
+        return {"unavailable": f"{type(e).__name__}: {str(e).splitlines()[0][:160]}"}
     ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
-    return {"value": w.flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-            "call": "torch.addmm" if (cin is not None or bias is not None or w.alpha != 1.0) else "torch.mm",
-            "note": "cuBLAS through torch on the same inputs and timing protocol; context, not a baseline"}
+    res = {"value": w.flops / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+           "call": ("torch._scaled_mm" if f8 else
+                    "torch.addmm" if (w.beta != 0.0 or bias is not None or w.alpha != 1.0) else "torch.mm"),
+           "note": "cuBLAS through torch on the same inputs and timing protocols; context, not a baseline"}
+    if sets:
+        calls = [make_call(bs["A"], bs["B"], bs["C"]) for bs in sets]
+        us = graph_step_us(lambda j, st: calls[j](), len(calls))
+        res["rotate"] = {"value": w.flops / (us / 1e6) / 1e12, "unit": "TFLOP/s", "us_per_step": us,
+                         "sets": len(calls)}
+    return res
 
 
 def _workload(args):
@@ -879,7 +905,7 @@ def run_ours(args, rank, world, local):
             "other_protocol": other_line,
             "sustained": sustained}
     if args.context_cublas:
-        line["context_cublas"] = cublas_context(w, A, B, bias, C, flush, args.steps, args.warmup, stream)
+        line["context_cublas"] = cublas_context(w, A, B, bias, C, flush, args.steps, args.warmup, stream, sets)
     if world == 1 and not args.no_cpu_baseline:
         def gpu_rows(r):
             if Cin_host is not None:
