@@ -61,6 +61,14 @@
  *   waits inside the kernels are bounded: on expiry a kernel records
  *   {code, role, tile, stage} in the status word and returns cleanly;
  *   gemm_get_device_status reports it as GEMM_ERR_TIMEOUT.
+ *
+ * Environment (read once, by gemm_create; none is needed in normal use)
+ *   GEMM_TEST_FAIL=optin|tmap|launch|alloc  (tests) force that host error path
+ *                                           of the handle; the names combine.
+ *   GEMM_TMA_RANK=2     (tuning) one 2-D TMA box per 64-element slab even where
+ *                       a 3-D box would fill a whole operand stage.
+ *   GEMM_K_ORDER=forward (tuning) every tile walks K upwards; by default whole
+ *                       tiles of odd waves walk it downwards for L2 reuse.
  */
 #ifndef GB300_GEMM_H
 #define GB300_GEMM_H
