@@ -410,6 +410,25 @@ __device__ __forceinline__ void prefetch_c_rows(const KernelParams& p, int row, 
         asm volatile("prefetch.global.L2 [%0];" :: "l"(reinterpret_cast<uint64_t>(base + max(off, 0))));
 }
 
+// The same for the transposed product: the warp's block of C^T is kernel rows row0 .. row0 + 31 and
+// kernel columns col0 .. col0 + kCols - 1, i.e. 32 consecutive elements of each of C's rows col0 + j;
+// lane l asks for rows col0 + l, col0 + 32 + l, ...
+template <int kOut, int kCols>
+__device__ __forceinline__ void prefetch_c_block_trans(const KernelParams& p, int row0, int col0, int lane) {
+    if (row0 >= p.M) return;
+    constexpr int kElt = (kOut == OUT_F32) ? 4 : 2;
+#pragma unroll
+    for (int t = 0; t < kCols / 32; ++t) {
+        const int j = col0 + 32 * t + lane;
+        if (j >= p.N) break;
+        const char* a = static_cast<const char*>(p.C) + (static_cast<long long>(j) * p.ldc + row0) * kElt;
+        asm volatile("prefetch.global.L2 [%0];" :: "l"(reinterpret_cast<uint64_t>(a)));
+        const int last = min(32, p.M - row0) * kElt - 1;   // the block's last byte in this row
+        if (((reinterpret_cast<uintptr_t>(a) & 127u) + last) >= 128u)
+            asm volatile("prefetch.global.L2 [%0];" :: "l"(reinterpret_cast<uint64_t>(a + last)));
+    }
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -1161,8 +1180,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int mb, nb;
             tile_coords(p, u.tile, mb, nb);
             const int row0 = mb * kClusterRows + static_cast<int>(rank) * Cfg::kBM + quarter * 32;
-            if (p.beta != 0.0f && u.kind != UNIT_TAIL && !p.c_trans)
-                prefetch_c_rows<kOut, Cfg::kEpiCols>(p, row0 + lane, nb * kBN + pcol0);   // C_in rows into L2
+            if (p.beta != 0.0f && u.kind != UNIT_TAIL) {        // C_in into L2 while the MMAs run
+                if (!p.c_trans) prefetch_c_rows<kOut, Cfg::kEpiCols>(p, row0 + lane, nb * kBN + pcol0);
+                else prefetch_c_block_trans<kOut, Cfg::kEpiCols>(p, row0, nb * kBN + pcol0, lane);
+            }
             bool ok = mbar_wait_bounded(smem_u32(&bar_tfull[acc]), acc_phase, p.timeout_ns, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
