@@ -924,7 +924,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __shared__ __align__(8) uint64_t bar_tfull[2];
     __shared__ __align__(8) uint64_t bar_tempty[2];
     __shared__ __align__(8) uint64_t bar_drain;
-    __shared__ __align__(8) uint64_t bar_epi_done;   // every epilogue warp has read TMEM for the last time
     __shared__ __align__(8) uint64_t bar_fix[Cfg::kEpiWarps * kFixBufs];   // stream-K head fix-up pieces
     __shared__ __align__(8) uint64_t bar_cin[Cfg::kEpiWarps];              // C_in boxes (beta != 0, TMA path)
     __shared__ __align__(8) uint64_t bar_rsx[Cfg::kEpiWarps];              // rs_cluster: blocks in / owner ready
@@ -1030,7 +1029,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             mbar_init(smem_u32(&bar_tempty[b]), Cfg::kEpiWarps * kCtaGroup);
         }
         mbar_init(smem_u32(&bar_drain), 1);
-        mbar_init(smem_u32(&bar_epi_done), Cfg::kEpiWarps);
         for (int b = 0; b < Cfg::kEpiWarps * kFixBufs; ++b) mbar_init(smem_u32(&bar_fix[b]), 1);
         for (int b = 0; b < Cfg::kEpiWarps; ++b) mbar_init(smem_u32(&bar_cin[b]), 1);
         for (int b = 0; b < Cfg::kEpiWarps; ++b) mbar_init(smem_u32(&bar_rsx[b]), 1);
@@ -1041,9 +1039,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         prefetch_tensormap(&tmB);
         if (p.use_tma_store) prefetch_tensormap(&tmC);
     }
-    if (warp == 1) tmem_alloc<kCtaGroup>(smem_u32(&s_tmem_base), Cfg::kTmemCols);
+    if (warp == 1) {
+        __syncwarp();    // tcgen05.alloc is .aligned: the whole warp, converged (lane 0 prefetched alone above)
+        tmem_alloc<kCtaGroup>(smem_u32(&s_tmem_base), Cfg::kTmemCols);
+    }
     tc_fence_before_sync();
-    __syncthreads();
+    cta_sync_all();
     if constexpr (kClusterCtas > 1) cluster_sync();
     else if (p.rs_cluster) cluster_sync();      // the other parts arrive on this CTA's barriers
     tc_fence_after_sync();
@@ -1342,9 +1343,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         if (lane == 0) bulk_wait_group<0>();
         __syncwarp();
-        // This warp's TMEM reads are over (also after an abort): TMEM may be freed once all have arrived.
-        tc_fence_before_sync();
-        if (lane == 0) mbar_arrive_local(smem_u32(&bar_epi_done));
     } else if constexpr (kQ4) {
         // ------------------------------------------------------------ Q4_0 dequantisation warps
         // Warp dw covers B rows dw * 16 .. +15 of this CTA's 128 (output columns); lane l takes block
@@ -1399,7 +1397,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint32_t all_got;
             asm volatile("{\n\t.reg .pred pin, pout;\n\t"
                          "setp.ne.u32 pin, %1, 0;\n\t"
-                         "bar.red.and.pred pout, 1, %2, pin;\n\t"
+                         "barrier.red.and.pred pout, 1, %2, pin;\n\t"
                          "selp.u32 %0, 1, 0, pout;\n\t}"
                          : "=r"(all_got) : "r"(got ? 1u : 0u), "n"(Cfg::kDqWarps * 32) : "memory");
             if (!all_got) {
@@ -1413,7 +1411,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             fence_proxy_async_smem();
             // The four dequantisation warps of this CTA meet (no exit path lies between the barrier
             // above and this one); one thread arrives for all of them.
-            asm volatile("bar.sync 1, %0;" :: "n"(Cfg::kDqWarps * 32) : "memory");
+            asm volatile("barrier.sync 1, %0;" :: "n"(Cfg::kDqWarps * 32) : "memory");
             if (dw == 0 && lane == 0) {
                 const uint32_t full_local = smem_u32(&bar_full[stage]);
                 if constexpr (kCtaGroup == 2) {
@@ -1442,16 +1440,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         while (global_timer_ns() - t0 < 200000ull) { }
     }
     tc_fence_before_sync();
-    __syncthreads();
+    cta_sync_all();
     if constexpr (kClusterCtas > 1) cluster_sync();
     else if (p.rs_cluster) cluster_sync();      // no part leaves while another may still write into it
     if (warp == 1) {
-        // TMEM is freed only after the epilogue warps' last reads, stated by their own barrier rather than
-        // left to the block barrier above.  The wait ignores the abort flag; only the time limit ends it.
-        if (lane == 0) {
-            volatile int never = 0;
-            mbar_wait_bounded(smem_u32(&bar_epi_done), 0u, p.timeout_ns, &never);
-        }
         __syncwarp();
         tc_fence_after_sync();
         tmem_dealloc<kCtaGroup>(tmem_base, Cfg::kTmemCols);

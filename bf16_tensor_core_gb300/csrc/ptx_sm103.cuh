@@ -37,9 +37,16 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 
+// Warp-specialised kernels reach their block- and cluster-wide barriers from different roles, some warps
+// with one lane still working alone: these are the forms of the barriers that allow a diverged warp
+// (no .aligned), so every thread is counted as it arrives.
 __device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.release;\n\t"
+                 "barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void cta_sync_all() {
+    asm volatile("barrier.sync 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v) {
