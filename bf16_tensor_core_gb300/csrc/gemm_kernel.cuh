@@ -1002,10 +1002,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         }
     };
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == (kQ4 ? 0 : 64)) {
         // The first ring of operand stages of this cluster's first unit into L2 before anything else: the
         // kernel before this one on the stream may still be running (the waits below come later), and the
-        // loads of these stages then hit L2.
+        // loads of these stages then hit L2.  Lane 0 of the first epilogue warp issues them, so that thread 0
+        // initialises the barriers at once and the set-up barrier releases sooner (with Q4_0 B thread 0 does,
+        // whose kernel has no registers to spare for it in the epilogue warps).
         UnitIter first_units;
         first_units.init(p, cluster_id, num_clusters);
         Unit fu;
