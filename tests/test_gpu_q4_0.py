@@ -416,3 +416,17 @@ def test_separate_pass_equals_plain_gemm_on_dequantised_weights(cfg):
     torch.cuda.synchronize()
     assert torch.equal(C1, C2)
     _check(c, C1)
+
+
+def test_decode_workload_q4_0_full_check():
+    """The benchmark's Q4_0 decode workload (1 x 4096 x 4096) with the benchmark's own inputs and handle options,
+    every element against the oracle."""
+    _need_gpu()
+    w = W.WORKLOADS[10]
+    d = W.generate(w)
+    c = dict(M=w.M, N=w.N, K=w.K, A=d["A"], bq=d["B"], bias=d["bias"], Cin=d["Cin"], dout=w.dtype_out,
+             layoutA=w.layoutA, alpha=w.alpha, beta=w.beta)
+    with G.Gemm(0, sync_check=1) as g:
+        C = _run(g, c)
+        assert g.last_plan()["config"] == -1          # the CUDA-core small-M route
+    _check(c, C)

@@ -260,3 +260,21 @@ def test_small_m_forced_where_it_does_not_apply():
         A16 = torch.zeros(16, 4096, dtype=torch.float16, device="cuda")
         C16 = torch.zeros(16, 4096, dtype=torch.float32, device="cuda")
         assert g.run(A16, B, C16, layoutB="col", check=False) == G.GEMM_ERR_UNSUPPORTED  # M > 8
+
+
+@pytest.mark.parametrize("wid", [7, 8])
+def test_decode_workloads_full_check(wid):
+    """The benchmark's decode workloads (1 x 4096 x 4096 on the CUDA-core kernel, 64 x 4096 x 4096 on the transposed
+    split product) with the benchmark's own inputs and handle options, every element against the oracle."""
+    _need_gpu()
+    w = W.WORKLOADS[wid]
+    d = W.generate(w)
+    dd = device_inputs(d)
+    C = alloc_c(w, d)
+    with G.Gemm(0, sync_check=1) as g:
+        run_gpu(g, w, dd, C)
+        plan = g.last_plan()
+        assert plan["gemv"] == (1 if wid == 7 else 0) and plan["transposed"] == (0 if wid == 7 else 1)
+    torch.cuda.synchronize()
+    rep = compare(w, d, C)
+    assert rep["passed"], rep
