@@ -134,3 +134,10 @@ def test_nvidia_smi_summary_reads_the_active_reasons():
     c = bench.ClockSampler.summarize(rows, t0, t0 + 3.0)
     assert c["samples"] == 3 and c["sm_mhz"] == 1500 and c["sm_max_mhz"] == 2070
     assert c["reasons"] == ["hw_slowdown", "sw_power_cap"]
+
+
+@pytest.mark.parametrize("wid", [4, 6, 10])
+def test_cublas_context_declines_products_torch_has_no_single_call_for(wid):
+    """The cuBLAS context leg returns None, before touching the device, where torch has no single call for the
+    product: Q4_0 weights (6, 10) and 16-bit inputs with another output type (4: f16 in, f32 out)."""
+    assert bench.cublas_context(W.WORKLOADS[wid], None, None, None, None, None, 1, 1, None) is None
