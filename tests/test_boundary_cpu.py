@@ -485,3 +485,19 @@ def test_header_compiles_as_c_and_links(lib, tmp_path):
     st, p = plan(4096, 4096, 4096, dout=0)
     assert r.stdout.split()[:7] == ["configs", str(G.gemm_num_configs()), "plan", str(p.config), "tiles",
                                     str(p.tiles_m), "x"], r.stdout
+
+
+def test_warp_specialised_kernel_uses_barriers_that_allow_diverged_warps():
+    """The tensor-core kernel's roles reach its block- and cluster-wide barriers with lane 0 of the producer and
+    MMA warps still working alone.  The .aligned forms (bar.sync / __syncthreads(), barrier.cluster.*.aligned,
+    bar.red) need converged warps and were measured to release early there; only the forms that count each thread
+    as it arrives may appear in the kernel and its PTX wrappers."""
+    import re
+    src = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "bf16_tensor_core_gb300", "csrc")
+    kernel = open(os.path.join(src, "gemm_kernel.cuh")).read()
+    ptx = open(os.path.join(src, "ptx_sm103.cuh")).read()
+    code = "\n".join(l for l in (kernel + ptx).splitlines() if not l.lstrip().startswith("//"))
+    assert "__syncthreads" not in code
+    assert not re.search(r"\bbar\.(sync|red|arrive)\b", code)
+    assert not re.search(r"barrier\.cluster\.(arrive|wait)[.\w]*\.aligned", code)
+    assert "barrier.sync 0" in code and "barrier.cluster.arrive.release;" in code
